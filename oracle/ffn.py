@@ -1,0 +1,118 @@
+"""The routed MoE FFN layer, fp64. Test infrastructure.
+
+Sources: "三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南"
+(section 瓶颈分析: each token runs the FFN of the k experts its router picked;
+section 优化策略三: decode fuses the gate and up mat-muls with the activation;
+section 优化策略二: per-expert formats, three tiers in one layer) and "一张 RTX
+3090 跑 Llama 70B：三层流式缓存 + NVMe 直连" (section 4.4: SwiGLU activation).
+
+Readings taken where the pages are silent:
+
+* Expert e: g = W_gate[e] x, u = W_up[e] x (W_gate, W_up are [I, H]),
+  h = silu(g) * u with silu(z) = z / (1 + exp(-z)), y = W_down[e] h (W_down is
+  [H, I]). The activation is applied to the gate branch.
+* The router weight scales the expert's down-projection output, and
+  out[t] = sum over slots j = 0..k-1, in ascending j, of w[t, j] * y_{t,j}.
+* x is the exact bf16 value; every weight is the exact decoded value; all
+  arithmetic is fp64.
+
+Experts are given as a list of mappings with keys "gate", "up", "down"; each
+value has attributes fmt, rows, cols, stride and data (uint8 bytes).
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+from . import formats, router, bucket as bucket_mod
+
+
+def bf16_bits_to_f64(xb: np.ndarray) -> np.ndarray:
+    u = np.asarray(xb, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def dense(m) -> np.ndarray:
+    return formats.dequant_matrix(m.fmt, m.rows, m.cols, m.stride, m.data)
+
+
+class DenseCache:
+    """Decodes each expert's matrices at most once."""
+
+    def __init__(self, experts):
+        self.experts = experts
+        self._d: Dict[int, tuple] = {}
+
+    def __call__(self, e: int):
+        if e not in self._d:
+            ex = self.experts[e]
+            self._d[e] = (dense(ex["gate"]), dense(ex["up"]), dense(ex["down"]))
+        return self._d[e]
+
+
+def expert_forward(Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, x: np.ndarray):
+    """x fp64 [n, H] -> (g, u, h [n, I], y [n, H])."""
+    g = x @ Wg.T
+    u = x @ Wu.T
+    h = silu(g) * u
+    y = h @ Wd.T
+    return g, u, h, y
+
+
+def moe_ffn(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, renormalize: bool = True,
+            expert_lo: int = 0, expert_hi: Optional[int] = None, format_mask: int = 0xFFFFFFFF,
+            tokens: Optional[Sequence[int]] = None, cache: Optional[DenseCache] = None,
+            gate_formats: Optional[Sequence[int]] = None):
+    """Layer output fp64 [len(tokens) or T, H].
+
+    Routing (router.route_topk) and bucketing (bucket.bucket) run on all T
+    tokens; ``tokens`` only restricts which output rows are evaluated.
+    ``experts`` may be any indexable of length E (e.g. a lazy generator); only
+    the experts that are routed to are read. ``gate_formats`` (format tag of
+    each expert's gate matrix) is needed by the format filter; by default it is
+    read from every expert."""
+    x = bf16_bits_to_f64(x_bf16)
+    T, H = x.shape
+    E = len(experts)
+    ids, w, _ = router.route_topk(logits, k, renormalize)
+    if gate_formats is None:
+        gate_formats = [experts[e]["gate"].fmt for e in range(E)]
+    _, _, pos, _, _ = bucket_mod.bucket(ids, E, expert_lo, expert_hi, format_mask, gate_formats)
+    cache = cache or DenseCache(experts)
+    tok = list(range(T)) if tokens is None else [int(t) for t in tokens]
+    out = np.zeros((len(tok), H), dtype=np.float64)
+    for row, t in enumerate(tok):
+        for j in range(k):                      # ascending slot order
+            if pos[t * k + j] < 0:
+                continue
+            Wg, Wu, Wd = cache(int(ids[t, j]))
+            _, _, _, y = expert_forward(Wg, Wu, Wd, x[t:t + 1])
+            out[row] += w[t, j] * y[0]
+    return out
+
+
+def moe_ffn_bruteforce(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int,
+                       renormalize: bool = True) -> np.ndarray:
+    """Independent second evaluation for small layers: every expert on every
+    token (dense fp64 matrices), then a dense [T, E] routing-weight matrix
+    selects and weights the results. Shares only the decoders and the router
+    with ``moe_ffn``; no bucketing, no per-pair loop."""
+    x = bf16_bits_to_f64(x_bf16)
+    T, H = x.shape
+    E = len(experts)
+    ids, w, _ = router.route_topk(logits, k, renormalize)
+    R = np.zeros((T, E), dtype=np.float64)
+    for t in range(T):
+        for j in range(k):
+            R[t, ids[t, j]] += w[t, j]
+    Y = np.empty((E, T, H), dtype=np.float64)
+    for e in range(E):
+        Wg, Wu, Wd = dense(experts[e]["gate"]), dense(experts[e]["up"]), dense(experts[e]["down"])
+        Y[e] = (silu(x @ Wg.T) * (x @ Wu.T)) @ Wd.T
+    return np.einsum("te,eth->th", R, Y)

@@ -1,0 +1,155 @@
+"""Block-format decoders, fp64. Test infrastructure (see ``oracle/__init__``).
+
+The pages name the formats (Q8_0, Q4_K, Q6_K, MXFP4 in the tiers of "三张 RTX
+3090 … 优化指南", section 优化策略二; Q8_0/Q4_K/Q6_K in the GGUF list of "一张
+RTX 3090 跑 Llama 70B", section 一) but print no byte layout. Reading taken: the
+public GGUF block layouts for Q8_0/Q4_K/Q6_K and the OCP Microscaling (MX) v1.0
+element/scale encoding for MXFP4, little-endian, fp16 = IEEE binary16
+(subnormals included). Each decoder below states its layout.
+
+A matrix is ``rows`` rows of ``cols`` weights; blocks run along the columns; row
+r starts at byte ``r * stride``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+Q8_0, Q4_K, Q6_K, MXFP4 = 1, 2, 3, 4
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17}
+
+# E2M1 magnitudes for codes 0..7 (sign is bit 3): OCP MX v1.0, FP4 E2M1 table.
+E2M1_MAGNITUDE = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0], dtype=np.float64)
+
+
+def _f16(b: np.ndarray) -> np.ndarray:
+    """uint8 [..., 2] little-endian binary16 -> fp64 [...]."""
+    b = np.ascontiguousarray(b, dtype=np.uint8)
+    return b.view("<f2")[..., 0].astype(np.float64)
+
+
+def dequant_q8_0(blk: np.ndarray) -> np.ndarray:
+    """Q8_0, 34 bytes per 32 weights: fp16 d at [0:2], int8 q[32] at [2:34];
+    w_i = d * q_i."""
+    d = _f16(blk[..., 0:2])
+    q = np.ascontiguousarray(blk[..., 2:34]).view(np.int8).astype(np.float64)
+    return d[..., None] * q
+
+
+def q4_k_scale_min(s: np.ndarray):
+    """The eight 6-bit (scale, min) pairs of a Q4_K block from its 12 scale
+    bytes s[0..11]: for j < 4, sc_j = s[j] & 63 and m_j = s[j+4] & 63; for
+    j >= 4 the low four bits come from s[j+4] (scale: low nibble, min: high
+    nibble) and the top two bits from bits 6-7 of s[j-4] (scale) and s[j]
+    (min)."""
+    s = s.astype(np.int64)
+    sc = np.empty(s.shape[:-1] + (8,), dtype=np.int64)
+    m = np.empty_like(sc)
+    for j in range(8):
+        if j < 4:
+            sc[..., j] = s[..., j] & 63
+            m[..., j] = s[..., j + 4] & 63
+        else:
+            sc[..., j] = (s[..., j + 4] & 15) | ((s[..., j - 4] >> 6) << 4)
+            m[..., j] = (s[..., j + 4] >> 4) | ((s[..., j] >> 6) << 4)
+    return sc, m
+
+
+def dequant_q4_k(blk: np.ndarray) -> np.ndarray:
+    """Q4_K, 144 bytes per 256 weights: fp16 d [0:2], fp16 dmin [2:4], 12 scale
+    bytes [4:16], 128 code bytes qs [16:144]. Weights 64g .. 64g+63 (g = 0..3)
+    use qs[32g .. 32g+31]: weight 64g+i (i < 32) is the low nibble of qs[32g+i]
+    and belongs to sub-block 2g; weight 64g+32+i is the high nibble and belongs
+    to sub-block 2g+1. w = d * sc_b * q - dmin * m_b."""
+    d = _f16(blk[..., 0:2])
+    dmin = _f16(blk[..., 2:4])
+    sc, m = q4_k_scale_min(blk[..., 4:16])
+    qs = blk[..., 16:144].astype(np.int64)
+    out = np.empty(blk.shape[:-1] + (256,), dtype=np.float64)
+    for g in range(4):
+        byte = qs[..., 32 * g: 32 * g + 32]
+        for half, q in ((0, byte & 15), (1, byte >> 4)):
+            b = 2 * g + half
+            scale = (d * sc[..., b])[..., None]
+            offset = (dmin * m[..., b])[..., None]
+            out[..., 64 * g + 32 * half: 64 * g + 32 * half + 32] = scale * q - offset
+    return out
+
+
+def q6_k_codes(blk: np.ndarray) -> np.ndarray:
+    """The 256 unsigned 6-bit codes of a Q6_K block (ql [0:128], qh [128:192]).
+    Half h in {0, 1} covers weights 128h .. 128h+127 and uses ql[64h ..],
+    qh[32h ..]. For i < 32 with Q = qh[32h+i]:
+      weight 128h+i    = low nibble of ql[64h+i]     | bits 0-1 of Q << 4
+      weight 128h+32+i = low nibble of ql[64h+32+i]  | bits 2-3 of Q << 4
+      weight 128h+64+i = high nibble of ql[64h+i]    | bits 4-5 of Q << 4
+      weight 128h+96+i = high nibble of ql[64h+32+i] | bits 6-7 of Q << 4"""
+    ql = blk[..., 0:128].astype(np.int64)
+    qh = blk[..., 128:192].astype(np.int64)
+    q = np.empty(blk.shape[:-1] + (256,), dtype=np.int64)
+    for h in range(2):
+        Q = qh[..., 32 * h: 32 * h + 32]
+        lo_a = ql[..., 64 * h: 64 * h + 32]
+        lo_b = ql[..., 64 * h + 32: 64 * h + 64]
+        base = 128 * h
+        q[..., base + 0: base + 32] = (lo_a & 15) | ((Q & 3) << 4)
+        q[..., base + 32: base + 64] = (lo_b & 15) | (((Q >> 2) & 3) << 4)
+        q[..., base + 64: base + 96] = (lo_a >> 4) | (((Q >> 4) & 3) << 4)
+        q[..., base + 96: base + 128] = (lo_b >> 4) | (((Q >> 6) & 3) << 4)
+    return q
+
+
+def dequant_q6_k(blk: np.ndarray) -> np.ndarray:
+    """Q6_K, 210 bytes per 256 weights: ql [0:128], qh [128:192], 16 int8
+    scales [192:208], fp16 d [208:210]. Weight 128h+32r+i (r = 0..3, i < 32)
+    uses scale number 8h + 2r + (i >= 16), i.e. one scale per 16 weights.
+    w = d * scale * (q - 32)."""
+    q = q6_k_codes(blk)
+    scales = np.ascontiguousarray(blk[..., 192:208]).view(np.int8).astype(np.float64)
+    d = _f16(blk[..., 208:210])
+    n = np.arange(256)
+    h, rem = n // 128, n % 128
+    r, i = rem // 32, rem % 32
+    scale_idx = 8 * h + 2 * r + (i >= 16)
+    return d[..., None] * scales[..., scale_idx] * (q - 32).astype(np.float64)
+
+
+def dequant_mxfp4(blk: np.ndarray) -> np.ndarray:
+    """MXFP4, 17 bytes per 32 weights: E8M0 scale byte e at [0], 16 code bytes
+    at [1:17]; weight i < 16 is the low nibble of byte 1+i, weight 16+i its high
+    nibble. An E2M1 nibble has the sign in bit 3 and magnitude index in bits
+    0-2. w = 2**(e - 127) * E2M1(code). e = 255 (NaN in E8M0) is rejected."""
+    e = blk[..., 0].astype(np.int64)
+    if np.any(e == 255):
+        raise ValueError("MXFP4 block with E8M0 scale 0xFF (NaN)")
+    qs = blk[..., 1:17].astype(np.int64)
+    codes = np.concatenate([qs & 15, qs >> 4], axis=-1)
+    mag = E2M1_MAGNITUDE[codes & 7]
+    val = np.where(codes & 8, -mag, mag)
+    return np.ldexp(1.0, e - 127)[..., None] * val
+
+
+DECODERS = {Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q6_K: dequant_q6_k, MXFP4: dequant_mxfp4}
+
+
+def dequant_matrix(fmt: int, rows: int, cols: int, stride: int, data: np.ndarray) -> np.ndarray:
+    """Whole matrix -> fp64 [rows, cols]."""
+    be, bb = BLOCK_ELEMS[fmt], BLOCK_BYTES[fmt]
+    if cols % be:
+        raise ValueError(f"cols={cols} is not a multiple of the block size {be}")
+    nb = cols // be
+    if stride < nb * bb:
+        raise ValueError("row stride shorter than a row")
+    raw = np.asarray(data, dtype=np.uint8).reshape(-1)[: rows * stride]
+    blocks = raw.reshape(rows, stride)[:, : nb * bb].reshape(rows, nb, bb)
+    return DECODERS[fmt](blocks).reshape(rows, cols)
+
+
+def dequant_rows(fmt: int, cols: int, stride: int, data: np.ndarray, rows_idx) -> np.ndarray:
+    """Selected rows only -> fp64 [len(rows_idx), cols]."""
+    be, bb = BLOCK_ELEMS[fmt], BLOCK_BYTES[fmt]
+    nb = cols // be
+    raw = np.asarray(data, dtype=np.uint8).reshape(-1)
+    rows_idx = np.asarray(rows_idx, dtype=np.int64)
+    sel = raw.reshape(-1, stride)[rows_idx][:, : nb * bb].reshape(len(rows_idx), nb, bb)
+    return DECODERS[fmt](sel).reshape(len(rows_idx), cols)

@@ -1,0 +1,154 @@
+"""Pins of the oracle FFN layer (CPU only).
+
+* Closed form: Q8_0 experts whose matrices are a permutation matrix, the
+  identity and twice the identity give out = w0*silu(Px)*x + w1*silu(x)*2x.
+  This fixes the matrix orientation, the branch that takes the activation, and
+  how the router weights enter.
+* Brute force: every expert on every token through dense matrices, then
+  selection by a dense routing matrix, equals the per-pair evaluation.
+* Mixed tiers: the full mixed-format layer equals the sum of format-masked
+  runs (one tier at a time), and an expert-range split sums back to the whole.
+* Permutation: permuting the expert table together with the logit columns
+  leaves the output unchanged.
+* All-zero scales give a zero output.
+"""
+import numpy as np
+import pytest
+
+import synth
+from oracle import ffn, formats
+from synth import MatrixBytes
+
+
+def q8_0_matrix(Q: np.ndarray, d: float = 1.0) -> MatrixBytes:
+    """Integer matrix [rows, cols] (|q| <= 127) -> Q8_0 bytes with scale d."""
+    rows, cols = Q.shape
+    nb = cols // 32
+    stride = synth.padded_stride(synth.Q8_0, cols)
+    data = np.zeros((rows, stride), np.uint8)
+    dbytes = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    for r in range(rows):
+        for b in range(nb):
+            data[r, 34 * b: 34 * b + 2] = dbytes
+            data[r, 34 * b + 2: 34 * b + 34] = Q[r, 32 * b: 32 * b + 32].astype(np.int8).view(np.uint8)
+    return MatrixBytes(synth.Q8_0, rows, cols, stride, data.reshape(-1))
+
+
+def bf16_bits(x: np.ndarray) -> np.ndarray:
+    return synth.f32_to_bf16_bits(x.astype(np.float32))
+
+
+def small_layer(tiers="mixed", E=12, k=3, H=256, I=64, T=5, seed=77, bias=True):
+    cfg = synth.LayerConfig("t", E, k, H, I, T, tiers, bias, seed)
+    return synth.make_layer(cfg, 0)
+
+
+def test_closed_form_identity_experts():
+    n = 32
+    P = np.roll(np.eye(n, dtype=np.int64), 5, axis=1)          # (Px)_i = x_{i+5 mod n}
+    Id = np.eye(n, dtype=np.int64)
+    experts = [
+        {"gate": q8_0_matrix(P), "up": q8_0_matrix(Id), "down": q8_0_matrix(Id)},
+        {"gate": q8_0_matrix(Id), "up": q8_0_matrix(2 * Id), "down": q8_0_matrix(Id)},
+    ]
+    rng = np.random.default_rng(30)
+    x = rng.standard_normal((3, n))
+    xb = bf16_bits(x)
+    xq = ffn.bf16_bits_to_f64(xb)
+    logits = np.array([[1.0, 0.25], [-0.5, 0.75], [0.0, 0.0]], np.float32)
+    out = ffn.moe_ffn(experts, xb, logits, k=2)
+    l = logits.astype(np.float64)
+    for t in range(3):
+        w0 = np.exp(l[t, 0]) / np.exp(l[t]).sum()
+        y0 = ffn.silu(xq[t] @ P.T) * xq[t]
+        y1 = ffn.silu(xq[t]) * 2 * xq[t]
+        np.testing.assert_allclose(out[t], w0 * y0 + (1 - w0) * y1, rtol=1e-13, atol=1e-15)
+    # k = 1 keeps only the best expert with weight 1
+    out1 = ffn.moe_ffn(experts, xb[:2], logits[:2], k=1)
+    np.testing.assert_allclose(out1[0], ffn.silu(xq[0] @ P.T) * xq[0], rtol=1e-14)
+    np.testing.assert_allclose(out1[1], ffn.silu(xq[1]) * 2 * xq[1], rtol=1e-14)
+
+
+def test_silu_values():
+    z = np.array([0.0, 1.0, -1.0, 40.0, -800.0])
+    s = ffn.silu(z)
+    assert s[0] == 0.0
+    np.testing.assert_allclose(s[1], 1 / (1 + np.exp(-1.0)), rtol=1e-15)
+    np.testing.assert_allclose(s[2], -1 / (1 + np.e), rtol=1e-15)
+    np.testing.assert_allclose(s[3], 40.0, rtol=1e-15)
+    assert s[4] == 0.0
+
+
+def test_tiny_config_matches_brute_force():
+    L = synth.make_layer(synth.CONFIGS["tiny"], 0)
+    out = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    bf = ffn.moe_ffn_bruteforce(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    np.testing.assert_allclose(out, bf, rtol=1e-12, atol=1e-12 * np.abs(bf).max())
+    assert np.abs(out).max() > 0
+
+
+@pytest.mark.parametrize("renorm", [True, False])
+def test_mixed_layer_matches_brute_force(renorm):
+    L = small_layer()
+    out = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, renormalize=renorm)
+    bf = ffn.moe_ffn_bruteforce(L.experts, L.x_bf16, L.logits, L.cfg.k, renormalize=renorm)
+    np.testing.assert_allclose(out, bf, rtol=1e-12, atol=1e-12 * np.abs(bf).max())
+
+
+def test_tier_decomposition():
+    L = small_layer(E=16, k=4, T=6)
+    fm = {ex["gate"].fmt for ex in L.experts}
+    assert len(fm) == 3
+    full = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    parts = sum(ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, format_mask=1 << f) for f in fm)
+    np.testing.assert_allclose(parts, full, rtol=1e-12, atol=1e-12 * np.abs(full).max())
+    lo = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, expert_lo=0, expert_hi=7)
+    hi = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, expert_lo=7, expert_hi=16)
+    np.testing.assert_allclose(lo + hi, full, rtol=1e-12, atol=1e-12 * np.abs(full).max())
+
+
+def test_permutation_invariance():
+    L = small_layer(E=10, k=3, T=4, seed=5)
+    full = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    perm = np.random.default_rng(31).permutation(10)       # new slot s holds old expert perm[s]
+    experts2 = [L.experts[int(p)] for p in perm]
+    logits2 = L.logits[:, perm]
+    out2 = ffn.moe_ffn(experts2, L.x_bf16, logits2, L.cfg.k)
+    np.testing.assert_allclose(out2, full, rtol=1e-12, atol=1e-13 * np.abs(full).max())
+
+
+def test_zero_scales_give_zero():
+    L = synth.make_layer(synth.CONFIGS["tiny"], 0)
+    experts = []
+    for ex in L.experts:
+        e2 = {}
+        for name, m in ex.items():
+            data = m.data.copy().reshape(m.rows, m.stride)
+            for b in range(m.cols // 32):
+                data[:, 34 * b: 34 * b + 2] = 0
+            e2[name] = MatrixBytes(m.fmt, m.rows, m.cols, m.stride, data.reshape(-1))
+        experts.append(e2)
+    out = ffn.moe_ffn(experts, L.x_bf16, L.logits, L.cfg.k)
+    assert np.all(out == 0)
+
+
+def test_token_subset_rows():
+    L = small_layer(T=7)
+    full = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    sub = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, tokens=[6, 2])
+    np.testing.assert_array_equal(sub, full[[6, 2]])
+
+
+def test_planted_transpose_fails_closed_form():
+    """A transposed gate (P^T instead of P) must break the closed form."""
+    n = 32
+    P = np.roll(np.eye(n, dtype=np.int64), 5, axis=1)
+    Id = np.eye(n, dtype=np.int64)
+    experts = [{"gate": q8_0_matrix(P), "up": q8_0_matrix(Id), "down": q8_0_matrix(Id)}]
+    x = np.random.default_rng(32).standard_normal((1, n))
+    xq = ffn.bf16_bits_to_f64(bf16_bits(x))
+    right = ffn.silu(xq[0] @ P.T) * xq[0]
+    wrong = ffn.silu(xq[0] @ P) * xq[0]
+    out = ffn.moe_ffn(experts, bf16_bits(x), np.zeros((1, 1), np.float32), k=1)[0]
+    np.testing.assert_allclose(out, right, rtol=1e-14)
+    assert np.abs(out - wrong).max() > 1e-3

@@ -1,0 +1,236 @@
+"""Pins of the oracle's block decoders (CPU only).
+
+* Hand-built single blocks with hand-computed weights (tests/golden/*_block.txt).
+* Round trips: codes and scales chosen at random, packed into bytes by an
+  encoder written here from the layout description (the inverse direction of
+  the decoders), decoded, and compared with the value formula evaluated
+  directly on the chosen codes.
+* Planted mistakes: each decoder with one plausible bug (dropped term, swapped
+  nibbles, wrong scale index, wrong sign bit) must fail the pins above.
+"""
+import glob
+import os
+
+import numpy as np
+import pytest
+
+from oracle import formats
+
+FMT = {"Q8_0": formats.Q8_0, "Q4_K": formats.Q4_K, "Q6_K": formats.Q6_K, "MXFP4": formats.MXFP4}
+
+
+def load_golden(path):
+    fmt, data, exp = None, None, []
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            p = line.split()
+            if p[0] == "format":
+                fmt = FMT[p[1]]
+            elif p[0] == "bytes":
+                data = np.array([int(x, 16) for x in p[1:]], dtype=np.uint8)
+            elif p[0] == "w":
+                exp.append((int(p[1]), float(p[2])))
+    return fmt, data, exp
+
+
+def golden_files(golden_dir):
+    files = sorted(glob.glob(os.path.join(golden_dir, "*_block.txt")))
+    assert len(files) >= 6
+    return files
+
+
+def check_golden(decoders, golden_dir):
+    for path in golden_files(golden_dir):
+        fmt, data, exp = load_golden(path)
+        assert data.shape[0] == formats.BLOCK_BYTES[fmt]
+        w = decoders[fmt](data[None, :])[0]
+        for i, v in exp:
+            if w[i] != v:
+                return False, (os.path.basename(path), i, w[i], v)
+    return True, None
+
+
+def test_golden_blocks(golden_dir):
+    ok, bad = check_golden(formats.DECODERS, golden_dir)
+    assert ok, bad
+
+
+def test_q8_0_unit_scale_gives_codes():
+    rng = np.random.default_rng(1)
+    q = rng.integers(-127, 128, size=(5, 32)).astype(np.int8)
+    blk = np.zeros((5, 34), dtype=np.uint8)
+    blk[:, 0:2] = np.frombuffer(np.float16(1.0).tobytes(), dtype=np.uint8)
+    blk[:, 2:] = q.view(np.uint8)
+    np.testing.assert_array_equal(formats.dequant_q8_0(blk), q.astype(np.float64))
+
+
+def test_mxfp4_scale_doubles(golden_dir):
+    _, b127, _ = load_golden(os.path.join(golden_dir, "mxfp4_e127_block.txt"))
+    _, b128, _ = load_golden(os.path.join(golden_dir, "mxfp4_e128_block.txt"))
+    w127 = formats.dequant_mxfp4(b127[None])[0]
+    w128 = formats.dequant_mxfp4(b128[None])[0]
+    np.testing.assert_array_equal(w128, 2 * w127)
+    assert sorted(set(np.abs(w127).tolist())) == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_mxfp4_rejects_nan_scale():
+    blk = np.zeros((1, 17), dtype=np.uint8)
+    blk[0, 0] = 255
+    with pytest.raises(ValueError):
+        formats.dequant_mxfp4(blk)
+
+
+# ---------------------------------------------------------------- encoders
+def enc_q4_k(d, dmin, sc, m, q):
+    """sc, m: int [8] (0..63); q: int [256] (0..15)."""
+    b = np.zeros(144, dtype=np.uint8)
+    b[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    b[2:4] = np.frombuffer(np.float16(dmin).tobytes(), np.uint8)
+    s = np.zeros(12, dtype=np.int64)
+    for j in range(4):
+        s[j] = (sc[j] & 63) | ((sc[j + 4] >> 4) << 6)
+        s[j + 4] = (m[j] & 63) | ((m[j + 4] >> 4) << 6)
+        s[j + 8] = (sc[j + 4] & 15) | ((m[j + 4] & 15) << 4)
+    b[4:16] = s
+    for g in range(4):
+        for i in range(32):
+            b[16 + 32 * g + i] = q[64 * g + i] | (q[64 * g + 32 + i] << 4)
+    return b
+
+
+def val_q4_k(d, dmin, sc, m, q):
+    d, dmin = float(np.float16(d)), float(np.float16(dmin))
+    sub = np.arange(256) // 32
+    return d * sc[sub] * q - dmin * m[sub]
+
+
+def enc_q6_k(d, scales, q):
+    """scales int [16] (-128..127); q int [256] (0..63)."""
+    b = np.zeros(210, dtype=np.uint8)
+    ql = np.zeros(128, dtype=np.int64)
+    qh = np.zeros(64, dtype=np.int64)
+    for n in range(256):
+        h, r, i = n // 128, (n % 128) // 32, n % 32
+        lo, hi = q[n] & 15, q[n] >> 4
+        ql_idx = 64 * h + (32 if r in (1, 3) else 0) + i
+        ql[ql_idx] |= lo << (4 if r >= 2 else 0)
+        qh[32 * h + i] |= hi << (2 * r)
+    b[0:128] = ql
+    b[128:192] = qh
+    b[192:208] = np.asarray(scales, dtype=np.int8).view(np.uint8)
+    b[208:210] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    return b
+
+
+def val_q6_k(d, scales, q):
+    d = float(np.float16(d))
+    return d * np.asarray(scales, dtype=np.float64)[np.arange(256) // 16] * (q - 32)
+
+
+def enc_mxfp4(e, codes):
+    b = np.zeros(17, dtype=np.uint8)
+    b[0] = e
+    b[1:17] = codes[:16] | (codes[16:] << 4)
+    return b
+
+
+def val_mxfp4(e, codes):
+    mag = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    sign = np.where(codes >= 8, -1.0, 1.0)
+    return 2.0 ** (e - 127) * sign * mag[codes & 7]
+
+
+def test_q4_k_roundtrip():
+    rng = np.random.default_rng(2)
+    for _ in range(20):
+        sc = rng.integers(0, 64, 8)
+        m = rng.integers(0, 64, 8)
+        q = rng.integers(0, 16, 256)
+        d, dmin = rng.uniform(1e-3, 1.0), rng.uniform(1e-3, 1.0)
+        blk = enc_q4_k(d, dmin, sc, m, q)
+        np.testing.assert_array_equal(formats.dequant_q4_k(blk[None])[0], val_q4_k(d, dmin, sc, m, q))
+
+
+def test_q6_k_roundtrip():
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        scales = rng.integers(-128, 128, 16)
+        q = rng.integers(0, 64, 256)
+        d = rng.uniform(1e-3, 1.0)
+        blk = enc_q6_k(d, scales, q)
+        np.testing.assert_array_equal(formats.dequant_q6_k(blk[None])[0], val_q6_k(d, scales, q))
+
+
+def test_mxfp4_roundtrip():
+    rng = np.random.default_rng(4)
+    for _ in range(20):
+        e = int(rng.integers(100, 150))
+        codes = rng.integers(0, 16, 32)
+        np.testing.assert_array_equal(formats.dequant_mxfp4(enc_mxfp4(e, codes)[None])[0],
+                                      val_mxfp4(e, codes))
+
+
+def test_matrix_rows_and_padding():
+    """A matrix with a padded stride decodes row by row like single blocks."""
+    rng = np.random.default_rng(5)
+    rows, cols, stride = 3, 64, 80          # Q8_0: 2 blocks = 68 bytes per row
+    data = rng.integers(0, 256, rows * stride).astype(np.uint8)
+    for r in range(rows):
+        data[r * stride: r * stride + 2] = np.frombuffer(np.float16(0.25).tobytes(), np.uint8)
+        data[r * stride + 34: r * stride + 36] = np.frombuffer(np.float16(-2.0).tobytes(), np.uint8)
+    W = formats.dequant_matrix(formats.Q8_0, rows, cols, stride, data)
+    for r in range(rows):
+        q0 = data[r * stride + 2: r * stride + 34].view(np.int8)
+        q1 = data[r * stride + 36: r * stride + 68].view(np.int8)
+        np.testing.assert_array_equal(W[r, :32], 0.25 * q0)
+        np.testing.assert_array_equal(W[r, 32:], -2.0 * q1)
+    np.testing.assert_array_equal(formats.dequant_rows(formats.Q8_0, cols, stride, data, [2, 0]), W[[2, 0]])
+
+
+# ---------------------------------------------------------------- planted mistakes
+def _q4_k_no_min(blk):
+    out = formats.dequant_q4_k(blk)
+    d = formats._f16(blk[..., 2:4])
+    _, m = formats.q4_k_scale_min(blk[..., 4:16])
+    sub = np.arange(256) // 32
+    return out + d[..., None] * m[..., sub]          # drops the "- dmin*m" term
+
+
+def _q4_k_swapped_nibbles(blk):
+    out = formats.dequant_q4_k(blk)
+    r = out.reshape(out.shape[:-1] + (4, 2, 32))
+    return r[..., ::-1, :].reshape(out.shape)
+
+
+def _q6_k_scale_per_32(blk):
+    q = formats.q6_k_codes(blk)
+    scales = np.ascontiguousarray(blk[..., 192:208]).view(np.int8).astype(np.float64)
+    d = formats._f16(blk[..., 208:210])
+    idx = np.minimum(np.arange(256) // 32 * 2, 15)   # wrong scale index
+    return d[..., None] * scales[..., idx] * (q - 32)
+
+
+def _mxfp4_unsigned(blk):
+    return np.abs(formats.dequant_mxfp4(blk))
+
+
+def _q8_0_wrong_offset(blk):
+    d = formats._f16(blk[..., 0:2])
+    q = np.ascontiguousarray(blk[..., 2:34]).view(np.uint8).astype(np.float64)   # unsigned read
+    return d[..., None] * q
+
+
+@pytest.mark.parametrize("fmt,bad", [
+    (formats.Q4_K, _q4_k_no_min),
+    (formats.Q4_K, _q4_k_swapped_nibbles),
+    (formats.Q6_K, _q6_k_scale_per_32),
+    (formats.MXFP4, _mxfp4_unsigned),
+    (formats.Q8_0, _q8_0_wrong_offset),
+])
+def test_planted_mistakes_fail_the_pins(golden_dir, fmt, bad):
+    decoders = dict(formats.DECODERS)
+    decoders[fmt] = bad
+    ok, _ = check_golden(decoders, golden_dir)
+    assert not ok
