@@ -1,0 +1,483 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE FFN layer over block-quantized experts.
+
+One step = one pass of the whole layer (router, bucketing, grouped gate/up
+with fused SwiGLU, grouped down, combine) through each of `--layers` stacked
+independent layers (different seeds, so the selected experts' weights stream
+from HBM rather than L2), replayed as one CUDA graph. Inputs are seeded
+synthetic data; the weights are written on the device by the seeded filler.
+
+Prints one JSON line. `value` is MoE-layer tokens/s (token-layers per second,
+i.e. T / per-layer time, summed over ranks); `e2e` is the same metric through
+the public API with pinned host buffers copied in and out every layer;
+`roofline` is the dominant kernel's algorithmic bytes per launch over its
+event-timed duration against the measured HBM copy bandwidth;
+`cpu_baseline` is the fp64 oracle on the host, single-threaded, on a bounded
+sample of the same workload.
+
+--impl reference runs the oracle as the reference arm (there is no runnable
+reference implementation: the source pages ship no code).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s; expert-weight HBM GB/s and % of GB300 roofline"
+UNIT = "tokens/s"
+KERNELS_PER_LAYER = 5   # route, bucket, gate/up, down, combine
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--config", default="decode1", help="tiny|decode1|decode16|mtp6|prefill2048")
+    p.add_argument("--layers", type=int, default=48)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true")
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------
+# oracle worker (host CPU baseline / reference arm); runs in a subprocess
+# started before any CUDA work, with BLAS limited to one thread
+# ----------------------------------------------------------------------------
+def oracle_worker(spec: dict) -> dict:
+    import numpy as np
+    import synth
+    from oracle import ffn as offn
+    from oracle import router as orouter
+
+    cfg = synth.CONFIGS[spec["config"]]
+    budget = float(spec["budget_s"])
+    pairs_per_sample = spec.get("pairs_per_sample")      # None: whole layers
+    # Untimed: inputs, routing and the routed experts' bytes (the oracle's
+    # input); timed: the oracle's arithmetic (decode + routed FFN).
+    t_work, token_layers, samples, layer = 0.0, 0.0, [], 0
+    while t_work < budget and layer < 1000:
+        L = synth.make_layer(cfg, layer % 48, with_weights=False)
+        lazy = synth.LazyExperts(cfg, L.seed, L.fmts)
+        ids, _, _ = orouter.route_topk(L.logits, cfg.k)
+        T = cfg.tokens
+        if pairs_per_sample is None:
+            toks = list(range(T))
+        else:
+            toks = list(range(min(T, max(1, pairs_per_sample // cfg.k))))
+        for e in np.unique(ids[toks]):
+            lazy[int(e)]
+        t0 = time.perf_counter()
+        offn.moe_ffn(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks, gate_formats=lazy.gate_formats())
+        dt = time.perf_counter() - t0
+        t_work += dt
+        token_layers += len(toks)
+        samples.append(dt)
+        layer += 1
+    return {"value": token_layers / t_work, "token_layers": token_layers, "seconds": t_work,
+            "layers": layer, "tokens_per_layer": len(toks)}
+
+
+def run_oracle_subprocess(spec: dict, threads: int = 1) -> dict:
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[v] = str(threads)
+    env["MOE_BENCH_ORACLE_WORKER"] = json.dumps(spec)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__)], env=env, capture_output=True, text=True,
+                       timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ----------------------------------------------------------------------------
+# clocks
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_end = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t_start - 0.1 <= r[0] <= self.t_end + 0.1]
+        window = "timed"
+        if not inside:
+            # timed region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: abs(r[0] - (self.t_start + self.t_end) / 2))[:3]
+            window = "adjacent"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_traffic(kernel: str, config: str):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source (same hash); else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(f"{kernel}:{config}")
+    if not ent:
+        return None
+    if ent.get("source_sha256") != source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "quantized_moe_expert_route_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        with open(os.path.join(cs, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def allreduce_max(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import synth
+    cfg = synth.CONFIGS[args.config]
+    n_steps = args.steps + args.warmup
+    # each step: a bounded sample of (token, slot) pairs, sized so the whole
+    # run stays within ~150 s of oracle work
+    probe = run_oracle_subprocess({"config": args.config, "budget_s": 0.5, "pairs_per_sample": cfg.k})
+    per_pair = probe["seconds"] / max(probe["token_layers"] * cfg.k, 1)
+    pairs = int(max(cfg.k, min(cfg.tokens * cfg.k, 150.0 / n_steps / max(per_pair, 1e-6))))
+    res = run_oracle_subprocess({"config": args.config, "budget_s": 150.0 * args.steps / n_steps,
+                                 "pairs_per_sample": pairs})
+    sample = (f"{args.config}: {res['layers']} layer samples of {res['tokens_per_layer']} token(s) "
+              f"(x {cfg.k} experts), {res['seconds']:.1f} s of oracle arithmetic")
+    v = res["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.config},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+def run_ours(args, world, rank, local, cpu_proc):
+    import numpy as np
+    import torch
+
+    import synth
+    from synth import gpu as sgpu
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_moe_expert_route_gb300 as M
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = synth.CONFIGS[args.config]
+    T, E, k, H, I = cfg.tokens, cfg.n_experts, cfg.k, cfg.hidden, cfg.inter
+    NL = args.layers
+
+    layers, tables, wss, outs = [], [], [], []
+    for l in range(NL):
+        DL = sgpu.make_device_layer(cfg, rank * NL + l)
+        layers.append(DL)
+        tables.append(M.WeightTable(DL.experts, H, I))
+        wss.append(M.Workspace(tables[-1], T, k))
+        outs.append(torch.empty((T, H), dtype=torch.float32, device=dev))
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(NL)]
+    opts_plain = M.make_options(n_experts=E)
+    opts_timed = [M.make_options(n_experts=E, timing_events=ev[l]) for l in range(NL)]
+
+    def step(timed: bool):
+        for l in range(NL):
+            M.ffn_forward(tables[l], layers[l].x_bf16, layers[l].logits, k, out=outs[l], ws=wss[l],
+                          options=opts_timed[l] if timed else opts_plain)
+
+    # eager warm-up (sets kernel attributes before any capture)
+    with torch.cuda.stream(stream):
+        step(False)
+    stream.synchronize()
+
+    graphs = {}
+    if not args.no_graph:
+        for timed in (False, True):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                step(timed)
+            graphs[timed] = g
+
+    def run(timed: bool):
+        if args.no_graph:
+            with torch.cuda.stream(stream):
+                step(timed)
+        else:
+            graphs[timed].replay()
+
+    # algorithmic bytes: distinct routed experts per layer, from the GPU's own
+    # bucketing output (read back outside the timed region)
+    per_layer_expert_bytes, per_layer_gu_bytes, per_layer_dn_bytes, per_layer_pairs = [], [], [], []
+    for l in range(NL):
+        routing = wss[l].routing()
+        active = routing["active"].cpu().numpy()
+        offsets = routing["offsets"].cpu().numpy()
+        ids = active[1:1 + active[0]]
+        gu = sum(2 * I * synth.row_bytes(layers[l].fmts[e][0], H) for e in ids)
+        dn = sum(H * synth.row_bytes(layers[l].fmts[e][1], I) for e in ids)
+        per_layer_gu_bytes.append(gu)
+        per_layer_dn_bytes.append(dn)
+        per_layer_expert_bytes.append(gu + dn)
+        per_layer_pairs.append(int(offsets[E]))
+    io_bytes = T * H * 2 + T * E * 4 + T * H * 4
+
+    for _ in range(args.warmup):
+        run(False)
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = str(getattr(props, "uuid", local))
+    if gpu_id and not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
+
+    # ---- timed region 1: the headline (no profiling hooks)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    e0.record(stream)
+    for _ in range(args.steps):
+        run(False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    barrier(world)
+    elapsed = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
+
+    # ---- timed region 2: same steps with event nodes around the mat-mul kernels
+    gu_ms, dn_ms = [], []
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    prof_steps = max(1, min(args.steps, 50))
+    for _ in range(prof_steps):
+        run(True)
+        torch.cuda.current_stream().wait_stream(stream)
+        stream.synchronize()
+        for l in range(NL):
+            gu_ms.append(ev[l][0].elapsed_time(ev[l][1]))
+            dn_ms.append(ev[l][1].elapsed_time(ev[l][2]))
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+
+    # ---- e2e: public API with pinned host buffers, copies inside the region
+    x_pin = [torch.from_numpy(L.x_host.view(np.int16).copy()).pin_memory() for L in layers]
+    lg_pin = [torch.from_numpy(L.logits_host.copy()).pin_memory() for L in layers]
+    out_pin = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in layers]
+    x_dev = [torch.empty((T, H), dtype=torch.int16, device=dev) for _ in layers]
+    lg_dev = [torch.empty((T, E), dtype=torch.float32, device=dev) for _ in layers]
+    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            for l in range(NL):
+                x_dev[l].copy_(x_pin[l], non_blocking=True)
+                lg_dev[l].copy_(lg_pin[l], non_blocking=True)
+                M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
+                out_pin[l].copy_(outs[l], non_blocking=True)
+    stream.synchronize()
+    barrier(world)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        h0.record(stream)
+        for _ in range(n_e2e):
+            for l in range(NL):
+                x_dev[l].copy_(x_pin[l], non_blocking=True)
+                lg_dev[l].copy_(lg_pin[l], non_blocking=True)
+                M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
+                out_pin[l].copy_(outs[l], non_blocking=True)
+        h1.record(stream)
+    stream.synchronize()
+    e2e_elapsed = allreduce_max(h0.elapsed_time(h1) / 1e3, world)
+
+    # status of every workspace (device-detected input errors) after all runs
+    bad = sum(ws.read_status() for ws in wss)
+
+    hbm_peak, peak_kind = measured_peaks()
+    token_layers = T * NL * args.steps * world
+    value = token_layers / elapsed
+    per_layer_s = elapsed / (args.steps * NL)
+    mean_expert_bytes = float(np.mean(per_layer_expert_bytes))
+    layer_bytes = mean_expert_bytes + io_bytes
+    gu_avg, dn_avg = statistics.mean(gu_ms) / 1e3, statistics.mean(dn_ms) / 1e3
+    # algorithmic bytes per launch: the routed experts' quantized bytes plus the
+    # kernel's activation traffic (x in, h out | h in, y out)
+    mean_pairs = float(np.mean(per_layer_pairs))
+    gu_bytes = float(np.mean(per_layer_gu_bytes)) + T * H * 2 + mean_pairs * I * 4
+    dn_bytes = float(np.mean(per_layer_dn_bytes)) + mean_pairs * I * 4 + mean_pairs * H * 4
+    if gu_avg >= dn_avg:
+        kname, kbytes, kdur = "gateup_gemv_kernel", gu_bytes, gu_avg
+    else:
+        kname, kbytes, kdur = "down_gemv_kernel", dn_bytes, dn_avg
+    achieved = kbytes / kdur / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 weights written on the device; bf16 N(0,1) activations; "
+                "Zipf-biased fp32 logits)",
+        "config": {"workload": f"{args.config}: E{E} k{k} H{H} I{I} T{T} ({cfg.tiers} tiers), "
+                               f"{NL} stacked layers per step",
+                   "tokens": T, "layers_per_step": NL, "graph": not args.no_graph,
+                   "l2": f"inputs exceed L2: {NL} distinct layers, {NL * mean_expert_bytes / 1e9:.2f} GB of "
+                         f"routed expert weights per step vs {props.L2_cache_size / 1e6:.0f} MB L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "per_layer_us": per_layer_s * 1e6,
+        "expert_weight_gbs": mean_expert_bytes / per_layer_s / 1e9,
+        "layer_roofline": {"bound": "hbm", "bytes_per_layer": layer_bytes,
+                           "achieved": layer_bytes / per_layer_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                           "frac": layer_bytes / per_layer_s / 1e9 / hbm_peak, "peak_kind": peak_kind},
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": kernel_traffic(kname, args.config),
+                     "bytes_per_launch": kbytes, "launch_us": kdur * 1e6, "peak_kind": peak_kind,
+                     "other_kernel_us": (dn_avg if kname.startswith("gateup") else gu_avg) * 1e6},
+        "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
+                "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
+        "gpu_launches": KERNELS_PER_LAYER * NL * args.steps,
+        "clocks": clk,
+        "device_status_flags": bad,
+        "gpu": props.name,
+    }
+    return line
+
+
+def main():
+    if "MOE_BENCH_ORACLE_WORKER" in os.environ:
+        print(json.dumps(oracle_worker(json.loads(os.environ["MOE_BENCH_ORACLE_WORKER"]))))
+        return
+    args = parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    # CPU baseline first (before any CUDA work in this process), rank 0, N = 1
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res = run_oracle_subprocess({"config": args.config, "budget_s": args.cpu_budget})
+        cpu = {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{args.config}: {res['layers']} whole layers ({res['tokens_per_layer']} token(s) each), "
+                         f"{res['seconds']:.1f} s of fp64 oracle arithmetic, BLAS limited to 1 thread"}
+    line = run_ours(args, world, rank, local, None)
+    if rank == 0:
+        line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

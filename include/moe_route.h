@@ -1,0 +1,224 @@
+/*
+ * moe_route.h -- C ABI of the GB300 (sm_103a) routed mixture-of-experts FFN
+ * layer over block-quantized expert weights.
+ *
+ * The layer (per token t, with x_t in bf16 and router logits in fp32):
+ *
+ *     ids[t, 0..k-1], w[t, 0..k-1] = top-k of softmax(logits[t])
+ *     out[t] = sum_{j = 0..k-1} w[t, j] * W_down[e] ( silu(W_gate[e] x_t) * (W_up[e] x_t) ),
+ *     e = ids[t, j],  silu(z) = z / (1 + exp(-z)),  sum in ascending slot j.
+ *
+ * Source: "三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南":
+ * section 瓶颈分析 (a light router picks 10 of a layer's 512 experts per token),
+ * section 优化策略二 (per-expert precision tiers: Q6_K gate/up with Q8_0 down,
+ * a middle tier, MXFP4 for the tail; down has K = 640, so only 32-weight
+ * block formats fit it), section 优化策略三 (one mul_mat_id drives experts of
+ * several formats in one layer; an expert-id range filter [min, max) skips
+ * the others) and section 关键 Bug 修复与调试踩坑记录 (-1 is a "skip" id that must
+ * stay signed; gate/up/activation are fused in decode). The grouped
+ * multi-session decode (one launch serves the decode rows of 16 sessions) is
+ * from "多卡 CUDA 张量并行：DwarfStar 如何在 8 张 L40S 上跑出 120 t/s", section
+ * "120 t/s 的秘密：微批次分组解码".
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" must be device memory of the current CUDA
+ *     device; "host" pointers are ordinary host memory.
+ *   - The caller owns every buffer. The library allocates no device memory.
+ *   - Work is enqueued asynchronously on `stream` (NULL = the legacy default
+ *     stream); no entry point synchronises the host except
+ *     moe_table_prepare and moe_ffn_read_status, which say so.
+ *   - Every entry point returns an moe_status code; no C++ exception crosses
+ *     the ABI. Argument errors are detected on the host before anything is
+ *     enqueued. Errors the GPU finds in the data (bad ids, non-finite logits)
+ *     are OR-ed into a device status word; see moe_device_flags.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *moe_stream_t;
+
+/* Return codes. */
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,         /* null pointer, bad count, misaligned pointer */
+    MOE_ERR_BAD_SHAPE = 2,           /* dims disagree, cols not a multiple of the block, bad stride */
+    MOE_ERR_BAD_FORMAT = 3,          /* unknown format tag, gate/up formats differ */
+    MOE_ERR_BAD_ID = 4,              /* reserved for host-checked ids */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 5, /* ws_bytes below the size query */
+    MOE_ERR_CUDA = 6,                /* a CUDA call failed; see moe_last_cuda_error */
+    MOE_ERR_NOT_PREPARED = 7,        /* weight table was not (successfully) prepared */
+    MOE_ERR_UNSUPPORTED = 8          /* valid, but beyond this build's limits (MOE_MAX_*) */
+} moe_status;
+
+/* Device status flags (OR-ed, sticky until read). */
+typedef enum {
+    MOE_FLAG_NONFINITE_LOGIT = 1,    /* a logit was NaN or +-inf (ranked last, weight 0) */
+    MOE_FLAG_BAD_ID = 2,             /* an id outside [-1, E) (the pair was skipped) */
+    MOE_FLAG_DUPLICATE_ID = 4,       /* an expert repeated within one token (still computed) */
+    MOE_FLAG_WAIT_TIMEOUT = 8        /* a bounded device wait gave up (the tile was skipped) */
+} moe_device_flags;
+
+/* Weight block formats (little-endian; fp16 = IEEE binary16).
+ *  Q8_0  : 34 B / 32 weights : fp16 d, int8 q[32];                 w = d*q
+ *  Q4_K  : 144 B / 256       : fp16 d, fp16 dmin, 12 B packed 6-bit
+ *                              (scale, min) x 8, 128 B 4-bit codes; w = d*sc*q - dmin*m
+ *  Q6_K  : 210 B / 256       : 128 B low nibbles, 64 B high 2-bit pairs,
+ *                              int8 scale x 16, fp16 d (last);      w = d*scale*(q - 32)
+ *  MXFP4 : 17 B / 32         : E8M0 scale e, 16 B E2M1 codes;       w = 2^(e-127) * E2M1
+ * These are the public GGUF layouts (Q8_0, Q4_K, Q6_K) and the OCP MX v1.0
+ * encoding (MXFP4); the pages name the formats but print no layout. */
+typedef enum { MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_Q6_K = 3, MOE_MXFP4 = 4 } moe_format;
+
+/* Limits of this build. */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_K 32
+#define MOE_MAX_HIDDEN 8192
+#define MOE_MAX_INTER 8192
+
+/* One quantized matrix: `rows` rows of `cols` weights, blocks along the
+ * columns (the reduction axis). Row r starts at data + r * row_stride_bytes.
+ * row_stride_bytes >= (cols / block_elems) * block_bytes and a multiple of 16;
+ * data is a 16-byte aligned device pointer to rows * row_stride_bytes bytes. */
+typedef struct {
+    int32_t format;            /* moe_format */
+    int32_t rows;
+    int32_t cols;
+    int32_t reserved;          /* 0 */
+    int64_t row_stride_bytes;
+    const void *data;          /* device */
+} moe_matrix;
+
+/* One expert: gate and up are [inter rows x hidden cols] in the same format;
+ * down is [hidden rows x inter cols]. */
+typedef struct {
+    moe_matrix gate, up, down;
+} moe_expert;
+
+#define MOE_TABLE_PREPARED 0x4d4f4554u
+
+/* The per-expert format-tagged weight table of one layer. The caller fills
+ * n_experts, hidden, inter and experts; moe_table_prepare fills the rest. */
+typedef struct {
+    int32_t n_experts;         /* E, 1..MOE_MAX_EXPERTS */
+    int32_t hidden;            /* H */
+    int32_t inter;             /* I */
+    int32_t reserved;
+    const moe_expert *experts; /* host array [E]; read by moe_table_prepare only */
+    /* ---- written by moe_table_prepare ---- */
+    void *device_table;        /* device copy of the descriptors */
+    uint32_t formats_present;  /* bit (1 << format) for every format in use */
+    uint32_t prepared;         /* MOE_TABLE_PREPARED after a successful prepare */
+    int64_t max_gateup_stride; /* largest gate/up row stride, bytes */
+    int64_t max_down_stride;   /* largest down row stride, bytes */
+} moe_weight_table;
+
+/* Paths for moe_options.path. */
+#define MOE_PATH_AUTO 0        /* GEMV up to MOE_GEMV_MAX_ROWS tokens, tensor cores above */
+#define MOE_PATH_GEMV 1        /* CUDA-core grouped GEMV, weights dequantized in registers */
+#define MOE_PATH_TENSOR 2      /* tcgen05 grouped GEMM (prefill chunks) */
+#define MOE_GEMV_MAX_ROWS 96
+
+/* Options of moe_ffn_forward (NULL = defaults). */
+typedef struct {
+    uint32_t struct_size;      /* sizeof(moe_options); checked */
+    int32_t renormalize;       /* 1 (default): the k selected weights sum to 1; 0: plain softmax values */
+    uint32_t format_mask;      /* keep an expert only if bit (1 << its gate format) is set; default all */
+    int32_t expert_lo;         /* keep experts in [expert_lo, expert_hi); default [0, E) */
+    int32_t expert_hi;
+    int32_t path;              /* MOE_PATH_* */
+    int32_t reserved;          /* 0 */
+    /* Profiling hook: NULL, or a host array of 3 cudaEvent_t that are recorded
+     * on the stream before the gate/up mat-mul kernel, between it and the down
+     * mat-mul kernel, and after the down kernel. During stream capture they
+     * are recorded as external event nodes. */
+    void *const *timing_events;
+} moe_options;
+
+/* Human-readable name of a moe_status code (static string). */
+const char *moe_strerror(int code);
+
+/* The last CUDA error seen by this thread (cudaError_t value, 0 if none). */
+int moe_last_cuda_error(void);
+
+/* Bytes of device memory moe_table_prepare needs for `n_experts` experts. */
+size_t moe_table_device_bytes(int32_t n_experts);
+
+/* Validate W (shapes, formats, strides, alignment) and copy its descriptors
+ * into `device_buf` (caller-owned device memory of at least
+ * moe_table_device_bytes(W->n_experts) bytes). Synchronises `stream`.
+ * On success sets W->device_table = device_buf, W->prepared and the summary
+ * fields. The weight data itself is not read or copied; its device pointers
+ * must stay valid while forwards that use W run. Re-prepare after changing
+ * W->experts. Errors: INVALID_ARG, BAD_SHAPE, BAD_FORMAT, UNSUPPORTED, CUDA. */
+int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes, moe_stream_t stream);
+
+/* Router (step 1). logits: device fp32 [T, E] row-major. For every row, the k
+ * experts with the largest logits (equal logits: lower expert index first;
+ * non-finite logits rank last) go to ids (device int32 [T, k], slot order =
+ * rank) and their softmax probabilities (fp32; divided by their sum when
+ * renormalize != 0) to weights (device fp32 [T, k]). Non-finite logits set
+ * MOE_FLAG_NONFINITE_LOGIT in *status (device uint32, may be NULL) and get
+ * weight 0. 1 <= k <= min(E, MOE_MAX_K), E <= MOE_MAX_EXPERTS, T >= 0. */
+int moe_route_topk(const float *logits, int32_t T, int32_t E, int32_t k, int32_t renormalize,
+                   int32_t *ids, float *weights, uint32_t *status, moe_stream_t stream);
+
+/* Bucketing (step 2). ids: device int32 [T, k]. Pair p = t*k + j is kept if
+ * expert_lo <= ids[p] < expert_hi; -1 is skipped silently, other ids outside
+ * [0, E) set MOE_FLAG_BAD_ID and are skipped, and an expert repeated within
+ * one token sets MOE_FLAG_DUPLICATE_ID (its pairs are still bucketed).
+ * Outputs (device int32): offsets [E + 1] = exclusive prefix sum of the kept
+ * per-expert counts; pairs [T*k] = kept pair numbers grouped by expert
+ * (ascending expert, ascending p within an expert; entries past offsets[E]
+ * are unspecified); pos [T*k] = bucket position of each pair or -1;
+ * active [E + 1] = {n_active, active expert ids ascending...}.
+ * status: device uint32 or NULL. E <= MOE_MAX_EXPERTS. */
+int moe_bucket(const int32_t *ids, int32_t T, int32_t k, int32_t E, int32_t expert_lo, int32_t expert_hi,
+               int32_t *offsets, int32_t *pairs, int32_t *pos, int32_t *active, uint32_t *status,
+               moe_stream_t stream);
+
+/* Workspace bytes moe_ffn_forward needs for a prepared W, T tokens and top-k
+ * (0 if the arguments are invalid). */
+size_t moe_ffn_workspace_size(const moe_weight_table *W, int32_t T, int32_t k);
+
+/* Zero a workspace's status word (once, before its first forward).
+ * ws: device, at least moe_ffn_workspace_size bytes. */
+int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole layer (steps 1-6): router, bucketing, grouped gate/up with the
+ * fused SwiGLU, grouped down projection and the slot-ordered combine.
+ * x: device bf16 bits [T, H]; logits: device fp32 [T, E]; out: device fp32
+ * [T, H] (fully overwritten; tokens whose pairs are all dropped get 0).
+ * ws: device workspace of ws_bytes >= moe_ffn_workspace_size(W, T, k), 256-byte
+ * aligned, initialised once with moe_ffn_workspace_init. opt: NULL or options
+ * (format_mask / expert range drop the other experts' contributions).
+ * Forwards that share a workspace must be ordered on one stream.
+ * Errors: INVALID_ARG, NOT_PREPARED, WORKSPACE_TOO_SMALL, UNSUPPORTED, CUDA. */
+int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *logits, int32_t T,
+                    int32_t k, const moe_options *opt, float *out, void *ws, size_t ws_bytes,
+                    moe_stream_t stream);
+
+/* Device pointers (into ws) of the routing results the last forward with this
+ * workspace left: ids [T*k], weights [T*k], offsets [E+1], active [E+1],
+ * pairs [T*k] and pos [T*k], with the meaning given at moe_route_topk and
+ * moe_bucket. Output pointers may be NULL. Host-only; no CUDA call. */
+int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, void *ws, int32_t **ids,
+                            float **weights, int32_t **offsets, int32_t **active, int32_t **pairs,
+                            int32_t **pos);
+
+/* Read and clear the device status flags of a workspace (moe_device_flags).
+ * Synchronises `stream`. *status_out is a host pointer. */
+int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

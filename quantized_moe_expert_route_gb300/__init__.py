@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) routed mixture-of-experts FFN over block-quantized experts.
+
+The layer runs in hand-written CUDA kernels behind a C ABI
+(``include/moe_route.h``, ``libmoe_route.so``); this package is the thin
+Python binding. Import is cheap: the library is loaded on first use, and a
+missing library raises instead of falling back to anything else.
+"""
+from ._lib import (  # noqa: F401
+    BLOCK_BYTES, BLOCK_ELEMS, EXPORTED, FLAG_BAD_ID, FLAG_DUPLICATE_ID, FLAG_NONFINITE_LOGIT,
+    FLAG_WAIT_TIMEOUT, MOE_TABLE_PREPARED, MXFP4, PATH_AUTO, PATH_GEMV, PATH_TENSOR, Q4_K, Q6_K, Q8_0,
+    MoeError, Options, WeightTable, Workspace, bucket, ffn_forward, load, make_options, route_topk,
+)

@@ -1,0 +1,224 @@
+// C ABI of the library: argument validation, workspace layout, launches.
+// Every step of the layer runs in this library's kernels; nothing here
+// computes on the host beyond checking arguments.
+#include <cstring>
+#include <vector>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+cudaError_t launch_route_topk(const float *logits, int T, int E, int k, int renorm, int32_t *ids, float *wts,
+                              uint32_t *status, cudaStream_t s);
+cudaError_t launch_bucket(const int32_t *ids, int T, int k, int E, int lo, int hi, uint32_t fmt_mask,
+                          const DevExpert *table, int32_t *offsets, int32_t *pairs, int32_t *pos, int32_t *active,
+                          uint32_t *status, cudaStream_t s);
+size_t bucket_smem_bytes(int E);
+size_t gateup_smem_bytes(int H, int64_t wstride);
+size_t down_smem_bytes(int I, int64_t wstride);
+cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
+                             int64_t dn_stride, const int32_t *offsets, const int32_t *pairs, const int32_t *active,
+                             const int32_t *pos, const float *wts, const uint16_t *x, float *h, float *y, float *out,
+                             uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return MOE_ERR_CUDA;
+}
+
+constexpr size_t SMEM_LIMIT = 227 * 1024;
+constexpr int MAX_T = 65535;
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_matrix(const moe_matrix &m, int rows, int cols) {
+    if (m.format < MOE_Q8_0 || m.format > MOE_MXFP4) return MOE_ERR_BAD_FORMAT;
+    if (m.rows != rows || m.cols != cols) return MOE_ERR_BAD_SHAPE;
+    const int be = BLOCK_ELEMS[m.format], bb = BLOCK_BYTES[m.format];
+    if (cols % be != 0) return MOE_ERR_BAD_SHAPE;
+    const int64_t row_bytes = (int64_t)(cols / be) * bb;
+    if (m.row_stride_bytes < row_bytes || m.row_stride_bytes % 16 != 0) return MOE_ERR_BAD_SHAPE;
+    if (!m.data || !aligned(m.data, 16)) return MOE_ERR_INVALID_ARG;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_BAD_SHAPE: return "bad shape";
+        case MOE_ERR_BAD_FORMAT: return "bad format";
+        case MOE_ERR_BAD_ID: return "bad expert id";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_NOT_PREPARED: return "weight table not prepared";
+        case MOE_ERR_UNSUPPORTED: return "unsupported size";
+        default: return "unknown status";
+    }
+}
+
+int moe_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t moe_table_device_bytes(int32_t n_experts) {
+    if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return 0;
+    return align_up((size_t)n_experts * sizeof(DevExpert), 256);
+}
+
+int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes, moe_stream_t stream) {
+    if (!W || !W->experts || !device_buf) return MOE_ERR_INVALID_ARG;
+    W->prepared = 0;
+    const int E = W->n_experts, H = W->hidden, I = W->inter;
+    if (E <= 0 || E > MOE_MAX_EXPERTS || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+    if (H > MOE_MAX_HIDDEN || I > MOE_MAX_INTER) return MOE_ERR_UNSUPPORTED;
+    if (device_bytes < moe_table_device_bytes(E) || !aligned(device_buf, 16)) return MOE_ERR_INVALID_ARG;
+    std::vector<DevExpert> dev(E);
+    uint32_t present = 0;
+    int64_t gu_max = 0, dn_max = 0;
+    for (int e = 0; e < E; ++e) {
+        const moe_expert &x = W->experts[e];
+        int rc;
+        if ((rc = check_matrix(x.gate, I, H)) != MOE_OK) return rc;
+        if ((rc = check_matrix(x.up, I, H)) != MOE_OK) return rc;
+        if ((rc = check_matrix(x.down, H, I)) != MOE_OK) return rc;
+        if (x.gate.format != x.up.format) return MOE_ERR_BAD_FORMAT;
+        present |= 1u << x.gate.format;
+        present |= 1u << x.down.format;
+        gu_max = std::max<int64_t>(gu_max, std::max(x.gate.row_stride_bytes, x.up.row_stride_bytes));
+        dn_max = std::max<int64_t>(dn_max, x.down.row_stride_bytes);
+        const moe_matrix *src[3] = {&x.gate, &x.up, &x.down};
+        DevMatrix *dst[3] = {&dev[e].gate, &dev[e].up, &dev[e].down};
+        for (int i = 0; i < 3; ++i) {
+            dst[i]->data = static_cast<const uint8_t *>(src[i]->data);
+            dst[i]->stride = src[i]->row_stride_bytes;
+            dst[i]->fmt = src[i]->format;
+            dst[i]->rows = src[i]->rows;
+        }
+    }
+    if (gateup_smem_bytes(H, gu_max) > SMEM_LIMIT || down_smem_bytes(I, dn_max) > SMEM_LIMIT)
+        return MOE_ERR_UNSUPPORTED;
+    cudaError_t err = cudaMemcpyAsync(device_buf, dev.data(), (size_t)E * sizeof(DevExpert), cudaMemcpyHostToDevice,
+                                      stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = cudaStreamSynchronize(stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    W->device_table = device_buf;
+    W->formats_present = present;
+    W->max_gateup_stride = gu_max;
+    W->max_down_stride = dn_max;
+    W->prepared = MOE_TABLE_PREPARED;
+    return MOE_OK;
+}
+
+int moe_route_topk(const float *logits, int32_t T, int32_t E, int32_t k, int32_t renormalize, int32_t *ids,
+                   float *weights, uint32_t *status, moe_stream_t stream) {
+    if (T < 0 || E <= 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS || k > MOE_MAX_K) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!logits || !ids || !weights)) return MOE_ERR_INVALID_ARG;
+    cudaError_t err = launch_route_topk(logits, T, E, k, renormalize, ids, weights, status, stream);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+int moe_bucket(const int32_t *ids, int32_t T, int32_t k, int32_t E, int32_t expert_lo, int32_t expert_hi,
+               int32_t *offsets, int32_t *pairs, int32_t *pos, int32_t *active, uint32_t *status,
+               moe_stream_t stream) {
+    if (T < 0 || k <= 0 || E <= 0) return MOE_ERR_INVALID_ARG;
+    if (E > MOE_MAX_EXPERTS || k > MOE_MAX_K || (int64_t)T * k > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+    if (!offsets || !active || (T > 0 && (!ids || !pairs || !pos))) return MOE_ERR_INVALID_ARG;
+    cudaError_t err = launch_bucket(ids, T, k, E, expert_lo, expert_hi, 0xffffffffu, nullptr, offsets, pairs, pos,
+                                    active, status, stream);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+size_t moe_ffn_workspace_size(const moe_weight_table *W, int32_t T, int32_t k) {
+    if (!W || T < 0 || k <= 0 || k > W->n_experts || W->n_experts <= 0) return 0;
+    return ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
+}
+
+int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!ws || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
+    cudaError_t err = cudaMemsetAsync(ws, 0, 256, stream);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *logits, int32_t T, int32_t k,
+                    const moe_options *opt, float *out, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!W) return MOE_ERR_INVALID_ARG;
+    if (W->prepared != MOE_TABLE_PREPARED || !W->device_table) return MOE_ERR_NOT_PREPARED;
+    const int E = W->n_experts, H = W->hidden, I = W->inter;
+    if (T < 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_K || T > MAX_T) return MOE_ERR_UNSUPPORTED;
+    if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!aligned(out, 16))) return MOE_ERR_INVALID_ARG;
+    moe_options o{sizeof(moe_options), 1, 0xffffffffu, 0, E, MOE_PATH_AUTO, 0, nullptr};
+    if (opt) {
+        if (opt->struct_size != sizeof(moe_options)) return MOE_ERR_INVALID_ARG;
+        o = *opt;
+        if (o.expert_lo < 0 || o.expert_hi > E || o.expert_lo > o.expert_hi) return MOE_ERR_INVALID_ARG;
+        if (o.path < MOE_PATH_AUTO || o.path > MOE_PATH_TENSOR) return MOE_ERR_INVALID_ARG;
+    }
+    if (o.path == MOE_PATH_TENSOR) return MOE_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(T, k, E, H, I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (T == 0) return MOE_OK;
+
+    char *base = static_cast<char *>(ws);
+    uint32_t *status = reinterpret_cast<uint32_t *>(base + L.status);
+    int32_t *ids = reinterpret_cast<int32_t *>(base + L.ids);
+    float *wts = reinterpret_cast<float *>(base + L.wts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(base + L.offsets);
+    int32_t *active = reinterpret_cast<int32_t *>(base + L.active);
+    int32_t *pairs = reinterpret_cast<int32_t *>(base + L.pairs);
+    int32_t *pos = reinterpret_cast<int32_t *>(base + L.pos);
+    float *h = reinterpret_cast<float *>(base + L.h);
+    float *y = reinterpret_cast<float *>(base + L.y);
+    const DevExpert *table = static_cast<const DevExpert *>(W->device_table);
+
+    cudaError_t err = launch_route_topk(logits, T, E, k, o.renormalize, ids, wts, status, stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = launch_bucket(ids, T, k, E, o.expert_lo, o.expert_hi, o.format_mask, table, offsets, pairs, pos, active,
+                        status, stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, offsets, pairs, active,
+                           pos, wts, x, h, y, out, status,
+                           reinterpret_cast<cudaEvent_t const *>(o.timing_events), stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    return MOE_OK;
+}
+
+int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, void *ws, int32_t **ids,
+                            float **weights, int32_t **offsets, int32_t **active, int32_t **pairs,
+                            int32_t **pos) {
+    if (!W || !ws || T < 0 || k <= 0 || W->n_experts <= 0 || k > W->n_experts) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, k, W->n_experts, W->hidden, W->inter);
+    char *b = static_cast<char *>(ws);
+    if (ids) *ids = reinterpret_cast<int32_t *>(b + L.ids);
+    if (weights) *weights = reinterpret_cast<float *>(b + L.wts);
+    if (offsets) *offsets = reinterpret_cast<int32_t *>(b + L.offsets);
+    if (active) *active = reinterpret_cast<int32_t *>(b + L.active);
+    if (pairs) *pairs = reinterpret_cast<int32_t *>(b + L.pairs);
+    if (pos) *pos = reinterpret_cast<int32_t *>(b + L.pos);
+    return MOE_OK;
+}
+
+int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream) {
+    if (!ws || !status_out) return MOE_ERR_INVALID_ARG;
+    cudaError_t err = cudaMemcpyAsync(status_out, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = cudaStreamSynchronize(stream);
+    return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+}  // extern "C"

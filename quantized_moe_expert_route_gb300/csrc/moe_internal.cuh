@@ -1,0 +1,112 @@
+// Internal definitions shared by the library's kernels (not part of the ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+
+#include "moe_route.h"
+
+namespace moe {
+
+// Device copy of one matrix descriptor (24 bytes).
+struct DevMatrix {
+    const uint8_t *data;
+    int64_t stride;
+    int32_t fmt;
+    int32_t rows;
+};
+
+struct DevExpert {
+    DevMatrix gate, up, down;
+};
+
+// Workspace layout of moe_ffn_forward; offsets in bytes from the workspace base.
+struct WsLayout {
+    size_t status, ids, wts, offsets, active, pairs, pos, h, y, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
+    WsLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    size_t P = (size_t)T * k;
+    L.status = take(256);
+    L.ids = take(P * 4);
+    L.wts = take(P * 4);
+    L.offsets = take((size_t)(E + 1) * 4);
+    L.active = take((size_t)(E + 1) * 4);
+    L.pairs = take(P * 4);
+    L.pos = take(P * 4);
+    L.h = take(P * (size_t)I * 4);
+    L.y = take(P * (size_t)H * 4);
+    L.total = o;
+    return L;
+}
+
+constexpr int BLOCK_ELEMS[5] = {0, 32, 256, 256, 32};
+constexpr int BLOCK_BYTES[5] = {0, 34, 144, 210, 17};
+
+// Bounded waits: a wait that exceeds this many polls sets MOE_FLAG_WAIT_TIMEOUT.
+constexpr uint32_t WAIT_LIMIT = 1u << 26;
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Returns true once the phase with the given parity has completed; false after
+// WAIT_LIMIT polls.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t addr = smem_addr(bar);
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+// 1-D bulk copy global -> shared (TMA engine). dst, src 16-byte aligned,
+// bytes a multiple of 16. Completion is signalled on `bar` as tx bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ float half_bits_to_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(h));
+}
+
+// 2^(e-128) for an E8M0 byte e, exact (subnormal for e < 2).
+__device__ __forceinline__ float e8m0_half_scale(uint32_t e) {
+    return e >= 2 ? __uint_as_float((e - 1) << 23) : __uint_as_float(0x00200000u << e);
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace moe

@@ -1,0 +1,233 @@
+"""GPU parity of the whole layer (moe_ffn_forward through the C ABI) against
+the fp64 oracle: relative L2 error <= 1e-3 and max abs error <= 1e-2 * RMS.
+
+Small layers are compared on every output; the full-size layers (512 experts,
+top-10, 2048/640) on all tokens of the decode shapes and on sampled tokens of
+the 2048-token prefill chunk, in the launch configuration the benchmark times.
+Also: tier decomposition and expert-range splits on the GPU, run-to-run
+bitwise reproducibility, permutation of the expert table, device status
+flags, guard bands around the output and the workspace, and argument errors.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import ffn as offn
+from tests.gpu_util import assert_parity, ensure_built, host_layer_to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def M():
+    ensure_built()
+    import quantized_moe_expert_route_gb300 as M
+    M.load()
+    return M
+
+
+def run_layer(M, L, k=None, options=None, T=None):
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    out = M.ffn_forward(table, x, logits, k or L.cfg.k, options=options)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), table, x, logits
+
+
+def small_cfg(tiers="mixed", E=16, k=4, H=256, I=64, T=5, seed=11, bias=True):
+    return synth.LayerConfig("small", E, k, H, I, T, tiers, bias, seed)
+
+
+def test_tiny_config(M):
+    L = synth.make_layer(synth.CONFIGS["tiny"], 0)
+    out, *_ = run_layer(M, L)
+    ref = offn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    assert_parity(out, ref, "tiny")
+
+
+@pytest.mark.parametrize("tiers,T", [("q8_0", 1), ("q4k", 3), ("mixed", 7), ("mixed", 33), ("mixed", 96),
+                                     ("q4k", 130)])
+def test_small_layers(M, tiers, T):
+    L = synth.make_layer(small_cfg(tiers=tiers, T=T, seed=T), 0)
+    out, *_ = run_layer(M, L)
+    ref = offn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k)
+    assert_parity(out, ref, f"{tiers} T={T}")
+
+
+def test_ragged_shapes(M):
+    # I not a multiple of the 16-row gate/up tile nor of the 32-row down tile;
+    # H spans several Q4_K super-blocks; k odd.
+    cfg = synth.LayerConfig("ragged", 9, 3, 512, 96 + 32, 11, "mixed", True, 5)
+    L = synth.make_layer(cfg, 0)
+    out, *_ = run_layer(M, L)
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), "ragged")
+    cfg = synth.LayerConfig("ragged2", 5, 5, 256, 32, 2, "q8_0", False, 6)   # k = E, I = one block
+    L = synth.make_layer(cfg, 0)
+    out, *_ = run_layer(M, L)
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), "k=E")
+
+
+def test_not_renormalized(M):
+    L = synth.make_layer(small_cfg(T=6, seed=21), 0)
+    opt = M.make_options(renormalize=False, n_experts=L.cfg.n_experts)
+    out, *_ = run_layer(M, L, options=opt)
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, renormalize=False), "no renorm")
+
+
+def test_tier_decomposition_and_range_split(M):
+    L = synth.make_layer(small_cfg(E=20, k=5, T=9, seed=31), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    E, k = L.cfg.n_experts, L.cfg.k
+    full = M.ffn_forward(table, x, logits, k).cpu().numpy().astype(np.float64)
+    ref = offn.moe_ffn(L.experts, L.x_bf16, L.logits, k)
+    assert_parity(full, ref, "full")
+    parts = np.zeros_like(full)
+    for f in sorted({fm for fm, _ in L.fmts}):
+        opt = M.make_options(format_mask=1 << f, n_experts=E)
+        part = M.ffn_forward(table, x, logits, k, options=opt).cpu().numpy()
+        assert_parity(part, offn.moe_ffn(L.experts, L.x_bf16, L.logits, k, format_mask=1 << f), f"tier {f}")
+        parts += part
+    assert_parity(parts, ref, "sum of tiers")
+    lo = M.ffn_forward(table, x, logits, k, options=M.make_options(expert_lo=0, expert_hi=8, n_experts=E))
+    hi = M.ffn_forward(table, x, logits, k, options=M.make_options(expert_lo=8, expert_hi=E, n_experts=E))
+    assert_parity(lo.cpu().numpy() + hi.cpu().numpy(), ref, "range split")
+
+
+def test_bitwise_reproducible(M):
+    L = synth.make_layer(small_cfg(T=40, seed=41), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    ws = M.Workspace(table, 40, L.cfg.k)
+    a = M.ffn_forward(table, x, logits, L.cfg.k, ws=ws).clone()
+    b = M.ffn_forward(table, x, logits, L.cfg.k, ws=ws).clone()
+    assert torch.equal(a, b)
+
+
+def test_permuted_table(M):
+    L = synth.make_layer(small_cfg(E=12, k=3, T=8, seed=51), 0)
+    experts, x, logits = host_layer_to_device(L)
+    t1 = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    a = M.ffn_forward(t1, x, logits, L.cfg.k)
+    perm = np.random.default_rng(52).permutation(12)
+    t2 = M.WeightTable([experts[int(p)] for p in perm], L.cfg.hidden, L.cfg.inter)
+    b = M.ffn_forward(t2, x, logits[:, torch.from_numpy(perm).cuda()].contiguous(), L.cfg.k)
+    # the schedule depends only on each expert's data, so the result is bit-identical
+    assert torch.equal(a, b)
+
+
+def test_status_and_nonfinite(M):
+    L = synth.make_layer(small_cfg(T=4, seed=61), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    ws = M.Workspace(table, 4, L.cfg.k)
+    M.ffn_forward(table, x, logits, L.cfg.k, ws=ws)
+    assert ws.read_status() == 0
+    lg = logits.clone()
+    lg[1, 3] = float("nan")
+    lg[2, :] = float("-inf")
+    out = M.ffn_forward(table, x, lg, L.cfg.k, ws=ws).cpu().numpy()
+    assert ws.read_status() & M.FLAG_NONFINITE_LOGIT
+    assert ws.read_status() == 0          # read clears
+    lgh = lg.cpu().numpy()
+    ref = offn.moe_ffn(L.experts, L.x_bf16, lgh, L.cfg.k)
+    assert np.all(out[2] == 0) and np.all(ref[2] == 0)
+    assert_parity(out, ref, "nonfinite")
+
+
+def test_guard_bands(M):
+    """Canary bytes around the output and the workspace survive a forward."""
+    L = synth.make_layer(small_cfg(T=13, seed=71), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    T, H, k = 13, L.cfg.hidden, L.cfg.k
+    G = 4096
+    ws_bytes = M.Workspace(table, T, k).nbytes
+    big = torch.full((G + ws_bytes + G,), 0xA5, dtype=torch.uint8, device="cuda")
+    ws = M.Workspace.__new__(M.Workspace)
+    ws.buf, ws.nbytes = big[G:G + ws_bytes], ws_bytes
+    torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ws.buf[:256].zero_()
+    outbig = torch.full((T * H + 2 * 1024,), 7.0, dtype=torch.float32, device="cuda")
+    out = outbig[1024:1024 + T * H].view(T, H)
+    M.ffn_forward(table, x, logits, k, out=out, ws=ws)
+    torch.cuda.synchronize()
+    assert torch.all(big[:G] == 0xA5) and torch.all(big[G + ws_bytes:] == 0xA5)
+    assert torch.all(outbig[:1024] == 7.0) and torch.all(outbig[1024 + T * H:] == 7.0)
+    assert_parity(out.cpu().numpy(), offn.moe_ffn(L.experts, L.x_bf16, L.logits, k), "guarded")
+
+
+def test_argument_errors(M):
+    L = synth.make_layer(small_cfg(T=2, seed=81), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    with pytest.raises(M.MoeError) as ei:
+        M.ffn_forward(table, x, logits, L.cfg.n_experts + 1)
+    assert ei.value.code == 1
+    small = M.Workspace(table, 1, L.cfg.k)
+    with pytest.raises(M.MoeError) as ei:
+        M.ffn_forward(table, x, logits, L.cfg.k, ws=small)
+    assert ei.value.code == 5
+    bad = [dict(e) for e in experts]
+    fmt, rows, cols, stride, data = bad[0]["gate"]
+    bad[0]["gate"] = (fmt, rows, cols + 32, stride, data)
+    with pytest.raises(M.MoeError) as ei:
+        M.WeightTable(bad, L.cfg.hidden, L.cfg.inter)
+    assert ei.value.code == 2
+    bad[0]["gate"] = (9, rows, cols, stride, data)
+    with pytest.raises(M.MoeError) as ei:
+        M.WeightTable(bad, L.cfg.hidden, L.cfg.inter)
+    assert ei.value.code == 3
+    bad[0]["gate"] = (fmt, rows, cols, stride + 8, data)
+    with pytest.raises(M.MoeError) as ei:
+        M.WeightTable(bad, L.cfg.hidden, L.cfg.inter)
+    assert ei.value.code == 2
+    # gate and up in different formats
+    bad[0]["gate"] = experts[0]["gate"]
+    f2 = synth.Q8_0 if fmt != synth.Q8_0 else synth.MXFP4
+    m2 = synth.gen_matrix(f2, rows, cols, 5)
+    bad[0]["up"] = (f2, rows, cols, m2.stride, torch.from_numpy(m2.data).cuda())
+    with pytest.raises(M.MoeError) as ei:
+        M.WeightTable(bad, L.cfg.hidden, L.cfg.inter)
+    assert ei.value.code == 3
+
+
+def test_zero_tokens(M):
+    L = synth.make_layer(small_cfg(T=0, seed=91), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    out = M.ffn_forward(table, x, logits, L.cfg.k)
+    assert out.shape == (0, L.cfg.hidden)
+
+
+# --------------------------------------------------------------- full size
+def full_layer_parity(M, name, tokens_to_check=None, layer=0):
+    from synth import gpu as sgpu
+    cfg = synth.CONFIGS[name]
+    DL = sgpu.make_device_layer(cfg, layer)
+    table = M.WeightTable(DL.experts, cfg.hidden, cfg.inter)
+    out = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k).cpu().numpy()
+    lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
+    tok = list(range(cfg.tokens)) if tokens_to_check is None else tokens_to_check
+    ref = offn.moe_ffn(lazy, DL.x_host, DL.logits_host, cfg.k, tokens=tok, gate_formats=lazy.gate_formats())
+    assert_parity(out[tok], ref, name)
+    del table, DL
+    torch.cuda.empty_cache()
+
+
+def test_full_decode1(M):
+    full_layer_parity(M, "decode1")
+    full_layer_parity(M, "decode1", layer=7)
+
+
+def test_full_decode16(M):
+    full_layer_parity(M, "decode16", tokens_to_check=[0, 5, 15])
+
+
+def test_full_mtp6(M):
+    full_layer_parity(M, "mtp6")
+
+
+def test_full_prefill_sampled(M):
+    full_layer_parity(M, "prefill2048", tokens_to_check=[0, 1, 777, 2047])
