@@ -229,6 +229,10 @@ def make_options(renormalize: bool = True, format_mask: int = 0xFFFFFFFF, expert
     if timing_events is not None:
         if len(timing_events) != 3:
             raise ValueError("timing_events needs 3 events")
+        for ev in timing_events:
+            if ev.cuda_event == 0:        # torch creates the CUDA event on first record
+                ev.record(torch.cuda.current_stream())
+        torch.cuda.current_stream().synchronize()
         arr = (ctypes.c_void_p * 3)(*[ev.cuda_event for ev in timing_events])
         o._events_keep = (arr, list(timing_events))
         o.timing_events = ctypes.cast(arr, ctypes.c_void_p)

@@ -32,7 +32,7 @@ int cuda_fail(cudaError_t e) {
     return MOE_ERR_CUDA;
 }
 
-constexpr size_t SMEM_LIMIT = 227 * 1024;
+constexpr size_t SMEM_LIMIT = 227 * 1024 - 1024;   // opt-in limit less the kernels' static shared memory
 constexpr int MAX_T = 65535;
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

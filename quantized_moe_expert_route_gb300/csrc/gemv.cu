@@ -363,6 +363,19 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
     return cudaEventRecordWithFlags(ev, s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0);
 }
 
+// Lets `fn` use all of the opt-in shared memory that its static shared
+// memory leaves free.
+cudaError_t allow_max_dynamic_smem(const void *fn) {
+    int dev = 0, optin = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err == cudaSuccess) err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (err == cudaSuccess) err = cudaFuncGetAttributes(&fa, fn);
+    if (err == cudaSuccess)
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+    return err;
+}
+
 int current_device() {
     int d = 0;
     cudaGetDevice(&d);
@@ -382,14 +395,11 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
                              uint32_t *status, cudaEvent_t const *events, cudaStream_t s) {
     static bool attr_done[64] = {};
     int dev = current_device();
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e1 = cudaFuncSetAttribute(gateup_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              227 * 1024);
-        cudaError_t e2 = cudaFuncSetAttribute(down_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              227 * 1024);
-        if (e1 != cudaSuccess) return e1;
-        if (e2 != cudaSuccess) return e2;
-        attr_done[dev] = true;
+    if (dev >= 64 || !attr_done[dev]) {
+        cudaError_t err = allow_max_dynamic_smem(reinterpret_cast<const void *>(gateup_gemv_kernel));
+        if (err == cudaSuccess) err = allow_max_dynamic_smem(reinterpret_cast<const void *>(down_gemv_kernel));
+        if (err != cudaSuccess) return err;
+        if (dev < 64) attr_done[dev] = true;
     }
     const int max_active = T * k < E ? T * k : E;
     if (T > 0 && max_active > 0) {

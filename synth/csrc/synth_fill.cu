@@ -26,8 +26,13 @@ __device__ __forceinline__ uint64_t draw(uint64_t key, uint64_t i) { return mix6
 __device__ __forceinline__ uint16_t f16_uniform(uint64_t r, float lo, float span) {
     const float u = (float)(r >> 40) * 5.9604644775390625e-08f;  // 2^-24, exact
     const float v = __fadd_rn(lo, __fmul_rn(span, u));
-    return __half_as_ushort(__float2half_rn(v));
+    unsigned short h;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(h) : "f"(v));
+    return h;
 }
+
+// fp16 fields sit at even offsets of 16-byte aligned rows: one 16-bit store.
+__device__ __forceinline__ void put16(uint8_t *p, uint16_t v) { *reinterpret_cast<uint16_t *>(p) = v; }
 
 __device__ __forceinline__ int ubelow16(uint64_t chunk, uint64_t n) { return (int)((chunk * n) >> 16); }
 
@@ -47,20 +52,14 @@ __global__ void synth_fill_kernel(const moe_synth_matrix *__restrict__ descs) {
     const uint64_t key = M.key;
 
     if (M.format == 1) {  // Q8_0
-        uint16_t d = f16_uniform(draw(key, base + 0), (float)0.002, (float)0.018);
-        out[0] = (uint8_t)d;
-        out[1] = (uint8_t)(d >> 8);
+        put16(out, f16_uniform(draw(key, base + 0), (float)0.002, (float)0.018));
         for (int g = 0; g < 8; ++g) {
             uint64_t r = draw(key, base + 1 + g);
             for (int c = 0; c < 4; ++c) out[2 + 4 * g + c] = (uint8_t)(ubelow16((r >> (16 * c)) & 0xFFFF, 255) - 127);
         }
     } else if (M.format == 2) {  // Q4_K
-        uint16_t d = f16_uniform(draw(key, base + 0), (float)0.0005, (float)0.0045);
-        uint16_t dm = f16_uniform(draw(key, base + 1), (float)0.0005, (float)0.0045);
-        out[0] = (uint8_t)d;
-        out[1] = (uint8_t)(d >> 8);
-        out[2] = (uint8_t)dm;
-        out[3] = (uint8_t)(dm >> 8);
+        put16(out, f16_uniform(draw(key, base + 0), (float)0.0005, (float)0.0045));
+        put16(out + 2, f16_uniform(draw(key, base + 1), (float)0.0005, (float)0.0045));
         for (int g = 0; g < 18; ++g) {
             uint64_t r = draw(key, base + 2 + g);
             for (int c = 0; c < 8; ++c) {
@@ -78,9 +77,7 @@ __global__ void synth_fill_kernel(const moe_synth_matrix *__restrict__ descs) {
             for (int c = 0; c < 4; ++c)
                 out[192 + 4 * g + c] = (uint8_t)(ubelow16((r >> (16 * c)) & 0xFFFF, 255) - 127);
         }
-        uint16_t d = f16_uniform(draw(key, base + 28), (float)1e-4, (float)9e-4);
-        out[208] = (uint8_t)d;
-        out[209] = (uint8_t)(d >> 8);
+        put16(out + 208, f16_uniform(draw(key, base + 28), (float)1e-4, (float)9e-4));
     } else {  // MXFP4
         uint64_t r0 = draw(key, base + 0);
         out[0] = (uint8_t)(124 + (((r0 & 0xFFFFFFFFull) * 3ull) >> 32));

@@ -162,8 +162,16 @@ def test_argument_errors(M):
     L = synth.make_layer(small_cfg(T=2, seed=81), 0)
     experts, x, logits = host_layer_to_device(L)
     table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    ws = M.Workspace(table, 2, L.cfg.k)
     with pytest.raises(M.MoeError) as ei:
-        M.ffn_forward(table, x, logits, L.cfg.n_experts + 1)
+        M.ffn_forward(table, x, logits, L.cfg.n_experts + 1, ws=ws)   # k > E
+    assert ei.value.code == 1
+    with pytest.raises(M.MoeError) as ei:
+        M.ffn_forward(table, x, logits, 0, ws=ws)
+    assert ei.value.code == 1
+    bad_opt = M.make_options(expert_lo=3, expert_hi=2, n_experts=L.cfg.n_experts)
+    with pytest.raises(M.MoeError) as ei:
+        M.ffn_forward(table, x, logits, L.cfg.k, ws=ws, options=bad_opt)
     assert ei.value.code == 1
     small = M.Workspace(table, 1, L.cfg.k)
     with pytest.raises(M.MoeError) as ei:

@@ -39,7 +39,7 @@ def check_route(M, logits_np, k, renorm=True):
 
 
 @pytest.mark.parametrize("T,E,k", [(4, 8, 2), (1, 512, 10), (16, 512, 10), (6, 512, 10), (2048, 512, 10),
-                                   (33, 100, 7), (5, 1024, 32), (3, 8, 8), (7, 1, 1), (9, 40, 40)])
+                                   (33, 100, 7), (5, 1024, 32), (3, 8, 8), (7, 1, 1), (9, 40, 32), (2, 32, 32)])
 def test_route_random(M, T, E, k):
     rng = np.random.default_rng(T * 1000 + E + k)
     logits = rng.standard_normal((T, E)).astype(np.float32)
