@@ -217,6 +217,30 @@ int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, voi
  * Synchronises `stream`. *status_out is a host pointer. */
 int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream);
 
+/* Size of the device scratch array that moe_ffn_forward_noalloc uses. */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* The whole layer, like moe_ffn_forward, for callers that cannot allocate
+ * device memory: a host framework whose memory planner owns all device memory,
+ * a latency-critical loop where cudaMalloc/cudaFree would synchronise the
+ * device, or a C client that only receives input and output pointers. The
+ * layer's scratch lives in a fixed device array of MOE_NOALLOC_SCRATCH_BYTES
+ * (4 MiB) inside this library, held by every GPU that loads the library until
+ * the process exits; no workspace argument, and no allocation of any kind.
+ * The source pages have no counterpart of this entry point.
+ *   - Sizes: accepted when moe_ffn_workspace_size(W, T, k) <= 4 MiB (e.g. up to
+ *     38 tokens at E = 512, k = 10, H = 2048, I = 640); larger sizes return
+ *     MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents:
+ *     calls whose work overlaps on the GPU (different streams, or several host
+ *     threads) race and corrupt each other's results; order them on one
+ *     stream. Device status flags are cleared at each call and not reported.
+ * Other arguments, errors and ownership as for moe_ffn_forward. */
+int moe_ffn_forward_noalloc(const moe_weight_table *W, const uint16_t *x, const float *logits, int32_t T,
+                            int32_t k, const moe_options *opt, float *out, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

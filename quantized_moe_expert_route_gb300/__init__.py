@@ -8,5 +8,6 @@ missing library raises instead of falling back to anything else.
 from ._lib import (  # noqa: F401
     BLOCK_BYTES, BLOCK_ELEMS, EXPORTED, FLAG_BAD_ID, FLAG_DUPLICATE_ID, FLAG_NONFINITE_LOGIT,
     FLAG_WAIT_TIMEOUT, MOE_TABLE_PREPARED, MXFP4, PATH_AUTO, PATH_GEMV, PATH_TENSOR, Q4_K, Q6_K, Q8_0,
-    MoeError, Options, WeightTable, Workspace, bucket, ffn_forward, load, make_options, route_topk,
+    MoeError, NOALLOC_SCRATCH_BYTES, Options, WeightTable, Workspace, bucket, ffn_forward,
+    ffn_forward_noalloc, load, make_options, route_topk,
 )

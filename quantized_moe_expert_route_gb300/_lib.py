@@ -27,8 +27,9 @@ FLAG_NONFINITE_LOGIT, FLAG_BAD_ID, FLAG_DUPLICATE_ID, FLAG_WAIT_TIMEOUT = 1, 2, 
 EXPORTED = [
     "moe_strerror", "moe_last_cuda_error", "moe_table_device_bytes", "moe_table_prepare",
     "moe_route_topk", "moe_bucket", "moe_ffn_workspace_size", "moe_ffn_workspace_init",
-    "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views",
+    "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc",
 ]
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class MoeError(RuntimeError):
@@ -87,8 +88,10 @@ def load() -> ctypes.CDLL:
     L.moe_ffn_read_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     pp = ctypes.POINTER(ctypes.c_void_p)
     L.moe_ffn_workspace_views.argtypes = [ctypes.POINTER(WeightTableC), i32, i32, vp, pp, pp, pp, pp, pp, pp]
+    L.moe_ffn_forward_noalloc.argtypes = [ctypes.POINTER(WeightTableC), vp, vp, i32, i32, ctypes.POINTER(Options),
+                                          vp, vp]
     for name in ("moe_table_prepare", "moe_route_topk", "moe_bucket", "moe_ffn_workspace_init",
-                 "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views"):
+                 "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -258,4 +261,26 @@ def ffn_forward(table: WeightTable, x_bf16: torch.Tensor, logits: torch.Tensor, 
     opt = ctypes.byref(options) if options is not None else None
     _check("moe_ffn_forward", load().moe_ffn_forward(ctypes.byref(table.c), _ptr(x_bits), _ptr(logits), T, k,
                                                       opt, _ptr(out), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    return out
+
+
+def ffn_forward_noalloc(table: WeightTable, x_bf16: torch.Tensor, logits: torch.Tensor, k: int,
+                        out: Optional[torch.Tensor] = None, options: Optional[Options] = None,
+                        stream=None) -> torch.Tensor:
+    """The whole layer without a workspace argument (moe_ffn_forward_noalloc):
+    the library keeps the scratch in its own fixed 4 MiB device array, for
+    callers that cannot allocate device memory. Calls share that array, so
+    calls that overlap on the GPU race; keep them on one stream. Sizes whose
+    workspace would exceed 4 MiB raise MoeError (code 8)."""
+    x_bits = x_bf16.view(torch.int16) if x_bf16.dtype == torch.bfloat16 else x_bf16
+    _dev(x_bits, "x", torch.int16)
+    _dev(logits, "logits", torch.float32)
+    T, H = x_bits.shape
+    if H != table.hidden or logits.shape != (T, table.n_experts):
+        raise ValueError("x / logits shape does not match the table")
+    out = out if out is not None else torch.empty((T, H), dtype=torch.float32, device=x_bits.device)
+    _dev(out, "out", torch.float32)
+    opt = ctypes.byref(options) if options is not None else None
+    _check("moe_ffn_forward_noalloc", load().moe_ffn_forward_noalloc(
+        ctypes.byref(table.c), _ptr(x_bits), _ptr(logits), T, k, opt, _ptr(out), _stream(stream)))
     return out
