@@ -417,7 +417,11 @@ def run_ours(args, world, rank, local, cpu_proc):
     mean_pairs = float(np.mean(per_layer_pairs))
     gu_bytes = float(np.mean(per_layer_gu_bytes)) + T * H * 2 + mean_pairs * I * 4
     dn_bytes = float(np.mean(per_layer_dn_bytes)) + mean_pairs * I * 4 + mean_pairs * H * 4
-    if gu_avg >= dn_avg:
+    path = M.ffn_path(tables[0], T, k)
+    if path == M.PATH_FUSED:
+        # one kernel runs the whole layer: its algorithmic bytes are the layer's
+        kname, kbytes, kdur = "decode_fused_kernel", layer_bytes, gu_avg + dn_avg
+    elif gu_avg >= dn_avg:
         kname, kbytes, kdur = "gateup_gemv_kernel", gu_bytes, gu_avg
     else:
         kname, kbytes, kdur = "down_gemv_kernel", dn_bytes, dn_avg
@@ -442,10 +446,13 @@ def run_ours(args, world, rank, local, cpu_proc):
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": kernel_traffic(kname, args.config),
                      "bytes_per_launch": kbytes, "launch_us": kdur * 1e6, "peak_kind": peak_kind,
-                     "other_kernel_us": (dn_avg if kname.startswith("gateup") else gu_avg) * 1e6},
+                     "other_kernel_us": (0.0 if path == M.PATH_FUSED else
+                                         (dn_avg if kname.startswith("gateup") else gu_avg) * 1e6)},
         "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
-        "gpu_launches": KERNELS_PER_LAYER * NL * args.steps,
+        "gpu_launches": (1 if path == M.PATH_FUSED else KERNELS_PER_LAYER) * NL * args.steps,
+        "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
+                 M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
         "clocks": clk,
         "device_status_flags": bad,
         "gpu": props.name,

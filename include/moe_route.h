@@ -116,14 +116,19 @@ typedef struct {
     void *device_table;        /* device copy of the descriptors */
     uint32_t formats_present;  /* bit (1 << format) for every format in use */
     uint32_t prepared;         /* MOE_TABLE_PREPARED after a successful prepare */
+    uint32_t gateup_formats;   /* bit (1 << format) for every gate/up format in use */
+    uint32_t down_formats;     /* bit (1 << format) for every down format in use */
     int64_t max_gateup_stride; /* largest gate/up row stride, bytes */
     int64_t max_down_stride;   /* largest down row stride, bytes */
 } moe_weight_table;
 
 /* Paths for moe_options.path. */
-#define MOE_PATH_AUTO 0        /* GEMV up to MOE_GEMV_MAX_ROWS tokens, tensor cores above */
-#define MOE_PATH_GEMV 1        /* CUDA-core grouped GEMV, weights dequantized in registers */
+#define MOE_PATH_AUTO 0        /* the fastest path that handles the layer (see moe_ffn_path) */
+#define MOE_PATH_GEMV 1        /* grouped GEMV kernels (route, bucket, gate/up, down, combine); any layer */
 #define MOE_PATH_TENSOR 2      /* tcgen05 grouped GEMM (prefill chunks) */
+#define MOE_PATH_FUSED 3       /* one persistent cooperative kernel per layer for decode rows:
+                                  T * k <= 64, Q4_K gate/up and Q8_0 down, H % 64 == 0,
+                                  I % 32 == 0, I <= 1024 */
 #define MOE_GEMV_MAX_ROWS 96
 
 /* Options of moe_ffn_forward (NULL = defaults). */
@@ -135,10 +140,11 @@ typedef struct {
     int32_t expert_hi;
     int32_t path;              /* MOE_PATH_* */
     int32_t reserved;          /* 0 */
-    /* Profiling hook: NULL, or a host array of 3 cudaEvent_t that are recorded
-     * on the stream before the gate/up mat-mul kernel, between it and the down
-     * mat-mul kernel, and after the down kernel. During stream capture they
-     * are recorded as external event nodes. */
+    /* Profiling hook: NULL, or a host array of 3 cudaEvent_t recorded on the
+     * stream around the expert mat-mul kernels: before the gate/up kernel,
+     * between it and the down kernel, and after the down kernel. On the fused
+     * path, where one kernel does both, events 1 and 2 are both recorded after
+     * it. During stream capture they become external event-record nodes. */
     void *const *timing_events;
 } moe_options;
 
@@ -188,7 +194,13 @@ int moe_bucket(const int32_t *ids, int32_t T, int32_t k, int32_t E, int32_t expe
  * (0 if the arguments are invalid). */
 size_t moe_ffn_workspace_size(const moe_weight_table *W, int32_t T, int32_t k);
 
-/* Zero a workspace's status word (once, before its first forward).
+/* The path moe_ffn_forward takes for these arguments (MOE_PATH_GEMV,
+ * MOE_PATH_TENSOR or MOE_PATH_FUSED; resolves MOE_PATH_AUTO), or -1 if the
+ * requested path cannot run this layer. Host-only. */
+int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_options *opt);
+
+/* Zero a workspace's status word and grid-barrier counter (once, before its
+ * first forward).
  * ws: device, at least moe_ffn_workspace_size bytes. */
 int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 

@@ -21,13 +21,14 @@ BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17}
 
 MOE_OK = 0
 MOE_TABLE_PREPARED = 0x4D4F4554
-PATH_AUTO, PATH_GEMV, PATH_TENSOR = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_TENSOR, PATH_FUSED = 0, 1, 2, 3
 FLAG_NONFINITE_LOGIT, FLAG_BAD_ID, FLAG_DUPLICATE_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED = [
     "moe_strerror", "moe_last_cuda_error", "moe_table_device_bytes", "moe_table_prepare",
     "moe_route_topk", "moe_bucket", "moe_ffn_workspace_size", "moe_ffn_workspace_init",
     "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc",
+    "moe_ffn_path",
 ]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -51,7 +52,8 @@ class WeightTableC(ctypes.Structure):
     _fields_ = [("n_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
                 ("reserved", ctypes.c_int32), ("experts", ctypes.POINTER(Expert)),
                 ("device_table", ctypes.c_void_p), ("formats_present", ctypes.c_uint32),
-                ("prepared", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
+                ("prepared", ctypes.c_uint32), ("gateup_formats", ctypes.c_uint32),
+                ("down_formats", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
                 ("max_down_stride", ctypes.c_int64)]
 
 
@@ -88,6 +90,8 @@ def load() -> ctypes.CDLL:
     L.moe_ffn_read_status.argtypes = [vp, ctypes.POINTER(u32), vp]
     pp = ctypes.POINTER(ctypes.c_void_p)
     L.moe_ffn_workspace_views.argtypes = [ctypes.POINTER(WeightTableC), i32, i32, vp, pp, pp, pp, pp, pp, pp]
+    L.moe_ffn_path.argtypes = [ctypes.POINTER(WeightTableC), i32, i32, ctypes.POINTER(Options)]
+    L.moe_ffn_path.restype = ctypes.c_int
     L.moe_ffn_forward_noalloc.argtypes = [ctypes.POINTER(WeightTableC), vp, vp, i32, i32, ctypes.POINTER(Options),
                                           vp, vp]
     for name in ("moe_table_prepare", "moe_route_topk", "moe_bucket", "moe_ffn_workspace_init",
@@ -142,7 +146,7 @@ class WeightTable:
                 self._keep.append(data)
                 setattr(arr[e], name, Matrix(fmt, rows, cols, 0, stride, data.data_ptr()))
         self._arr = arr
-        self.c = WeightTableC(E, hidden, inter, 0, ctypes.cast(arr, ctypes.POINTER(Expert)), None, 0, 0, 0, 0)
+        self.c = WeightTableC(E, hidden, inter, 0, ctypes.cast(arr, ctypes.POINTER(Expert)), None, 0, 0, 0, 0, 0, 0)
         nbytes = L.moe_table_device_bytes(E)
         if nbytes == 0:
             raise ValueError(f"bad expert count {E}")
@@ -220,6 +224,12 @@ def bucket(ids: torch.Tensor, n_experts: int, expert_lo: int = 0, expert_hi: Opt
     _check("moe_bucket", load().moe_bucket(_ptr(ids), T, k, E, expert_lo, hi, _ptr(offsets), _ptr(pairs),
                                             _ptr(pos), _ptr(active), _ptr(status), _stream(stream)))
     return offsets, pairs[: T * k], pos[: T * k], active
+
+
+def ffn_path(table: "WeightTable", T: int, k: int, options: Optional[Options] = None) -> int:
+    """The path moe_ffn_forward takes (PATH_GEMV / PATH_TENSOR / PATH_FUSED), -1 if none."""
+    opt = ctypes.byref(options) if options is not None else None
+    return load().moe_ffn_path(ctypes.byref(table.c), T, k, opt)
 
 
 def make_options(renormalize: bool = True, format_mask: int = 0xFFFFFFFF, expert_lo: int = 0,

@@ -19,6 +19,13 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
                              int64_t dn_stride, const int32_t *offsets, const int32_t *pairs, const int32_t *active,
                              const int32_t *pos, const float *wts, const uint16_t *x, float *h, float *y, float *out,
                              uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
+bool decode_fused_eligible(int T, int k, int E, int H, int I, uint32_t gateup_formats, uint32_t down_formats,
+                           int64_t gu_stride, int64_t dn_stride);
+cudaError_t launch_decode_fused(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
+                                int64_t dn_stride, int renorm, int lo, int hi, uint32_t fmt_mask, const float *logits,
+                                const uint16_t *x, float *out, float *h, int32_t *ids, float *wts, int32_t *offsets,
+                                int32_t *active, int32_t *pairs, int32_t *pos, unsigned char *sync, uint32_t *status,
+                                cudaStream_t s);
 }  // namespace moe
 
 using namespace moe;
@@ -35,6 +42,13 @@ int cuda_fail(cudaError_t e) {
 constexpr size_t SMEM_LIMIT = 227 * 1024 - 1024;   // opt-in limit less the kernels' static shared memory
 constexpr int MAX_T = 65535;
 
+cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t err = cudaStreamIsCapturing(s, &cs);
+    if (err != cudaSuccess) return err;
+    return cudaEventRecordWithFlags(ev, s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : 0);
+}
+
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_matrix(const moe_matrix &m, int rows, int cols) {
@@ -46,6 +60,29 @@ int check_matrix(const moe_matrix &m, int rows, int cols) {
     if (m.row_stride_bytes < row_bytes || m.row_stride_bytes % 16 != 0) return MOE_ERR_BAD_SHAPE;
     if (!m.data || !aligned(m.data, 16)) return MOE_ERR_INVALID_ARG;
     return MOE_OK;
+}
+
+// Resolve the path of a forward; -1 if the requested path cannot run it.
+int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
+    const bool fused_ok = decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
+                                                W->down_formats, W->max_gateup_stride, W->max_down_stride);
+    switch (requested) {
+        case MOE_PATH_AUTO: return fused_ok ? MOE_PATH_FUSED : MOE_PATH_GEMV;
+        case MOE_PATH_GEMV: return MOE_PATH_GEMV;
+        case MOE_PATH_FUSED: return fused_ok ? MOE_PATH_FUSED : -1;
+        default: return -1;
+    }
+}
+
+// Options with defaults filled in; false if they are invalid.
+bool effective_options(const moe_weight_table *W, const moe_options *opt, moe_options &o) {
+    o = moe_options{sizeof(moe_options), 1, 0xffffffffu, 0, W->n_experts, MOE_PATH_AUTO, 0, nullptr};
+    if (!opt) return true;
+    if (opt->struct_size != sizeof(moe_options)) return false;
+    o = *opt;
+    if (o.expert_lo < 0 || o.expert_hi > W->n_experts || o.expert_lo > o.expert_hi) return false;
+    if (o.path < MOE_PATH_AUTO || o.path > MOE_PATH_FUSED) return false;
+    return true;
 }
 
 }  // namespace
@@ -82,7 +119,7 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     if (H > MOE_MAX_HIDDEN || I > MOE_MAX_INTER) return MOE_ERR_UNSUPPORTED;
     if (device_bytes < moe_table_device_bytes(E) || !aligned(device_buf, 16)) return MOE_ERR_INVALID_ARG;
     std::vector<DevExpert> dev(E);
-    uint32_t present = 0;
+    uint32_t present = 0, gu_present = 0, dn_present = 0;
     int64_t gu_max = 0, dn_max = 0;
     for (int e = 0; e < E; ++e) {
         const moe_expert &x = W->experts[e];
@@ -93,6 +130,8 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
         if (x.gate.format != x.up.format) return MOE_ERR_BAD_FORMAT;
         present |= 1u << x.gate.format;
         present |= 1u << x.down.format;
+        gu_present |= 1u << x.gate.format;
+        dn_present |= 1u << x.down.format;
         gu_max = std::max<int64_t>(gu_max, std::max(x.gate.row_stride_bytes, x.up.row_stride_bytes));
         dn_max = std::max<int64_t>(dn_max, x.down.row_stride_bytes);
         const moe_matrix *src[3] = {&x.gate, &x.up, &x.down};
@@ -113,6 +152,8 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     if (err != cudaSuccess) return cuda_fail(err);
     W->device_table = device_buf;
     W->formats_present = present;
+    W->gateup_formats = gu_present;
+    W->down_formats = dn_present;
     W->max_gateup_stride = gu_max;
     W->max_down_stride = dn_max;
     W->prepared = MOE_TABLE_PREPARED;
@@ -145,8 +186,8 @@ size_t moe_ffn_workspace_size(const moe_weight_table *W, int32_t T, int32_t k) {
 }
 
 int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
-    if (!ws || ws_bytes < 256) return MOE_ERR_INVALID_ARG;
-    cudaError_t err = cudaMemsetAsync(ws, 0, 256, stream);
+    if (!ws || ws_bytes < SYNC_BYTES) return MOE_ERR_INVALID_ARG;
+    cudaError_t err = cudaMemsetAsync(ws, 0, SYNC_BYTES, stream);
     return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
 
@@ -160,14 +201,12 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!aligned(out, 16))) return MOE_ERR_INVALID_ARG;
-    moe_options o{sizeof(moe_options), 1, 0xffffffffu, 0, E, MOE_PATH_AUTO, 0, nullptr};
-    if (opt) {
-        if (opt->struct_size != sizeof(moe_options)) return MOE_ERR_INVALID_ARG;
-        o = *opt;
-        if (o.expert_lo < 0 || o.expert_hi > E || o.expert_lo > o.expert_hi) return MOE_ERR_INVALID_ARG;
-        if (o.path < MOE_PATH_AUTO || o.path > MOE_PATH_TENSOR) return MOE_ERR_INVALID_ARG;
-    }
-    if (o.path == MOE_PATH_TENSOR) return MOE_ERR_UNSUPPORTED;
+    moe_options o;
+    if (!effective_options(W, opt, o)) return MOE_ERR_INVALID_ARG;
+    int path = resolve_path(W, T > 0 ? T : 1, k, o.path);
+    // the fused kernel reads activation rows with 16-byte loads
+    if (path == MOE_PATH_FUSED && T > 0 && !aligned(x, 16)) path = o.path == MOE_PATH_AUTO ? MOE_PATH_GEMV : -1;
+    if (path < 0 || path == MOE_PATH_TENSOR) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, k, E, H, I);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if (T == 0) return MOE_OK;
@@ -184,16 +223,37 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     float *y = reinterpret_cast<float *>(base + L.y);
     const DevExpert *table = static_cast<const DevExpert *>(W->device_table);
 
-    cudaError_t err = launch_route_topk(logits, T, E, k, o.renormalize, ids, wts, status, stream);
+    cudaEvent_t const *events = reinterpret_cast<cudaEvent_t const *>(o.timing_events);
+    cudaError_t err;
+    if (path == MOE_PATH_FUSED) {
+        if (events && (err = record_timing_event(events[0], stream)) != cudaSuccess) return cuda_fail(err);
+        err = launch_decode_fused(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, o.renormalize,
+                                  o.expert_lo, o.expert_hi, o.format_mask, logits,
+                                  x, out, h, ids, wts, offsets, active, pairs, pos,
+                                  reinterpret_cast<unsigned char *>(base + L.status), status, stream);
+        if (err != cudaSuccess) return cuda_fail(err);
+        if (events) {
+            if ((err = record_timing_event(events[1], stream)) != cudaSuccess) return cuda_fail(err);
+            if ((err = record_timing_event(events[2], stream)) != cudaSuccess) return cuda_fail(err);
+        }
+        return MOE_OK;
+    }
+    err = launch_route_topk(logits, T, E, k, o.renormalize, ids, wts, status, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     err = launch_bucket(ids, T, k, E, o.expert_lo, o.expert_hi, o.format_mask, table, offsets, pairs, pos, active,
                         status, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, offsets, pairs, active,
-                           pos, wts, x, h, y, out, status,
-                           reinterpret_cast<cudaEvent_t const *>(o.timing_events), stream);
+                           pos, wts, x, h, y, out, status, events, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     return MOE_OK;
+}
+
+int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_options *opt) {
+    if (!W || W->prepared != MOE_TABLE_PREPARED || T < 0 || k <= 0 || k > W->n_experts) return -1;
+    moe_options o;
+    if (!effective_options(W, opt, o)) return -1;
+    return resolve_path(W, T > 0 ? T : 1, k, o.path);
 }
 
 int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, void *ws, int32_t **ids,

@@ -1,0 +1,1009 @@
+// Fused decode path: the whole routed-expert FFN of a few token rows in one
+// persistent, cooperative kernel (one CTA per SM).
+//
+// The pages' decode kernels are prior art here: the grouped multi-session
+// decode of "多卡 CUDA 张量并行：DwarfStar 如何在 8 张 L40S 上跑出 120 t/s" (section
+// 120 t/s 的秘密: one launch serves the decode rows of all sessions over a
+// Q4_K routed-expert layout), the gate/up + activation fusion of "三张 RTX 3090
+// 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南" (section 关键 Bug 修复与调试
+// 踩坑记录, item 4) and the single-token GEMV of "一张 RTX 3090 跑 Llama 70B" (section
+// 4.4). On GB300 a decode layer is a few microseconds of HBM streaming and
+// every dependent global-memory round trip costs about a microsecond, so the
+// design removes kernel boundaries and round trips:
+//
+//   1. Every CTA computes the softmax top-k and the per-expert bucketing of
+//      the token rows itself: each warp sorts a 32-logit slice (bitonic, in
+//      registers), then candidates are ranked by counting. The routed
+//      experts' descriptors are requested right after selection.
+//   2. The routed experts' gate/up rows are split evenly across the CTAs. A
+//      producer warp streams the CTA's gate/up rows, then its down rows, into
+//      a ring of 12 KB shared-memory stages with TMA bulk copies; for one
+//      token the whole share is in flight at once. Four groups of four
+//      consumer warps decode the stages and write h = silu(W_gate x) * (W_up x)
+//      (fp32) plus a per-pair running max |h| to global memory.
+//   3. A bounded grid barrier (cooperative launch: all CTAs co-resident)
+//      separates gate/up from down.
+//   4. Each CTA owns a slice of output rows for every routed expert, so the
+//      router-weighted combine runs in-CTA in ascending slot order.
+//
+// Arithmetic: codes become exact fp16 values with bit operations (a 4-bit
+// code q as 1024 + q or 1024 + 16 q, an 8-bit code as 1152 + q), activations
+// are fp16 with a per-row power-of-two scale, products accumulate in fp32 with
+// the mixed fp16 x fp16 -> fp32 FMA; the constant offsets are removed with
+// exact per-group activation sums. This path handles Q4_K gate/up with Q8_0
+// down; other layers take the general grouped GEMV path.
+#include <algorithm>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int DC_CW = 16;                        // consumer warps
+constexpr int DC_WARPS = DC_CW + 1;              // + one producer warp
+constexpr int DC_THREADS = DC_WARPS * 32;
+constexpr int DC_STAGE_MAX = 12 * 1024;          // ring stage bytes (smaller when shared memory is tight)
+constexpr int DC_NSTAGE = DC_CW;                 // one ring slot per consumer warp: warp w owns slot w
+constexpr int DC_MAX_PAIRS = 64;                 // T * k
+constexpr int DC_ROWS_A = 4;                     // max gate/up row pairs per chunk
+constexpr uint32_t DC_MAGIC = 0x64006400u;       // fp16 1024.0 in both halves
+constexpr size_t DC_SYNC_HMAX = 256;             // offset of the per-pair |h| maxima in the sync region
+
+struct DcLayout {
+    size_t ring, xs, xsum, xsc, xmax, hs, hsum, hsc, ybuf, ckey, cidx, sm, ss, selk, ids, wts, keep, act, aoff, plist,
+        dpair, chunks, full, empty, misc, total;
+    int rb, ns, C;
+};
+
+__host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I, int G, int stage, int chunk_cap) {
+    DcLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t r = o;
+        o = align_up(o + bytes, 128);
+        return r;
+    };
+    const int P = T * k;
+    L.rb = (H + G - 1) / G;
+    L.ns = (E + 31) / 32;
+    L.C = (L.ns * k + 3) / 4 * 4;
+    L.ring = take((size_t)DC_NSTAGE * stage);
+    L.xs = take((size_t)T * H * 2);
+    L.xsum = take((size_t)T * (H / 64) * 2 * 4);
+    L.xsc = take((size_t)T * 4);
+    L.xmax = take((size_t)T * 4);
+    L.hs = take((size_t)P * I * 2);
+    L.hsum = take((size_t)P * 32 * 4);
+    L.hsc = take((size_t)P * 4);
+    L.ybuf = take((size_t)P * L.rb * 4);
+    L.ckey = take((size_t)T * L.C * 4);
+    L.cidx = take((size_t)T * L.C * 4);
+    L.sm = take((size_t)T * L.ns * 4);
+    L.ss = take((size_t)T * L.ns * 4);
+    L.selk = take((size_t)P * 4);
+    L.ids = take((size_t)P * 4);
+    L.wts = take((size_t)P * 4);
+    L.keep = take((size_t)P);
+    L.act = take((size_t)P * 4);
+    L.aoff = take((size_t)(P + 1) * 4);
+    L.plist = take((size_t)P * 4);
+    L.dpair = take((size_t)P * sizeof(DevExpert));
+    L.chunks = take((size_t)chunk_cap * 16);
+    L.full = take((size_t)DC_NSTAGE * 8);
+    L.empty = take((size_t)DC_NSTAGE * 8);
+    L.misc = take(64);
+    L.total = o;
+    return L;
+}
+
+struct DcArgs {
+    const DevExpert *table;
+    int E, H, I, T, k, renorm, lo, hi;
+    uint32_t fmt_mask;
+    const float *logits;
+    const uint16_t *x;
+    float *out;
+    float *h;                       // [T*k][I] fp32, pair p = t*k + j
+    int32_t *ids_out, *offsets_out, *active_out, *pairs_out, *pos_out;
+    float *wts_out;
+    unsigned char *sync;            // zero-initialised sync region: barrier counter, |h| maxima
+    uint32_t *status;
+    int stage;                      // bytes per ring slot
+    int rows_a, rows_b;             // gate/up row pairs per chunk, down rows per chunk
+    int chunk_cap;                  // capacity of the shared-memory chunk table
+};
+
+// ---------------------------------------------------------------- small PTX helpers
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// acc += lo(a) * lo(b) + hi(a) * hi(b), fp16 operands, fp32 accumulation
+__device__ __forceinline__ void fma2_f16_f32(float &acc, uint32_t a, uint32_t b) {
+    asm("{ .reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.f16 %0, ah, bh, %0; }"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xffff))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+    uint16_t lo, hi;
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(lo) : "f"(a));
+    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(hi) : "f"(b));
+    return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(DC_CW * 32) : "memory");
+}
+
+// Power-of-two scale for fp16: returns sigma with max * 2^sigma in [2^14, 2^15)
+// (0 for max == 0), clamped so that 2^sigma and 2^-sigma are normal floats.
+__device__ __forceinline__ int pow2_shift(float maxabs) {
+    if (!(maxabs > 0.0f)) return 0;
+    const int e = (int)((__float_as_uint(maxabs) >> 23) & 0xff);
+    int s = 141 - e;
+    return s < -126 ? -126 : (s > 126 ? 126 : s);
+}
+__device__ __forceinline__ float exp2i(int s) { return __uint_as_float((uint32_t)(127 + s) << 23); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Descending bitonic sort of one (key, index) pair per lane under topk_beats.
+__device__ __forceinline__ void warp_sort_desc(float &key, int &idx) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, key, stride);
+            const int oi = __shfl_xor_sync(0xffffffffu, idx, stride);
+            const bool desc = (lane & size) == 0 || size == 32;
+            const bool lower = (lane & stride) == 0;
+            const bool mine = topk_beats(key, idx, ok, oi);
+            if (mine != (lower == desc)) {
+                key = ok;
+                idx = oi;
+            }
+        }
+    }
+}
+
+// cp.async of 8 bytes global -> shared (L1-allocating); completion via cp_async_wait_all.
+__device__ __forceinline__ void cp_async8(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ void red_release_add(unsigned long long *p, unsigned long long v) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Sums of 8 per-lane values over the warp: value j ends in lanes 4j .. 4j+3
+// (9 shuffles instead of 40).
+__device__ __forceinline__ float warp_reduce8(const float v[8]) {
+    const int lane = threadIdx.x & 31;
+    const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
+    float w[4], x[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b16 ? v[i] : v[i + 4], keep = b16 ? v[i + 4] : v[i];
+        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b8 ? w[i] : w[i + 2], keep = b8 ? w[i + 2] : w[i];
+        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    float y = (b4 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b4 ? x[0] : x[1], 4);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    return y;
+}
+
+// Sums of 4 per-lane values over the warp: value j ends in lanes 8j .. 8j+7.
+__device__ __forceinline__ float warp_reduce4(const float v[4]) {
+    const int lane = threadIdx.x & 31;
+    const bool b16 = lane & 16, b8 = lane & 8;
+    float w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b16 ? v[i] : v[i + 2], keep = b16 ? v[i + 2] : v[i];
+        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float y = (b8 ? w[1] : w[0]) + __shfl_xor_sync(0xffffffffu, b8 ? w[0] : w[1], 8);
+    y += __shfl_xor_sync(0xffffffffu, y, 4);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    return y;
+}
+
+// Scales and mins of Q4_K sub-blocks 2g and 2g+1 from the 12 scale bytes
+// (three little-endian words), without branches: bytes j' = 2 (g & 1) and
+// j' + 1 of each word; for g >= 2 the low four bits come from s[8..11] and
+// the top two from bits 6-7 of s[0..3] (scales) and s[4..7] (mins).
+__device__ __forceinline__ void q4k_pair_scales(int g, uint32_t s03, uint32_t s47, uint32_t s811, float &sc0,
+                                                float &sc1, float &m0, float &m1) {
+    const int sh = (g & 1) * 16;
+    const uint32_t a = (s03 >> sh) & 0xFFFFu, m = (s47 >> sh) & 0xFFFFu, h = (s811 >> sh) & 0xFFFFu;
+    const uint32_t sc_lo = a & 0x3F3Fu, mn_lo = m & 0x3F3Fu;
+    const uint32_t sc_hi = (h & 0x0F0Fu) | ((a >> 2) & 0x3030u);
+    const uint32_t mn_hi = ((h >> 4) & 0x0F0Fu) | ((m >> 2) & 0x3030u);
+    const uint32_t scp = g < 2 ? sc_lo : sc_hi, mnp = g < 2 ? mn_lo : mn_hi;
+    sc0 = (float)(scp & 0xFFu);
+    sc1 = (float)(scp >> 8);
+    m0 = (float)(mnp & 0xFFu);
+    m1 = (float)(mnp >> 8);
+}
+
+// One lane's share of a Q4_K row dot product: the 64 weights of pair g of
+// super-block blk (sub-blocks 2g, 2g+1) times 64 fp16 activations xv (order
+// of the activation layout), with XA, XB the sums of those activations per
+// sub-block. Returns sum_i w_i x_i.
+__device__ __forceinline__ float q4k_dot64(const uint8_t *blk, int g, const uint32_t xv[32], float XA, float XB) {
+    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
+    const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * g);
+    const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * g);
+    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    float sA0 = 0.0f, sA1 = 0.0f, sB0 = 0.0f, sB1 = 0.0f;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t w = cw[m], w8 = w >> 8;
+        fma2_f16_f32(sA0, lop3_and_or(w, 0x000F000Fu, DC_MAGIC), xv[4 * m + 0]);
+        fma2_f16_f32(sB0, lop3_and_or(w, 0x00F000F0u, DC_MAGIC), xv[4 * m + 1]);
+        fma2_f16_f32(sA1, lop3_and_or(w8, 0x000F000Fu, DC_MAGIC), xv[4 * m + 2]);
+        fma2_f16_f32(sB1, lop3_and_or(w8, 0x00F000F0u, DC_MAGIC), xv[4 * m + 3]);
+    }
+    float sc0, sc1, m0, m1;
+    q4k_pair_scales(g, hdr.y, hdr.z, hdr.w, sc0, sc1, m0, m1);
+    const float d = half_lo(hdr.x), dmin = half_hi(hdr.x);
+    // SA = sum (1024 + q) x over sub-block 2g, SB = sum (1024 + 16 q) x over 2g+1
+    return d * (sc0 * ((sA0 + sA1) - 1024.0f * XA) + sc1 * 0.0625f * ((sB0 + sB1) - 1024.0f * XB)) -
+           dmin * (m0 * XA + m1 * XB);
+}
+
+// One lane's share of a Q8_0 row dot product: the 32-weight block at blk
+// (fp16 d, int8 q[32]) times 32 fp16 activations hv (natural order) whose sum
+// is hsu. Codes become fp16 1152 + q (bias 128, exponent of 1024).
+__device__ __forceinline__ float q8_0_dot32(const uint8_t *blk, const uint32_t hv[16], float hsu) {
+    const float d = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(blk));
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(blk + 2);
+    const uint32_t *w4 = reinterpret_cast<const uint32_t *>(qa & ~(uintptr_t)3);
+    const uint32_t sh = (uint32_t)(qa & 3) * 8;
+    float acc0 = 0.0f, acc1 = 0.0f;
+    uint32_t prev = w4[0];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t next = w4[j + 1];
+        const uint32_t w = __funnelshift_r(prev, next, sh) ^ 0x80808080u;
+        prev = next;
+        fma2_f16_f32(acc0, prmt(w, 0x64646464u, 0x5140), hv[2 * j]);
+        fma2_f16_f32(acc1, prmt(w, 0x64646464u, 0x7362), hv[2 * j + 1]);
+    }
+    return d * ((acc0 + acc1) - 1152.0f * hsu);
+}
+
+// On an abort, thread 0 waits (bounded) for the bulk copies the producer
+// issued into stages nobody will consume, so none lands after the CTA exits.
+// (Each slot's latest issue completes after the slot's earlier ones.)
+__device__ __forceinline__ void drain_copies(uint64_t *full, int *misc) {
+    if (threadIdx.x != 0) return;
+    const int issued = *reinterpret_cast<volatile int *>(&misc[3]);
+    for (int ci = issued - DC_NSTAGE < 0 ? 0 : issued - DC_NSTAGE; ci < issued; ++ci)
+        mbar_wait(&full[ci % DC_NSTAGE], (uint32_t)(ci / DC_NSTAGE) & 1u);
+}
+
+__device__ __forceinline__ void set_abort(int *misc, uint32_t *status) {
+    atomicOr(status, (uint32_t)MOE_FLAG_WAIT_TIMEOUT);
+    *reinterpret_cast<volatile int *>(&misc[1]) = 1;
+}
+
+// ---------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int G = gridDim.x, c = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = A.T, k = A.k, E = A.E, H = A.H, I = A.I, P = T * k;
+    const DcLayout L = dc_layout(T, k, E, H, I, G, A.stage, A.chunk_cap);
+    const int NS = L.ns, C = L.C, H64 = H / 64, U = I / 32;
+
+    uint8_t *ring = smem + L.ring;
+    uint32_t *xs = reinterpret_cast<uint32_t *>(smem + L.xs);     // per token: [8][H/64] uint4 (half2 words)
+    float *xsum = reinterpret_cast<float *>(smem + L.xsum);       // [T][H/64][2]
+    float *xsc = reinterpret_cast<float *>(smem + L.xsc);
+    unsigned *xmax = reinterpret_cast<unsigned *>(smem + L.xmax);
+    uint32_t *hs = reinterpret_cast<uint32_t *>(smem + L.hs);     // [P][I/2] half2
+    float *hsum = reinterpret_cast<float *>(smem + L.hsum);       // [P][32]
+    float *hsc = reinterpret_cast<float *>(smem + L.hsc);
+    float *ybuf = reinterpret_cast<float *>(smem + L.ybuf);       // [P][rb]
+    float *ckey = reinterpret_cast<float *>(smem + L.ckey);       // [T][C]
+    int *cidx = reinterpret_cast<int *>(smem + L.cidx);
+    float *slm = reinterpret_cast<float *>(smem + L.sm);          // [T][NS] slice max
+    float *sls = reinterpret_cast<float *>(smem + L.ss);          // [T][NS] slice sum exp(l - max)
+    float *selk = reinterpret_cast<float *>(smem + L.selk);       // [P] selected logits
+    int *ids = reinterpret_cast<int *>(smem + L.ids);
+    float *wts = reinterpret_cast<float *>(smem + L.wts);
+    uint8_t *keep = smem + L.keep;
+    int *act = reinterpret_cast<int *>(smem + L.act);             // active experts, ascending
+    int *aoff = reinterpret_cast<int *>(smem + L.aoff);           // [n_act + 1] starts in plist
+    int *plist = reinterpret_cast<int *>(smem + L.plist);         // kept pairs by (expert, pair)
+    DevExpert *dpair = reinterpret_cast<DevExpert *>(smem + L.dpair);   // descriptor of each pair's expert
+    int4 *chunk = reinterpret_cast<int4 *>(smem + L.chunks);   // (a, first row, rows): gate/up, then down
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
+    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
+    int *misc = reinterpret_cast<int *>(smem + L.misc);   // [0] n_act [1] abort [2] flags [3] issued [4] nchunks_a [5] nchunks [6] n_kept
+    unsigned long long *barrier = reinterpret_cast<unsigned long long *>(A.sync + 8);
+    unsigned *hmax_g = reinterpret_cast<unsigned *>(A.sync + DC_SYNC_HMAX);   // [2][DC_MAX_PAIRS]
+
+    // The layer's inputs may come from the previous kernel in the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // barrier generation of this launch (no CTA of it has passed the barrier
+    // yet); first used in the gate/up phase, so the load latency is hidden
+    const unsigned long long gen = ld_acquire_u64(barrier) / (unsigned long long)G;
+
+    if (tid == 0) {
+        for (int s = 0; s < DC_NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+        for (int i = 0; i < 8; ++i) misc[i] = 0;
+    }
+    for (int t = tid; t < T; t += DC_THREADS) xmax[t] = 0u;
+    for (int i = tid; i < T * C; i += DC_THREADS) {      // candidate padding
+        ckey[i] = -INFINITY;
+        cidx[i] = 0x7fffffff;
+    }
+    __syncthreads();
+
+    // ---- 1. each warp sorts one 32-logit slice of one token row; all threads
+    // take activation maxima (16-byte loads of 8 bf16)
+    for (int task = warp; task < T * NS; task += DC_WARPS) {
+        const int t = task / NS, w = task - t * NS;
+        const int e = 32 * w + lane;
+        const float v = e < E ? A.logits[(size_t)t * E + e] : -INFINITY;
+        const bool fin = isfinite(v);
+        float key = fin ? v : -INFINITY;
+        int idx = e < E ? e : 0x7fffffff;
+        if (__any_sync(0xffffffffu, e < E && !fin) && lane == 0)
+            atomicOr(reinterpret_cast<unsigned *>(&misc[2]), (unsigned)MOE_FLAG_NONFINITE_LOGIT);
+        const float m = warp_max(key);
+        const float s = warp_sum((m > -INFINITY && key > -INFINITY) ? expf(key - m) : 0.0f);
+        if (lane == 0) {
+            slm[t * NS + w] = m;
+            sls[t * NS + w] = s;
+        }
+        warp_sort_desc(key, idx);
+        if (lane < k) {
+            ckey[t * C + w * k + lane] = key;
+            cidx[t * C + w * k + lane] = idx;
+        }
+    }
+    for (int i = tid; i < T * (H / 8); i += DC_THREADS) {
+        const int t = i / (H / 8);
+        const uint4 q = reinterpret_cast<const uint4 *>(A.x)[i];
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+        atomicMax(&xmax[t], __float_as_uint(m));
+    }
+    __syncthreads();
+
+    // ---- 2. warp t < T: top-k of row t. The k-th best slice maximum tau is a
+    // lower bound of the row's k-th best logit, so only candidates that tau
+    // does not beat are ranked. Then the router weights, the kept flags and
+    // the (asynchronous) fetch of the selected experts' descriptors.
+    // Warps >= T meanwhile convert the activations.
+    if (warp < T) {
+        const int t = warp;
+        float hk = lane < NS ? ckey[t * C + lane * k] : -INFINITY;
+        int hi = lane < NS ? cidx[t * C + lane * k] : 0x7fffffff;
+        warp_sort_desc(hk, hi);
+        float tk = -INFINITY;
+        int ti = 0x7fffffff;
+        if (NS >= k) {
+            tk = __shfl_sync(0xffffffffu, hk, k - 1);
+            ti = __shfl_sync(0xffffffffu, hi, k - 1);
+        }
+        float *sk = ckey + t * C;   // survivors compacted in place, in chunks of 32
+        int *si = cidx + t * C;
+        int M = 0;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            const int ci = c0 + lane;
+            const float kk = ci < C ? sk[ci] : -INFINITY;
+            const int ii = ci < C ? si[ci] : 0x7fffffff;
+            const bool surv = ci < C && ii < E && !topk_beats(tk, ti, kk, ii);
+            const unsigned b = __ballot_sync(0xffffffffu, surv);
+            __syncwarp();
+            if (surv) {
+                const int dst = M + __popc(b & ((1u << lane) - 1u));
+                sk[dst] = kk;
+                si[dst] = ii;
+            }
+            M += __popc(b);
+            __syncwarp();
+        }
+        for (int m = lane; m < M; m += 32) {
+            const float kk = sk[m];
+            const int ii = si[m];
+            int rank = 0;
+            for (int o = 0; o < M; ++o) rank += topk_beats(sk[o], si[o], kk, ii) ? 1 : 0;
+            if (rank < k) {
+                ids[t * k + rank] = ii;
+                selk[t * k + rank] = kk;
+            }
+        }
+        __syncwarp();
+        const float m = selk[t * k];                     // the row's largest logit (or -inf)
+        const bool any_finite = m > -INFINITY;
+        const float kj = lane < k ? selk[t * k + lane] : -INFINITY;
+        const float ex = (lane < k && any_finite && kj > -INFINITY) ? expf(kj - m) : 0.0f;
+        float denom;
+        if (A.renorm) {
+            denom = warp_sum(ex);
+        } else {
+            float s = 0.0f;
+            for (int w = lane; w < NS; w += 32) {
+                const float mw = slm[t * NS + w];
+                if (any_finite && mw > -INFINITY) s += sls[t * NS + w] * expf(mw - m);
+            }
+            denom = warp_sum(s);
+        }
+        if (lane < k) {
+            const int p = t * k + lane;
+            wts[p] = denom > 0.0f ? ex / denom : 0.0f;
+            const int e = ids[p];
+            bool kp = e >= A.lo && e < A.hi;
+            if (kp && A.fmt_mask != 0xffffffffu) kp = (A.fmt_mask >> A.table[e].gate.fmt) & 1u;
+            keep[p] = kp ? 1 : 0;
+        }
+        constexpr int DW = (int)(sizeof(DevExpert) / 8);
+        for (int i = lane; i < k * DW; i += 32) {
+            const int p = t * k + i / DW, w = i % DW;
+            cp_async8(reinterpret_cast<uint64_t *>(dpair + p) + w,
+                      reinterpret_cast<const uint64_t *>(A.table + ids[p]) + w);
+        }
+        cp_async_commit();
+    } else {
+        // activations -> fp16 (per-token power-of-two scale), ordered as the
+        // Q4_K decoder pairs codes with, stored [v][group] for conflict-free reads
+        for (int task = tid - 32 * T; task < T * H64; task += DC_THREADS - 32 * T) {
+            const int t = task / H64, G64 = task - t * H64;
+            const int sg = pow2_shift(__uint_as_float(xmax[t]));
+            const float up = exp2i(sg);
+            const uint4 *src = reinterpret_cast<const uint4 *>(A.x + (size_t)t * H + 64 * G64);
+            float xf[64];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 q = src[v];
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    xf[8 * v + 2 * i] = __uint_as_float(w[i] << 16) * up;
+                    xf[8 * v + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * up;
+                }
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)t * H / 2);
+            float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+            for (int mm = 0; mm < 8; ++mm) {
+                const int i = 4 * mm;
+                const uint32_t w0 = pack_half2(xf[i], xf[i + 2]), w1 = pack_half2(xf[32 + i], xf[32 + i + 2]);
+                const uint32_t w2 = pack_half2(xf[i + 1], xf[i + 3]), w3 = pack_half2(xf[32 + i + 1], xf[32 + i + 3]);
+                dst[mm * H64 + G64] = make_uint4(w0, w1, w2, w3);
+                sa += half_lo(w0) + half_hi(w0) + half_lo(w2) + half_hi(w2);
+                sb += half_lo(w1) + half_hi(w1) + half_lo(w3) + half_hi(w3);
+            }
+            xsum[((size_t)t * H64 + G64) * 2 + 0] = sa;
+            xsum[((size_t)t * H64 + G64) * 2 + 1] = sb;
+            if (G64 == 0) xsc[t] = exp2i(-sg);
+        }
+    }
+    __syncthreads();
+
+    // ---- 3. bucketing: warp 0 sorts the (expert, pair) keys of the kept pairs
+    // (at most 64: two per lane), which yields the active experts in ascending
+    // order and each expert's pairs in ascending pair order
+    if (warp == 0) {
+        constexpr int SENT = 0x7fffffff;
+        int key[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int p = lane + 32 * r;
+            key[r] = (p < P && keep[p]) ? ((ids[p] << 8) | p) : SENT;
+        }
+#pragma unroll
+        for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                if (stride == 32) {
+                    const int lo = min(key[0], key[1]), hi = max(key[0], key[1]);   // size == 64: ascending
+                    key[0] = lo;
+                    key[1] = hi;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int i = lane + 32 * r;
+                        const int other = __shfl_xor_sync(0xffffffffu, key[r], stride);
+                        const bool asc = (i & size) == 0;
+                        const bool lower = (lane & stride) == 0;
+                        key[r] = (lower == asc) ? min(key[r], other) : max(key[r], other);
+                    }
+                }
+            }
+        }
+        // element i = lane + 32 r holds key[r]; starts of expert runs
+        const int prev0 = __shfl_up_sync(0xffffffffu, key[0], 1);
+        const int prev1 = __shfl_up_sync(0xffffffffu, key[1], 1);
+        const int last0 = __shfl_sync(0xffffffffu, key[0], 31);
+        const int pk[2] = {lane == 0 ? -1 : prev0, lane == 0 ? last0 : prev1};
+        bool start[2], valid[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            valid[r] = key[r] != SENT;
+            start[r] = valid[r] && (pk[r] < 0 || (pk[r] >> 8) != (key[r] >> 8));
+        }
+        const unsigned s0 = __ballot_sync(0xffffffffu, start[0]), s1 = __ballot_sync(0xffffffffu, start[1]);
+        const unsigned v0 = __ballot_sync(0xffffffffu, valid[0]), v1 = __ballot_sync(0xffffffffu, valid[1]);
+        const int n_kept = __popc(v0) + __popc(v1), n_act = __popc(s0) + __popc(s1);
+        const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int i = lane + 32 * r;
+            if (valid[r]) plist[i] = key[r] & 0xff;
+            if (start[r]) {
+                const int a = r == 0 ? __popc(s0 & below) : __popc(s0) + __popc(s1 & below);
+                act[a] = key[r] >> 8;
+                aoff[a] = i;
+            }
+        }
+        if (lane == 0) {
+            aoff[n_act] = n_kept;
+            misc[0] = n_act;
+            misc[6] = n_kept;
+        }
+    }
+    __syncthreads();
+    const int n_act = misc[0];
+    // this CTA's share: gate/up row pairs [a_begin, a_end) over (active expert, row)
+    const int NA = n_act * I;
+    const int a_begin = (int)((long long)NA * c / G), a_end = (int)((long long)NA * (c + 1) / G);
+    const int b0 = (int)((long long)H * c / G), b1 = (int)((long long)H * (c + 1) / G);
+    const int nrows_b = b1 - b0;
+    if (warp == 0) {
+        // the chunk table: gate/up chunks of at most rows_a row pairs, never
+        // crossing an expert (lane j: the j-th expert segment of the share);
+        // then, per active expert, the CTA's down rows in chunks of rows_b
+        const int a_first = a_begin / I, a_last = a_end > a_begin ? (a_end - 1) / I : a_first - 1;
+        int total = 0;
+        for (int seg0 = a_first; seg0 <= a_last; seg0 += 32) {
+            const int a = seg0 + lane;
+            int len = 0, rs = 0;
+            if (a <= a_last) {
+                rs = max(a_begin, a * I);
+                len = min(a_end, (a + 1) * I) - rs;
+            }
+            const int nch = (len + A.rows_a - 1) / A.rows_a;
+            int inc = nch;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += v;
+            }
+            int n = total + inc - nch;
+            for (int j = 0; j < nch && n < A.chunk_cap; ++j, ++n) {
+                const int r = rs + j * A.rows_a;
+                chunk[n] = make_int4(a, r - a * I, min(A.rows_a, rs + len - r), 0);
+            }
+            total += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        const int nb = (nrows_b + A.rows_b - 1) / A.rows_b;
+        for (int i = lane; i < n_act * nb; i += 32) {
+            const int a = i / nb, j = i - a * nb;
+            if (total + i < A.chunk_cap) chunk[total + i] = make_int4(a, j * A.rows_b, min(A.rows_b, nrows_b - j * A.rows_b), 1);
+        }
+        if (lane == 0) {
+            misc[4] = min(total, A.chunk_cap);
+            misc[5] = min(total + n_act * nb, A.chunk_cap);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    const int nchunks_a = misc[4], nchunks = misc[5];
+    // the next kernel in the stream may begin its launch; it waits for this
+    // grid's completion before reading anything this grid writes
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    if (warp == DC_CW) {
+        // ---------------- producer: one thread streams the CTA's rows
+        if (lane == 0) {
+            for (int ci = 0; ci < nchunks; ++ci) {
+                const int s = ci % DC_NSTAGE;
+                if (ci >= DC_NSTAGE && !mbar_wait(&empty[s], (uint32_t)((ci / DC_NSTAGE) - 1) & 1u)) {
+                    set_abort(misc, A.status);
+                    break;
+                }
+                uint8_t *dst = ring + (size_t)s * A.stage;
+                const int4 ch = chunk[ci];
+                const DevExpert &X = dpair[plist[aoff[ch.x]]];
+                if (ci < nchunks_a) {
+                    const uint32_t bg = (uint32_t)(ch.z * X.gate.stride), bu = (uint32_t)(ch.z * X.up.stride);
+                    mbar_expect_tx(&full[s], bg + bu);
+                    bulk_g2s(dst, X.gate.data + (size_t)ch.y * X.gate.stride, bg, &full[s]);
+                    bulk_g2s(dst + bg, X.up.data + (size_t)ch.y * X.up.stride, bu, &full[s]);
+                } else {
+                    const uint32_t bd = (uint32_t)(ch.z * X.down.stride);
+                    mbar_expect_tx(&full[s], bd);
+                    bulk_g2s(dst, X.down.data + (size_t)(b0 + ch.y) * X.down.stride, bd, &full[s]);
+                }
+                *reinterpret_cast<volatile int *>(&misc[3]) = ci + 1;   // chunks issued
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumers: chunk ci -> warp ci % 16 = the warp owning its
+    // ring slot, so a warp waits on a slot at most one phase ahead
+    unsigned *hmax = hmax_g + (gen & 1) * DC_MAX_PAIRS;
+    for (int ci = warp; ci < nchunks_a; ci += DC_CW) {
+        const int s = ci % DC_NSTAGE;
+        if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+            if (lane == 0) set_abort(misc, A.status);
+            break;
+        }
+        const int4 ch = chunk[ci];
+        const int n = ch.z, r0 = ch.y;
+        const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
+        const DevExpert &X = dpair[plist[q0]];
+        const uint8_t *stage = ring + (size_t)s * A.stage;
+        const int sg = (int)X.gate.stride, su = (int)X.up.stride;
+        const uint8_t *ubase = stage + n * sg;
+        for (int qi = 0; qi < ne; ++qi) {
+            const int p = plist[q0 + qi], t = p / k;
+            float part[2 * DC_ROWS_A];
+#pragma unroll
+            for (int i = 0; i < 2 * DC_ROWS_A; ++i) part[i] = 0.0f;
+            const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs + (size_t)t * H / 2);
+            for (int G64 = lane; G64 < H64; G64 += 32) {
+                const int sb = G64 >> 2, g = G64 & 3;
+                uint32_t xv[32];
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                    const uint4 q = xv4[v * H64 + G64];
+                    xv[4 * v + 0] = q.x;
+                    xv[4 * v + 1] = q.y;
+                    xv[4 * v + 2] = q.z;
+                    xv[4 * v + 3] = q.w;
+                }
+                const float XA = xsum[((size_t)t * H64 + G64) * 2 + 0];
+                const float XB = xsum[((size_t)t * H64 + G64) * 2 + 1];
+#pragma unroll
+                for (int i = 0; i < 2 * DC_ROWS_A; ++i) {
+                    const int row = i % DC_ROWS_A;
+                    if (row < n) {
+                        const uint8_t *blk = (i < DC_ROWS_A ? stage + row * sg : ubase + row * su) + 144 * sb;
+                        part[i] += q4k_dot64(blk, g, xv, XA, XB);
+                    }
+                }
+            }
+            // part[0..3] gate rows, part[4..7] up rows -> value j in lanes 4j .. 4j+3
+            const float tot = warp_reduce8(part) * xsc[t];
+            const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
+            if (lane < 16 && (lane & 3) == 0 && (lane >> 2) < n) {
+                const float hv = silu_f32(tot) * upv;
+                A.h[(size_t)p * I + r0 + (lane >> 2)] = hv;
+                atomicMax(&hmax[p], __float_as_uint(fabsf(hv)));
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- grid barrier: every CTA's h and |h| maxima are complete and visible
+    consumer_sync();
+    if (tid == 0) {
+        __threadfence();
+        red_release_add(barrier, 1ull);
+        const unsigned long long target = (gen + 1ull) * (unsigned long long)G;
+        uint32_t it = 0;
+        while (ld_acquire_u64(barrier) < target) {
+            if (++it > WAIT_LIMIT) {
+                set_abort(misc, A.status);
+                break;
+            }
+        }
+        __threadfence();
+    }
+    consumer_sync();
+    if (*reinterpret_cast<volatile int *>(&misc[1])) {
+        drain_copies(full, misc);
+        return;
+    }
+
+    if (nrows_b > 0) {
+        // ---- h of every kept pair -> fp16 with a per-pair power-of-two scale;
+        // one warp per pair, lane u converts and sums 32-column unit u
+        for (int p = warp; p < P; p += DC_CW) {
+            if (!keep[p]) continue;
+            const float mx = __uint_as_float(__ldcg(&hmax[p]));
+            float4 v[8];
+            if (lane < U) {
+                const float4 *src = reinterpret_cast<const float4 *>(A.h + (size_t)p * I + 32 * lane);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + i);
+            }
+            const int sgm = pow2_shift(mx);
+            const float up = exp2i(sgm);
+            if (lane < U) {
+                uint4 *dst = reinterpret_cast<uint4 *>(hs + ((size_t)p * I + 32 * lane) / 2);
+                float sum = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t w0 = pack_half2(v[2 * i].x * up, v[2 * i].y * up);
+                    const uint32_t w1 = pack_half2(v[2 * i].z * up, v[2 * i].w * up);
+                    const uint32_t w2 = pack_half2(v[2 * i + 1].x * up, v[2 * i + 1].y * up);
+                    const uint32_t w3 = pack_half2(v[2 * i + 1].z * up, v[2 * i + 1].w * up);
+                    dst[i] = make_uint4(w0, w1, w2, w3);
+                    sum += half_lo(w0) + half_hi(w0) + half_lo(w1) + half_hi(w1) + half_lo(w2) + half_hi(w2) +
+                           half_lo(w3) + half_hi(w3);
+                }
+                hsum[p * 32 + lane] = sum;
+            }
+            if (lane == 0) hsc[p] = exp2i(-sgm);
+        }
+        consumer_sync();
+
+        // ---- down: this CTA's output rows [b0, b1) of every routed expert
+        for (int ci = nchunks_a + ((warp - nchunks_a) % DC_CW + DC_CW) % DC_CW; ci < nchunks; ci += DC_CW) {
+            const int s = ci % DC_NSTAGE;
+            if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+                if (lane == 0) set_abort(misc, A.status);
+                break;
+            }
+            const int4 ch = chunk[ci];
+            const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
+            const DevMatrix &D = dpair[plist[q0]].down;
+            const uint8_t *stage = ring + (size_t)s * A.stage;
+            const int sd = (int)D.stride, rbase = ch.y, nr = ch.z;
+            for (int qi = 0; qi < ne; ++qi) {
+                const int p = plist[q0 + qi];
+                uint32_t hv[16];
+                float hsu = 0.0f;
+                if (lane < U) {
+                    const uint4 *h4 = reinterpret_cast<const uint4 *>(hs + ((size_t)p * I + 32 * lane) / 2);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        const uint4 q = h4[v];
+                        hv[4 * v] = q.x;
+                        hv[4 * v + 1] = q.y;
+                        hv[4 * v + 2] = q.z;
+                        hv[4 * v + 3] = q.w;
+                    }
+                    hsu = hsum[p * 32 + lane];
+                }
+                const float scale = hsc[p];
+                for (int rb = 0; rb < nr; rb += 4) {
+                    float part[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        part[j] = 0.0f;
+                        if (lane < U && rb + j < nr)
+                            part[j] = q8_0_dot32(stage + (size_t)(rb + j) * sd + 34 * lane, hv, hsu);
+                    }
+                    const float tot = warp_reduce4(part);   // row rb + j in lanes 8j .. 8j+7
+                    const int j = lane >> 3;
+                    if ((lane & 7) == 0 && rb + j < nr) ybuf[p * L.rb + rbase + rb + j] = tot * scale;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+    consumer_sync();
+    if (*reinterpret_cast<volatile int *>(&misc[1])) {
+        drain_copies(full, misc);
+        return;
+    }
+
+    // ---- combine in ascending slot order
+    for (int i = tid; i < T * nrows_b; i += DC_CW * 32) {
+        const int t = i / nrows_b, rr = i - t * nrows_b;
+        float acc = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int p = t * k + j;
+            if (keep[p]) acc = fmaf(wts[p], ybuf[p * L.rb + rr], acc);
+        }
+        A.out[(size_t)t * H + b0 + rr] = acc;
+    }
+
+    // CTA 0 publishes the routing results to the workspace and clears the
+    // |h| buffer of the next launch (this launch does not use it)
+    if (c == 0) {
+        const int n_kept = misc[6];
+        for (int p = tid; p < P; p += DC_CW * 32) {
+            A.ids_out[p] = ids[p];
+            A.wts_out[p] = wts[p];
+            if (!keep[p]) A.pos_out[p] = -1;
+        }
+        for (int e = tid; e <= E; e += DC_CW * 32) {
+            int lo = 0, hi = n_act;          // first active expert >= e
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (act[mid] < e) lo = mid + 1; else hi = mid;
+            }
+            A.offsets_out[e] = aoff[lo];
+        }
+        for (int a = tid; a < n_act; a += DC_CW * 32) A.active_out[1 + a] = act[a];
+        if (tid == 0) A.active_out[0] = n_act;
+        for (int q = tid; q < n_kept; q += DC_CW * 32) {
+            A.pairs_out[q] = plist[q];
+            A.pos_out[plist[q]] = q;
+        }
+        for (int p = tid; p < DC_MAX_PAIRS; p += DC_CW * 32) hmax_g[((gen + 1) & 1) * DC_MAX_PAIRS + p] = 0u;
+        if (tid == 0 && misc[2]) atomicOr(A.status, (uint32_t)misc[2]);
+    }
+}
+
+int g_sm_count[64] = {};
+bool g_attr_done[64] = {};
+
+}  // namespace
+
+int sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 64 && g_sm_count[dev]) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) g_sm_count[dev] = n;
+    return n;
+}
+
+struct DcPlan {
+    int stage, rows_a, rows_b, chunk_cap;
+    size_t smem;
+};
+
+// Ring slot size, rows per chunk and shared-memory bytes of the fused decode
+// kernel for a layer shape; smem = 0 if the shape does not fit.
+DcPlan decode_fused_plan(int T, int k, int E, int H, int I, int G, int64_t gu_stride, int64_t dn_stride) {
+    DcPlan pl{0, 0, 0, 0, 0};
+    const size_t limit = 227 * 1024 - 1024;   // opt-in limit less the kernel's static shared memory
+    const int64_t rowpair = 2 * gu_stride;
+    const int rb = (H + G - 1) / G;
+    for (int stage = DC_STAGE_MAX; stage >= 2048; stage -= 512) {
+        const int rows_a = (int)std::min<int64_t>(DC_ROWS_A, stage / rowpair);
+        const int rows_b = (int)std::min<int64_t>(rb, stage / dn_stride);
+        if (rows_a < 1 || rows_b < 1) return pl;
+        const int P = T * k;
+        const int share = P * I / G + 1;
+        const int cap = share / rows_a + P + 2 + P * ((rb + rows_b - 1) / rows_b);
+        const DcLayout L = dc_layout(T, k, E, H, I, G, stage, cap);
+        if (L.total <= limit) {
+            pl.stage = stage;
+            pl.rows_a = rows_a;
+            pl.rows_b = rows_b;
+            pl.chunk_cap = cap;
+            pl.smem = L.total;
+            return pl;
+        }
+    }
+    return pl;
+}
+
+// Whether the fused decode kernel handles this layer shape.
+bool decode_fused_eligible(int T, int k, int E, int H, int I, uint32_t gateup_formats, uint32_t down_formats,
+                           int64_t gu_stride, int64_t dn_stride) {
+    if (T < 1 || T > DC_WARPS - 1 || T * k > DC_MAX_PAIRS || E > MOE_MAX_EXPERTS || E > 2 * DC_THREADS) return false;
+    if (gateup_formats != (1u << MOE_Q4_K) || down_formats != (1u << MOE_Q8_0)) return false;
+    if (H % 64 != 0 || I % 32 != 0 || I / 32 > 32) return false;
+    const int G = sm_count();
+    if (G <= 0) return false;
+    return decode_fused_plan(T, k, E, H, I, G, gu_stride, dn_stride).smem != 0;
+}
+
+cudaError_t launch_decode_fused(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
+                                int64_t dn_stride, int renorm, int lo, int hi, uint32_t fmt_mask, const float *logits,
+                                const uint16_t *x, float *out, float *h, int32_t *ids, float *wts, int32_t *offsets,
+                                int32_t *active, int32_t *pairs, int32_t *pos, unsigned char *sync, uint32_t *status,
+                                cudaStream_t s) {
+    const int G = sm_count();
+    const DcPlan pl = decode_fused_plan(T, k, E, H, I, G, gu_stride, dn_stride);
+    const size_t smem = pl.smem;
+    if (G <= 0 || smem == 0) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 64 || !g_attr_done[dev]) {
+        int optin = 0;
+        err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (err != cudaSuccess) return err;
+        cudaFuncAttributes fa;
+        err = cudaFuncGetAttributes(&fa, decode_fused_kernel);
+        if (err != cudaSuccess) return err;
+        err = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   optin - (int)fa.sharedSizeBytes);
+        if (err != cudaSuccess) return err;
+        if (dev < 64) g_attr_done[dev] = true;
+    }
+    DcArgs A;
+    A.table = table;
+    A.E = E;
+    A.H = H;
+    A.I = I;
+    A.T = T;
+    A.k = k;
+    A.renorm = renorm;
+    A.lo = lo;
+    A.hi = hi;
+    A.fmt_mask = fmt_mask;
+    A.logits = logits;
+    A.x = x;
+    A.out = out;
+    A.h = h;
+    A.ids_out = ids;
+    A.wts_out = wts;
+    A.offsets_out = offsets;
+    A.active_out = active;
+    A.pairs_out = pairs;
+    A.pos_out = pos;
+    A.sync = sync;
+    A.status = status;
+    A.stage = pl.stage;
+    A.rows_a = pl.rows_a;
+    A.rows_b = pl.rows_b;
+    A.chunk_cap = pl.chunk_cap;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G);
+    cfg.blockDim = dim3(DC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel, A);
+}
+
+}  // namespace moe

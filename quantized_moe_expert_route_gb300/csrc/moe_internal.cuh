@@ -21,6 +21,11 @@ struct DevExpert {
     DevMatrix gate, up, down;
 };
 
+// Bytes at the start of a workspace that must be zero before its first use:
+// the device status word (offset 0), the fused kernel's grid-barrier counter
+// (offset 8) and its per-pair |h| maxima (offset 256).
+constexpr size_t SYNC_BYTES = 1024;
+
 // Workspace layout of moe_ffn_forward; offsets in bytes from the workspace base.
 struct WsLayout {
     size_t status, ids, wts, offsets, active, pairs, pos, h, y, total;
@@ -33,7 +38,7 @@ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
     size_t P = (size_t)T * k;
-    L.status = take(256);
+    L.status = take(SYNC_BYTES);
     L.ids = take(P * 4);
     L.wts = take(P * 4);
     L.offsets = take((size_t)(E + 1) * 4);
@@ -108,5 +113,87 @@ __device__ __forceinline__ float e8m0_half_scale(uint32_t e) {
 }
 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+// (key, idx) a ranks before (key, idx) b: larger key, or equal key and lower index.
+__device__ __forceinline__ bool topk_beats(float ka, int ia, float kb, int ib) {
+    return ka > kb || (ka == kb && ia < ib);
+}
+
+// Softmax top-k of one row of E logits by one warp (E <= 32 * V, k <= 32).
+// Selection compares the raw fp32 logits (largest first, equal logits to the
+// lower expert index); non-finite logits rank last with probability 0. Lane
+// j < k receives slot j's expert id and weight: its softmax probability,
+// divided by the sum over the k selected ones when renorm != 0. Returns true
+// (in every lane) if the row holds a non-finite logit.
+template <int V>
+__device__ __forceinline__ bool warp_topk(const float *__restrict__ lr, int E, int k, int renorm, int &sel_idx,
+                                          float &weight) {
+    const int lane = threadIdx.x & 31;
+    float key[V];
+    bool nonfinite = false;
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+        const int e = lane + 32 * i;
+        const float v = e < E ? lr[e] : -INFINITY;
+        const bool fin = isfinite(v);
+        if (e < E && !fin) nonfinite = true;
+        key[i] = fin ? v : -INFINITY;
+        m = fmaxf(m, key[i]);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const bool any_finite = m > -INFINITY;
+    nonfinite = __any_sync(0xffffffffu, nonfinite);
+
+    uint32_t taken = 0;
+    float sel_key = -INFINITY;
+    sel_idx = 0;
+    for (int j = 0; j < k; ++j) {
+        float bk = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !(taken & (1u << i)) && topk_beats(key[i], e, bk, bi)) {
+                bk = key[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (topk_beats(ok, oi, bk, bi)) {
+                bk = ok;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            sel_key = bk;
+            sel_idx = bi;
+        }
+    }
+    const float ex = (lane < k && any_finite && sel_key > -INFINITY) ? expf(sel_key - m) : 0.0f;
+    float denom;
+    if (renorm) {
+        denom = ex;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
+    } else {
+        float s = 0.0f;
+        if (any_finite) {
+#pragma unroll
+            for (int i = 0; i < V; ++i)
+                if (key[i] > -INFINITY) s += expf(key[i] - m);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        denom = s;
+    }
+    weight = denom > 0.0f ? ex / denom : 0.0f;
+    return nonfinite;
+}
 
 }  // namespace moe

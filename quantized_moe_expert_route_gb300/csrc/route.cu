@@ -14,11 +14,6 @@ namespace {
 
 constexpr int ROUTE_WARPS = 8;
 
-// (key, idx) a beats (key, idx) b: larger key, or equal key and lower index.
-__device__ __forceinline__ bool beats(float ka, int ia, float kb, int ib) {
-    return ka > kb || (ka == kb && ia < ib);
-}
-
 template <int V>  // logits per lane: E <= 32 * V
 __global__ void __launch_bounds__(ROUTE_WARPS * 32)
 route_topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm, int32_t *__restrict__ ids,
@@ -26,77 +21,12 @@ route_topk_kernel(const float *__restrict__ logits, int T, int E, int k, int ren
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * ROUTE_WARPS + (threadIdx.x >> 5);
     if (row >= T) return;
-    const float *lr = logits + (size_t)row * E;
-
-    float key[V];
-    bool nonfinite = false;
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < V; ++i) {
-        int e = lane + 32 * i;
-        float v = e < E ? lr[e] : -INFINITY;
-        bool fin = isfinite(v);
-        if (e < E && !fin) nonfinite = true;
-        key[i] = fin ? v : -INFINITY;
-        m = fmaxf(m, key[i]);
-    }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const bool any_finite = m > -INFINITY;
-    nonfinite = __any_sync(0xffffffffu, nonfinite);
-
-    // top-k by repeated warp arg-max over the untaken entries
-    uint32_t taken = 0;
-    float sel_key = -INFINITY;
-    int sel_idx = 0;
-    for (int j = 0; j < k; ++j) {
-        float bk = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            int e = lane + 32 * i;
-            if (e < E && !(taken & (1u << i)) && beats(key[i], e, bk, bi)) {
-                bk = key[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            float ok = __shfl_xor_sync(0xffffffffu, bk, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (beats(ok, oi, bk, bi)) {
-                bk = ok;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) {
-            sel_key = bk;
-            sel_idx = bi;
-        }
-    }
-
-    // weights
-    float ex = (lane < k && any_finite && sel_key > -INFINITY) ? expf(sel_key - m) : 0.0f;
-    float denom;
-    if (renorm) {
-        denom = ex;
-#pragma unroll
-        for (int o = 16; o; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
-    } else {
-        float s = 0.0f;
-        if (any_finite) {
-#pragma unroll
-            for (int i = 0; i < V; ++i)
-                if (key[i] > -INFINITY) s += expf(key[i] - m);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        denom = s;
-    }
+    int sel;
+    float w;
+    const bool nonfinite = warp_topk<V>(logits + (size_t)row * E, E, k, renorm, sel, w);
     if (lane < k) {
-        ids[(size_t)row * k + lane] = sel_idx;
-        wts[(size_t)row * k + lane] = denom > 0.0f ? ex / denom : 0.0f;
+        ids[(size_t)row * k + lane] = sel;
+        wts[(size_t)row * k + lane] = w;
     }
     if (nonfinite && lane == 0 && status) atomicOr(status, (uint32_t)MOE_FLAG_NONFINITE_LOGIT);
 }

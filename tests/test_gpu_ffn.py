@@ -239,3 +239,90 @@ def test_full_mtp6(M):
 
 def test_full_prefill_sampled(M):
     full_layer_parity(M, "prefill2048", tokens_to_check=[0, 1, 777, 2047])
+
+
+# --------------------------------------------------------------- fused decode path
+def run_path(M, L, path, k=None, options=None):
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    opt = options or M.make_options(n_experts=L.cfg.n_experts, path=path)
+    assert M.ffn_path(table, L.cfg.tokens, k or L.cfg.k, opt) == path
+    ws = M.Workspace(table, L.cfg.tokens, k or L.cfg.k)
+    out = M.ffn_forward(table, x, logits, k or L.cfg.k, ws=ws, options=opt)
+    torch.cuda.synchronize()
+    return out.cpu().numpy(), table, ws
+
+
+@pytest.mark.parametrize("T,k,E,H,I", [(1, 10, 64, 2048, 640), (2, 4, 16, 256, 64), (3, 8, 40, 512, 96),
+                                       (6, 10, 512, 2048, 640), (1, 1, 4, 256, 32), (5, 12, 20, 1024, 1024)])
+def test_fused_decode_small(M, T, k, E, H, I):
+    cfg = synth.LayerConfig("fz", E, k, H, I, T, "q4k", True, 7 * T + E)
+    L = synth.make_layer(cfg, 0)
+    out, table, ws = run_path(M, L, M.PATH_FUSED)
+    ref = offn.moe_ffn(L.experts, L.x_bf16, L.logits, k)
+    assert_parity(out, ref, f"fused T={T} E={E}")
+    # the routing it publishes is the oracle's, bit for bit
+    from oracle import router as orouter, bucket as obucket
+    rid, rw, _ = orouter.route_topk(L.logits, k)
+    R = ws.routing()
+    np.testing.assert_array_equal(R["ids"].cpu().numpy(), rid)
+    roff, rpairs, rpos, ract, _ = obucket.bucket(rid, E)
+    np.testing.assert_array_equal(R["offsets"].cpu().numpy(), roff)
+    act = R["active"].cpu().numpy()
+    np.testing.assert_array_equal(act[1:1 + act[0]], ract)
+    np.testing.assert_array_equal(R["pos"].cpu().numpy(), rpos)
+    assert ws.read_status() == 0
+
+
+def test_fused_decode_filters_and_reproducible(M):
+    cfg = synth.LayerConfig("ff", 24, 6, 512, 128, 4, "q4k", True, 99)
+    L = synth.make_layer(cfg, 0)
+    E, k = cfg.n_experts, cfg.k
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, cfg.hidden, cfg.inter)
+    ref = offn.moe_ffn(L.experts, L.x_bf16, L.logits, k)
+    ws = M.Workspace(table, cfg.tokens, k)
+    full = M.ffn_forward(table, x, logits, k, ws=ws, options=M.make_options(n_experts=E, path=M.PATH_FUSED))
+    again = M.ffn_forward(table, x, logits, k, ws=ws, options=M.make_options(n_experts=E, path=M.PATH_FUSED))
+    assert torch.equal(full, again)
+    assert_parity(full.cpu().numpy(), ref, "fused full")
+    lo = M.ffn_forward(table, x, logits, k, ws=ws,
+                       options=M.make_options(expert_lo=0, expert_hi=10, n_experts=E, path=M.PATH_FUSED))
+    hi = M.ffn_forward(table, x, logits, k, ws=ws,
+                       options=M.make_options(expert_lo=10, expert_hi=E, n_experts=E, path=M.PATH_FUSED))
+    assert_parity(lo.cpu().numpy() + hi.cpu().numpy(), ref, "fused range split")
+    nr = M.ffn_forward(table, x, logits, k, ws=ws,
+                       options=M.make_options(renormalize=False, n_experts=E, path=M.PATH_FUSED))
+    assert_parity(nr.cpu().numpy(), offn.moe_ffn(L.experts, L.x_bf16, L.logits, k, renormalize=False), "fused nr")
+    lg = logits.clone()
+    lg[2, 5] = float("nan")
+    M.ffn_forward(table, x, lg, k, ws=ws, options=M.make_options(n_experts=E, path=M.PATH_FUSED))
+    assert ws.read_status() & M.FLAG_NONFINITE_LOGIT
+
+
+def test_fused_path_rejects_ineligible(M):
+    L = synth.make_layer(small_cfg(tiers="mixed", T=3, seed=5), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    opt = M.make_options(n_experts=L.cfg.n_experts, path=M.PATH_FUSED)
+    assert M.ffn_path(table, 3, L.cfg.k, opt) == -1
+    with pytest.raises(M.MoeError) as ei:
+        M.ffn_forward(table, x, logits, L.cfg.k, options=opt)
+    assert ei.value.code == 8
+    assert M.ffn_path(table, 3, L.cfg.k) == M.PATH_GEMV
+
+
+def test_full_decode1_gemv_path(M):
+    """The general grouped GEMV path on the full-size single-token layer."""
+    from synth import gpu as sgpu
+    cfg = synth.CONFIGS["decode1"]
+    DL = sgpu.make_device_layer(cfg, 2)
+    table = M.WeightTable(DL.experts, cfg.hidden, cfg.inter)
+    opt = M.make_options(n_experts=cfg.n_experts, path=M.PATH_GEMV)
+    out = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k, options=opt).cpu().numpy()
+    fused = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k).cpu().numpy()
+    assert M.ffn_path(table, 1, cfg.k) == M.PATH_FUSED
+    lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
+    ref = offn.moe_ffn(lazy, DL.x_host, DL.logits_host, cfg.k, gate_formats=lazy.gate_formats())
+    assert_parity(out, ref, "decode1 gemv")
+    assert_parity(fused, ref, "decode1 fused")
