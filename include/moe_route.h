@@ -120,6 +120,14 @@ typedef struct {
     uint32_t down_formats;     /* bit (1 << format) for every down format in use */
     int64_t max_gateup_stride; /* largest gate/up row stride, bytes */
     int64_t max_down_stride;   /* largest down row stride, bytes */
+    /* Set when every expert has the formats and strides of expert 0 and its
+     * gate/up/down data sit at expert 0's plus e * uniform_step[0/1/2] bytes
+     * (experts stored as one strided tensor): kernels then compute the
+     * descriptors instead of reading them. */
+    int32_t uniform_layout;
+    int32_t reserved2;
+    moe_expert uniform_base;
+    int64_t uniform_step[3];
 } moe_weight_table;
 
 /* Paths for moe_options.path. */

@@ -54,7 +54,9 @@ class WeightTableC(ctypes.Structure):
                 ("device_table", ctypes.c_void_p), ("formats_present", ctypes.c_uint32),
                 ("prepared", ctypes.c_uint32), ("gateup_formats", ctypes.c_uint32),
                 ("down_formats", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
-                ("max_down_stride", ctypes.c_int64)]
+                ("max_down_stride", ctypes.c_int64), ("uniform_layout", ctypes.c_int32),
+                ("reserved2", ctypes.c_int32), ("uniform_base", Expert),
+                ("uniform_step", ctypes.c_int64 * 3)]
 
 
 class Options(ctypes.Structure):
@@ -146,7 +148,7 @@ class WeightTable:
                 self._keep.append(data)
                 setattr(arr[e], name, Matrix(fmt, rows, cols, 0, stride, data.data_ptr()))
         self._arr = arr
-        self.c = WeightTableC(E, hidden, inter, 0, ctypes.cast(arr, ctypes.POINTER(Expert)), None, 0, 0, 0, 0, 0, 0)
+        self.c = WeightTableC(E, hidden, inter, 0, ctypes.cast(arr, ctypes.POINTER(Expert)))
         nbytes = L.moe_table_device_bytes(E)
         if nbytes == 0:
             raise ValueError(f"bad expert count {E}")

@@ -21,8 +21,8 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
                              uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
 bool decode_fused_eligible(int T, int k, int E, int H, int I, uint32_t gateup_formats, uint32_t down_formats,
                            int64_t gu_stride, int64_t dn_stride);
-cudaError_t launch_decode_fused(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
-                                int64_t dn_stride, int renorm, int lo, int hi, uint32_t fmt_mask, const float *logits,
+cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *W, int T, int k, int E, int H, int I,
+                                int64_t gu_stride, int64_t dn_stride, int renorm, int lo, int hi, uint32_t fmt_mask, const float *logits,
                                 const uint16_t *x, float *out, float *h, int32_t *ids, float *wts, int32_t *offsets,
                                 int32_t *active, int32_t *pairs, int32_t *pos, unsigned char *sync, uint32_t *status,
                                 cudaStream_t s);
@@ -150,6 +150,26 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     if (err != cudaSuccess) return cuda_fail(err);
     err = cudaStreamSynchronize(stream);
     if (err != cudaSuccess) return cuda_fail(err);
+    // uniform layout: experts at a constant step with identical formats and strides
+    int uniform = 1;
+    int64_t step[3] = {0, 0, 0};
+    if (E > 1) {
+        const moe_matrix *m0[3] = {&W->experts[0].gate, &W->experts[0].up, &W->experts[0].down};
+        const moe_matrix *m1[3] = {&W->experts[1].gate, &W->experts[1].up, &W->experts[1].down};
+        for (int i = 0; i < 3; ++i)
+            step[i] = (int64_t)((const char *)m1[i]->data - (const char *)m0[i]->data);
+        for (int e = 0; e < E && uniform; ++e) {
+            const moe_matrix *me[3] = {&W->experts[e].gate, &W->experts[e].up, &W->experts[e].down};
+            for (int i = 0; i < 3; ++i) {
+                if (me[i]->format != m0[i]->format || me[i]->row_stride_bytes != m0[i]->row_stride_bytes ||
+                    (const char *)me[i]->data != (const char *)m0[i]->data + step[i] * e)
+                    uniform = 0;
+            }
+        }
+    }
+    W->uniform_layout = uniform;
+    W->uniform_base = W->experts[0];
+    for (int i = 0; i < 3; ++i) W->uniform_step[i] = step[i];
     W->device_table = device_buf;
     W->formats_present = present;
     W->gateup_formats = gu_present;
@@ -227,7 +247,7 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     cudaError_t err;
     if (path == MOE_PATH_FUSED) {
         if (events && (err = record_timing_event(events[0], stream)) != cudaSuccess) return cuda_fail(err);
-        err = launch_decode_fused(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, o.renormalize,
+        err = launch_decode_fused(table, W, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, o.renormalize,
                                   o.expert_lo, o.expert_hi, o.format_mask, logits,
                                   x, out, h, ids, wts, offsets, active, pairs, pos,
                                   reinterpret_cast<unsigned char *>(base + L.status), status, stream);

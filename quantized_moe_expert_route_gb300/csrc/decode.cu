@@ -112,6 +112,9 @@ struct DcArgs {
     int stage;                      // bytes per ring slot
     int rows_a, rows_b;             // gate/up row pairs per chunk, down rows per chunk
     int chunk_cap;                  // capacity of the shared-memory chunk table
+    int uniform;                    // experts at a constant step: descriptor = u + e * ustep
+    DevExpert u;
+    long long ustep[3];
 };
 
 // ---------------------------------------------------------------- small PTX helpers
@@ -232,6 +235,17 @@ __device__ __forceinline__ float warp_reduce8(const float v[8]) {
         x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
     }
     float y = (b4 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b4 ? x[0] : x[1], 4);
+    y += __shfl_xor_sync(0xffffffffu, y, 2);
+    y += __shfl_xor_sync(0xffffffffu, y, 1);
+    return y;
+}
+
+// Sums of 2 per-lane values over the warp: value 0 ends in lanes 0..15, value 1 in 16..31.
+__device__ __forceinline__ float warp_reduce2(const float v[2]) {
+    const bool b16 = threadIdx.x & 16;
+    float y = (b16 ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, b16 ? v[0] : v[1], 16);
+    y += __shfl_xor_sync(0xffffffffu, y, 8);
+    y += __shfl_xor_sync(0xffffffffu, y, 4);
     y += __shfl_xor_sync(0xffffffffu, y, 2);
     y += __shfl_xor_sync(0xffffffffu, y, 1);
     return y;
@@ -495,13 +509,26 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             if (kp && A.fmt_mask != 0xffffffffu) kp = (A.fmt_mask >> A.table[e].gate.fmt) & 1u;
             keep[p] = kp ? 1 : 0;
         }
-        constexpr int DW = (int)(sizeof(DevExpert) / 8);
-        for (int i = lane; i < k * DW; i += 32) {
-            const int p = t * k + i / DW, w = i % DW;
-            cp_async8(reinterpret_cast<uint64_t *>(dpair + p) + w,
-                      reinterpret_cast<const uint64_t *>(A.table + ids[p]) + w);
+        if (A.uniform) {
+            // experts laid out at a constant step: no descriptor load
+            if (lane < k) {
+                const int p = t * k + lane;
+                const long long e = ids[p];
+                DevExpert d = A.u;
+                d.gate.data += e * A.ustep[0];
+                d.up.data += e * A.ustep[1];
+                d.down.data += e * A.ustep[2];
+                dpair[p] = d;
+            }
+        } else {
+            constexpr int DW = (int)(sizeof(DevExpert) / 8);
+            for (int i = lane; i < k * DW; i += 32) {
+                const int p = t * k + i / DW, w = i % DW;
+                cp_async8(reinterpret_cast<uint64_t *>(dpair + p) + w,
+                          reinterpret_cast<const uint64_t *>(A.table + ids[p]) + w);
+            }
+            cp_async_commit();
         }
-        cp_async_commit();
     } else {
         // activations -> fp16 (per-token power-of-two scale), ordered as the
         // Q4_K decoder pairs codes with, stored [v][group] for conflict-free reads
@@ -680,61 +707,83 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         return;
     }
 
-    // ---------------- consumers: chunk ci -> warp ci % 16 = the warp owning its
-    // ring slot, so a warp waits on a slot at most one phase ahead
+    // ---------------- consumers, in rounds of up to 16 chunks (the ring): the
+    // round's work items are spread over all 16 warps; a consumer barrier ends
+    // the round and then its slots are released, so no warp ever waits on a
+    // slot more than one phase ahead.
     unsigned *hmax = hmax_g + (gen & 1) * DC_MAX_PAIRS;
-    for (int ci = warp; ci < nchunks_a; ci += DC_CW) {
-        const int s = ci % DC_NSTAGE;
-        if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
-            if (lane == 0) set_abort(misc, A.status);
-            break;
+    // T = 1: every gate/up row meets the same activations; keep them in registers
+    uint32_t xv1[32];
+    float XA1 = 0.0f, XB1 = 0.0f;
+    const bool x_hoist = T == 1 && H64 <= 32;
+    if (x_hoist && lane < H64) {
+        const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            const uint4 q = xv4[v * H64 + lane];
+            xv1[4 * v + 0] = q.x;
+            xv1[4 * v + 1] = q.y;
+            xv1[4 * v + 2] = q.z;
+            xv1[4 * v + 3] = q.w;
         }
-        const int4 ch = chunk[ci];
-        const int n = ch.z, r0 = ch.y;
-        const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
-        const DevExpert &X = dpair[plist[q0]];
-        const uint8_t *stage = ring + (size_t)s * A.stage;
-        const int sg = (int)X.gate.stride, su = (int)X.up.stride;
-        const uint8_t *ubase = stage + n * sg;
-        for (int qi = 0; qi < ne; ++qi) {
-            const int p = plist[q0 + qi], t = p / k;
-            float part[2 * DC_ROWS_A];
+        XA1 = xsum[lane * 2 + 0];
+        XB1 = xsum[lane * 2 + 1];
+    }
+    for (int cr = 0; cr < nchunks_a; cr += DC_NSTAGE) {
+        const int cend = min(cr + DC_NSTAGE, nchunks_a);
+        for (int f = cr * A.rows_a + warp; f < cend * A.rows_a; f += DC_CW) {
+            const int ci = f / A.rows_a, row = f - ci * A.rows_a;
+            const int4 ch = chunk[ci];
+            const int n = ch.z, r0 = ch.y;
+            if (row >= n) continue;
+            const int s = ci % DC_NSTAGE;
+            if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+                if (lane == 0) set_abort(misc, A.status);
+                break;
+            }
+            const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
+            const DevExpert &X = dpair[plist[q0]];
+            const uint8_t *stage = ring + (size_t)s * A.stage;
+            const uint8_t *grow = stage + row * (int)X.gate.stride;
+            const uint8_t *urow = stage + n * (int)X.gate.stride + row * (int)X.up.stride;
+            for (int qi = 0; qi < ne; ++qi) {
+                const int p = plist[q0 + qi], t = p / k;
+                float part[2] = {0.0f, 0.0f};
+                if (x_hoist) {
+                    if (lane < H64) {
+                        part[0] = q4k_dot64(grow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
+                        part[1] = q4k_dot64(urow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
+                    }
+                } else {
+                    const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs + (size_t)t * H / 2);
+                    for (int G64 = lane; G64 < H64; G64 += 32) {
+                        uint32_t xv[32];
 #pragma unroll
-            for (int i = 0; i < 2 * DC_ROWS_A; ++i) part[i] = 0.0f;
-            const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs + (size_t)t * H / 2);
-            for (int G64 = lane; G64 < H64; G64 += 32) {
-                const int sb = G64 >> 2, g = G64 & 3;
-                uint32_t xv[32];
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const uint4 q = xv4[v * H64 + G64];
-                    xv[4 * v + 0] = q.x;
-                    xv[4 * v + 1] = q.y;
-                    xv[4 * v + 2] = q.z;
-                    xv[4 * v + 3] = q.w;
-                }
-                const float XA = xsum[((size_t)t * H64 + G64) * 2 + 0];
-                const float XB = xsum[((size_t)t * H64 + G64) * 2 + 1];
-#pragma unroll
-                for (int i = 0; i < 2 * DC_ROWS_A; ++i) {
-                    const int row = i % DC_ROWS_A;
-                    if (row < n) {
-                        const uint8_t *blk = (i < DC_ROWS_A ? stage + row * sg : ubase + row * su) + 144 * sb;
-                        part[i] += q4k_dot64(blk, g, xv, XA, XB);
+                        for (int v = 0; v < 8; ++v) {
+                            const uint4 q = xv4[v * H64 + G64];
+                            xv[4 * v + 0] = q.x;
+                            xv[4 * v + 1] = q.y;
+                            xv[4 * v + 2] = q.z;
+                            xv[4 * v + 3] = q.w;
+                        }
+                        const float XA = xsum[((size_t)t * H64 + G64) * 2 + 0];
+                        const float XB = xsum[((size_t)t * H64 + G64) * 2 + 1];
+                        part[0] += q4k_dot64(grow + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
+                        part[1] += q4k_dot64(urow + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
                     }
                 }
-            }
-            // part[0..3] gate rows, part[4..7] up rows -> value j in lanes 4j .. 4j+3
-            const float tot = warp_reduce8(part) * xsc[t];
-            const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
-            if (lane < 16 && (lane & 3) == 0 && (lane >> 2) < n) {
-                const float hv = silu_f32(tot) * upv;
-                A.h[(size_t)p * I + r0 + (lane >> 2)] = hv;
-                atomicMax(&hmax[p], __float_as_uint(fabsf(hv)));
+                // gate total in lanes 0..15, up total in lanes 16..31
+                const float tot = warp_reduce2(part) * xsc[t];
+                const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
+                if (lane == 0) {
+                    const float hv = silu_f32(tot) * upv;
+                    A.h[(size_t)p * I + r0 + row] = hv;
+                    atomicMax(&hmax[p], __float_as_uint(fabsf(hv)));
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        consumer_sync();
+        if (tid < cend - cr) mbar_arrive(&empty[(cr + tid) % DC_NSTAGE]);
     }
 
     // ---- grid barrier: every CTA's h and |h| maxima are complete and visible
@@ -791,36 +840,41 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         }
         consumer_sync();
 
-        // ---- down: this CTA's output rows [b0, b1) of every routed expert
-        for (int ci = nchunks_a + ((warp - nchunks_a) % DC_CW + DC_CW) % DC_CW; ci < nchunks; ci += DC_CW) {
-            const int s = ci % DC_NSTAGE;
-            if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
-                if (lane == 0) set_abort(misc, A.status);
-                break;
-            }
-            const int4 ch = chunk[ci];
-            const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
-            const DevMatrix &D = dpair[plist[q0]].down;
-            const uint8_t *stage = ring + (size_t)s * A.stage;
-            const int sd = (int)D.stride, rbase = ch.y, nr = ch.z;
-            for (int qi = 0; qi < ne; ++qi) {
-                const int p = plist[q0 + qi];
-                uint32_t hv[16];
-                float hsu = 0.0f;
-                if (lane < U) {
-                    const uint4 *h4 = reinterpret_cast<const uint4 *>(hs + ((size_t)p * I + 32 * lane) / 2);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        const uint4 q = h4[v];
-                        hv[4 * v] = q.x;
-                        hv[4 * v + 1] = q.y;
-                        hv[4 * v + 2] = q.z;
-                        hv[4 * v + 3] = q.w;
-                    }
-                    hsu = hsum[p * 32 + lane];
+        // ---- down: this CTA's output rows [b0, b1) of every routed expert;
+        // work item = (chunk, batch of 4 rows)
+        const int bpc = (A.rows_b + 3) / 4;
+        for (int cr = nchunks_a; cr < nchunks; cr += DC_NSTAGE) {
+            const int cend = min(cr + DC_NSTAGE, nchunks);
+            for (int f = (cr - nchunks_a) * bpc + warp; f < (cend - nchunks_a) * bpc; f += DC_CW) {
+                const int ci = nchunks_a + f / bpc, rb = 4 * (f % bpc);
+                const int4 ch = chunk[ci];
+                const int nr = ch.z;
+                if (rb >= nr) continue;
+                const int s = ci % DC_NSTAGE;
+                if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+                    if (lane == 0) set_abort(misc, A.status);
+                    break;
                 }
-                const float scale = hsc[p];
-                for (int rb = 0; rb < nr; rb += 4) {
+                const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
+                const DevMatrix &D = dpair[plist[q0]].down;
+                const uint8_t *stage = ring + (size_t)s * A.stage;
+                const int sd = (int)D.stride, rbase = ch.y;
+                for (int qi = 0; qi < ne; ++qi) {
+                    const int p = plist[q0 + qi];
+                    uint32_t hv[16];
+                    float hsu = 0.0f;
+                    if (lane < U) {
+                        const uint4 *h4 = reinterpret_cast<const uint4 *>(hs + ((size_t)p * I + 32 * lane) / 2);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint4 q = h4[v];
+                            hv[4 * v] = q.x;
+                            hv[4 * v + 1] = q.y;
+                            hv[4 * v + 2] = q.z;
+                            hv[4 * v + 3] = q.w;
+                        }
+                        hsu = hsum[p * 32 + lane];
+                    }
                     float part[4];
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -830,11 +884,11 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                     }
                     const float tot = warp_reduce4(part);   // row rb + j in lanes 8j .. 8j+7
                     const int j = lane >> 3;
-                    if ((lane & 7) == 0 && rb + j < nr) ybuf[p * L.rb + rbase + rb + j] = tot * scale;
+                    if ((lane & 7) == 0 && rb + j < nr) ybuf[p * L.rb + rbase + rb + j] = tot * hsc[p];
                 }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            consumer_sync();
+            if (tid < cend - cr) mbar_arrive(&empty[(cr + tid) % DC_NSTAGE]);
         }
     }
     consumer_sync();
@@ -940,8 +994,8 @@ bool decode_fused_eligible(int T, int k, int E, int H, int I, uint32_t gateup_fo
     return decode_fused_plan(T, k, E, H, I, G, gu_stride, dn_stride).smem != 0;
 }
 
-cudaError_t launch_decode_fused(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
-                                int64_t dn_stride, int renorm, int lo, int hi, uint32_t fmt_mask, const float *logits,
+cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *W, int T, int k, int E, int H, int I,
+                                int64_t gu_stride, int64_t dn_stride, int renorm, int lo, int hi, uint32_t fmt_mask, const float *logits,
                                 const uint16_t *x, float *out, float *h, int32_t *ids, float *wts, int32_t *offsets,
                                 int32_t *active, int32_t *pairs, int32_t *pos, unsigned char *sync, uint32_t *status,
                                 cudaStream_t s) {
@@ -991,6 +1045,18 @@ cudaError_t launch_decode_fused(const DevExpert *table, int T, int k, int E, int
     A.rows_a = pl.rows_a;
     A.rows_b = pl.rows_b;
     A.chunk_cap = pl.chunk_cap;
+    A.uniform = W->uniform_layout;
+    {
+        const moe_matrix *src[3] = {&W->uniform_base.gate, &W->uniform_base.up, &W->uniform_base.down};
+        DevMatrix *dst[3] = {&A.u.gate, &A.u.up, &A.u.down};
+        for (int i = 0; i < 3; ++i) {
+            dst[i]->data = static_cast<const uint8_t *>(src[i]->data);
+            dst[i]->stride = src[i]->row_stride_bytes;
+            dst[i]->fmt = src[i]->format;
+            dst[i]->rows = src[i]->rows;
+            A.ustep[i] = W->uniform_step[i];
+        }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(DC_THREADS);

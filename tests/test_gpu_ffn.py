@@ -326,3 +326,25 @@ def test_full_decode1_gemv_path(M):
     ref = offn.moe_ffn(lazy, DL.x_host, DL.logits_host, cfg.k, gate_formats=lazy.gate_formats())
     assert_parity(out, ref, "decode1 gemv")
     assert_parity(fused, ref, "decode1 fused")
+
+
+def test_uniform_layout_matches_descriptor_table(M):
+    """Experts stored as one strided tensor (descriptors computed in the
+    kernel) and the same bytes in separate allocations (descriptors read from
+    the table) give bit-identical outputs on every path."""
+    from synth import gpu as sgpu
+    cfg = synth.LayerConfig("uni", 48, 6, 512, 128, 3, "q4k", True, 123)
+    DL = sgpu.make_device_layer(cfg, 0)
+    t_uni = M.WeightTable(DL.experts, cfg.hidden, cfg.inter)
+    assert t_uni.c.uniform_layout == 1
+    copies = [{n: (f, r, cc, st, v.clone()) for n, (f, r, cc, st, v) in ex.items()} for ex in DL.experts]
+    t_sep = M.WeightTable(copies, cfg.hidden, cfg.inter)
+    assert t_sep.c.uniform_layout == 0
+    for path in (M.PATH_FUSED, M.PATH_GEMV):
+        opt = M.make_options(n_experts=cfg.n_experts, path=path)
+        a = M.ffn_forward(t_uni, DL.x_bf16, DL.logits, cfg.k, options=opt)
+        b = M.ffn_forward(t_sep, DL.x_bf16, DL.logits, cfg.k, options=opt)
+        assert torch.equal(a, b), path
+    lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
+    ref = offn.moe_ffn(lazy, DL.x_host, DL.logits_host, cfg.k, gate_formats=lazy.gate_formats())
+    assert_parity(a.cpu().numpy(), ref, "uniform layout")
