@@ -181,7 +181,8 @@ def measured_peaks():
 
 def kernel_traffic(kernel: str, config: str):
     """dram bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source (same hash); else None."""
+    the current source of that kernel (same hash of the files it lists); else
+    None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -190,15 +191,16 @@ def kernel_traffic(kernel: str, config: str):
     ent = d.get(f"{kernel}:{config}")
     if not ent:
         return None
-    if ent.get("source_sha256") != source_hash():
+    if ent.get("source_sha256") != source_hash(ent.get("sources", [])):
         return None
     return ent.get("dram_bytes_per_launch")
 
 
-def source_hash() -> str:
+def source_hash(files) -> str:
+    """sha256 (16 hex digits) over the named files of the package's csrc/."""
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "quantized_moe_expert_route_gb300", "csrc")
-    for f in sorted(os.listdir(cs)):
+    for f in sorted(files):
         with open(os.path.join(cs, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
