@@ -133,7 +133,11 @@ typedef struct {
 /* Paths for moe_options.path. */
 #define MOE_PATH_AUTO 0        /* the fastest path that handles the layer (see moe_ffn_path) */
 #define MOE_PATH_GEMV 1        /* grouped GEMV kernels (route, bucket, gate/up, down, combine); any layer */
-#define MOE_PATH_TENSOR 2      /* tcgen05 grouped GEMM (prefill chunks) */
+#define MOE_PATH_TENSOR 2      /* tcgen05 grouped GEMMs with TMEM-resident dequantised weights
+                                  (prefill chunks; AUTO takes it above MOE_GEMV_MAX_ROWS rows):
+                                  H % 128 == 0, I % 64 == 0, any format mix. Each weight is
+                                  represented in fp16, so it must lie within fp16 range
+                                  (|w| <= 65504; quantized LLM weights are O(1)). */
 #define MOE_PATH_FUSED 3       /* one persistent cooperative kernel per layer for decode rows:
                                   T * k <= 64, Q4_K gate/up and Q8_0 down, H % 64 == 0,
                                   I % 32 == 0, I <= 1024 */
@@ -152,7 +156,7 @@ typedef struct {
      * stream around the expert mat-mul kernels: before the gate/up kernel,
      * between it and the down kernel, and after the down kernel. On the fused
      * path, where one kernel does both, events 1 and 2 are both recorded after
-     * it. During stream capture they become external event-record nodes. */
+     * it; on the tensor path the h conversion falls between events 1 and 2. During stream capture they become external event-record nodes. */
     void *const *timing_events;
 } moe_options;
 
@@ -199,8 +203,15 @@ int moe_bucket(const int32_t *ids, int32_t T, int32_t k, int32_t E, int32_t expe
                moe_stream_t stream);
 
 /* Workspace bytes moe_ffn_forward needs for a prepared W, T tokens and top-k
- * (0 if the arguments are invalid). */
+ * on the path MOE_PATH_AUTO picks (0 if the arguments are invalid). */
 size_t moe_ffn_workspace_size(const moe_weight_table *W, int32_t T, int32_t k);
+
+/* The same for an explicitly requested path (MOE_PATH_*); 0 if the arguments
+ * are invalid or the path cannot run this layer. The tensor path needs
+ * about P * (2H + 2I + 12) + 16 * (P/128 + min(P, E)) bytes more than the
+ * others (P = T * k): its fp16 activation and h copies in bucket order, row
+ * scales and chunk table. */
+size_t moe_ffn_workspace_size_for_path(const moe_weight_table *W, int32_t T, int32_t k, int32_t path);
 
 /* The path moe_ffn_forward takes for these arguments (MOE_PATH_GEMV,
  * MOE_PATH_TENSOR or MOE_PATH_FUSED; resolves MOE_PATH_AUTO), or -1 if the

@@ -28,7 +28,7 @@ EXPORTED = [
     "moe_strerror", "moe_last_cuda_error", "moe_table_device_bytes", "moe_table_prepare",
     "moe_route_topk", "moe_bucket", "moe_ffn_workspace_size", "moe_ffn_workspace_init",
     "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc",
-    "moe_ffn_path",
+    "moe_ffn_path", "moe_ffn_workspace_size_for_path",
 ]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -86,6 +86,8 @@ def load() -> ctypes.CDLL:
     L.moe_bucket.argtypes = [vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp]
     L.moe_ffn_workspace_size.argtypes = [ctypes.POINTER(WeightTableC), i32, i32]
     L.moe_ffn_workspace_size.restype = sz
+    L.moe_ffn_workspace_size_for_path.argtypes = [ctypes.POINTER(WeightTableC), i32, i32, i32]
+    L.moe_ffn_workspace_size_for_path.restype = sz
     L.moe_ffn_workspace_init.argtypes = [vp, sz, vp]
     L.moe_ffn_forward.argtypes = [ctypes.POINTER(WeightTableC), vp, vp, i32, i32, ctypes.POINTER(Options),
                                   vp, vp, sz, vp]
@@ -165,10 +167,11 @@ class WeightTable:
 class Workspace:
     """Device workspace of moe_ffn_forward for (table, T, k), zero-initialised."""
 
-    def __init__(self, table: WeightTable, T: int, k: int, stream=None):
+    def __init__(self, table: WeightTable, T: int, k: int, stream=None, path: int = 0):
+        """path: size for that MOE_PATH_* (0 = the one AUTO picks)."""
         L = load()
         self.table, self.T, self.k = table, T, k
-        self.nbytes = L.moe_ffn_workspace_size(ctypes.byref(table.c), T, k)
+        self.nbytes = L.moe_ffn_workspace_size_for_path(ctypes.byref(table.c), T, k, path)
         if self.nbytes == 0:
             raise ValueError("bad workspace arguments")
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device="cuda")

@@ -26,6 +26,12 @@ cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *
                                 const uint16_t *x, float *out, float *h, int32_t *ids, float *wts, int32_t *offsets,
                                 int32_t *active, int32_t *pairs, int32_t *pos, unsigned char *sync, uint32_t *status,
                                 cudaStream_t s);
+bool tc_path_eligible(int H, int I);
+cudaError_t launch_tc_path(const DevExpert *table, uint32_t gu_formats, uint32_t dn_formats, int T, int k, int E,
+                           int H, int I, const int32_t *offsets, const int32_t *active, const int32_t *pos,
+                           const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
+                           const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
+                           cudaStream_t s);
 }  // namespace moe
 
 using namespace moe;
@@ -66,12 +72,21 @@ int check_matrix(const moe_matrix &m, int rows, int cols) {
 int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
     const bool fused_ok = decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
                                                 W->down_formats, W->max_gateup_stride, W->max_down_stride);
+    const bool tc_ok = tc_path_eligible(W->hidden, W->inter);
     switch (requested) {
-        case MOE_PATH_AUTO: return fused_ok ? MOE_PATH_FUSED : MOE_PATH_GEMV;
+        case MOE_PATH_AUTO:
+            return fused_ok ? MOE_PATH_FUSED : (T > MOE_GEMV_MAX_ROWS && tc_ok) ? MOE_PATH_TENSOR : MOE_PATH_GEMV;
         case MOE_PATH_GEMV: return MOE_PATH_GEMV;
+        case MOE_PATH_TENSOR: return tc_ok ? MOE_PATH_TENSOR : -1;
         case MOE_PATH_FUSED: return fused_ok ? MOE_PATH_FUSED : -1;
         default: return -1;
     }
+}
+
+// Workspace bytes of a forward on `path` (the tensor path adds its regions).
+size_t path_ws_bytes(const moe_weight_table *W, int T, int k, int path) {
+    if (path == MOE_PATH_TENSOR) return tc_ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
+    return ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
 }
 
 // Options with defaults filled in; false if they are invalid.
@@ -201,8 +216,16 @@ int moe_bucket(const int32_t *ids, int32_t T, int32_t k, int32_t E, int32_t expe
 }
 
 size_t moe_ffn_workspace_size(const moe_weight_table *W, int32_t T, int32_t k) {
+    return moe_ffn_workspace_size_for_path(W, T, k, MOE_PATH_AUTO);
+}
+
+size_t moe_ffn_workspace_size_for_path(const moe_weight_table *W, int32_t T, int32_t k, int32_t path) {
     if (!W || T < 0 || k <= 0 || k > W->n_experts || W->n_experts <= 0) return 0;
-    return ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
+    if (path < MOE_PATH_AUTO || path > MOE_PATH_FUSED) return 0;
+    const int p = W->prepared == MOE_TABLE_PREPARED ? resolve_path(W, T > 0 ? T : 1, k, path)
+                                                    : (path == MOE_PATH_AUTO ? MOE_PATH_GEMV : path);
+    if (p < 0) return 0;
+    return path_ws_bytes(W, T, k, p);
 }
 
 int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
@@ -224,11 +247,12 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     moe_options o;
     if (!effective_options(W, opt, o)) return MOE_ERR_INVALID_ARG;
     int path = resolve_path(W, T > 0 ? T : 1, k, o.path);
-    // the fused kernel reads activation rows with 16-byte loads
-    if (path == MOE_PATH_FUSED && T > 0 && !aligned(x, 16)) path = o.path == MOE_PATH_AUTO ? MOE_PATH_GEMV : -1;
-    if (path < 0 || path == MOE_PATH_TENSOR) return MOE_ERR_UNSUPPORTED;
+    // the fused and tensor paths read activation rows with 16-byte loads
+    if ((path == MOE_PATH_FUSED || path == MOE_PATH_TENSOR) && T > 0 && !aligned(x, 16))
+        path = o.path == MOE_PATH_AUTO ? MOE_PATH_GEMV : -1;
+    if (path < 0) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, k, E, H, I);
-    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < path_ws_bytes(W, T, k, path)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if (T == 0) return MOE_OK;
 
     char *base = static_cast<char *>(ws);
@@ -263,8 +287,12 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     err = launch_bucket(ids, T, k, E, o.expert_lo, o.expert_hi, o.format_mask, table, offsets, pairs, pos, active,
                         status, stream);
     if (err != cudaSuccess) return cuda_fail(err);
-    err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, offsets, pairs, active,
-                           pos, wts, x, h, y, out, status, events, stream);
+    if (path == MOE_PATH_TENSOR)
+        err = launch_tc_path(table, W->gateup_formats, W->down_formats, T, k, E, H, I, offsets, active, pos, wts, x,
+                             h, y, base, tc_ws_layout(T, k, E, H, I), out, status, events, stream);
+    else
+        err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, offsets, pairs,
+                               active, pos, wts, x, h, y, out, status, events, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     return MOE_OK;
 }

@@ -354,6 +354,8 @@ __global__ void combine_kernel(int T, int k, int H, const int32_t *__restrict__ 
     reinterpret_cast<float4 *>(out + (size_t)t * H)[i4] = acc;
 }
 
+}  // namespace
+
 // Records a profiling event; inside a stream capture it becomes an external
 // event-record node of the graph.
 cudaError_t record_event(cudaEvent_t ev, cudaStream_t s) {
@@ -382,7 +384,13 @@ int current_device() {
     return d;
 }
 
-}  // namespace
+cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float *wts, const float *y, float *out,
+                           cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    dim3 g((H / 4 + 127) / 128, T);
+    combine_kernel<<<g, 128, 0, s>>>(T, k, H, pos, wts, y, out);
+    return cudaGetLastError();
+}
 
 size_t gateup_smem_bytes(int H, int64_t wstride) {
     return (size_t)(2 * GU_ROWS * wstride) + (size_t)GV_NT * H * 4 + 2 * GU_ROWS * GV_NT * 4;

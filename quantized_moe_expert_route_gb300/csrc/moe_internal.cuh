@@ -51,11 +51,50 @@ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
     return L;
 }
 
+// Extra workspace of the tensor-core path, after the common layout (only
+// sized in when that path can run; offsets from the workspace base):
+// activations in bucket order as fp16 [P][H] with inverse row scales, |h|
+// maxima, h as fp16 [P][I] with inverse row scales, and the chunk table.
+struct TcLayout {
+    size_t xg, xinv, hmax, h16, hinv, chunks, n_chunks, total;
+};
+
+inline size_t tc_max_chunks(int T, int k, int E) {
+    const size_t P = (size_t)T * k;
+    return P / 128 + (P < (size_t)E ? P : (size_t)E) + 1;
+}
+
+inline TcLayout tc_ws_layout(int T, int k, int E, int H, int I) {
+    const WsLayout L = ws_layout(T, k, E, H, I);
+    TcLayout C;
+    size_t o = L.total;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    const size_t P = (size_t)T * k;
+    C.xg = take(P * H * 2);
+    C.xinv = take(P * 4);
+    C.hmax = take(P * 4);
+    C.h16 = take(P * I * 2);
+    C.hinv = take(P * 4);
+    C.chunks = take(tc_max_chunks(T, k, E) * 16);
+    C.n_chunks = take(4);
+    C.total = o;
+    return C;
+}
+
 constexpr int BLOCK_ELEMS[5] = {0, 32, 256, 256, 32};
 constexpr int BLOCK_BYTES[5] = {0, 34, 144, 210, 17};
 
 // Bounded waits: a wait that exceeds this many polls sets MOE_FLAG_WAIT_TIMEOUT.
 constexpr uint32_t WAIT_LIMIT = 1u << 26;
+
+// Host helpers shared by the launchers (gemv.cu, decode.cu).
+cudaError_t record_event(cudaEvent_t ev, cudaStream_t s);   // event (graph node when capturing)
+cudaError_t allow_max_dynamic_smem(const void *fn);         // opt in to all free shared memory
+int current_device();
+int sm_count();
+// out[t] = sum over slots j ascending of w[t,j] * y[pos[t,j]]; y in bucket order
+cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float *wts, const float *y, float *out,
+                           cudaStream_t s);
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

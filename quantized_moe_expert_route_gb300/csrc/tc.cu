@@ -1,0 +1,968 @@
+// Tensor-core grouped path: the gate/up and down projections of every active
+// expert as grouped GEMMs on the 5th-generation tensor cores, for prefill
+// chunks (hundreds to thousands of rows per layer).
+//
+// "三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南",
+// 优化策略二/三: one grouped mat-mul over the routed experts of a layer, whose
+// weights come in per-expert tiers of block formats (Q6_K/Q8_0, 4-bit,
+// MXFP4), with explicit skipping of unrouted (-1) ids. "一张 RTX 3090 跑 Llama
+// 70B", 4.4: SwiGLU fused with the FC so g and u never reach memory.
+//
+// Layer = route -> bucket -> tc_prep (fp16 activations in bucket order, chunk
+// table) -> tc_gemm<gate/up> (SwiGLU epilogue, fp32 h) -> tc_hprep (fp16 h
+// with a per-row power-of-two scale) -> tc_gemm<down> (fp32 y in bucket order)
+// -> combine (ascending slot).
+//
+// tc_gemm is a persistent kernel, one CTA per SM, that works through units of
+// (chunk of <= 128 bucket rows of one expert, 128 weight rows). Per unit it
+// computes D[128 weight rows, n act rows] = W_e[rows, :] . act[chunk, :]^T with
+// tcgen05.mma (M = 128, N = n rounded up to 16, K = 16 per instruction):
+//   - A (weights) lives in TMEM. A TMA producer warp streams each weight row's
+//     quantized blocks (256 K at a time) into a shared-memory ring with 1-D
+//     bulk copies; 16 dequantising warps turn them into exact-then-rounded
+//     fp16 and write them to TMEM with tcgen05.st, 64 K per stage.
+//   - B (activations, fp16, K-major) is TMA-tiled from the bucket-ordered
+//     activation matrix with 128-byte swizzle, 16 rows per box.
+//   - D accumulates in fp32 in TMEM (two buffers, so the epilogue of one unit
+//     overlaps the next unit's MMAs); 4 epilogue warps read it with tcgen05.ld.
+// Gate/up units hold 64 gate rows (TMEM lanes 0-63) and the same 64 up rows
+// (lanes 64-127), so SwiGLU needs only the CTA's own accumulator.
+#include <cuda.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int TC_M = 128;                    // weight rows per unit = TMEM lanes
+constexpr int TC_NCHUNK = 128;               // activation rows per chunk (MMA N <= 128)
+constexpr int TC_KA = 64;                    // K per A/B stage: one 128-byte row of fp16
+constexpr int TC_KR = 256;                   // K per raw (quantized) stage
+constexpr int TC_ASTAGES = 8;                // A stages in TMEM, 32 columns each
+constexpr int TC_BSTAGES = 4;                // B stages in shared memory
+constexpr int TC_BSTAGE_BYTES = TC_NCHUNK * 128;
+constexpr int TC_BOX_ROWS = 16;              // rows per B TMA box
+constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups = A stages per raw stage
+constexpr int TC_DQ0 = 4;                    // warps 0-3 epilogue, 4..19 dequant
+constexpr int TC_PROD = TC_DQ0 + 4 * TC_DG;  // 20: TMA producer
+constexpr int TC_MMA = TC_PROD + 1;          // 21: MMA issuer
+constexpr int TC_WARPS = TC_MMA + 1;
+constexpr int TC_THREADS = TC_WARPS * 32;    // 704
+constexpr int TC_TMEM_COLS = 512;
+constexpr int TC_ACOL0 = 2 * TC_NCHUNK;      // A stages after the two accumulators
+constexpr int TC_RS_MAX = 6;
+constexpr int TC_UBUF_FLOATS = 32 * 64;
+constexpr int TC_NBARS = 2 * TC_RS_MAX + 2 * TC_ASTAGES + 2 * TC_BSTAGES + 4 + 1;
+constexpr uint32_t TC_NEG1152 = 0xE480E480u;  // fp16 pair (-1152, -1152)
+constexpr uint32_t TC_NEG1056 = 0xE420E420u;  // fp16 pair (-1056, -1056)
+constexpr uint32_t TC_MAGIC = 0x64006400u;    // fp16 pair (1024, 1024)
+
+static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
+static_assert(TC_DG == 4, "one dequantising warpgroup per 64-K piece of a raw stage");
+
+struct TcArgs {
+    const DevExpert *table;
+    const int4 *chunks;      // {expert, first bucket row, rows, 0}
+    const int32_t *n_chunks;
+    int K;                   // reduction length: H (gate/up) or I (down)
+    int S;                   // units per chunk: I/64 (gate/up) or H/128 (down)
+    int H, I;
+    int RB;                  // raw row pitch in shared memory, bytes
+    int RS;                  // raw stages in the ring
+    const float *ascale;     // per bucket row: 2^-sigma of its fp16 activation row
+    float *h32;              // gate/up: h [rows][I] fp32, bucket order
+    uint32_t *hmax;          // gate/up: max |h| bits per bucket row
+    float *y;                // down: y [rows][H] fp32, bucket order
+    uint32_t *status;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));  // (a & mask) | bits
+    return d;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t half2_bits(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+__device__ __forceinline__ uint32_t splat_half(__half h) { return half2_bits(h, h); }
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+// N little-endian words starting at any byte address of shared memory.
+template <int N>
+__device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&w)[N]) {
+    const uint32_t base = addr & ~3u, sh = (addr & 3u) * 8u;
+    uint32_t v[N + 1];
+#pragma unroll
+    for (int i = 0; i <= N; ++i) v[i] = lds32(base + 4 * i);
+#pragma unroll
+    for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// A wait that lasts this long (ns) has failed: a whole layer takes well under
+// a millisecond.
+constexpr uint64_t TC_WAIT_NS = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Bounded parity wait (TC_WAIT_NS, or WAIT_LIMIT polls) that also gives up
+// once another role has aborted.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t addr = smem_addr(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 255u) == 255u) {
+            if (*abort_flag) return false;
+            const uint64_t now = global_ns();
+            if (i == 255u)
+                t0 = now;
+            else if (now - t0 > TC_WAIT_NS)
+                return false;
+        }
+    }
+    return false;
+}
+__device__ __forceinline__ void tc_fail(volatile int *abort_flag, uint32_t *status) {
+    if (!*abort_flag) {
+        *abort_flag = 1;
+        atomicOr(status, (uint32_t)MOE_FLAG_WAIT_TIMEOUT);
+    }
+}
+
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, "
+        "%14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] . B[smem]^T, kind::f16 (fp16 A and B, fp32 D), cta_group::1.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart; the tile starts 1024-aligned.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= (uint64_t)1 << 16;                      // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                      // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                      // 128-byte swizzle
+    return d;
+}
+// Instruction descriptor, kind::f16: fp32 D, fp16 A and B, both K-major, M = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ------------------------------------------------------------------ dequantisation
+// Each function turns one weight row's 64 consecutive K elements (piece g of
+// a raw stage) into 32 fp16 pairs in K order (low half = lower K), the TMEM
+// layout of the MMA's A operand. Integer codes become exact fp16 values
+// through the 1024 + q exponent trick; the block scales are applied in fp16
+// FMAs, so each weight is rounded once or twice to fp16 (11-bit significand).
+
+// Q4_K 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes.
+__device__ __forceinline__ void q4k_scale_min(int j, uint32_t s03, uint32_t s47, uint32_t s811, int &sc, int &m) {
+    const int sh = 8 * (j & 3);
+    const int a = (s03 >> sh) & 0xff, b = (s47 >> sh) & 0xff, c = (s811 >> sh) & 0xff;
+    if (j < 4) {
+        sc = a & 63;
+        m = b & 63;
+    } else {
+        sc = (c & 15) | ((a >> 6) << 4);
+        m = (c >> 4) | ((b >> 6) << 4);
+    }
+}
+
+// Q4_K super-block at `blk` (16-aligned); piece g = elements 64g..64g+63:
+// low nibbles of qs[32g..32g+31] (sub-block 2g), then their high nibbles
+// (sub-block 2g+1). w = d*sc*q - dmin*m.
+__device__ __forceinline__ void dq_q4k(uint32_t blk, int g, uint32_t (&r)[32]) {
+    uint32_t h0, s03, s47, s811;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(h0), "=r"(s03), "=r"(s47), "=r"(s811) : "r"(blk));
+    int sc0, m0, sc1, m1;
+    q4k_scale_min(2 * g, s03, s47, s811, sc0, m0);
+    q4k_scale_min(2 * g + 1, s03, s47, s811, sc1, m1);
+    const uint32_t D2 = (h0 & 0xffffu) * 0x10001u;
+    const float dmin = __half2float(__ushort_as_half((uint16_t)(h0 >> 16)));
+    // (1024 + q) * sc - 1024 * sc = sc * q exactly (<= 945); likewise for the
+    // high nibble read as 1024 + 16 q with sc / 16
+    const uint32_t SC0 = splat_half(__int2half_rn(sc0)), NS0 = splat_half(__int2half_rn(-1024 * sc0));
+    const uint32_t SC1 = splat_half(__float2half_rn(0.0625f * (float)sc1)), NS1 = splat_half(__int2half_rn(-64 * sc1));
+    const uint32_t MT0 = splat_half(__float2half_rn(-dmin * (float)m0));
+    const uint32_t MT1 = splat_half(__float2half_rn(-dmin * (float)m1));
+    uint32_t w[8];
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                 : "r"(blk + 16 + 32 * g));
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "r"(blk + 32 + 32 * g));
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t t0 = prmt(w[m], 0u, 0x4140u), t1 = prmt(w[m], 0u, 0x4342u);
+        r[2 * m] = hfma2(hfma2(lop_and_or(t0, 0x000F000Fu, TC_MAGIC), SC0, NS0), D2, MT0);
+        r[2 * m + 1] = hfma2(hfma2(lop_and_or(t1, 0x000F000Fu, TC_MAGIC), SC0, NS0), D2, MT0);
+        r[16 + 2 * m] = hfma2(hfma2(lop_and_or(t0, 0x00F000F0u, TC_MAGIC), SC1, NS1), D2, MT1);
+        r[17 + 2 * m] = hfma2(hfma2(lop_and_or(t1, 0x00F000F0u, TC_MAGIC), SC1, NS1), D2, MT1);
+    }
+}
+
+// Q8_0: piece g = blocks 2g and 2g+1 of the stage, at bytes 68g and 68g + 34
+// of the 16-aligned stage row. w = d*q.
+__device__ __forceinline__ void dq_q8_0(uint32_t row, int g, uint32_t (&r)[32]) {
+    const uint32_t p = row + 68 * g;  // 4-aligned
+    uint32_t v[17];
+#pragma unroll
+    for (int i = 0; i < 17; ++i) v[i] = lds32(p + 4 * i);
+    const uint32_t D0 = (v[0] & 0xffffu) * 0x10001u, D1 = (v[8] >> 16) * 0x10001u;
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        // bytes as 1152 + q (q + 128 in the low byte of 0x64xx), less 1152
+        const uint32_t c0 = __funnelshift_r(v[m], v[m + 1], 16) ^ 0x80808080u;
+        const uint32_t c1 = v[9 + m] ^ 0x80808080u;
+        r[2 * m] = hmul2(hadd2(prmt(c0, 0x64646464u, 0x5140u), TC_NEG1152), D0);
+        r[2 * m + 1] = hmul2(hadd2(prmt(c0, 0x64646464u, 0x7362u), TC_NEG1152), D0);
+        r[16 + 2 * m] = hmul2(hadd2(prmt(c1, 0x64646464u, 0x5140u), TC_NEG1152), D1);
+        r[17 + 2 * m] = hmul2(hadd2(prmt(c1, 0x64646464u, 0x7362u), TC_NEG1152), D1);
+    }
+}
+
+// Q6_K super-block at `blk` (2-aligned); piece g covers quarters r0 = 2(g&1)
+// and r0+1 of half g>>1. w = d*scale*(q - 32).
+__device__ __forceinline__ void dq_q6k(uint32_t blk, int g, uint32_t (&r)[32]) {
+    const int hh = g >> 1, r0 = 2 * (g & 1);
+    uint32_t L0[8], L1[8], Q[8], SC[1], DW[1];
+    lds_words<8>(blk + 64 * hh, L0);
+    lds_words<8>(blk + 64 * hh + 32, L1);
+    lds_words<8>(blk + 128 + 32 * hh, Q);
+    lds_words<1>(blk + 192 + 8 * hh + 2 * r0, SC);
+    lds_words<1>(blk + 208, DW);
+    const uint32_t D2 = (DW[0] & 0xffffu) * 0x10001u;
+    uint32_t S[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) S[i] = splat_half(__int2half_rn((int)(int8_t)(SC[0] >> (8 * i))));
+    const int ns = 4 * (g & 1);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        const uint32_t q0 = ((L0[m] >> ns) & 0x0F0F0F0Fu) | (((Q[m] >> (2 * r0)) & 0x03030303u) << 4);
+        const uint32_t q1 = ((L1[m] >> ns) & 0x0F0F0F0Fu) | (((Q[m] >> (2 * r0 + 2)) & 0x03030303u) << 4);
+        const uint32_t sa = m < 4 ? S[0] : S[1], sb = m < 4 ? S[2] : S[3];
+        r[2 * m] = hmul2(hmul2(hadd2(prmt(q0, 0x64646464u, 0x5140u), TC_NEG1056), sa), D2);
+        r[2 * m + 1] = hmul2(hmul2(hadd2(prmt(q0, 0x64646464u, 0x7362u), TC_NEG1056), sa), D2);
+        r[16 + 2 * m] = hmul2(hmul2(hadd2(prmt(q1, 0x64646464u, 0x5140u), TC_NEG1056), sb), D2);
+        r[17 + 2 * m] = hmul2(hmul2(hadd2(prmt(q1, 0x64646464u, 0x7362u), TC_NEG1056), sb), D2);
+    }
+}
+
+// E2M1 nibble pair (bits 0-3 of each 16-bit half) as fp16 of value * 2^-14.
+__device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t x) {
+    return ((x & 0x00070007u) << 9) | ((x & 0x00080008u) << 12);
+}
+// The same pair for any scale byte, through fp32 (E8M0 255 is NaN).
+__device__ __forceinline__ uint32_t mxfp4_pair_slow(uint32_t x, uint32_t e) {
+    float v[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const uint32_t c = (x >> (16 * i)) & 0xf, ex = (c >> 1) & 3, mb = c & 1;
+        const float mag = ex == 0 ? 0.5f * (float)mb : ldexpf(1.0f + 0.5f * (float)mb, (int)ex - 1);
+        const float sc = e == 255 ? __int_as_float(0x7fc00000) : ldexpf(1.0f, (int)e - 127);
+        v[i] = ((c & 8) ? -mag : mag) * sc;
+    }
+    return half2_bits(__float2half_rn(v[0]), __float2half_rn(v[1]));
+}
+// MXFP4: piece g = blocks 2g and 2g+1 of the stage (17 bytes each) at byte
+// 34g of `blk`; element i < 16 of a block is the low nibble of qs[i], element
+// 16 + i the high nibble. w = 2^(e-127) * E2M1.
+__device__ __forceinline__ void dq_mxfp4(uint32_t blk, int g, uint32_t (&r)[32]) {
+    uint32_t w[9];
+    lds_words<9>(blk + 34 * g, w);
+    uint32_t qs[2][4], e[2];
+    e[0] = w[0] & 0xffu;
+    e[1] = (w[4] >> 8) & 0xffu;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        qs[0][k] = __funnelshift_r(w[k], w[k + 1], 8);
+        qs[1][k] = __funnelshift_r(w[4 + k], w[5 + k], 16);
+    }
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const bool fast = e[b] >= 99 && e[b] <= 128;   // 2^(e-113) is a normal fp16
+        const uint32_t S2 = ((e[b] - 98u) << 10) * 0x10001u;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+            const uint32_t t = prmt(qs[b][(jj & 7) >> 1], 0u, (jj & 1) ? 0x4342u : 0x4140u);
+            const uint32_t x = (jj >= 8 ? (t >> 4) : t) & 0x000F000Fu;
+            r[16 * b + jj] = fast ? hmul2(e2m1_pair_bits(x), S2) : mxfp4_pair_slow(x, e[b]);
+        }
+    }
+}
+
+// Raw bytes one weight row needs for the K range [k0, k1): the blocks that
+// cover it, widened to 16-byte boundaries. `lead` = offset of the first block
+// inside the copied range.
+struct RawSpan {
+    const uint8_t *src;
+    uint32_t bytes, lead;
+};
+__device__ __forceinline__ RawSpan raw_span(const uint8_t *row, int fmt, int k0, int k1) {
+    const int be = fmt == MOE_Q4_K || fmt == MOE_Q6_K ? 256 : 32;
+    const int bb = fmt == MOE_Q8_0 ? 34 : fmt == MOE_Q4_K ? 144 : fmt == MOE_Q6_K ? 210 : 17;
+    const uintptr_t s = reinterpret_cast<uintptr_t>(row) + (uintptr_t)(k0 / be) * bb;
+    const uintptr_t t = reinterpret_cast<uintptr_t>(row) + (uintptr_t)((k1 + be - 1) / be) * bb;
+    const uintptr_t a0 = s & ~(uintptr_t)15, a1 = (t + 15) & ~(uintptr_t)15;
+    return RawSpan{reinterpret_cast<const uint8_t *>(a0), (uint32_t)(a1 - a0), (uint32_t)(s - a0)};
+}
+
+// ------------------------------------------------------------------ the grouped GEMM
+size_t tc_smem_bytes(int RB, int RS) {
+    return 1024 + (size_t)TC_BSTAGES * TC_BSTAGE_BYTES + (size_t)RS * TC_M * RB + TC_UBUF_FLOATS * 4 + TC_NBARS * 8 +
+           16;
+}
+
+// The weight row behind TMEM lane l of unit slice s.
+template <bool GATEUP>
+__device__ __forceinline__ void unit_row(const DevExpert *ex, int s, int l, const uint8_t *&row, int &fmt) {
+    const DevMatrix *m;
+    int r;
+    if (GATEUP) {
+        m = l < 64 ? &ex->gate : &ex->up;
+        r = 64 * s + (l & 63);
+    } else {
+        m = &ex->down;
+        r = TC_M * s + l;
+    }
+    row = m->data + (size_t)r * m->stride;
+    fmt = m->fmt;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort_flag);
+    return __shfl_sync(0xffffffffu, ok, 0);
+}
+
+// AND of `pred` over the 128 epilogue threads (warps 0-3), with a barrier.
+__device__ __forceinline__ bool epi_all(bool pred) {
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, 128, p; selp.u32 %0, 1, 0, q; }"
+                 : "=r"(r)
+                 : "r"((uint32_t)pred)
+                 : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const TcArgs A) {
+    extern __shared__ __align__(16) uint8_t tc_smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *bring = sm;
+    uint8_t *raw = bring + TC_BSTAGES * TC_BSTAGE_BYTES;
+    float *ubuf = reinterpret_cast<float *>(raw + (size_t)A.RS * TC_M * A.RB);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ubuf + TC_UBUF_FLOATS);
+    uint64_t *raw_full = bars, *raw_empty = bars + TC_RS_MAX;
+    uint64_t *a_full = bars + 2 * TC_RS_MAX, *a_empty = a_full + TC_ASTAGES;
+    uint64_t *b_full = a_empty + TC_ASTAGES, *b_empty = b_full + TC_BSTAGES;
+    uint64_t *acc_full = b_empty + TC_BSTAGES, *acc_empty = acc_full + 2, *fin = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + TC_NBARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < A.RS; ++i) {
+            mbar_init(&raw_full[i], 1);
+            mbar_init(&raw_empty[i], 4 * TC_DG);
+        }
+        for (int i = 0; i < TC_ASTAGES; ++i) {
+            mbar_init(&a_full[i], 4);
+            mbar_init(&a_empty[i], 1);
+        }
+        for (int i = 0; i < TC_BSTAGES; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(tmem_slot)),
+                     "r"(TC_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_units = *A.n_chunks * A.S;
+    const int nR = (A.K + TC_KR - 1) / TC_KR, nA = A.K / TC_KA;
+
+    if (warp == TC_PROD) {
+        // ---- producer: quantized weight rows (1-D bulk copies) and activation tiles (2-D TMA)
+        uint32_t rg = 0, bg = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const int4 ch = A.chunks[u / A.S];
+            const int s = u % A.S;
+            const uint8_t *rows[4];
+            int fmts[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) unit_row<GATEUP>(A.table + ch.x, s, lane + 32 * i, rows[i], fmts[i]);
+            const int nb = (ch.z + TC_BOX_ROWS - 1) / TC_BOX_ROWS;
+            for (int rs = 0; rs < nR && ok; ++rs) {
+                const uint32_t slot = rg % A.RS, use = rg / A.RS;
+                if (use > 0 && !warp_wait(&raw_empty[slot], (use - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int k0 = rs * TC_KR, k1 = min(A.K, k0 + TC_KR);
+                RawSpan sp[4];
+                int tot = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    sp[i] = raw_span(rows[i], fmts[i], k0, k1);
+                    tot += (int)sp[i].bytes;
+                }
+                tot = warp_sum_i(tot);
+                if (lane == 0) mbar_expect_tx(&raw_full[slot], (uint32_t)tot);
+                __syncwarp();
+                uint8_t *dst = raw + (size_t)slot * TC_M * A.RB;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    bulk_g2s(dst + (size_t)(lane + 32 * i) * A.RB, sp[i].src, sp[i].bytes, &raw_full[slot]);
+                ++rg;
+                const int a_end = min(nA, 4 * rs + 4);
+                for (int a = 4 * rs; a < a_end; ++a) {
+                    const uint32_t bs = bg % TC_BSTAGES, buse = bg / TC_BSTAGES;
+                    if (buse > 0 && !warp_wait(&b_empty[bs], (buse - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_expect_tx(&b_full[bs], (uint32_t)(nb * TC_BOX_ROWS * 128));
+                        for (int i = 0; i < nb; ++i)
+                            tma_load_2d(bring + bs * TC_BSTAGE_BYTES + i * TC_BOX_ROWS * 128, &bmap, a * TC_KA,
+                                        ch.y + i * TC_BOX_ROWS, &b_full[bs]);
+                    }
+                    __syncwarp();
+                    ++bg;
+                }
+            }
+        }
+        if (!ok) {
+            if (lane == 0) tc_fail(abort_flag, A.status);
+            // let the copies already issued land before the CTA can exit
+            if (lane == 0) {
+                for (uint32_t j = rg > (uint32_t)A.RS ? rg - A.RS : 0; j < rg; ++j)
+                    mbar_wait(&raw_full[j % A.RS], (j / A.RS) & 1);
+                for (uint32_t j = bg > (uint32_t)TC_BSTAGES ? bg - TC_BSTAGES : 0; j < bg; ++j)
+                    mbar_wait(&b_full[j % TC_BSTAGES], (j / TC_BSTAGES) & 1);
+            }
+        }
+    } else if (warp == TC_MMA) {
+        // ---- MMA issuer: one thread
+        if (lane == 0) {
+            uint32_t ag = 0, bg = 0, uc = 0;
+            bool ok = true, issued = false;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int4 ch = A.chunks[u / A.S];
+                const int N = (ch.z + 15) & ~15;
+                const uint32_t idesc = idesc_f16(N);
+                const uint32_t d = uc & 1, use = uc >> 1;
+                if (use > 0 && !tc_wait(&acc_empty[d], (use - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tmem_fence_after();
+                const uint32_t dcol = tmem + d * TC_NCHUNK;
+                for (int a = 0; a < nA; ++a) {
+                    const uint32_t t = ag % TC_ASTAGES, bs = bg % TC_BSTAGES;
+                    if (!tc_wait(&a_full[t], (ag / TC_ASTAGES) & 1, abort_flag) ||
+                        !tc_wait(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tmem_fence_after();
+                    const uint64_t bdesc = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES));
+#pragma unroll
+                    for (int kk = 0; kk < TC_KA / 16; ++kk)
+                        mma_f16_ts(dcol, tmem + TC_ACOL0 + t * 32 + kk * 8, bdesc + 2 * kk, idesc, (a | kk) != 0);
+                    mma_commit(&a_empty[t]);
+                    mma_commit(&b_empty[bs]);
+                    issued = true;
+                    ++ag;
+                    ++bg;
+                }
+                if (!ok) break;
+                mma_commit(&acc_full[d]);
+                ++uc;
+            }
+            if (!ok) tc_fail(abort_flag, A.status);
+            if (issued) {
+                // every MMA has completed before TMEM is released
+                mma_commit(fin);
+                mbar_wait(fin, 0);
+            }
+        }
+    } else if (warp >= TC_DQ0) {
+        // ---- dequantisers: group g writes piece g (64 K) of every raw stage to TMEM
+        const int g = (warp - TC_DQ0) >> 2, qd = warp & 3, l = 32 * qd + lane;
+        uint32_t rg = 0, ag0 = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const int4 ch = A.chunks[u / A.S];
+            const int s = u % A.S;
+            const uint8_t *row;
+            int fmt;
+            unit_row<GATEUP>(A.table + ch.x, s, l, row, fmt);
+            for (int rs = 0; rs < nR; ++rs) {
+                const uint32_t slot = rg % A.RS;
+                if (!warp_wait(&raw_full[slot], (rg / A.RS) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int a = 4 * rs + g;
+                if (a < nA) {
+                    const uint32_t AG = ag0 + a, t = AG % TC_ASTAGES, use = AG / TC_ASTAGES;
+                    if (use > 0 && !warp_wait(&a_empty[t], (use - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tmem_fence_after();
+                    const int k0 = rs * TC_KR;
+                    const RawSpan sp = raw_span(row, fmt, k0, min(A.K, k0 + TC_KR));
+                    const uint32_t base = smem_addr(raw + (size_t)slot * TC_M * A.RB + (size_t)l * A.RB) + sp.lead;
+                    uint32_t r[32];
+                    if (fmt == MOE_Q4_K)
+                        dq_q4k(base, g, r);
+                    else if (fmt == MOE_Q8_0)
+                        dq_q8_0(base, g, r);
+                    else if (fmt == MOE_Q6_K)
+                        dq_q6k(base, g, r);
+                    else
+                        dq_mxfp4(base, g, r);
+                    tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + t * 32, r);
+                    tmem_wait_st();
+                    tmem_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cta(&a_full[t]);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cta(&raw_empty[slot]);
+                ++rg;
+            }
+            ag0 += nA;
+        }
+        if (!ok && lane == 0) tc_fail(abort_flag, A.status);
+    } else {
+        // ---- epilogue: warps 0-3 read TMEM lanes 32w..32w+31
+        const int l = 32 * warp + lane;
+        uint32_t uc = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            const int4 ch = A.chunks[u / A.S];
+            const int s = u % A.S, n = ch.z, row0 = ch.y;
+            const uint32_t d = uc & 1;
+            bool ok = warp_wait(&acc_full[d], (uc >> 1) & 1, abort_flag);
+            if (GATEUP) ok = epi_all(ok);
+            if (!ok) {
+                if (lane == 0) tc_fail(abort_flag, A.status);
+                break;
+            }
+            tmem_fence_after();
+            for (int cb = 0; cb < n; cb += 32) {
+                uint32_t v[32];
+                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + d * TC_NCHUNK + cb, v);
+                tmem_wait_ld();
+                if (GATEUP) {
+                    if (warp >= 2) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) ubuf[j * 64 + (l - 64)] = __uint_as_float(v[j]);
+                    }
+                    epi_sync();
+                    if (warp < 2) {
+                        const int jn = min(32, n - cb);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            if (j >= jn) break;
+                            const int qrow = row0 + cb + j;
+                            const float sc = A.ascale[qrow];
+                            const float gv = __uint_as_float(v[j]) * sc, uv = ubuf[j * 64 + l] * sc;
+                            const float h = silu_f32(gv) * uv;
+                            A.h32[(size_t)qrow * A.I + 64 * s + l] = h;
+                            const float m = warp_max_f(fabsf(h));
+                            if (lane == 0) atomicMax(&A.hmax[qrow], __float_as_uint(m));
+                        }
+                    }
+                    epi_sync();
+                } else {
+                    const int jn = min(32, n - cb);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j >= jn) break;
+                        const int qrow = row0 + cb + j;
+                        A.y[(size_t)qrow * A.H + TC_M * s + l] = __uint_as_float(v[j]) * A.ascale[qrow];
+                    }
+                }
+            }
+            tmem_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cta(&acc_empty[d]);
+            ++uc;
+        }
+    }
+
+    tmem_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tmem_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ preparation kernels
+constexpr int PREP_THREADS = 256;
+
+// sigma with maxabs * 2^sigma in [2^14, 2^15): fp16 keeps 11 significant bits
+// of every value within 2^-10 of the row's largest and cannot overflow.
+__device__ __forceinline__ int row_shift(float maxabs) {
+    if (!(maxabs > 0.0f) || !isfinite(maxabs)) return 0;
+    int e;
+    frexpf(maxabs, &e);  // maxabs = f * 2^e, f in [0.5, 1)
+    return max(-120, min(120, 15 - e));
+}
+__device__ __forceinline__ float pow2f(int s) { return ldexpf(1.0f, s); }
+
+__device__ __forceinline__ float block_max(float v, float *red) {
+    v = warp_max_f(v);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        v = lane < PREP_THREADS / 32 ? red[lane] : 0.0f;
+        v = warp_max_f(v);
+        if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    return red[0];
+}
+
+// Blocks 0..T-1: token t's bf16 row -> fp16 scaled by 2^sigma_t, copied to the
+// bucket row of each of its kept pairs (so every expert's rows are contiguous
+// for the B tiles); that row's inverse scale; its |h| maximum cleared.
+// Block T: the chunk table, <= 128 bucket rows of one expert per chunk, in
+// ascending expert order.
+__global__ void __launch_bounds__(PREP_THREADS) tc_prep_kernel(const uint16_t *__restrict__ x, int T, int k, int H,
+                                                               int E, const int32_t *__restrict__ pos,
+                                                               const int32_t *__restrict__ offsets,
+                                                               const int32_t *__restrict__ active, __half *xg,
+                                                               float *xinv, uint32_t *hmax, int4 *chunks,
+                                                               int32_t *n_chunks) {
+    __shared__ float red[PREP_THREADS / 32];
+    __shared__ int scan[PREP_THREADS];
+    if ((int)blockIdx.x < T) {
+        const int t = blockIdx.x;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+        const int n8 = H / 8;
+        float m = 0.0f;
+        for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
+            const uint4 v = xr[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+        }
+        m = block_max(m, red);
+        const int sg = row_shift(m);
+        const float sc = pow2f(sg), inv = pow2f(-sg);
+        for (int j = 0; j < k; ++j) {
+            const int q = pos[(size_t)t * k + j];
+            if (q < 0) continue;
+            uint4 *dst = reinterpret_cast<uint4 *>(xg + (size_t)q * H);
+            for (int i = threadIdx.x; i < n8; i += PREP_THREADS) {
+                const uint4 v = xr[i];
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const __half2 h2 = __floats2half2_rn(__uint_as_float(w[jj] << 16) * sc,
+                                                         __uint_as_float(w[jj] & 0xffff0000u) * sc);
+                    o[jj] = *reinterpret_cast<const uint32_t *>(&h2);
+                }
+                dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+            if (threadIdx.x == 0) {
+                xinv[q] = inv;
+                hmax[q] = 0u;
+            }
+        }
+        return;
+    }
+    // chunk table
+    const int n_act = active[0];
+    int total = 0;
+    for (int base = 0; base < n_act; base += PREP_THREADS) {
+        const int i = base + threadIdx.x;
+        int e = 0, cnt = 0, nch = 0;
+        if (i < n_act) {
+            e = active[1 + i];
+            cnt = offsets[e + 1] - offsets[e];
+            nch = (cnt + TC_NCHUNK - 1) / TC_NCHUNK;
+        }
+        scan[threadIdx.x] = nch;
+        __syncthreads();
+        for (int o = 1; o < PREP_THREADS; o <<= 1) {
+            const int v = threadIdx.x >= o ? scan[threadIdx.x - o] : 0;
+            __syncthreads();
+            scan[threadIdx.x] += v;
+            __syncthreads();
+        }
+        const int first = total + scan[threadIdx.x] - nch;
+        for (int c = 0; c < nch; ++c)
+            chunks[first + c] = make_int4(e, offsets[e] + c * TC_NCHUNK, min(TC_NCHUNK, cnt - c * TC_NCHUNK), 0);
+        total += scan[PREP_THREADS - 1];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *n_chunks = total;
+}
+
+// One warp per bucket row: h (fp32) -> fp16 scaled by 2^sigma from the row's
+// |h| maximum, and the inverse scale.
+__global__ void __launch_bounds__(PREP_THREADS) tc_hprep_kernel(const float *__restrict__ h32,
+                                                                const uint32_t *__restrict__ hmax,
+                                                                const int32_t *__restrict__ offsets, int E, int I,
+                                                                __half *h16, float *hinv) {
+    const int q = blockIdx.x * (PREP_THREADS / 32) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (q >= offsets[E]) return;
+    const int sg = row_shift(__uint_as_float(hmax[q]));
+    const float sc = pow2f(sg);
+    const float4 *src = reinterpret_cast<const float4 *>(h32 + (size_t)q * I);
+    uint2 *dst = reinterpret_cast<uint2 *>(h16 + (size_t)q * I);
+    for (int i = lane; i < I / 4; i += 32) {
+        const float4 v = src[i];
+        const __half2 a = __floats2half2_rn(v.x * sc, v.y * sc), b = __floats2half2_rn(v.z * sc, v.w * sc);
+        dst[i] = make_uint2(*reinterpret_cast<const uint32_t *>(&a), *reinterpret_cast<const uint32_t *>(&b));
+    }
+    if (lane == 0) hinv[q] = pow2f(-sg);
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime
+// (no link-time dependency on libcuda).
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// fp16 matrix [rows][cols] row-major: boxes of 64 columns (128 bytes) x 16
+// rows, 128-byte swizzle, zero fill outside.
+bool encode_act_map(CUtensorMap *map, const void *base, int rows, int cols) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {TC_KA, TC_BOX_ROWS};
+    const cuuint32_t es[2] = {1, 1};
+    return f(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Shared-memory pitch of one weight row's raw stage: its blocks for 256 K plus
+// up to 30 bytes of 16-byte widening, as an odd number of 16-byte units so
+// that the 16-byte loads of 8 consecutive rows hit distinct banks.
+int raw_pitch(uint32_t fmask) {
+    int rb = 0;
+    for (int f = MOE_Q8_0; f <= MOE_MXFP4; ++f) {
+        if (!(fmask & (1u << f))) continue;
+        int b = (TC_KR / BLOCK_ELEMS[f]) * BLOCK_BYTES[f] + 30;
+        b = (b + 15) & ~15;
+        if (((b / 16) & 1) == 0) b += 16;
+        rb = b > rb ? b : rb;
+    }
+    return rb;
+}
+
+int g_tc_smem_optin[64] = {};
+
+int smem_optin() {
+    const int dev = current_device();
+    if (dev < 64 && g_tc_smem_optin[dev]) return g_tc_smem_optin[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    if (cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess)
+        return 0;
+    if (dev < 64) g_tc_smem_optin[dev] = v;
+    return v;
+}
+
+// Raw ring depth that fits next to the fixed shared memory; 0 if < 2.
+int raw_stages(int rb) {
+    const int optin = smem_optin();
+    if (optin <= 0 || rb <= 0) return 0;
+    const long room = (long)optin - (long)tc_smem_bytes(rb, 0);
+    long rs = room / ((long)TC_M * rb);
+    if (rs > TC_RS_MAX) rs = TC_RS_MAX;
+    return rs >= 2 ? (int)rs : 0;
+}
+
+}  // namespace
+
+bool tc_path_eligible(int H, int I) { return H >= TC_M && H % TC_M == 0 && I >= 64 && I % 64 == 0; }
+
+cudaError_t launch_tc_path(const DevExpert *table, uint32_t gu_formats, uint32_t dn_formats, int T, int k, int E,
+                           int H, int I, const int32_t *offsets, const int32_t *active, const int32_t *pos,
+                           const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
+                           const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
+                           cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    const int P = T * k;
+    const int rb1 = raw_pitch(gu_formats), rb2 = raw_pitch(dn_formats);
+    const int rs1 = raw_stages(rb1), rs2 = raw_stages(rb2);
+    const int G = sm_count();
+    if (!rs1 || !rs2 || G <= 0) return cudaErrorInvalidConfiguration;
+    __half *xg = reinterpret_cast<__half *>(ws_base + C.xg);
+    __half *h16 = reinterpret_cast<__half *>(ws_base + C.h16);
+    float *xinv = reinterpret_cast<float *>(ws_base + C.xinv);
+    float *hinv = reinterpret_cast<float *>(ws_base + C.hinv);
+    uint32_t *hmax = reinterpret_cast<uint32_t *>(ws_base + C.hmax);
+    int4 *chunks = reinterpret_cast<int4 *>(ws_base + C.chunks);
+    int32_t *n_chunks = reinterpret_cast<int32_t *>(ws_base + C.n_chunks);
+    CUtensorMap xmap, hmap;
+    if (!encode_act_map(&xmap, xg, P, H) || !encode_act_map(&hmap, h16, P, I)) return cudaErrorInvalidValue;
+
+    cudaError_t err;
+    tc_prep_kernel<<<T + 1, PREP_THREADS, 0, s>>>(x, T, k, H, E, pos, offsets, active, xg, xinv, hmax, chunks,
+                                                   n_chunks);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
+
+    TcArgs a1{table, chunks, n_chunks, H, I / 64, H, I, rb1, rs1, xinv, h32, hmax, nullptr, status};
+    tc_gemm_kernel<true><<<G, TC_THREADS, tc_smem_bytes(rb1, rs1), s>>>(xmap, a1);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (events && (err = record_event(events[1], s)) != cudaSuccess) return err;
+
+    tc_hprep_kernel<<<(P + PREP_THREADS / 32 - 1) / (PREP_THREADS / 32), PREP_THREADS, 0, s>>>(h32, hmax, offsets, E,
+                                                                                             I, h16, hinv);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    TcArgs a2{table, chunks, n_chunks, I, H / TC_M, H, I, rb2, rs2, hinv, nullptr, nullptr, y, status};
+    tc_gemm_kernel<false><<<G, TC_THREADS, tc_smem_bytes(rb2, rs2), s>>>(hmap, a2);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
+    return launch_combine(T, k, H, pos, wts, y, out, s);
+}
+
+}  // namespace moe
