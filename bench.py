@@ -35,7 +35,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s; expert-weight HBM GB/s and % of GB300 roofline"
 UNIT = "tokens/s"
-KERNELS_PER_LAYER = 5   # route, bucket, gate/up, down, combine
+KERNELS_PER_LAYER = {1: 5,   # GEMV: route, bucket, gate/up, down, combine
+                     2: 7,   # tensor: route, bucket, prep, gate/up GEMM, h conversion, down GEMM, combine
+                     3: 1}   # fused decode: one kernel
 
 
 def parse_args(argv=None):
@@ -50,6 +52,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--path", type=int, default=0, help="0 auto, 1 grouped GEMV, 2 tensor cores, 3 fused decode")
     return p.parse_args(argv)
 
 
@@ -284,14 +287,14 @@ def run_ours(args, world, rank, local, cpu_proc):
         DL = sgpu.make_device_layer(cfg, rank * NL + l)
         layers.append(DL)
         tables.append(M.WeightTable(DL.experts, H, I))
-        wss.append(M.Workspace(tables[-1], T, k))
+        wss.append(M.Workspace(tables[-1], T, k, path=args.path))
         outs.append(torch.empty((T, H), dtype=torch.float32, device=dev))
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(NL)]
-    opts_plain = M.make_options(n_experts=E)
-    opts_timed = [M.make_options(n_experts=E, timing_events=ev[l]) for l in range(NL)]
+    opts_plain = M.make_options(n_experts=E, path=args.path)
+    opts_timed = [M.make_options(n_experts=E, path=args.path, timing_events=ev[l]) for l in range(NL)]
 
     def step(timed: bool):
         for l in range(NL):
@@ -419,15 +422,32 @@ def run_ours(args, world, rank, local, cpu_proc):
     mean_pairs = float(np.mean(per_layer_pairs))
     gu_bytes = float(np.mean(per_layer_gu_bytes)) + T * H * 2 + mean_pairs * I * 4
     dn_bytes = float(np.mean(per_layer_dn_bytes)) + mean_pairs * I * 4 + mean_pairs * H * 4
-    path = M.ffn_path(tables[0], T, k)
+    path = M.ffn_path(tables[0], T, k, opts_plain)
+    gu_name, dn_name = (("tc_gemm_kernel<gate/up>", "tc_hprep_kernel + tc_gemm_kernel<down>")
+                        if path == M.PATH_TENSOR else ("gateup_gemv_kernel", "down_gemv_kernel"))
+    if path == M.PATH_TENSOR:
+        # the h conversion runs between the two timing events of the down projection
+        dn_bytes += mean_pairs * I * 2
     if path == M.PATH_FUSED:
         # one kernel runs the whole layer: its algorithmic bytes are the layer's
         kname, kbytes, kdur = "decode_fused_kernel", layer_bytes, gu_avg + dn_avg
     elif gu_avg >= dn_avg:
-        kname, kbytes, kdur = "gateup_gemv_kernel", gu_bytes, gu_avg
+        kname, kbytes, kdur = gu_name, gu_bytes, gu_avg
     else:
-        kname, kbytes, kdur = "down_gemv_kernel", dn_bytes, dn_avg
+        kname, kbytes, kdur = dn_name, dn_bytes, dn_avg
     achieved = kbytes / kdur / 1e9
+    tensor_pipe = None
+    if path == M.PATH_TENSOR:
+        # dense fp16 MMA work of the gate/up and down GEMMs (2 flops per MAC,
+        # 3 matrices of H x I per routed pair), against the measured bf16
+        # peak (fp16 and bf16 share the dense tensor rate)
+        flops = 2.0 * mean_pairs * 3 * H * I
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        tf = flops / (gu_avg + dn_avg) / 1e12
+        tensor_pipe = {"flops_per_layer": flops, "achieved_tflops": tf, "peak_tflops": pk["bf16_tflops"],
+                       "frac": tf / pk["bf16_tflops"], "peak_kind": "measured bf16 dense burst",
+                       "window": "gate/up GEMM + h conversion + down GEMM"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
@@ -449,10 +469,11 @@ def run_ours(args, world, rank, local, cpu_proc):
                      "frac": achieved / hbm_peak, "traffic": kernel_traffic(kname, args.config),
                      "bytes_per_launch": kbytes, "launch_us": kdur * 1e6, "peak_kind": peak_kind,
                      "other_kernel_us": (0.0 if path == M.PATH_FUSED else
-                                         (dn_avg if kname.startswith("gateup") else gu_avg) * 1e6)},
+                                         (dn_avg if kname == gu_name else gu_avg) * 1e6)},
+        "tensor_pipe": tensor_pipe,
         "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
-        "gpu_launches": (1 if path == M.PATH_FUSED else KERNELS_PER_LAYER) * NL * args.steps,
+        "gpu_launches": KERNELS_PER_LAYER[path] * NL * args.steps,
         "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
                  M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
         "clocks": clk,

@@ -125,7 +125,7 @@ typedef struct {
      * (experts stored as one strided tensor): kernels then compute the
      * descriptors instead of reading them. */
     int32_t uniform_layout;
-    int32_t reserved2;
+    int32_t tc_maps;           /* 1 when the tensor path's per-matrix TMA descriptors were built */
     moe_expert uniform_base;
     int64_t uniform_step[3];
 } moe_weight_table;
@@ -166,7 +166,9 @@ const char *moe_strerror(int code);
 /* The last CUDA error seen by this thread (cudaError_t value, 0 if none). */
 int moe_last_cuda_error(void);
 
-/* Bytes of device memory moe_table_prepare needs for `n_experts` experts. */
+/* Bytes of device memory moe_table_prepare needs for `n_experts` experts:
+ * the 72-byte descriptors, then 3 x 128-byte TMA tensor maps per expert for
+ * the tensor path. */
 size_t moe_table_device_bytes(int32_t n_experts);
 
 /* Validate W (shapes, formats, strides, alignment) and copy its descriptors

@@ -55,7 +55,7 @@ class WeightTableC(ctypes.Structure):
                 ("prepared", ctypes.c_uint32), ("gateup_formats", ctypes.c_uint32),
                 ("down_formats", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
                 ("max_down_stride", ctypes.c_int64), ("uniform_layout", ctypes.c_int32),
-                ("reserved2", ctypes.c_int32), ("uniform_base", Expert),
+                ("tc_maps", ctypes.c_int32), ("uniform_base", Expert),
                 ("uniform_step", ctypes.c_int64 * 3)]
 
 

@@ -27,7 +27,10 @@ cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *
                                 int32_t *active, int32_t *pairs, int32_t *pos, unsigned char *sync, uint32_t *status,
                                 cudaStream_t s);
 bool tc_path_eligible(int H, int I);
-cudaError_t launch_tc_path(const DevExpert *table, uint32_t gu_formats, uint32_t dn_formats, int T, int k, int E,
+size_t tc_weight_map_bytes(int E);
+bool tc_encode_weight_maps(const moe_weight_table *W, void *out);
+cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t gu_formats, uint32_t dn_formats,
+                           int T, int k, int E,
                            int H, int I, const int32_t *offsets, const int32_t *active, const int32_t *pos,
                            const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
                            const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
@@ -57,6 +60,9 @@ cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// Offset of the tensor path's weight maps in the prepared device table.
+size_t map_offset(int E) { return align_up((size_t)E * sizeof(DevExpert), 128); }
+
 int check_matrix(const moe_matrix &m, int rows, int cols) {
     if (m.format < MOE_Q8_0 || m.format > MOE_MXFP4) return MOE_ERR_BAD_FORMAT;
     if (m.rows != rows || m.cols != cols) return MOE_ERR_BAD_SHAPE;
@@ -72,7 +78,7 @@ int check_matrix(const moe_matrix &m, int rows, int cols) {
 int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
     const bool fused_ok = decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
                                                 W->down_formats, W->max_gateup_stride, W->max_down_stride);
-    const bool tc_ok = tc_path_eligible(W->hidden, W->inter);
+    const bool tc_ok = W->tc_maps == 1 && tc_path_eligible(W->hidden, W->inter);
     switch (requested) {
         case MOE_PATH_AUTO:
             return fused_ok ? MOE_PATH_FUSED : (T > MOE_GEMV_MAX_ROWS && tc_ok) ? MOE_PATH_TENSOR : MOE_PATH_GEMV;
@@ -123,7 +129,7 @@ int moe_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t moe_table_device_bytes(int32_t n_experts) {
     if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return 0;
-    return align_up((size_t)n_experts * sizeof(DevExpert), 256);
+    return align_up(map_offset(n_experts) + tc_weight_map_bytes(n_experts), 256);
 }
 
 int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes, moe_stream_t stream) {
@@ -163,6 +169,18 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     cudaError_t err = cudaMemcpyAsync(device_buf, dev.data(), (size_t)E * sizeof(DevExpert), cudaMemcpyHostToDevice,
                                       stream);
     if (err != cudaSuccess) return cuda_fail(err);
+    // the tensor path's TMA descriptors of every weight matrix
+    std::vector<unsigned char> maps;
+    W->tc_maps = 0;
+    if (tc_path_eligible(H, I)) {
+        maps.resize(tc_weight_map_bytes(E));
+        if (tc_encode_weight_maps(W, maps.data())) {
+            err = cudaMemcpyAsync(static_cast<char *>(device_buf) + map_offset(E), maps.data(), maps.size(),
+                                  cudaMemcpyHostToDevice, stream);
+            if (err != cudaSuccess) return cuda_fail(err);
+            W->tc_maps = 1;
+        }
+    }
     err = cudaStreamSynchronize(stream);
     if (err != cudaSuccess) return cuda_fail(err);
     // uniform layout: experts at a constant step with identical formats and strides
@@ -288,7 +306,8 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
                         status, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     if (path == MOE_PATH_TENSOR)
-        err = launch_tc_path(table, W->gateup_formats, W->down_formats, T, k, E, H, I, offsets, active, pos, wts, x,
+        err = launch_tc_path(table, static_cast<const char *>(W->device_table) + map_offset(E), W->gateup_formats,
+                             W->down_formats, T, k, E, H, I, offsets, active, pos, wts, x,
                              h, y, base, tc_ws_layout(T, k, E, H, I), out, status, events, stream);
     else
         err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, offsets, pairs,

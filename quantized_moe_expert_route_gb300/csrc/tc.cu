@@ -29,6 +29,8 @@
 // (lanes 64-127), so SwiGLU needs only the CTA's own accumulator.
 #include <cuda.h>
 
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -37,43 +39,55 @@ namespace {
 
 constexpr int TC_M = 128;                    // weight rows per unit = TMEM lanes
 constexpr int TC_NCHUNK = 128;               // activation rows per chunk (MMA N <= 128)
-constexpr int TC_KA = 64;                    // K per A/B stage: one 128-byte row of fp16
+constexpr int TC_KA = 64;                    // K per A step: one 128-byte row of fp16
 constexpr int TC_KR = 256;                   // K per raw (quantized) stage
 constexpr int TC_ASTAGES = 8;                // A stages in TMEM, 32 columns each
 constexpr int TC_BSTAGES = 4;                // B stages in shared memory
 constexpr int TC_BSTAGE_BYTES = TC_NCHUNK * 128;
-constexpr int TC_BOX_ROWS = 16;              // rows per B TMA box
-constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups = A stages per raw stage
+constexpr int TC_BOX_ROWS = 16;              // rows per activation TMA box
+constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups = A steps per raw stage
 constexpr int TC_DQ0 = 4;                    // warps 0-3 epilogue, 4..19 dequant
-constexpr int TC_PROD = TC_DQ0 + 4 * TC_DG;  // 20: TMA producer
+constexpr int TC_PROD = TC_DQ0 + 4 * TC_DG;  // 20: weight producer (TMA)
 constexpr int TC_MMA = TC_PROD + 1;          // 21: MMA issuer
-constexpr int TC_WARPS = TC_MMA + 1;
-constexpr int TC_THREADS = TC_WARPS * 32;    // 704
+constexpr int TC_BPROD = TC_MMA + 1;         // 22: activation producer (TMA)
+constexpr int TC_WARPS = TC_BPROD + 1;
+constexpr int TC_THREADS = TC_WARPS * 32;    // 736
 constexpr int TC_TMEM_COLS = 512;
 constexpr int TC_ACOL0 = 2 * TC_NCHUNK;      // A stages after the two accumulators
-constexpr int TC_RS_MAX = 6;
+constexpr int TC_RS_MAX = 8;
 constexpr int TC_UBUF_FLOATS = 32 * 64;
 constexpr int TC_NBARS = 2 * TC_RS_MAX + 2 * TC_ASTAGES + 2 * TC_BSTAGES + 4 + 1;
 constexpr uint32_t TC_NEG1152 = 0xE480E480u;  // fp16 pair (-1152, -1152)
 constexpr uint32_t TC_NEG1056 = 0xE420E420u;  // fp16 pair (-1056, -1056)
 constexpr uint32_t TC_MAGIC = 0x64006400u;    // fp16 pair (1024, 1024)
 
+// Raw stage geometry per format (index = moe_format): a stage holds, for each
+// weight row, the blocks of 256 K as TMA boxes of RAW_W bytes (widened to
+// 16-byte boundaries); Q8_0's 272 bytes take two boxes, 128 bytes apart.
+__host__ __device__ constexpr int raw_w(int f) { return f == MOE_Q6_K ? 240 : 144; }
+__host__ __device__ constexpr int raw_nbox(int f) { return f == MOE_Q8_0 ? 2 : 1; }
+__host__ __device__ constexpr int blk_elems(int f) { return f == MOE_Q4_K || f == MOE_Q6_K ? 256 : 32; }
+__host__ __device__ constexpr int blk_bytes(int f) {
+    return f == MOE_Q8_0 ? 34 : f == MOE_Q4_K ? 144 : f == MOE_Q6_K ? 210 : 17;
+}
+
 static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
 static_assert(TC_DG == 4, "one dequantising warpgroup per 64-K piece of a raw stage");
 
 struct TcArgs {
     const DevExpert *table;
-    const int4 *chunks;      // {expert, first bucket row, rows, 0}
+    const CUtensorMap *wmaps;  // per expert: gate, up, down weight maps (bytes [rows][stride])
+    const int4 *chunks;        // {expert, first bucket row, rows, 0}
     const int32_t *n_chunks;
-    int K;                   // reduction length: H (gate/up) or I (down)
-    int S;                   // units per chunk: I/64 (gate/up) or H/128 (down)
+    int K;                     // reduction length: H (gate/up) or I (down)
+    int S;                     // units per chunk: I/64 (gate/up) or H/128 (down)
     int H, I;
-    int RB;                  // raw row pitch in shared memory, bytes
-    int RS;                  // raw stages in the ring
-    const float *ascale;     // per bucket row: 2^-sigma of its fp16 activation row
-    float *h32;              // gate/up: h [rows][I] fp32, bucket order
-    uint32_t *hmax;          // gate/up: max |h| bits per bucket row
-    float *y;                // down: y [rows][H] fp32, bucket order
+    int slot_bytes;            // raw stage bytes
+    int RS;                    // raw stages in the ring
+    const float *ascale;       // per bucket row: 2^-sigma of its fp16 activation row
+    float *h32;                // gate/up: h [rows][I] fp32, bucket order
+    uint32_t *hmax;            // gate/up: max |h| bits per bucket row
+    float *y;                  // down: y [rows][H] fp32, bucket order
     uint32_t *status;
 };
 
@@ -135,6 +149,10 @@ __device__ __forceinline__ uint64_t global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// Each poll may suspend the thread up to this long (ns); it resumes as soon
+// as the phase completes, so waiting warps do not spin on the issue slots.
+constexpr uint32_t TC_SUSPEND_NS = 20000;
+
 // Bounded parity wait (TC_WAIT_NS, or WAIT_LIMIT polls) that also gives up
 // once another role has aborted.
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
@@ -143,15 +161,15 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         uint32_t done;
         asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
             : "=r"(done)
-            : "r"(addr), "r"(parity)
+            : "r"(addr), "r"(parity), "r"(TC_SUSPEND_NS)
             : "memory");
         if (done) return true;
-        if ((i & 255u) == 255u) {
+        if ((i & 15u) == 15u) {
             if (*abort_flag) return false;
             const uint64_t now = global_ns();
-            if (i == 255u)
+            if (i == 15u)
                 t0 = now;
             else if (now - t0 > TC_WAIT_NS)
                 return false;
@@ -298,10 +316,8 @@ __device__ __forceinline__ void dq_q4k(uint32_t blk, int g, uint32_t (&r)[32]) {
     }
 }
 
-// Q8_0: piece g = blocks 2g and 2g+1 of the stage, at bytes 68g and 68g + 34
-// of the 16-aligned stage row. w = d*q.
-__device__ __forceinline__ void dq_q8_0(uint32_t row, int g, uint32_t (&r)[32]) {
-    const uint32_t p = row + 68 * g;  // 4-aligned
+// Q8_0: a piece is two consecutive blocks (68 bytes, 4-aligned at p). w = d*q.
+__device__ __forceinline__ void dq_q8_0(uint32_t p, uint32_t (&r)[32]) {
     uint32_t v[17];
 #pragma unroll
     for (int i = 0; i < 17; ++i) v[i] = lds32(p + 4 * i);
@@ -388,42 +404,36 @@ __device__ __forceinline__ void dq_mxfp4(uint32_t blk, int g, uint32_t (&r)[32])
     }
 }
 
-// Raw bytes one weight row needs for the K range [k0, k1): the blocks that
-// cover it, widened to 16-byte boundaries. `lead` = offset of the first block
-// inside the copied range.
-struct RawSpan {
-    const uint8_t *src;
-    uint32_t bytes, lead;
-};
-__device__ __forceinline__ RawSpan raw_span(const uint8_t *row, int fmt, int k0, int k1) {
-    const int be = fmt == MOE_Q4_K || fmt == MOE_Q6_K ? 256 : 32;
-    const int bb = fmt == MOE_Q8_0 ? 34 : fmt == MOE_Q4_K ? 144 : fmt == MOE_Q6_K ? 210 : 17;
-    const uintptr_t s = reinterpret_cast<uintptr_t>(row) + (uintptr_t)(k0 / be) * bb;
-    const uintptr_t t = reinterpret_cast<uintptr_t>(row) + (uintptr_t)((k1 + be - 1) / be) * bb;
-    const uintptr_t a0 = s & ~(uintptr_t)15, a1 = (t + 15) & ~(uintptr_t)15;
-    return RawSpan{reinterpret_cast<const uint8_t *>(a0), (uint32_t)(a1 - a0), (uint32_t)(s - a0)};
+// Raw stage rs of a weight row: the byte offset (within the row) of the first
+// block of K range [256 rs, ...), the 16-byte-aligned x of its TMA box and the
+// lead of the block inside the box.
+__host__ __device__ __forceinline__ void raw_x(int fmt, int rs, int &x0, int &lead) {
+    const int s = (rs * TC_KR / blk_elems(fmt)) * blk_bytes(fmt);
+    x0 = s & ~15;
+    lead = s - x0;
 }
 
 // ------------------------------------------------------------------ the grouped GEMM
-size_t tc_smem_bytes(int RB, int RS) {
-    return 1024 + (size_t)TC_BSTAGES * TC_BSTAGE_BYTES + (size_t)RS * TC_M * RB + TC_UBUF_FLOATS * 4 + TC_NBARS * 8 +
-           16;
+size_t tc_smem_bytes(int slot_bytes, int RS) {
+    return 1024 + (size_t)TC_BSTAGES * TC_BSTAGE_BYTES + (size_t)RS * slot_bytes + TC_UBUF_FLOATS * 4 +
+           TC_NBARS * 8 + 64;
 }
 
-// The weight row behind TMEM lane l of unit slice s.
+struct Unit {
+    int e, row0, n, s, fmt;
+};
+
+// Unit u: its chunk, slice and (for the producer) the weight format.
 template <bool GATEUP>
-__device__ __forceinline__ void unit_row(const DevExpert *ex, int s, int l, const uint8_t *&row, int &fmt) {
-    const DevMatrix *m;
-    int r;
-    if (GATEUP) {
-        m = l < 64 ? &ex->gate : &ex->up;
-        r = 64 * s + (l & 63);
-    } else {
-        m = &ex->down;
-        r = TC_M * s + l;
-    }
-    row = m->data + (size_t)r * m->stride;
-    fmt = m->fmt;
+__device__ __forceinline__ Unit load_unit(const TcArgs &A, int u, bool want_fmt) {
+    Unit x{0, 0, 0, 0, 0};
+    const int4 ch = A.chunks[u / A.S];
+    x.e = ch.x;
+    x.row0 = ch.y;
+    x.n = ch.z;
+    x.s = u % A.S;
+    if (want_fmt) x.fmt = GATEUP ? A.table[x.e].gate.fmt : A.table[x.e].down.fmt;
+    return x;
 }
 
 // Warp-uniform bounded wait: lane 0 polls, the result is broadcast.
@@ -444,22 +454,31 @@ __device__ __forceinline__ bool epi_all(bool pred) {
 }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Activation rows per B stage for a unit of n rows: q A steps of Npad rows.
+__device__ __forceinline__ int b_steps_per_stage(int n) {
+    const int npad = (n + 15) & ~15;
+    return TC_NCHUNK / npad;
+}
+
 template <bool GATEUP>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const TcArgs A) {
     extern __shared__ __align__(16) uint8_t tc_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t *bring = sm;
     uint8_t *raw = bring + TC_BSTAGES * TC_BSTAGE_BYTES;
-    float *ubuf = reinterpret_cast<float *>(raw + (size_t)A.RS * TC_M * A.RB);
+    float *ubuf = reinterpret_cast<float *>(raw + (size_t)A.RS * A.slot_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(ubuf + TC_UBUF_FLOATS);
     uint64_t *raw_full = bars, *raw_empty = bars + TC_RS_MAX;
     uint64_t *a_full = bars + 2 * TC_RS_MAX, *a_empty = a_full + TC_ASTAGES;
     uint64_t *b_full = a_empty + TC_ASTAGES, *b_empty = b_full + TC_BSTAGES;
     uint64_t *acc_full = b_empty + TC_BSTAGES, *acc_empty = acc_full + 2, *fin = acc_empty + 2;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + TC_NBARS);
+    uint32_t *raw_info = reinterpret_cast<uint32_t *>(bars + TC_NBARS);  // [TC_RS_MAX]: fmt | lead << 8
+    uint32_t *tmem_slot = raw_info + TC_RS_MAX;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int R = GATEUP ? 64 : 128;          // weight rows per matrix box
+    constexpr int NMAT = GATEUP ? 2 : 1;
     if (threadIdx.x == 0) {
         for (int i = 0; i < A.RS; ++i) {
             mbar_init(&raw_full[i], 1);
@@ -494,65 +513,72 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 
     const int n_units = *A.n_chunks * A.S;
     const int nR = (A.K + TC_KR - 1) / TC_KR, nA = A.K / TC_KA;
+    const int G = gridDim.x;
 
     if (warp == TC_PROD) {
-        // ---- producer: quantized weight rows (1-D bulk copies) and activation tiles (2-D TMA)
-        uint32_t rg = 0, bg = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const int4 ch = A.chunks[u / A.S];
-            const int s = u % A.S;
-            const uint8_t *rows[4];
-            int fmts[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) unit_row<GATEUP>(A.table + ch.x, s, lane + 32 * i, rows[i], fmts[i]);
-            const int nb = (ch.z + TC_BOX_ROWS - 1) / TC_BOX_ROWS;
-            for (int rs = 0; rs < nR && ok; ++rs) {
-                const uint32_t slot = rg % A.RS, use = rg / A.RS;
-                if (use > 0 && !warp_wait(&raw_empty[slot], (use - 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                const int k0 = rs * TC_KR, k1 = min(A.K, k0 + TC_KR);
-                RawSpan sp[4];
-                int tot = 0;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    sp[i] = raw_span(rows[i], fmts[i], k0, k1);
-                    tot += (int)sp[i].bytes;
-                }
-                tot = warp_sum_i(tot);
-                if (lane == 0) mbar_expect_tx(&raw_full[slot], (uint32_t)tot);
-                __syncwarp();
-                uint8_t *dst = raw + (size_t)slot * TC_M * A.RB;
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    bulk_g2s(dst + (size_t)(lane + 32 * i) * A.RB, sp[i].src, sp[i].bytes, &raw_full[slot]);
-                ++rg;
-                const int a_end = min(nA, 4 * rs + 4);
-                for (int a = 4 * rs; a < a_end; ++a) {
-                    const uint32_t bs = bg % TC_BSTAGES, buse = bg / TC_BSTAGES;
-                    if (buse > 0 && !warp_wait(&b_empty[bs], (buse - 1) & 1, abort_flag)) {
+        // ---- weight producer: per raw stage one 2-D TMA box per matrix (two for Q8_0)
+        if (lane == 0) {
+            uint32_t rg = 0;
+            bool ok = true;
+            Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, true) : Unit{};
+            for (int u = blockIdx.x; u < n_units && ok; u += G) {
+                const Unit cu = nxt;
+                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, true);
+                const int W = raw_w(cu.fmt), nbox = raw_nbox(cu.fmt);
+                const uint32_t bytes = (uint32_t)(NMAT * nbox * R * W);
+                const CUtensorMap *m0 = A.wmaps + 3 * cu.e + (GATEUP ? 0 : 2);
+                for (int rs = 0; rs < nR; ++rs) {
+                    const uint32_t slot = rg % A.RS, use = rg / A.RS;
+                    if (use > 0 && !tc_wait(&raw_empty[slot], (use - 1) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0) {
-                        mbar_expect_tx(&b_full[bs], (uint32_t)(nb * TC_BOX_ROWS * 128));
-                        for (int i = 0; i < nb; ++i)
-                            tma_load_2d(bring + bs * TC_BSTAGE_BYTES + i * TC_BOX_ROWS * 128, &bmap, a * TC_KA,
-                                        ch.y + i * TC_BOX_ROWS, &b_full[bs]);
+                    int x0, lead;
+                    raw_x(cu.fmt, rs, x0, lead);
+                    raw_info[slot] = (uint32_t)cu.fmt | ((uint32_t)lead << 8);
+                    mbar_expect_tx(&raw_full[slot], bytes);
+                    uint8_t *dst = raw + (size_t)slot * A.slot_bytes;
+                    for (int m = 0; m < NMAT; ++m)
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(dst + (m * nbox + b) * R * W, m0 + m, x0 + 128 * b, R * cu.s,
+                                        &raw_full[slot]);
+                    ++rg;
+                }
+            }
+            if (!ok) {
+                tc_fail(abort_flag, A.status);
+                for (uint32_t j = rg > (uint32_t)A.RS ? rg - A.RS : 0; j < rg; ++j)
+                    mbar_wait(&raw_full[j % A.RS], (j / A.RS) & 1);
+            }
+        }
+    } else if (warp == TC_BPROD) {
+        // ---- activation producer: q A steps of the unit's rows per B stage
+        if (lane == 0) {
+            uint32_t bg = 0;
+            bool ok = true;
+            Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
+            for (int u = blockIdx.x; u < n_units && ok; u += G) {
+                const Unit cu = nxt;
+                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+                const int nb = (cu.n + TC_BOX_ROWS - 1) / TC_BOX_ROWS, q = b_steps_per_stage(cu.n);
+                const int sub_bytes = nb * TC_BOX_ROWS * 128;
+                for (int a0 = 0; a0 < nA; a0 += q) {
+                    const uint32_t bs = bg % TC_BSTAGES, buse = bg / TC_BSTAGES;
+                    if (buse > 0 && !tc_wait(&b_empty[bs], (buse - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
-                    __syncwarp();
+                    const int qa = min(q, nA - a0);
+                    mbar_expect_tx(&b_full[bs], (uint32_t)(qa * sub_bytes));
+                    for (int j = 0; j < qa; ++j)
+                        for (int i = 0; i < nb; ++i)
+                            tma_load_2d(bring + bs * TC_BSTAGE_BYTES + j * sub_bytes + i * TC_BOX_ROWS * 128, &bmap,
+                                        (a0 + j) * TC_KA, cu.row0 + i * TC_BOX_ROWS, &b_full[bs]);
                     ++bg;
                 }
             }
-        }
-        if (!ok) {
-            if (lane == 0) tc_fail(abort_flag, A.status);
-            // let the copies already issued land before the CTA can exit
-            if (lane == 0) {
-                for (uint32_t j = rg > (uint32_t)A.RS ? rg - A.RS : 0; j < rg; ++j)
-                    mbar_wait(&raw_full[j % A.RS], (j / A.RS) & 1);
+            if (!ok) {
+                tc_fail(abort_flag, A.status);
                 for (uint32_t j = bg > (uint32_t)TC_BSTAGES ? bg - TC_BSTAGES : 0; j < bg; ++j)
                     mbar_wait(&b_full[j % TC_BSTAGES], (j / TC_BSTAGES) & 1);
             }
@@ -562,9 +588,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         if (lane == 0) {
             uint32_t ag = 0, bg = 0, uc = 0;
             bool ok = true, issued = false;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const int4 ch = A.chunks[u / A.S];
-                const int N = (ch.z + 15) & ~15;
+            Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
+            for (int u = blockIdx.x; u < n_units && ok; u += G) {
+                const Unit cu = nxt;
+                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+                const int N = (cu.n + 15) & ~15, q = b_steps_per_stage(cu.n);
                 const uint32_t idesc = idesc_f16(N);
                 const uint32_t d = uc & 1, use = uc >> 1;
                 if (use > 0 && !tc_wait(&acc_empty[d], (use - 1) & 1, abort_flag)) {
@@ -573,23 +601,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 }
                 tmem_fence_after();
                 const uint32_t dcol = tmem + d * TC_NCHUNK;
+                int sub = 0;
                 for (int a = 0; a < nA; ++a) {
                     const uint32_t t = ag % TC_ASTAGES, bs = bg % TC_BSTAGES;
-                    if (!tc_wait(&a_full[t], (ag / TC_ASTAGES) & 1, abort_flag) ||
-                        !tc_wait(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) {
+                    if ((sub == 0 && !tc_wait(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) ||
+                        !tc_wait(&a_full[t], (ag / TC_ASTAGES) & 1, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tmem_fence_after();
-                    const uint64_t bdesc = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES));
+                    const uint64_t bdesc = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES + sub * N * 128));
 #pragma unroll
                     for (int kk = 0; kk < TC_KA / 16; ++kk)
                         mma_f16_ts(dcol, tmem + TC_ACOL0 + t * 32 + kk * 8, bdesc + 2 * kk, idesc, (a | kk) != 0);
                     mma_commit(&a_empty[t]);
-                    mma_commit(&b_empty[bs]);
                     issued = true;
                     ++ag;
-                    ++bg;
+                    if (++sub == q || a == nA - 1) {
+                        mma_commit(&b_empty[bs]);
+                        ++bg;
+                        sub = 0;
+                    }
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[d]);
@@ -605,14 +637,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     } else if (warp >= TC_DQ0) {
         // ---- dequantisers: group g writes piece g (64 K) of every raw stage to TMEM
         const int g = (warp - TC_DQ0) >> 2, qd = warp & 3, l = 32 * qd + lane;
+        const int mat = GATEUP ? (l >> 6) : 0, row = GATEUP ? (l & 63) : l;
         uint32_t rg = 0, ag0 = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const int4 ch = A.chunks[u / A.S];
-            const int s = u % A.S;
-            const uint8_t *row;
-            int fmt;
-            unit_row<GATEUP>(A.table + ch.x, s, l, row, fmt);
+        for (int u = blockIdx.x; u < n_units && ok; u += G) {
             for (int rs = 0; rs < nR; ++rs) {
                 const uint32_t slot = rg % A.RS;
                 if (!warp_wait(&raw_full[slot], (rg / A.RS) & 1, abort_flag)) {
@@ -627,14 +655,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         break;
                     }
                     tmem_fence_after();
-                    const int k0 = rs * TC_KR;
-                    const RawSpan sp = raw_span(row, fmt, k0, min(A.K, k0 + TC_KR));
-                    const uint32_t base = smem_addr(raw + (size_t)slot * TC_M * A.RB + (size_t)l * A.RB) + sp.lead;
+                    const uint32_t info = raw_info[slot];
+                    const int fmt = info & 0xff, lead = info >> 8;
+                    const int W = raw_w(fmt), nbox = raw_nbox(fmt);
+                    const uint32_t tile = smem_addr(raw + (size_t)slot * A.slot_bytes) + (uint32_t)(mat * nbox * R * W);
+                    const uint32_t base = tile + (uint32_t)(row * W + lead);
                     uint32_t r[32];
                     if (fmt == MOE_Q4_K)
                         dq_q4k(base, g, r);
                     else if (fmt == MOE_Q8_0)
-                        dq_q8_0(base, g, r);
+                        dq_q8_0(g < 2 ? base + 68 * g : base + (uint32_t)(R * W) + 68 * g - 128, r);
                     else if (fmt == MOE_Q6_K)
                         dq_q6k(base, g, r);
                     else
@@ -656,9 +686,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // ---- epilogue: warps 0-3 read TMEM lanes 32w..32w+31
         const int l = 32 * warp + lane;
         uint32_t uc = 0;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-            const int4 ch = A.chunks[u / A.S];
-            const int s = u % A.S, n = ch.z, row0 = ch.y;
+        Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
+        for (int u = blockIdx.x; u < n_units; u += G) {
+            const Unit cu = nxt;
+            if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+            const int n = cu.n, row0 = cu.row0, s = cu.s;
             const uint32_t d = uc & 1;
             bool ok = warp_wait(&acc_full[d], (uc >> 1) & 1, abort_flag);
             if (GATEUP) ok = epi_all(ok);
@@ -671,6 +703,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 uint32_t v[32];
                 tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + d * TC_NCHUNK + cb, v);
                 tmem_wait_ld();
+                const int jn = min(32, n - cb);
                 if (GATEUP) {
                     if (warp >= 2) {
 #pragma unroll
@@ -678,7 +711,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                     epi_sync();
                     if (warp < 2) {
-                        const int jn = min(32, n - cb);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             if (j >= jn) break;
@@ -693,7 +725,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                     epi_sync();
                 } else {
-                    const int jn = min(32, n - cb);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         if (j >= jn) break;
@@ -880,19 +911,14 @@ bool encode_act_map(CUtensorMap *map, const void *base, int rows, int cols) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Shared-memory pitch of one weight row's raw stage: its blocks for 256 K plus
-// up to 30 bytes of 16-byte widening, as an odd number of 16-byte units so
-// that the 16-byte loads of 8 consecutive rows hit distinct banks.
-int raw_pitch(uint32_t fmask) {
-    int rb = 0;
-    for (int f = MOE_Q8_0; f <= MOE_MXFP4; ++f) {
-        if (!(fmask & (1u << f))) continue;
-        int b = (TC_KR / BLOCK_ELEMS[f]) * BLOCK_BYTES[f] + 30;
-        b = (b + 15) & ~15;
-        if (((b / 16) & 1) == 0) b += 16;
-        rb = b > rb ? b : rb;
-    }
-    return rb;
+// Bytes of one raw stage for the formats in `fmask`: per weight matrix of the
+// unit, its box(es) of R rows x raw_w bytes.
+int raw_slot_bytes(uint32_t fmask, bool gateup) {
+    const int R = gateup ? 64 : 128, nmat = gateup ? 2 : 1;
+    int sb = 0;
+    for (int f = MOE_Q8_0; f <= MOE_MXFP4; ++f)
+        if (fmask & (1u << f)) sb = std::max(sb, nmat * raw_nbox(f) * R * raw_w(f));
+    return sb;
 }
 
 int g_tc_smem_optin[64] = {};
@@ -910,11 +936,11 @@ int smem_optin() {
 }
 
 // Raw ring depth that fits next to the fixed shared memory; 0 if < 2.
-int raw_stages(int rb) {
+int raw_stages(int slot_bytes) {
     const int optin = smem_optin();
-    if (optin <= 0 || rb <= 0) return 0;
-    const long room = (long)optin - (long)tc_smem_bytes(rb, 0);
-    long rs = room / ((long)TC_M * rb);
+    if (optin <= 0 || slot_bytes <= 0) return 0;
+    const long room = (long)optin - (long)tc_smem_bytes(slot_bytes, 0);
+    long rs = room / slot_bytes;
     if (rs > TC_RS_MAX) rs = TC_RS_MAX;
     return rs >= 2 ? (int)rs : 0;
 }
@@ -923,15 +949,43 @@ int raw_stages(int rb) {
 
 bool tc_path_eligible(int H, int I) { return H >= TC_M && H % TC_M == 0 && I >= 64 && I % 64 == 0; }
 
-cudaError_t launch_tc_path(const DevExpert *table, uint32_t gu_formats, uint32_t dn_formats, int T, int k, int E,
+size_t tc_weight_map_bytes(int E) { return (size_t)E * 3 * sizeof(CUtensorMap); }
+
+// The tensor path's weight tensor maps, 3 per expert (gate, up, down) into
+// `out` (host memory, tc_weight_map_bytes(E) bytes): the matrix's bytes as a
+// 2-D uint8 tensor [rows][row stride], boxes of raw_w(format) bytes x 64 rows
+// (gate/up) or 128 rows (down). False if the driver refuses one.
+bool tc_encode_weight_maps(const moe_weight_table *W, void *out) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    CUtensorMap *maps = static_cast<CUtensorMap *>(out);
+    for (int e = 0; e < W->n_experts; ++e) {
+        const moe_matrix *m[3] = {&W->experts[e].gate, &W->experts[e].up, &W->experts[e].down};
+        for (int i = 0; i < 3; ++i) {
+            const cuuint64_t dims[2] = {(cuuint64_t)m[i]->row_stride_bytes, (cuuint64_t)m[i]->rows};
+            const cuuint64_t strides[1] = {(cuuint64_t)m[i]->row_stride_bytes};
+            const cuuint32_t box[2] = {(cuuint32_t)raw_w(m[i]->format), (cuuint32_t)(i < 2 ? 64 : 128)};
+            const cuuint32_t es[2] = {1, 1};
+            if (f(&maps[3 * e + i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(m[i]->data), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                return false;
+        }
+    }
+    return true;
+}
+
+cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t gu_formats, uint32_t dn_formats,
+                           int T, int k, int E,
                            int H, int I, const int32_t *offsets, const int32_t *active, const int32_t *pos,
                            const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
                            const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
                            cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
     const int P = T * k;
-    const int rb1 = raw_pitch(gu_formats), rb2 = raw_pitch(dn_formats);
-    const int rs1 = raw_stages(rb1), rs2 = raw_stages(rb2);
+    const int sb1 = raw_slot_bytes(gu_formats, true), sb2 = raw_slot_bytes(dn_formats, false);
+    const int rs1 = raw_stages(sb1), rs2 = raw_stages(sb2);
+    const CUtensorMap *maps = static_cast<const CUtensorMap *>(wmaps);
     const int G = sm_count();
     if (!rs1 || !rs2 || G <= 0) return cudaErrorInvalidConfiguration;
     __half *xg = reinterpret_cast<__half *>(ws_base + C.xg);
@@ -950,16 +1004,16 @@ cudaError_t launch_tc_path(const DevExpert *table, uint32_t gu_formats, uint32_t
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
 
-    TcArgs a1{table, chunks, n_chunks, H, I / 64, H, I, rb1, rs1, xinv, h32, hmax, nullptr, status};
-    tc_gemm_kernel<true><<<G, TC_THREADS, tc_smem_bytes(rb1, rs1), s>>>(xmap, a1);
+    TcArgs a1{table, maps, chunks, n_chunks, H, I / 64, H, I, sb1, rs1, xinv, h32, hmax, nullptr, status};
+    tc_gemm_kernel<true><<<G, TC_THREADS, tc_smem_bytes(sb1, rs1), s>>>(xmap, a1);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[1], s)) != cudaSuccess) return err;
 
     tc_hprep_kernel<<<(P + PREP_THREADS / 32 - 1) / (PREP_THREADS / 32), PREP_THREADS, 0, s>>>(h32, hmax, offsets, E,
                                                                                              I, h16, hinv);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    TcArgs a2{table, chunks, n_chunks, I, H / TC_M, H, I, rb2, rs2, hinv, nullptr, nullptr, y, status};
-    tc_gemm_kernel<false><<<G, TC_THREADS, tc_smem_bytes(rb2, rs2), s>>>(hmap, a2);
+    TcArgs a2{table, maps, chunks, n_chunks, I, H / TC_M, H, I, sb2, rs2, hinv, nullptr, nullptr, y, status};
+    tc_gemm_kernel<false><<<G, TC_THREADS, tc_smem_bytes(sb2, rs2), s>>>(hmap, a2);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
     return launch_combine(T, k, H, pos, wts, y, out, s);
