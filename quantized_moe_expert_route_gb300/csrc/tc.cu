@@ -41,9 +41,11 @@ constexpr int TC_M = 128;                    // weight rows per unit = TMEM lane
 constexpr int TC_NCHUNK = 128;               // activation rows per chunk (MMA N <= 128)
 constexpr int TC_KA = 64;                    // K per A step: one 128-byte row of fp16
 constexpr int TC_KR = 256;                   // K per raw (quantized) stage
-constexpr int TC_ASTAGES = 8;                // A stages in TMEM, 32 columns each
-constexpr int TC_BSTAGES = 4;                // B stages in shared memory
-constexpr int TC_BSTAGE_BYTES = TC_NCHUNK * 128;
+constexpr int TC_ASTAGES = 8;                // A stages in TMEM, 32 columns each: 2 events of 4
+constexpr int TC_AEV = 4;                    // A steps per event (one raw stage)
+constexpr int TC_EVSLOTS = TC_ASTAGES / TC_AEV;
+constexpr int TC_BSTAGES = 3;                // B stages in shared memory
+constexpr int TC_BSTAGE_BYTES = 2 * TC_NCHUNK * 128;   // 32 KB: up to 4 A steps of <= 64 rows
 constexpr int TC_BOX_ROWS = 16;              // rows per activation TMA box
 constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups = A steps per raw stage
 constexpr int TC_DQ0 = 4;                    // warps 0-3 epilogue, 4..19 dequant
@@ -55,8 +57,8 @@ constexpr int TC_THREADS = TC_WARPS * 32;    // 736
 constexpr int TC_TMEM_COLS = 512;
 constexpr int TC_ACOL0 = 2 * TC_NCHUNK;      // A stages after the two accumulators
 constexpr int TC_RS_MAX = 8;
-constexpr int TC_UBUF_FLOATS = 32 * 64;
-constexpr int TC_NBARS = 2 * TC_RS_MAX + 2 * TC_ASTAGES + 2 * TC_BSTAGES + 4 + 1;
+constexpr int TC_UBUF_FLOATS = 16 * 128;     // epilogue exchange: 16 columns x 128 lanes
+constexpr int TC_NBARS = 2 * TC_RS_MAX + TC_EVSLOTS + 2 * TC_BSTAGES + 4 + 1;
 constexpr uint32_t TC_NEG1152 = 0xE480E480u;  // fp16 pair (-1152, -1152)
 constexpr uint32_t TC_NEG1056 = 0xE420E420u;  // fp16 pair (-1056, -1056)
 constexpr uint32_t TC_MAGIC = 0x64006400u;    // fp16 pair (1024, 1024)
@@ -73,6 +75,7 @@ __host__ __device__ constexpr int blk_bytes(int f) {
 
 static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
 static_assert(TC_DG == 4, "one dequantising warpgroup per 64-K piece of a raw stage");
+static_assert(TC_AEV == TC_KR / TC_KA, "an event is one raw stage");
 
 struct TcArgs {
     const DevExpert *table;
@@ -177,6 +180,31 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
     }
     return false;
 }
+// The same without a suspend hint, for the MMA issuer: its waits are short and
+// on the critical path.
+__device__ __forceinline__ bool tc_spin(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t addr = smem_addr(bar);
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if ((i & 1023u) == 1023u) {
+            if (*abort_flag) return false;
+            const uint64_t now = global_ns();
+            if (i == 1023u)
+                t0 = now;
+            else if (now - t0 > TC_WAIT_NS)
+                return false;
+        }
+    }
+    return false;
+}
+
 __device__ __forceinline__ void tc_fail(volatile int *abort_flag, uint32_t *status) {
     if (!*abort_flag) {
         *abort_flag = 1;
@@ -207,6 +235,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
 }
@@ -256,11 +293,28 @@ __device__ __forceinline__ float warp_max_f(float v) {
     for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
-__device__ __forceinline__ int warp_sum_i(int v) {
+// silu(z) = z / (1 + e^-z) with the hardware exponential and reciprocal
+// (relative error ~1e-6, far inside the layer's 1e-3 bound).
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// v[j] (j < 8) of every lane -> lanes 0..7 return the max over the warp of
+// v[lane]; v is clobbered.
+__device__ __forceinline__ float warp_colmax8(float (&v)[8]) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    for (int o = 4; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < o; ++j) {
+            const float send = up ? v[j] : v[j + o];
+            const float keep = up ? v[j + o] : v[j];
+            v[j] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+    float m = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], 8));
+    return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
 }
+
 
 // ------------------------------------------------------------------ dequantisation
 // Each function turns one weight row's 64 consecutive K elements (piece g of
@@ -454,10 +508,36 @@ __device__ __forceinline__ bool epi_all(bool pred) {
 }
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// Activation rows per B stage for a unit of n rows: q A steps of Npad rows.
+// A steps per B stage for a unit of n rows (Npad = n rounded up to 16): 4 if
+// four Npad-row tiles fit a stage, else 2. Either divides an event.
 __device__ __forceinline__ int b_steps_per_stage(int n) {
     const int npad = (n + 15) & ~15;
-    return TC_NCHUNK / npad;
+    return npad <= 64 ? 4 : 2;
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_shared(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.cta.shared.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+// Spin until the counter reaches `target` (wrapping compare); bounded like tc_spin.
+__device__ __forceinline__ bool counter_spin(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if ((int32_t)(ld_acquire_shared(p) - target) >= 0) return true;
+        if ((i & 1023u) == 1023u) {
+            if (*abort_flag) return false;
+            const uint64_t now = global_ns();
+            if (i == 1023u)
+                t0 = now;
+            else if (now - t0 > TC_WAIT_NS)
+                return false;
+        }
+    }
+    return false;
 }
 
 template <bool GATEUP>
@@ -469,11 +549,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     float *ubuf = reinterpret_cast<float *>(raw + (size_t)A.RS * A.slot_bytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(ubuf + TC_UBUF_FLOATS);
     uint64_t *raw_full = bars, *raw_empty = bars + TC_RS_MAX;
-    uint64_t *a_full = bars + 2 * TC_RS_MAX, *a_empty = a_full + TC_ASTAGES;
-    uint64_t *b_full = a_empty + TC_ASTAGES, *b_empty = b_full + TC_BSTAGES;
+    uint64_t *a_empty = bars + 2 * TC_RS_MAX;   // per event slot, committed by the MMA thread
+    uint64_t *b_full = a_empty + TC_EVSLOTS, *b_empty = b_full + TC_BSTAGES;
     uint64_t *acc_full = b_empty + TC_BSTAGES, *acc_empty = acc_full + 2, *fin = acc_empty + 2;
     uint32_t *raw_info = reinterpret_cast<uint32_t *>(bars + TC_NBARS);  // [TC_RS_MAX]: fmt | lead << 8
-    uint32_t *tmem_slot = raw_info + TC_RS_MAX;
+    uint32_t *a_ready = raw_info + TC_RS_MAX;   // [TC_EVSLOTS]: dequant warps done, 16 per use
+    uint32_t *tmem_slot = a_ready + TC_EVSLOTS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -484,9 +565,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             mbar_init(&raw_full[i], 1);
             mbar_init(&raw_empty[i], 4 * TC_DG);
         }
-        for (int i = 0; i < TC_ASTAGES; ++i) {
-            mbar_init(&a_full[i], 4);
+        for (int i = 0; i < TC_EVSLOTS; ++i) {
             mbar_init(&a_empty[i], 1);
+            a_ready[i] = 0;
         }
         for (int i = 0; i < TC_BSTAGES; ++i) {
             mbar_init(&b_full[i], 1);
@@ -584,9 +665,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             }
         }
     } else if (warp == TC_MMA) {
-        // ---- MMA issuer: one thread
+        // ---- MMA issuer: one thread; per event (raw stage) one wait on the dequantisers'
+        // counter, up to 16 MMAs back to back, one commit
         if (lane == 0) {
-            uint32_t ag = 0, bg = 0, uc = 0;
+            uint32_t ev = 0, bg = 0, uc = 0;
             bool ok = true, issued = false;
             Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
             for (int u = blockIdx.x; u < n_units && ok; u += G) {
@@ -594,6 +676,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
                 const int N = (cu.n + 15) & ~15, q = b_steps_per_stage(cu.n);
                 const uint32_t idesc = idesc_f16(N);
+                const uint32_t sub_step = (uint32_t)(N * 128) >> 4;   // descriptor units per B tile
                 const uint32_t d = uc & 1, use = uc >> 1;
                 if (use > 0 && !tc_wait(&acc_empty[d], (use - 1) & 1, abort_flag)) {
                     ok = false;
@@ -602,26 +685,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 tmem_fence_after();
                 const uint32_t dcol = tmem + d * TC_NCHUNK;
                 int sub = 0;
-                for (int a = 0; a < nA; ++a) {
-                    const uint32_t t = ag % TC_ASTAGES, bs = bg % TC_BSTAGES;
-                    if ((sub == 0 && !tc_wait(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) ||
-                        !tc_wait(&a_full[t], (ag / TC_ASTAGES) & 1, abort_flag)) {
+                uint64_t bdesc = 0;
+                for (int rs = 0; rs < nR; ++rs) {
+                    const int na = min(TC_AEV, nA - TC_AEV * rs);
+                    const uint32_t slot = ev & (TC_EVSLOTS - 1);
+                    if (!counter_spin(&a_ready[slot], 4u * TC_DG * ((ev >> 1) + 1), abort_flag)) {
                         ok = false;
                         break;
                     }
                     tmem_fence_after();
-                    const uint64_t bdesc = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES + sub * N * 128));
+                    const uint32_t acol0 = tmem + TC_ACOL0 + slot * (TC_AEV * 32);
 #pragma unroll
-                    for (int kk = 0; kk < TC_KA / 16; ++kk)
-                        mma_f16_ts(dcol, tmem + TC_ACOL0 + t * 32 + kk * 8, bdesc + 2 * kk, idesc, (a | kk) != 0);
-                    mma_commit(&a_empty[t]);
-                    issued = true;
-                    ++ag;
-                    if (++sub == q || a == nA - 1) {
-                        mma_commit(&b_empty[bs]);
-                        ++bg;
-                        sub = 0;
+                    for (int i = 0; i < TC_AEV; ++i) {
+                        if (i >= na) break;
+                        if (sub == 0) {
+                            const uint32_t bs = bg % TC_BSTAGES;
+                            if (!tc_spin(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) {
+                                ok = false;
+                                break;
+                            }
+                            tmem_fence_after();
+                            bdesc = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES));
+                        }
+                        const uint32_t acol = acol0 + 32 * i;
+                        mma_f16_ts(dcol, acol, bdesc, idesc, (rs | i) != 0);
+                        mma_f16_ts(dcol, acol + 8, bdesc + 2, idesc, 1);
+                        mma_f16_ts(dcol, acol + 16, bdesc + 4, idesc, 1);
+                        mma_f16_ts(dcol, acol + 24, bdesc + 6, idesc, 1);
+                        issued = true;
+                        bdesc += sub_step;
+                        if (++sub == q || TC_AEV * rs + i == nA - 1) {
+                            mma_commit(&b_empty[bg % TC_BSTAGES]);
+                            ++bg;
+                            sub = 0;
+                        }
                     }
+                    if (!ok) break;
+                    mma_commit(&a_empty[slot]);
+                    ++ev;
                 }
                 if (!ok) break;
                 mma_commit(&acc_full[d]);
@@ -638,22 +739,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // ---- dequantisers: group g writes piece g (64 K) of every raw stage to TMEM
         const int g = (warp - TC_DQ0) >> 2, qd = warp & 3, l = 32 * qd + lane;
         const int mat = GATEUP ? (l >> 6) : 0, row = GATEUP ? (l & 63) : l;
-        uint32_t rg = 0, ag0 = 0;
+        uint32_t rg = 0;   // raw stages = events seen
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += G) {
             for (int rs = 0; rs < nR; ++rs) {
-                const uint32_t slot = rg % A.RS;
-                if (!warp_wait(&raw_full[slot], (rg / A.RS) & 1, abort_flag)) {
+                const uint32_t slot = rg % A.RS, es = rg & (TC_EVSLOTS - 1), euse = rg >> 1;
+                if (!warp_wait(&raw_full[slot], (rg / A.RS) & 1, abort_flag) ||
+                    (euse > 0 && !warp_wait(&a_empty[es], (euse - 1) & 1, abort_flag))) {
                     ok = false;
                     break;
                 }
-                const int a = 4 * rs + g;
+                const int a = TC_AEV * rs + g;
                 if (a < nA) {
-                    const uint32_t AG = ag0 + a, t = AG % TC_ASTAGES, use = AG / TC_ASTAGES;
-                    if (use > 0 && !warp_wait(&a_empty[t], (use - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
                     tmem_fence_after();
                     const uint32_t info = raw_info[slot];
                     const int fmt = info & 0xff, lead = info >> 8;
@@ -669,17 +766,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         dq_q6k(base, g, r);
                     else
                         dq_mxfp4(base, g, r);
-                    tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + t * 32, r);
+                    tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + es * (TC_AEV * 32) + g * 32, r);
                     tmem_wait_st();
                     tmem_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cta(&a_full[t]);
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cta(&raw_empty[slot]);
+                if (lane == 0) {
+                    red_release_shared(&a_ready[es], 1u);
+                    mbar_arrive_cta(&raw_empty[slot]);
+                }
                 ++rg;
             }
-            ag0 += nA;
         }
         if (!ok && lane == 0) tc_fail(abort_flag, A.status);
     } else {
@@ -699,37 +796,48 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 break;
             }
             tmem_fence_after();
-            for (int cb = 0; cb < n; cb += 32) {
-                uint32_t v[32];
-                tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + d * TC_NCHUNK + cb, v);
-                tmem_wait_ld();
-                const int jn = min(32, n - cb);
-                if (GATEUP) {
-                    if (warp >= 2) {
+            if (GATEUP) {
+                // 16 columns at a time: every lane's g or u to shared memory, then
+                // thread l computes h for row l & 63 and 8 of the columns
+                const int r = l & 63, ch = l >> 6;
+                for (int cb = 0; cb < n; cb += 16) {
+                    uint32_t v[16];
+                    tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + d * TC_NCHUNK + cb, v);
+                    const int jn = min(16, n - cb);
+                    const float scl = lane < jn ? A.ascale[row0 + cb + lane] : 0.0f;
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) ubuf[j * 64 + (l - 64)] = __uint_as_float(v[j]);
-                    }
+                    for (int j = 0; j < 16; ++j) ubuf[j * 128 + l] = __uint_as_float(v[j]);
                     epi_sync();
-                    if (warp < 2) {
+                    float hv[8];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (j >= jn) break;
-                            const int qrow = row0 + cb + j;
-                            const float sc = A.ascale[qrow];
-                            const float gv = __uint_as_float(v[j]) * sc, uv = ubuf[j * 64 + l] * sc;
-                            const float h = silu_f32(gv) * uv;
-                            A.h32[(size_t)qrow * A.I + 64 * s + l] = h;
-                            const float m = warp_max_f(fabsf(h));
-                            if (lane == 0) atomicMax(&A.hmax[qrow], __float_as_uint(m));
-                        }
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = 8 * ch + jj;
+                        const float sc = __shfl_sync(0xffffffffu, scl, j);
+                        hv[jj] = silu_fast(ubuf[j * 128 + r] * sc) * (ubuf[j * 128 + 64 + r] * sc);
                     }
+                    float *hrow = A.h32 + (size_t)(row0 + cb + 8 * ch) * A.I + 64 * s + r;
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj)
+                        if (8 * ch + jj < jn) hrow[(size_t)jj * A.I] = hv[jj];
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) hv[jj] = fabsf(hv[jj]);
+                    const float m = warp_colmax8(hv);
+                    if (lane < 8 && 8 * ch + lane < jn) atomicMax(&A.hmax[row0 + cb + 8 * ch + lane], __float_as_uint(m));
                     epi_sync();
-                } else {
+                }
+            } else {
+                for (int cb = 0; cb < n; cb += 32) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem + ((uint32_t)(32 * warp) << 16) + d * TC_NCHUNK + cb, v);
+                    const int jn = min(32, n - cb);
+                    const float scl = lane < jn ? A.ascale[row0 + cb + lane] : 0.0f;
+                    tmem_wait_ld();
+                    float *yrow = A.y + (size_t)(row0 + cb) * A.H + TC_M * s + l;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        if (j >= jn) break;
-                        const int qrow = row0 + cb + j;
-                        A.y[(size_t)qrow * A.H + TC_M * s + l] = __uint_as_float(v[j]) * A.ascale[qrow];
+                        const float sc = __shfl_sync(0xffffffffu, scl, j);
+                        if (j < jn) yrow[(size_t)j * A.H] = __uint_as_float(v[j]) * sc;
                     }
                 }
             }
