@@ -48,10 +48,9 @@ constexpr int DC_NSTAGE = DC_CW;                 // one ring slot per consumer w
 constexpr int DC_MAX_PAIRS = 64;                 // T * k
 constexpr int DC_ROWS_A = 4;                     // max gate/up row pairs per chunk
 constexpr uint32_t DC_MAGIC = 0x64006400u;       // fp16 1024.0 in both halves
-constexpr size_t DC_SYNC_HMAX = 256;             // offset of the per-pair |h| maxima in the sync region
 
 struct DcLayout {
-    size_t ring, xs, xsum, xsc, xmax, hs, hsum, hsc, ybuf, ckey, cidx, sm, ss, selk, ids, wts, keep, act, aoff, plist,
+    size_t ring, xs, xsum, xsc, xmax, ybuf, ckey, cidx, sm, ss, selk, ids, wts, keep, act, aoff, plist,
         dpair, chunks, full, empty, misc, total;
     int rb, ns, C;
 };
@@ -73,9 +72,6 @@ __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I,
     L.xsum = take((size_t)T * (H / 64) * 2 * 4);
     L.xsc = take((size_t)T * 4);
     L.xmax = take((size_t)T * 4);
-    L.hs = take((size_t)P * I * 2);
-    L.hsum = take((size_t)P * 32 * 4);
-    L.hsc = take((size_t)P * 4);
     L.ybuf = take((size_t)P * L.rb * 4);
     L.ckey = take((size_t)T * L.C * 4);
     L.cidx = take((size_t)T * L.C * 4);
@@ -124,11 +120,6 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
     return r;
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
 
 // acc += lo(a) * lo(b) + hi(a) * hi(b), fp16 operands, fp32 accumulation
 __device__ __forceinline__ void fma2_f16_f32(float &acc, uint32_t a, uint32_t b) {
@@ -218,27 +209,6 @@ __device__ __forceinline__ void red_release_add(unsigned long long *p, unsigned 
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Sums of 8 per-lane values over the warp: value j ends in lanes 4j .. 4j+3
-// (9 shuffles instead of 40).
-__device__ __forceinline__ float warp_reduce8(const float v[8]) {
-    const int lane = threadIdx.x & 31;
-    const bool b16 = lane & 16, b8 = lane & 8, b4 = lane & 4;
-    float w[4], x[2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float send = b16 ? v[i] : v[i + 4], keep = b16 ? v[i + 4] : v[i];
-        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = b8 ? w[i] : w[i + 2], keep = b8 ? w[i + 2] : w[i];
-        x[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-    }
-    float y = (b4 ? x[1] : x[0]) + __shfl_xor_sync(0xffffffffu, b4 ? x[0] : x[1], 4);
-    y += __shfl_xor_sync(0xffffffffu, y, 2);
-    y += __shfl_xor_sync(0xffffffffu, y, 1);
-    return y;
-}
 
 // Sums of 2 per-lane values over the warp: value 0 ends in lanes 0..15, value 1 in 16..31.
 __device__ __forceinline__ float warp_reduce2(const float v[2]) {
@@ -251,22 +221,6 @@ __device__ __forceinline__ float warp_reduce2(const float v[2]) {
     return y;
 }
 
-// Sums of 4 per-lane values over the warp: value j ends in lanes 8j .. 8j+7.
-__device__ __forceinline__ float warp_reduce4(const float v[4]) {
-    const int lane = threadIdx.x & 31;
-    const bool b16 = lane & 16, b8 = lane & 8;
-    float w[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const float send = b16 ? v[i] : v[i + 2], keep = b16 ? v[i + 2] : v[i];
-        w[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-    float y = (b8 ? w[1] : w[0]) + __shfl_xor_sync(0xffffffffu, b8 ? w[0] : w[1], 8);
-    y += __shfl_xor_sync(0xffffffffu, y, 4);
-    y += __shfl_xor_sync(0xffffffffu, y, 2);
-    y += __shfl_xor_sync(0xffffffffu, y, 1);
-    return y;
-}
 
 // Scales and mins of Q4_K sub-blocks 2g and 2g+1 from the 12 scale bytes
 // (three little-endian words), without branches: bytes j' = 2 (g & 1) and
@@ -312,30 +266,56 @@ __device__ __forceinline__ float q4k_dot64(const uint8_t *blk, int g, const uint
            dmin * (m0 * XA + m1 * XB);
 }
 
-// One lane's share of a Q8_0 row dot product: the 32-weight block at blk
-// (fp16 d, int8 q[32]) times 32 fp16 activations hv (natural order) whose sum
-// is hsu. Codes become fp16 1152 + q (bias 128, exponent of 1024).
-__device__ __forceinline__ float q8_0_dot32(const uint8_t *blk, const uint32_t hv[16], float hsu) {
-    const float d = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(blk));
-    const uintptr_t qa = reinterpret_cast<uintptr_t>(blk + 2);
-    const uint32_t *w4 = reinterpret_cast<const uint32_t *>(qa & ~(uintptr_t)3);
-    const uint32_t sh = (uint32_t)(qa & 3) * 8;
-    float acc0 = 0.0f, acc1 = 0.0f;
-    uint32_t prev = w4[0];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t next = w4[j + 1];
-        const uint32_t w = __funnelshift_r(prev, next, sh) ^ 0x80808080u;
-        prev = next;
-        fma2_f16_f32(acc0, prmt(w, 0x64646464u, 0x5140), hv[2 * j]);
-        fma2_f16_f32(acc1, prmt(w, 0x64646464u, 0x7362), hv[2 * j + 1]);
-    }
-    return d * ((acc0 + acc1) - 1152.0f * hsu);
-}
 
 // On an abort, thread 0 waits (bounded) for the bulk copies the producer
 // issued into stages nobody will consume, so none lands after the CTA exits.
 // (Each slot's latest issue completes after the slot's earlier ones.)
+// 32 activations of one block -> int16 pairs scaled by 2^sigma (block max
+// |v| * 2^sigma in [2^13, 2^14), so no value can round past 2^15) and the
+// inverse scale; exponent arithmetic on the float bits (no library calls). A
+// block with a non-finite value gets a NaN inverse scale.
+__device__ __forceinline__ float quant_i16x32(const float v[32], uint32_t q[16]) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+    const int be = (int)((__float_as_uint(m) >> 23) & 0xffu);   // biased exponent: m in [2^(be-127), 2^(be-126))
+    if (be == 255) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] = 0u;
+        return __int_as_float(0x7fc00000);
+    }
+    // m * 2^sg in [2^13, 2^14): sg = 140 - be, kept where both scales are normal
+    const int sg = m > 0.0f ? max(-100, min(100, 140 - be)) : 0;
+    const float up = __uint_as_float((uint32_t)(127 + sg) << 23);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int lo = __float2int_rn(v[2 * i] * up), hi = __float2int_rn(v[2 * i + 1] * up);
+        q[i] = ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
+    }
+    return __uint_as_float((uint32_t)(127 - sg) << 23);
+}
+
+// Q8_0 block (fp16 scale, then 32 int8 codes; any 2-byte alignment) dotted
+// with 32 int16 activations: exact int32 products and sums (two per dp2a).
+__device__ __forceinline__ float q8_0_dot32_i16(const uint8_t *blk, const uint32_t hq[16]) {
+    const float d = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(blk));
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(blk + 2);
+    const uint32_t *w4 = reinterpret_cast<const uint32_t *>(qa & ~(uintptr_t)3);
+    const uint32_t sh = (uint32_t)(qa & 3) * 8;
+    int acc0 = 0, acc1 = 0;
+    uint32_t prev = w4[0];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t next = w4[j + 1];
+        const uint32_t w = __funnelshift_r(prev, next, sh);   // codes 4j .. 4j+3
+        prev = next;
+        asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(acc0) : "r"(hq[2 * j]), "r"(w));
+        asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc1) : "r"(hq[2 * j + 1]), "r"(w));
+    }
+    return d * (float)(acc0 + acc1);
+}
+
+
 __device__ __forceinline__ void drain_copies(uint64_t *full, int *misc) {
     if (threadIdx.x != 0) return;
     const int issued = *reinterpret_cast<volatile int *>(&misc[3]);
@@ -362,9 +342,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);       // [T][H/64][2]
     float *xsc = reinterpret_cast<float *>(smem + L.xsc);
     unsigned *xmax = reinterpret_cast<unsigned *>(smem + L.xmax);
-    uint32_t *hs = reinterpret_cast<uint32_t *>(smem + L.hs);     // [P][I/2] half2
-    float *hsum = reinterpret_cast<float *>(smem + L.hsum);       // [P][32]
-    float *hsc = reinterpret_cast<float *>(smem + L.hsc);
     float *ybuf = reinterpret_cast<float *>(smem + L.ybuf);       // [P][rb]
     float *ckey = reinterpret_cast<float *>(smem + L.ckey);       // [T][C]
     int *cidx = reinterpret_cast<int *>(smem + L.cidx);
@@ -383,7 +360,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     int *misc = reinterpret_cast<int *>(smem + L.misc);   // [0] n_act [1] abort [2] flags [3] issued [4] nchunks_a [5] nchunks [6] n_kept
     unsigned long long *barrier = reinterpret_cast<unsigned long long *>(A.sync + 8);
-    unsigned *hmax_g = reinterpret_cast<unsigned *>(A.sync + DC_SYNC_HMAX);   // [2][DC_MAX_PAIRS]
 
     // The layer's inputs may come from the previous kernel in the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -406,12 +382,30 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     }
     __syncthreads();
 
-    // ---- 1. each warp sorts one 32-logit slice of one token row; all threads
-    // take activation maxima (16-byte loads of 8 bf16)
+    // ---- 1. activation maxima (16-byte loads of 8 bf16; the raw rows are kept
+    // in the ring, which is unused until the producer starts) and one sorted
+    // 32-logit slice of one token row per warp. Each warp's first logit load
+    // is issued before the activation loads so the two latencies overlap.
+    float lv0 = -INFINITY;
+    if (warp < T * NS) {
+        const int t = warp / NS, e = 32 * (warp - t * NS) + lane;
+        if (e < E) lv0 = A.logits[(size_t)t * E + e];
+    }
+    for (int i = tid; i < T * (H / 8); i += DC_THREADS) {
+        const int t = i / (H / 8);
+        const uint4 q = reinterpret_cast<const uint4 *>(A.x)[i];
+        reinterpret_cast<uint4 *>(ring)[i] = q;
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+        atomicMax(&xmax[t], __float_as_uint(m));
+    }
     for (int task = warp; task < T * NS; task += DC_WARPS) {
         const int t = task / NS, w = task - t * NS;
         const int e = 32 * w + lane;
-        const float v = e < E ? A.logits[(size_t)t * E + e] : -INFINITY;
+        const float v = task == warp ? lv0 : (e < E ? A.logits[(size_t)t * E + e] : -INFINITY);
         const bool fin = isfinite(v);
         float key = fin ? v : -INFINITY;
         int idx = e < E ? e : 0x7fffffff;
@@ -428,16 +422,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             ckey[t * C + w * k + lane] = key;
             cidx[t * C + w * k + lane] = idx;
         }
-    }
-    for (int i = tid; i < T * (H / 8); i += DC_THREADS) {
-        const int t = i / (H / 8);
-        const uint4 q = reinterpret_cast<const uint4 *>(A.x)[i];
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        float m = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
-        atomicMax(&xmax[t], __float_as_uint(m));
     }
     __syncthreads();
 
@@ -536,7 +520,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             const int t = task / H64, G64 = task - t * H64;
             const int sg = pow2_shift(__uint_as_float(xmax[t]));
             const float up = exp2i(sg);
-            const uint4 *src = reinterpret_cast<const uint4 *>(A.x + (size_t)t * H + 64 * G64);
+            const uint4 *src = reinterpret_cast<const uint4 *>(ring) + (size_t)t * (H / 8) + 8 * G64;
             float xf[64];
 #pragma unroll
             for (int v = 0; v < 8; ++v) {
@@ -632,8 +616,8 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     const int n_act = misc[0];
     // this CTA's share: gate/up row pairs [a_begin, a_end) over (active expert, row)
     const int NA = n_act * I;
-    const int a_begin = (int)((long long)NA * c / G), a_end = (int)((long long)NA * (c + 1) / G);
-    const int b0 = (int)((long long)H * c / G), b1 = (int)((long long)H * (c + 1) / G);
+    const int a_begin = (int)((unsigned)NA * c / G), a_end = (int)((unsigned)NA * (c + 1) / G);
+    const int b0 = (int)((unsigned)H * c / G), b1 = (int)((unsigned)H * (c + 1) / G);
     const int nrows_b = b1 - b0;
     if (warp == 0) {
         // the chunk table: gate/up chunks of at most rows_a row pairs, never
@@ -711,7 +695,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     // round's work items are spread over all 16 warps; a consumer barrier ends
     // the round and then its slots are released, so no warp ever waits on a
     // slot more than one phase ahead.
-    unsigned *hmax = hmax_g + (gen & 1) * DC_MAX_PAIRS;
     // T = 1: every gate/up row meets the same activations; keep them in registers
     uint32_t xv1[32];
     float XA1 = 0.0f, XB1 = 0.0f;
@@ -775,11 +758,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 // gate total in lanes 0..15, up total in lanes 16..31
                 const float tot = warp_reduce2(part) * xsc[t];
                 const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
-                if (lane == 0) {
-                    const float hv = silu_f32(tot) * upv;
-                    A.h[(size_t)p * I + r0 + row] = hv;
-                    atomicMax(&hmax[p], __float_as_uint(fabsf(hv)));
-                }
+                if (lane == 0) A.h[(size_t)p * I + r0 + row] = silu_f32(tot) * upv;
             }
         }
         consumer_sync();
@@ -789,7 +768,8 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     // ---- grid barrier: every CTA's h and |h| maxima are complete and visible
     consumer_sync();
     if (tid == 0) {
-        __threadfence();
+        // the consumer barrier orders every warp's h stores before this
+        // release; the other CTAs' acquire of the counter then sees them
         red_release_add(barrier, 1ull);
         const unsigned long long target = (gen + 1ull) * (unsigned long long)G;
         uint32_t it = 0;
@@ -799,7 +779,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 break;
             }
         }
-        __threadfence();
     }
     consumer_sync();
     if (*reinterpret_cast<volatile int *>(&misc[1])) {
@@ -808,45 +787,24 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     }
 
     if (nrows_b > 0) {
-        // ---- h of every kept pair -> fp16 with a per-pair power-of-two scale;
-        // one warp per pair, lane u converts and sums 32-column unit u
-        for (int p = warp; p < P; p += DC_CW) {
-            if (!keep[p]) continue;
-            const float mx = __uint_as_float(__ldcg(&hmax[p]));
-            float4 v[8];
-            if (lane < U) {
-                const float4 *src = reinterpret_cast<const float4 *>(A.h + (size_t)p * I + 32 * lane);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + i);
-            }
-            const int sgm = pow2_shift(mx);
-            const float up = exp2i(sgm);
-            if (lane < U) {
-                uint4 *dst = reinterpret_cast<uint4 *>(hs + ((size_t)p * I + 32 * lane) / 2);
-                float sum = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t w0 = pack_half2(v[2 * i].x * up, v[2 * i].y * up);
-                    const uint32_t w1 = pack_half2(v[2 * i].z * up, v[2 * i].w * up);
-                    const uint32_t w2 = pack_half2(v[2 * i + 1].x * up, v[2 * i + 1].y * up);
-                    const uint32_t w3 = pack_half2(v[2 * i + 1].z * up, v[2 * i + 1].w * up);
-                    dst[i] = make_uint4(w0, w1, w2, w3);
-                    sum += half_lo(w0) + half_hi(w0) + half_lo(w1) + half_hi(w1) + half_lo(w2) + half_hi(w2) +
-                           half_lo(w3) + half_hi(w3);
-                }
-                hsum[p * 32 + lane] = sum;
-            }
-            if (lane == 0) hsc[p] = exp2i(-sgm);
-        }
-        consumer_sync();
-
-        // ---- down: this CTA's output rows [b0, b1) of every routed expert;
-        // work item = (chunk, batch of 4 rows)
-        const int bpc = (A.rows_b + 3) / 4;
+        // ---- down: this CTA's output rows [b0, b1) of every routed expert.
+        // Work item = (chunk, pair of rows); each warp takes a contiguous run of
+        // a round's items. Lane u < U owns the u-th 32-column block: its 32 h
+        // values (fp32, written by every CTA before the barrier, read through
+        // L2) become int16 with a per-block power-of-two scale and stay in
+        // registers while the warp's items use the same pair; the Q8_0 codes
+        // then enter dp2a (int16 x int8, exact int32 sums) undecoded.
+        const int bpc = (A.rows_b + 1) / 2;
         for (int cr = nchunks_a; cr < nchunks; cr += DC_NSTAGE) {
             const int cend = min(cr + DC_NSTAGE, nchunks);
-            for (int f = (cr - nchunks_a) * bpc + warp; f < (cend - nchunks_a) * bpc; f += DC_CW) {
-                const int ci = nchunks_a + f / bpc, rb = 4 * (f % bpc);
+            const int nit = (cend - cr) * bpc;
+            const int f0 = (cr - nchunks_a) * bpc + warp * nit / DC_CW;
+            const int f1 = (cr - nchunks_a) * bpc + (warp + 1) * nit / DC_CW;
+            int hp = -1;
+            uint32_t hq[16];
+            float hinv = 0.0f;
+            for (int f = f0; f < f1; ++f) {
+                const int ci = nchunks_a + f / bpc, rb = 2 * (f % bpc);
                 const int4 ch = chunk[ci];
                 const int nr = ch.z;
                 if (rb >= nr) continue;
@@ -861,30 +819,29 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 const int sd = (int)D.stride, rbase = ch.y;
                 for (int qi = 0; qi < ne; ++qi) {
                     const int p = plist[q0 + qi];
-                    uint32_t hv[16];
-                    float hsu = 0.0f;
-                    if (lane < U) {
-                        const uint4 *h4 = reinterpret_cast<const uint4 *>(hs + ((size_t)p * I + 32 * lane) / 2);
+                    if (p != hp) {
+                        hp = p;
+                        if (lane < U) {
+                            float hf[32];
+                            const float4 *src = reinterpret_cast<const float4 *>(A.h + (size_t)p * I + 32 * lane);
 #pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint4 q = h4[v];
-                            hv[4 * v] = q.x;
-                            hv[4 * v + 1] = q.y;
-                            hv[4 * v + 2] = q.z;
-                            hv[4 * v + 3] = q.w;
+                            for (int v = 0; v < 8; ++v) {
+                                const float4 q = __ldcg(src + v);
+                                hf[4 * v] = q.x;
+                                hf[4 * v + 1] = q.y;
+                                hf[4 * v + 2] = q.z;
+                                hf[4 * v + 3] = q.w;
+                            }
+                            hinv = quant_i16x32(hf, hq);
                         }
-                        hsu = hsum[p * 32 + lane];
                     }
-                    float part[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        part[j] = 0.0f;
-                        if (lane < U && rb + j < nr)
-                            part[j] = q8_0_dot32(stage + (size_t)(rb + j) * sd + 34 * lane, hv, hsu);
+                    float part[2] = {0.0f, 0.0f};
+                    if (lane < U) {
+                        part[0] = q8_0_dot32_i16(stage + (size_t)rb * sd + 34 * lane, hq) * hinv;
+                        if (rb + 1 < nr) part[1] = q8_0_dot32_i16(stage + (size_t)(rb + 1) * sd + 34 * lane, hq) * hinv;
                     }
-                    const float tot = warp_reduce4(part);   // row rb + j in lanes 8j .. 8j+7
-                    const int j = lane >> 3;
-                    if ((lane & 7) == 0 && rb + j < nr) ybuf[p * L.rb + rbase + rb + j] = tot * hsc[p];
+                    const float tot = warp_reduce2(part);   // row rb in lanes 0..15, row rb + 1 in 16..31
+                    if ((lane & 15) == 0 && rb + (lane >> 4) < nr) ybuf[p * L.rb + rbase + rb + (lane >> 4)] = tot;
                 }
             }
             consumer_sync();
@@ -908,8 +865,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         A.out[(size_t)t * H + b0 + rr] = acc;
     }
 
-    // CTA 0 publishes the routing results to the workspace and clears the
-    // |h| buffer of the next launch (this launch does not use it)
+    // CTA 0 publishes the routing results to the workspace
     if (c == 0) {
         const int n_kept = misc[6];
         for (int p = tid; p < P; p += DC_CW * 32) {
@@ -931,7 +887,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             A.pairs_out[q] = plist[q];
             A.pos_out[plist[q]] = q;
         }
-        for (int p = tid; p < DC_MAX_PAIRS; p += DC_CW * 32) hmax_g[((gen + 1) & 1) * DC_MAX_PAIRS + p] = 0u;
         if (tid == 0 && misc[2]) atomicOr(A.status, (uint32_t)misc[2]);
     }
 }
@@ -971,6 +926,8 @@ DcPlan decode_fused_plan(int T, int k, int E, int H, int I, int G, int64_t gu_st
         const int share = P * I / G + 1;
         const int cap = share / rows_a + P + 2 + P * ((rb + rows_b - 1) / rows_b);
         const DcLayout L = dc_layout(T, k, E, H, I, G, stage, cap);
+        // the raw activation rows are staged in the ring during the prologue
+        if ((size_t)T * H * 2 > (size_t)DC_NSTAGE * stage) continue;
         if (L.total <= limit) {
             pl.stage = stage;
             pl.rows_a = rows_a;

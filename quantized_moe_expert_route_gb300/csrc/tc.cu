@@ -47,7 +47,12 @@ constexpr int TC_EVSLOTS = TC_ASTAGES / TC_AEV;
 constexpr int TC_BSTAGES = 3;                // B stages in shared memory
 constexpr int TC_BSTAGE_BYTES = 2 * TC_NCHUNK * 128;   // 32 KB: up to 4 A steps of <= 64 rows
 constexpr int TC_BOX_ROWS = 16;              // rows per activation TMA box
-constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups = A steps per raw stage
+#ifndef TC_DG_OVERRIDE
+constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups
+#else
+constexpr int TC_DG = TC_DG_OVERRIDE;
+#endif
+constexpr int TC_PPG = (TC_KR / TC_KA) / TC_DG;   // 64-K pieces per group per raw stage
 constexpr int TC_DQ0 = 4;                    // warps 0-3 epilogue, 4..19 dequant
 constexpr int TC_PROD = TC_DQ0 + 4 * TC_DG;  // 20: weight producer (TMA)
 constexpr int TC_MMA = TC_PROD + 1;          // 21: MMA issuer
@@ -74,7 +79,7 @@ __host__ __device__ constexpr int blk_bytes(int f) {
 }
 
 static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
-static_assert(TC_DG == 4, "one dequantising warpgroup per 64-K piece of a raw stage");
+static_assert(TC_DG * TC_PPG == TC_KR / TC_KA, "groups x pieces cover a raw stage");
 static_assert(TC_AEV == TC_KR / TC_KA, "an event is one raw stage");
 
 struct TcArgs {
@@ -749,7 +754,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     ok = false;
                     break;
                 }
-                const int a = TC_AEV * rs + g;
+#pragma unroll
+                for (int pp = 0; pp < TC_PPG; ++pp) {
+                const int gp = g + TC_DG * pp;   // the piece this warp decodes
+                const int a = TC_AEV * rs + gp;
                 if (a < nA) {
                     tmem_fence_after();
                     const uint32_t info = raw_info[slot];
@@ -759,17 +767,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     const uint32_t base = tile + (uint32_t)(row * W + lead);
                     uint32_t r[32];
                     if (fmt == MOE_Q4_K)
-                        dq_q4k(base, g, r);
+                        dq_q4k(base, gp, r);
                     else if (fmt == MOE_Q8_0)
-                        dq_q8_0(g < 2 ? base + 68 * g : base + (uint32_t)(R * W) + 68 * g - 128, r);
+                        dq_q8_0(gp < 2 ? base + 68 * gp : base + (uint32_t)(R * W) + 68 * gp - 128, r);
                     else if (fmt == MOE_Q6_K)
-                        dq_q6k(base, g, r);
+                        dq_q6k(base, gp, r);
                     else
-                        dq_mxfp4(base, g, r);
-                    tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + es * (TC_AEV * 32) + g * 32, r);
-                    tmem_wait_st();
-                    tmem_fence_before();
+                        dq_mxfp4(base, gp, r);
+                    tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + es * (TC_AEV * 32) + gp * 32, r);
                 }
+                }
+                tmem_wait_st();
+                tmem_fence_before();
                 __syncwarp();
                 if (lane == 0) {
                     red_release_shared(&a_ready[es], 1u);
