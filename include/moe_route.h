@@ -131,17 +131,17 @@ typedef struct {
 } moe_weight_table;
 
 /* Paths for moe_options.path. */
-#define MOE_PATH_AUTO 0        /* the fastest path that handles the layer (see moe_ffn_path) */
+#define MOE_PATH_AUTO 0        /* FUSED where it applies, else TENSOR where it applies, else GEMV
+                                  (see moe_ffn_path) */
 #define MOE_PATH_GEMV 1        /* grouped GEMV kernels (route, bucket, gate/up, down, combine); any layer */
 #define MOE_PATH_TENSOR 2      /* tcgen05 grouped GEMMs with TMEM-resident dequantised weights
-                                  (prefill chunks; AUTO takes it above MOE_GEMV_MAX_ROWS rows):
+                                  (prefill chunks and multi-row decode):
                                   H % 128 == 0, I % 64 == 0, any format mix. Each weight is
                                   represented in fp16, so it must lie within fp16 range
                                   (|w| <= 65504; quantized LLM weights are O(1)). */
 #define MOE_PATH_FUSED 3       /* one persistent cooperative kernel per layer for decode rows:
                                   T * k <= 64, Q4_K gate/up and Q8_0 down, H % 64 == 0,
                                   I % 32 == 0, I <= 1024 */
-#define MOE_GEMV_MAX_ROWS 96
 
 /* Options of moe_ffn_forward (NULL = defaults). */
 typedef struct {
@@ -262,7 +262,8 @@ int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream);
  * the process exits; no workspace argument, and no allocation of any kind.
  * The source pages have no counterpart of this entry point.
  *   - Sizes: accepted when moe_ffn_workspace_size(W, T, k) <= 4 MiB (e.g. up to
- *     38 tokens at E = 512, k = 10, H = 2048, I = 640); larger sizes return
+ *     25 tokens at E = 512, k = 10, H = 2048, I = 640, where rows beyond the
+ *     fused kernel's reach take the tensor path); larger sizes return
  *     MOE_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.

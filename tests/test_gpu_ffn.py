@@ -309,7 +309,19 @@ def test_fused_path_rejects_ineligible(M):
     with pytest.raises(M.MoeError) as ei:
         M.ffn_forward(table, x, logits, L.cfg.k, options=opt)
     assert ei.value.code == 8
-    assert M.ffn_path(table, 3, L.cfg.k) == M.PATH_GEMV
+    # AUTO takes the tensor path for this shape (H % 128 == 0, I % 64 == 0)
+    assert M.ffn_path(table, 3, L.cfg.k) == M.PATH_TENSOR
+
+
+@pytest.mark.parametrize("tiers,T,H,I", [("q8_0", 1, 256, 64), ("q4k", 3, 256, 64), ("mixed", 7, 256, 64),
+                                         ("mixed", 33, 512, 96 + 32), ("mixed", 96, 256, 64), ("q4k", 130, 256, 64)])
+def test_gemv_path_small(M, tiers, T, H, I):
+    """The grouped GEMV path requested explicitly, on shapes AUTO sends elsewhere."""
+    cfg = synth.LayerConfig("gv", 16, 4, H, I, T, tiers, True, 900 + T)
+    L = synth.make_layer(cfg, 0)
+    opt = M.make_options(n_experts=cfg.n_experts, path=M.PATH_GEMV)
+    out, *_ = run_layer(M, L, options=opt)
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), f"gemv {tiers} T={T}")
 
 
 def test_full_decode1_gemv_path(M):
