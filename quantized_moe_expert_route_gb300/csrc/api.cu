@@ -11,7 +11,7 @@ cudaError_t launch_route_topk(const float *logits, int T, int E, int k, int reno
                               uint32_t *status, cudaStream_t s);
 cudaError_t launch_bucket(const int32_t *ids, int T, int k, int E, int lo, int hi, uint32_t fmt_mask,
                           const DevExpert *table, int32_t *offsets, int32_t *pairs, int32_t *pos, int32_t *active,
-                          uint32_t *status, cudaStream_t s);
+                          uint32_t *status, int32_t *scratch, cudaStream_t s);
 size_t bucket_smem_bytes(int E);
 size_t gateup_smem_bytes(int H, int64_t wstride);
 size_t down_smem_bytes(int I, int64_t wstride);
@@ -232,7 +232,7 @@ int moe_bucket(const int32_t *ids, int32_t T, int32_t k, int32_t E, int32_t expe
     if (E > MOE_MAX_EXPERTS || k > MOE_MAX_K || (int64_t)T * k > (1 << 24)) return MOE_ERR_UNSUPPORTED;
     if (!offsets || !active || (T > 0 && (!ids || !pairs || !pos))) return MOE_ERR_INVALID_ARG;
     cudaError_t err = launch_bucket(ids, T, k, E, expert_lo, expert_hi, 0xffffffffu, nullptr, offsets, pairs, pos,
-                                    active, status, stream);
+                                    active, status, nullptr, stream);
     return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
 
@@ -306,7 +306,7 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     err = launch_route_topk(logits, T, E, k, o.renormalize, ids, wts, status, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     err = launch_bucket(ids, T, k, E, o.expert_lo, o.expert_hi, o.format_mask, table, offsets, pairs, pos, active,
-                        status, stream);
+                        status, reinterpret_cast<int32_t *>(base + L.bscratch), stream);
     if (err != cudaSuccess) return cuda_fail(err);
     if (path == MOE_PATH_TENSOR)
         err = launch_tc_path(table, static_cast<const char *>(W->device_table) + map_offset(E), W->gateup_formats,

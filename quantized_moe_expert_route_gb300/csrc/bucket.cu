@@ -156,13 +156,113 @@ bucket_kernel(const int32_t *__restrict__ ids, int T, int k, int E, int lo, int 
     if (flags && lane == 0 && status) atomicOr(status, flags);
 }
 
+// ---- many pairs: three short kernels over 512-pair ranges (one CTA each)
+constexpr int BM_THREADS = BUCKET_RANGE;
+constexpr int BM_WARPS = BM_THREADS / 32;
+
+// 1. per-range expert histograms -> cnt[c][e]; duplicate-id flags per token
+__global__ void __launch_bounds__(BM_THREADS) bucket_count_kernel(const int32_t *__restrict__ ids, int T, int k, int E,
+                                                                 int lo, int hi, uint32_t fmt_mask,
+                                                                 const DevExpert *__restrict__ table,
+                                                                 int32_t *__restrict__ cnt, uint32_t *__restrict__ status) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    int *hist = reinterpret_cast<int *>(smem);   // [E]
+    const int tid = threadIdx.x, P = T * k;
+    for (int e = tid; e < E; e += BM_THREADS) hist[e] = 0;
+    __syncthreads();
+    uint32_t flags = 0;
+    const int p = blockIdx.x * BM_THREADS + tid;
+    if (p < P) {
+        const int e = ids[p];
+        if (keep_pair(e, E, lo, hi, fmt_mask, table, flags)) atomicAdd(&hist[e], 1);
+        // duplicates: compare with the later slots of the same token
+        const int t = p / k, j = p - t * k;
+        if (e >= 0 && e < E)
+            for (int b = j + 1; b < k; ++b)
+                if (ids[(size_t)t * k + b] == e) flags |= MOE_FLAG_DUPLICATE_ID;
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += BM_THREADS) cnt[(size_t)blockIdx.x * E + e] = hist[e];
+    flags = __reduce_or_sync(0xffffffffu, flags);
+    if (flags && (tid & 31) == 0 && status) atomicOr(status, flags);
+}
+
+// 2. one CTA: per expert, exclusive scan over the ranges (cnt becomes each
+// range's first bucket position), offsets, active list
+__global__ void __launch_bounds__(BK_THREADS, 1) bucket_scan_kernel(int G, int E, int32_t *__restrict__ cnt,
+                                                                    int32_t *__restrict__ offsets,
+                                                                    int32_t *__restrict__ active) {
+    __shared__ int warp_tot[33];
+    const int tid = threadIdx.x;
+    int c = 0;
+    if (tid < E) {
+        for (int r = 0; r < G; ++r) {
+            const int v = cnt[(size_t)r * E + tid];
+            cnt[(size_t)r * E + tid] = c;
+            c += v;
+        }
+    }
+    int total, nact;
+    const int excl = block_excl_scan(c, warp_tot, total);
+    const int aexcl = block_excl_scan(c > 0 ? 1 : 0, warp_tot, nact);
+    if (tid < E) {
+        offsets[tid] = excl;
+        if (c > 0) active[1 + aexcl] = tid;
+        for (int r = 0; r < G; ++r) cnt[(size_t)r * E + tid] += excl;
+    }
+    if (tid == 0) {
+        offsets[E] = total;
+        active[0] = nact;
+    }
+}
+
+// 3. per range: stable scatter (warps in order, lanes in order within a warp)
+__global__ void __launch_bounds__(BM_THREADS) bucket_scatter_kernel(const int32_t *__restrict__ ids, int P, int E,
+                                                                   int lo, int hi, uint32_t fmt_mask,
+                                                                   const DevExpert *__restrict__ table,
+                                                                   const int32_t *__restrict__ cnt,
+                                                                   int32_t *__restrict__ pairs,
+                                                                   int32_t *__restrict__ pos) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    uint16_t *wcnt = reinterpret_cast<uint16_t *>(smem);   // [BM_WARPS][E]: exclusive per-warp offsets
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < BM_WARPS * E; i += BM_THREADS) wcnt[i] = 0;
+    __syncthreads();
+    const int p = blockIdx.x * BM_THREADS + tid;
+    uint32_t dummy = 0;
+    const int e = p < P ? ids[p] : -1;
+    const bool kp = p < P && keep_pair(e, E, lo, hi, fmt_mask, table, dummy);
+    const int key = kp ? e : -1;
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (kp && rank == 0) wcnt[warp * E + e] = (uint16_t)__popc(peers);
+    __syncthreads();
+    for (int x = tid; x < E; x += BM_THREADS) {
+        int acc = 0;
+        for (int w = 0; w < BM_WARPS; ++w) {
+            const int v = wcnt[w * E + x];
+            wcnt[w * E + x] = (uint16_t)acc;
+            acc += v;
+        }
+    }
+    __syncthreads();
+    if (kp) {
+        const int q = cnt[(size_t)blockIdx.x * E + e] + wcnt[warp * E + e] + rank;
+        pairs[q] = p;
+        pos[p] = q;
+    } else if (p < P) {
+        pos[p] = -1;
+    }
+}
+
 }  // namespace
 
 size_t bucket_smem_bytes(int E) { return (size_t)E * 4 * 4 + (size_t)BK_WARPS * E * 2; }
 
+
 cudaError_t launch_bucket(const int32_t *ids, int T, int k, int E, int lo, int hi, uint32_t fmt_mask,
                           const DevExpert *table, int32_t *offsets, int32_t *pairs, int32_t *pos, int32_t *active,
-                          uint32_t *status, cudaStream_t s) {
+                          uint32_t *status, int32_t *scratch, cudaStream_t s) {
     size_t smem = bucket_smem_bytes(E);
     static bool attr_set[64] = {};  // the attribute is per device
     int dev = 0;
@@ -172,6 +272,19 @@ cudaError_t launch_bucket(const int32_t *ids, int T, int k, int E, int lo, int h
             cudaFuncSetAttribute(bucket_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
         if (err != cudaSuccess) return err;
         if (dev < 64) attr_set[dev] = true;
+    }
+    const int P = T * k;
+    if (P > BUCKET_MANY && scratch) {
+        const int G = (P + BM_THREADS - 1) / BM_THREADS;
+        bucket_count_kernel<<<G, BM_THREADS, (size_t)E * 4, s>>>(ids, T, k, E, lo, hi, fmt_mask, table, scratch,
+                                                                 status);
+        cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess) return err;
+        bucket_scan_kernel<<<1, BK_THREADS, 0, s>>>(G, E, scratch, offsets, active);
+        if ((err = cudaGetLastError()) != cudaSuccess) return err;
+        bucket_scatter_kernel<<<G, BM_THREADS, (size_t)BM_WARPS * E * 2, s>>>(ids, P, E, lo, hi, fmt_mask, table,
+                                                                             scratch, pairs, pos);
+        return cudaGetLastError();
     }
     bucket_kernel<<<1, BK_THREADS, smem, s>>>(ids, T, k, E, lo, hi, fmt_mask, table, offsets, pairs, pos, active,
                                                status);

@@ -26,9 +26,18 @@ struct DevExpert {
 // (offset 8) and its per-pair |h| maxima (offset 256).
 constexpr size_t SYNC_BYTES = 1024;
 
+// Bucketing of more than BUCKET_MANY pairs runs over ranges of BUCKET_RANGE
+// pairs and needs per-range expert histograms in the workspace.
+constexpr int BUCKET_MANY = 2048;
+constexpr int BUCKET_RANGE = 512;
+inline size_t bucket_scratch_bytes(int T, int k, int E) {
+    const size_t P = (size_t)T * k;
+    return P > (size_t)BUCKET_MANY ? ((P + BUCKET_RANGE - 1) / BUCKET_RANGE) * (size_t)E * 4 : 0;
+}
+
 // Workspace layout of moe_ffn_forward; offsets in bytes from the workspace base.
 struct WsLayout {
-    size_t status, ids, wts, offsets, active, pairs, pos, h, y, total;
+    size_t status, ids, wts, offsets, active, pairs, pos, h, y, bscratch, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -47,6 +56,7 @@ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
     L.pos = take(P * 4);
     L.h = take(P * (size_t)I * 4);
     L.y = take(P * (size_t)H * 4);
+    L.bscratch = take(bucket_scratch_bytes(T, k, E));
     L.total = o;
     return L;
 }

@@ -49,6 +49,7 @@ def run_tensor(M, L, options=None, table=None, dev=None):
     ("mixed", 4, 2, 512, 192, 300),    # ~150 rows per expert: two chunks each; down K = 192 (< 256)
     ("q8_0", 12, 3, 384, 64, 37),      # H = 3 x 128
     ("mixed", 40, 8, 1024, 320, 97),   # down K = 320: a partial second raw stage
+    ("q8_0", 64, 8, 256, 64, 400),     # 3200 pairs: the many-pair (multi-CTA) bucketing
 ])
 def test_tensor_small(M, tiers, E, k, H, I, T):
     cfg = synth.LayerConfig("tc", E, k, H, I, T, tiers, tiers != "q8_0", 1000 + 7 * T + E)
