@@ -49,8 +49,11 @@ constexpr int DC_MAX_PAIRS = 64;                 // T * k
 constexpr int DC_ROWS_A = 4;                     // max gate/up row pairs per chunk
 constexpr uint32_t DC_MAGIC = 0x64006400u;       // fp16 1024.0 in both halves
 
+constexpr size_t DC_HSM_MAX = 48 * 1024;          // largest h staged in shared memory, bytes
+__host__ __device__ inline bool dc_stage_h(int P, int I) { return (size_t)P * I * 4 <= DC_HSM_MAX; }
+
 struct DcLayout {
-    size_t ring, xs, xsum, xsc, xmax, ybuf, ckey, cidx, sm, ss, selk, ids, wts, keep, act, aoff, plist,
+    size_t ring, xs, xsum, xsc, xmax, hsm, ybuf, ckey, cidx, sm, ss, selk, ids, wts, keep, act, aoff, plist,
         dpair, chunks, full, empty, misc, total;
     int rb, ns, C;
 };
@@ -72,6 +75,9 @@ __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I,
     L.xsum = take((size_t)T * (H / 64) * 2 * 4);
     L.xsc = take((size_t)T * 4);
     L.xmax = take((size_t)T * 4);
+    // h of every pair staged in shared memory after the barrier (32-column
+    // blocks at a 36-float pitch) when it is small; else read from L2 per lane
+    L.hsm = take(dc_stage_h(T * k, I) ? (size_t)T * k * (I / 32) * 36 * 4 : 0);
     L.ybuf = take((size_t)P * L.rb * 4);
     L.ckey = take((size_t)T * L.C * 4);
     L.cidx = take((size_t)T * L.C * 4);
@@ -343,6 +349,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     float *xsc = reinterpret_cast<float *>(smem + L.xsc);
     unsigned *xmax = reinterpret_cast<unsigned *>(smem + L.xmax);
     float *ybuf = reinterpret_cast<float *>(smem + L.ybuf);       // [P][rb]
+    float *hsm = reinterpret_cast<float *>(smem + L.hsm);         // [P][I/32][36] when staged
     float *ckey = reinterpret_cast<float *>(smem + L.ckey);       // [T][C]
     int *cidx = reinterpret_cast<int *>(smem + L.cidx);
     float *slm = reinterpret_cast<float *>(smem + L.sm);          // [T][NS] slice max
@@ -786,6 +793,21 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         return;
     }
 
+    const bool hstaged = dc_stage_h(P, I);
+    if (nrows_b > 0 && hstaged) {
+        // every kept pair's h -> shared memory, coalesced (16-byte loads by
+        // consecutive threads), at a 36-float block pitch so that the 16-byte
+        // reads of one block per lane below are free of bank conflicts
+        const int n4 = I / 4;
+        for (int f = tid; f < P * n4; f += DC_CW * 32) {
+            const int p = f / n4, i4 = f - p * n4;
+            if (!keep[p]) continue;
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(A.h + (size_t)p * I) + i4);
+            const int i = 4 * i4;
+            *reinterpret_cast<float4 *>(hsm + ((size_t)p * (I / 32) + (i >> 5)) * 36 + (i & 31)) = v;
+        }
+        consumer_sync();
+    }
     if (nrows_b > 0) {
         // ---- down: this CTA's output rows [b0, b1) of every routed expert.
         // Work item = (chunk, pair of rows); each warp takes a contiguous run of
@@ -823,10 +845,12 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                         hp = p;
                         if (lane < U) {
                             float hf[32];
-                            const float4 *src = reinterpret_cast<const float4 *>(A.h + (size_t)p * I + 32 * lane);
+                            const float4 *src = hstaged
+                                ? reinterpret_cast<const float4 *>(hsm + ((size_t)p * U + lane) * 36)
+                                : reinterpret_cast<const float4 *>(A.h + (size_t)p * I + 32 * lane);
 #pragma unroll
                             for (int v = 0; v < 8; ++v) {
-                                const float4 q = __ldcg(src + v);
+                                const float4 q = hstaged ? src[v] : __ldcg(src + v);
                                 hf[4 * v] = q.x;
                                 hf[4 * v + 1] = q.y;
                                 hf[4 * v + 2] = q.z;
