@@ -15,24 +15,26 @@
 //      the token rows itself: each warp sorts a 32-logit slice (bitonic, in
 //      registers), then candidates are ranked by counting. The routed
 //      experts' descriptors are requested right after selection.
-//   2. The routed experts' gate/up rows are split evenly across the CTAs. A
-//      producer warp streams the CTA's gate/up rows, then its down rows, into
-//      a ring of 12 KB shared-memory stages with TMA bulk copies; for one
-//      token the whole share is in flight at once. Four groups of four
-//      consumer warps decode the stages and write h = silu(W_gate x) * (W_up x)
-//      (fp32) plus a per-pair running max |h| to global memory.
+//   2. The routed experts' gate/up rows are split evenly across the CTAs.
+//      Lane s of warp 0 streams the CTA's gate/up rows, then its down rows,
+//      through ring slot s of 16 shared-memory stages of up to 12 KB with TMA
+//      bulk copies: the first fill as soon as the chunk table exists (for one
+//      token nearly the whole share is then in flight), each refill when the
+//      16 warps have finished a round of chunks. The warps decode the stages
+//      and write h = silu(W_gate x) * (W_up x) (fp32) to global memory.
 //   3. A bounded grid barrier (cooperative launch: all CTAs co-resident)
 //      separates gate/up from down.
 //   4. Each CTA owns a slice of output rows for every routed expert, so the
 //      router-weighted combine runs in-CTA in ascending slot order.
 //
-// Arithmetic: codes become exact fp16 values with bit operations (a 4-bit
-// code q as 1024 + q or 1024 + 16 q, an 8-bit code as 1152 + q), activations
-// are fp16 with a per-row power-of-two scale, products accumulate in fp32 with
-// the mixed fp16 x fp16 -> fp32 FMA; the constant offsets are removed with
-// exact per-group activation sums. This path handles Q4_K gate/up with Q8_0
-// down; other layers take the general grouped GEMV path.
+// Arithmetic: activations become int16 with a per-row power-of-two scale (x)
+// or a per-32-block one (h); the quantised codes enter dp2a (int16 x int8 ->
+// int32) undecoded (Q8_0) or unpacked to bytes (Q4_K), so each block's sum is
+// an exact integer, scaled once per block in fp32. The Q4_K minimum term uses
+// the exact per-sub-block activation sums. This path handles Q4_K gate/up with
+// Q8_0 down; other layers take the tensor-core or grouped GEMV path.
 #include <algorithm>
+#include <type_traits>
 
 #include "moe_internal.cuh"
 
@@ -40,22 +42,23 @@ namespace moe {
 
 namespace {
 
-constexpr int DC_CW = 16;                        // consumer warps
-constexpr int DC_WARPS = DC_CW + 1;              // + one producer warp
-constexpr int DC_THREADS = DC_WARPS * 32;
+constexpr int DC_CW = 16;                        // warps (all consume; warp 0 also issues the copies)
+constexpr int DC_WARPS = DC_CW;
+constexpr int DC_THREADS = DC_WARPS * 32;        // 4 warps per SM sub-partition: up to 128 registers
 constexpr int DC_STAGE_MAX = 12 * 1024;          // ring stage bytes (smaller when shared memory is tight)
-constexpr int DC_NSTAGE = DC_CW;                 // one ring slot per consumer warp: warp w owns slot w
+constexpr int DC_NSTAGE = 16;                    // ring slots; slot s is served by lane s of warp 0
 constexpr int DC_MAX_PAIRS = 64;                 // T * k
 constexpr int DC_ROWS_A = 4;                     // max gate/up row pairs per chunk
-constexpr uint32_t DC_MAGIC = 0x64006400u;       // fp16 1024.0 in both halves
+constexpr int DC_SURV = 64;                      // top-k survivors ranked from the short list
 
 constexpr size_t DC_HSM_MAX = 48 * 1024;          // largest h staged in shared memory, bytes
 __host__ __device__ inline bool dc_stage_h(int P, int I) { return (size_t)P * I * 4 <= DC_HSM_MAX; }
 
 struct DcLayout {
-    size_t ring, xs, xsum, xsc, xmax, hsm, ybuf, ckey, cidx, sm, ss, selk, ids, wts, keep, act, aoff, plist,
-        dpair, chunks, full, empty, misc, total;
-    int rb, ns, C;
+    size_t ring, xs, xsum, xsc, xmax, hsm, ybuf, rowk, smax, surv, scnt, tau, ss, selk, ids, wts, keep, act, aoff,
+        plist,
+        dpair, chunks, full, misc, total;
+    int rb, ns;
 };
 
 __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I, int G, int stage, int chunk_cap) {
@@ -69,7 +72,6 @@ __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I,
     const int P = T * k;
     L.rb = (H + G - 1) / G;
     L.ns = (E + 31) / 32;
-    L.C = (L.ns * k + 3) / 4 * 4;
     L.ring = take((size_t)DC_NSTAGE * stage);
     L.xs = take((size_t)T * H * 2);
     L.xsum = take((size_t)T * (H / 64) * 2 * 4);
@@ -79,9 +81,11 @@ __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I,
     // blocks at a 36-float pitch) when it is small; else read from L2 per lane
     L.hsm = take(dc_stage_h(T * k, I) ? (size_t)T * k * (I / 32) * 36 * 4 : 0);
     L.ybuf = take((size_t)P * L.rb * 4);
-    L.ckey = take((size_t)T * L.C * 4);
-    L.cidx = take((size_t)T * L.C * 4);
-    L.sm = take((size_t)T * L.ns * 4);
+    L.rowk = take((size_t)T * L.ns * 32 * 4);
+    L.smax = take((size_t)T * L.ns * 8);
+    L.surv = take((size_t)T * DC_SURV * 8);
+    L.scnt = take((size_t)T * 4);
+    L.tau = take((size_t)T * 8);
     L.ss = take((size_t)T * L.ns * 4);
     L.selk = take((size_t)P * 4);
     L.ids = take((size_t)P * 4);
@@ -93,8 +97,7 @@ __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I,
     L.dpair = take((size_t)P * sizeof(DevExpert));
     L.chunks = take((size_t)chunk_cap * 16);
     L.full = take((size_t)DC_NSTAGE * 8);
-    L.empty = take((size_t)DC_NSTAGE * 8);
-    L.misc = take(64);
+    L.misc = take(128);
     L.total = o;
     return L;
 }
@@ -119,34 +122,8 @@ struct DcArgs {
     long long ustep[3];
 };
 
-// ---------------------------------------------------------------- small PTX helpers
-__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
-    return r;
-}
-
-
-// acc += lo(a) * lo(b) + hi(a) * hi(b), fp16 operands, fp32 accumulation
-__device__ __forceinline__ void fma2_f16_f32(float &acc, uint32_t a, uint32_t b) {
-    asm("{ .reg .b16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %1;\n\t"
-        "mov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.f16 %0, al, bl, %0;\n\t"
-        "fma.rn.f32.f16 %0, ah, bh, %0; }"
-        : "+f"(acc)
-        : "r"(a), "r"(b));
-}
-
 __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xffff))); }
 __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
-
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-    uint16_t lo, hi;
-    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(lo) : "f"(a));
-    asm("cvt.rn.f16.f32 %0, %1;" : "=h"(hi) : "f"(b));
-    return (uint32_t)lo | ((uint32_t)hi << 16);
-}
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
     unsigned long long v;
@@ -154,8 +131,10 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
     return v;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -178,30 +157,21 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
-// Descending bitonic sort of one (key, index) pair per lane under topk_beats.
-__device__ __forceinline__ void warp_sort_desc(float &key, int &idx) {
+// Ascending bitonic sort of one int key per lane within each group of W lanes.
+template <int W>
+__device__ __forceinline__ int warp_sort_asc(int key) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
+    for (int size = 2; size <= W; size <<= 1) {
 #pragma unroll
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float ok = __shfl_xor_sync(0xffffffffu, key, stride);
-            const int oi = __shfl_xor_sync(0xffffffffu, idx, stride);
-            const bool desc = (lane & size) == 0 || size == 32;
+            const int other = __shfl_xor_sync(0xffffffffu, key, stride);
+            const bool asc = (lane & size) == 0 || size == W;
             const bool lower = (lane & stride) == 0;
-            const bool mine = topk_beats(key, idx, ok, oi);
-            if (mine != (lower == desc)) {
-                key = ok;
-                idx = oi;
-            }
+            key = (lower == asc) ? min(key, other) : max(key, other);
         }
     }
+    return key;
 }
 
 // cp.async of 8 bytes global -> shared (L1-allocating); completion via cp_async_wait_all.
@@ -246,30 +216,39 @@ __device__ __forceinline__ void q4k_pair_scales(int g, uint32_t s03, uint32_t s4
     m1 = (float)(mnp >> 8);
 }
 
+__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(c) : "r"(a), "r"(b));
+    return c;
+}
+__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(c) : "r"(a), "r"(b));
+    return c;
+}
+
 // One lane's share of a Q4_K row dot product: the 64 weights of pair g of
-// super-block blk (sub-blocks 2g, 2g+1) times 64 fp16 activations xv (order
-// of the activation layout), with XA, XB the sums of those activations per
-// sub-block. Returns sum_i w_i x_i.
-__device__ __forceinline__ float q4k_dot64(const uint8_t *blk, int g, const uint32_t xv[32], float XA, float XB) {
+// super-block blk (sub-blocks 2g, 2g+1) times 64 int16 activations xq (two
+// per word: xq[4m], xq[4m+1] hold sub-block 2g's weights 4m..4m+3 and
+// xq[4m+2], xq[4m+3] sub-block 2g+1's), with XA, XB the sums of those
+// activations per sub-block. The 4-bit codes enter dp2a as bytes, so the
+// products and sums per sub-block are exact integers. Returns sum_i w_i x_i.
+__device__ __forceinline__ float q4k_dot64(const uint8_t *blk, int g, const uint32_t xq[32], float XA, float XB) {
     const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
     const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * g);
     const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * g);
     const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    float sA0 = 0.0f, sA1 = 0.0f, sB0 = 0.0f, sB1 = 0.0f;
+    int sA0 = 0, sA1 = 0, sB0 = 0, sB1 = 0;
 #pragma unroll
     for (int m = 0; m < 8; ++m) {
-        const uint32_t w = cw[m], w8 = w >> 8;
-        fma2_f16_f32(sA0, lop3_and_or(w, 0x000F000Fu, DC_MAGIC), xv[4 * m + 0]);
-        fma2_f16_f32(sB0, lop3_and_or(w, 0x00F000F0u, DC_MAGIC), xv[4 * m + 1]);
-        fma2_f16_f32(sA1, lop3_and_or(w8, 0x000F000Fu, DC_MAGIC), xv[4 * m + 2]);
-        fma2_f16_f32(sB1, lop3_and_or(w8, 0x00F000F0u, DC_MAGIC), xv[4 * m + 3]);
+        const uint32_t lo = cw[m] & 0x0F0F0F0Fu, hi = (cw[m] >> 4) & 0x0F0F0F0Fu;
+        sA0 = dp2a_lo(xq[4 * m + 0], lo, sA0);
+        sA1 = dp2a_hi(xq[4 * m + 1], lo, sA1);
+        sB0 = dp2a_lo(xq[4 * m + 2], hi, sB0);
+        sB1 = dp2a_hi(xq[4 * m + 3], hi, sB1);
     }
     float sc0, sc1, m0, m1;
     q4k_pair_scales(g, hdr.y, hdr.z, hdr.w, sc0, sc1, m0, m1);
     const float d = half_lo(hdr.x), dmin = half_hi(hdr.x);
-    // SA = sum (1024 + q) x over sub-block 2g, SB = sum (1024 + 16 q) x over 2g+1
-    return d * (sc0 * ((sA0 + sA1) - 1024.0f * XA) + sc1 * 0.0625f * ((sB0 + sB1) - 1024.0f * XB)) -
-           dmin * (m0 * XA + m1 * XB);
+    return d * (sc0 * (float)(sA0 + sA1) + sc1 * (float)(sB0 + sB1)) - dmin * (m0 * XA + m1 * XB);
 }
 
 
@@ -322,16 +301,195 @@ __device__ __forceinline__ float q8_0_dot32_i16(const uint8_t *blk, const uint32
 }
 
 
+// Before an aborting CTA exits (after a CTA barrier, so no copy is issued
+// any more): wait (bounded) for the bulk copy last issued into each ring
+// slot, so that none still writes its shared memory.
 __device__ __forceinline__ void drain_copies(uint64_t *full, int *misc) {
     if (threadIdx.x != 0) return;
-    const int issued = *reinterpret_cast<volatile int *>(&misc[3]);
-    for (int ci = issued - DC_NSTAGE < 0 ? 0 : issued - DC_NSTAGE; ci < issued; ++ci)
-        mbar_wait(&full[ci % DC_NSTAGE], (uint32_t)(ci / DC_NSTAGE) & 1u);
+    for (int s = 0; s < DC_NSTAGE; ++s) {
+        const int ci = *reinterpret_cast<volatile int *>(&misc[16 + s]);
+        if (ci >= 0) mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u);
+    }
 }
 
 __device__ __forceinline__ void set_abort(int *misc, uint32_t *status) {
     atomicOr(status, (uint32_t)MOE_FLAG_WAIT_TIMEOUT);
     *reinterpret_cast<volatile int *>(&misc[1]) = 1;
+}
+
+// ---------------------------------------------------------------- once-per-launch steps
+// (out of line: one copy each keeps the kernel's code small)
+
+__device__ __noinline__ int dc_bucket_sorted(int P, const uint8_t *keep, const int *ids, int *plist, int *act,
+                                             int *aoff, int *misc) {
+    const int lane = threadIdx.x & 31;
+    constexpr int SENT = 0x7fffffff;
+    int key[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int p = lane + 32 * r;
+        key[r] = (p < P && keep[p]) ? ((ids[p] << 8) | p) : SENT;
+    }
+    if (P <= 16) {
+        key[0] = warp_sort_asc<16>(key[0]);
+        if (lane >= 16) key[0] = SENT;
+    } else if (P <= 32) {
+        key[0] = warp_sort_asc<32>(key[0]);
+    } else {
+#pragma unroll 1
+        for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll 1
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                if (stride == 32) {
+                    const int lo = min(key[0], key[1]), hi = max(key[0], key[1]);   // size == 64: ascending
+                    key[0] = lo;
+                    key[1] = hi;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int i = lane + 32 * r;
+                        const int other = __shfl_xor_sync(0xffffffffu, key[r], stride);
+                        const bool asc = (i & size) == 0;
+                        const bool lower = (lane & stride) == 0;
+                        key[r] = (lower == asc) ? min(key[r], other) : max(key[r], other);
+                    }
+                }
+            }
+        }
+    }
+    // element i = lane + 32 r holds key[r]; starts of expert runs
+    const int prev0 = __shfl_up_sync(0xffffffffu, key[0], 1);
+    const int prev1 = __shfl_up_sync(0xffffffffu, key[1], 1);
+    const int last0 = __shfl_sync(0xffffffffu, key[0], 31);
+    const int pk[2] = {lane == 0 ? -1 : prev0, lane == 0 ? last0 : prev1};
+    bool start[2], valid[2];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        valid[r] = key[r] != SENT;
+        start[r] = valid[r] && (pk[r] < 0 || (pk[r] >> 8) != (key[r] >> 8));
+    }
+    const unsigned s0 = __ballot_sync(0xffffffffu, start[0]), s1 = __ballot_sync(0xffffffffu, start[1]);
+    const unsigned v0 = __ballot_sync(0xffffffffu, valid[0]), v1 = __ballot_sync(0xffffffffu, valid[1]);
+    const int n_kept = __popc(v0) + __popc(v1), n_act = __popc(s0) + __popc(s1);
+    const unsigned below = (1u << lane) - 1u;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int i = lane + 32 * r;
+        if (valid[r]) plist[i] = key[r] & 0xff;
+        if (start[r]) {
+            const int a = r == 0 ? __popc(s0 & below) : __popc(s0) + __popc(s1 & below);
+            act[a] = key[r] >> 8;
+            aoff[a] = i;
+        }
+    }
+    if (lane == 0) {
+        aoff[n_act] = n_kept;
+        misc[0] = n_act;
+        misc[6] = n_kept;
+    }
+
+    return n_act;
+}
+
+__device__ __noinline__ void dc_route_weights(int t, int k, int NS, int renorm, const float *selk, const float2 *smax,
+                                              const float *sls, float *wts) {
+    const int lane = threadIdx.x & 31;
+    const float m = selk[t * k];                     // the row's largest logit (or -inf)
+    const bool any_finite = m > -INFINITY;
+    const float kj = lane < k ? selk[t * k + lane] : -INFINITY;
+    const float ex = (lane < k && any_finite && kj > -INFINITY) ? expf(kj - m) : 0.0f;
+    float denom;
+    if (renorm) {
+        denom = warp_sum(ex);
+    } else {
+        float s = 0.0f;
+        for (int w = lane; w < NS; w += 32) {
+            const float mw = smax[t * NS + w].x;
+            if (any_finite && mw > -INFINITY) s += sls[t * NS + w] * expf(mw - m);
+        }
+        denom = warp_sum(s);
+    }
+    if (lane < k) {
+        const int p = t * k + lane;
+        wts[p] = denom > 0.0f ? ex / denom : 0.0f;
+    }
+}
+
+__device__ __noinline__ void dc_build_chunks(int n_act, int I, int H, int c, int G, int rows_a, int rows_b,
+                                             int chunk_cap, int4 *chunk, int *misc) {
+    const int lane = threadIdx.x & 31;
+    // the chunk table: gate/up chunks of at most rows_a row pairs, never
+    // crossing an expert, over this CTA's share [a_begin, a_end) of the
+    // (active expert, row) space; then, per active expert, the CTA's down
+    // rows in chunks of rows_b. Lane j first sizes the j-th expert
+    // segment of the share; then each lane fills chunk entries.
+    const int NA = n_act * I;
+    const int a_begin = (int)((unsigned)NA * c / G), a_end = (int)((unsigned)NA * (c + 1) / G);
+    const int b0 = (int)((unsigned)H * c / G), b1 = (int)((unsigned)H * (c + 1) / G);
+    const int nrows_b = b1 - b0;
+    const int a_first = a_begin / I, a_last = a_end > a_begin ? (a_end - 1) / I : a_first - 1;
+    int total = 0;
+    for (int seg0 = a_first; seg0 <= a_last; seg0 += 32) {
+        const int a = seg0 + lane;
+        int len = 0, rs = 0;
+        if (a <= a_last) {
+            rs = max(a_begin, a * I);
+            len = min(a_end, (a + 1) * I) - rs;
+        }
+        const int nch = (len + rows_a - 1) / rows_a;
+        int inc = nch;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += v;
+        }
+        const int first = total + inc - nch;          // this segment's first chunk
+        const int nseg = min(32, a_last - seg0 + 1);
+        const int segtot = __shfl_sync(0xffffffffu, inc, 31);
+        for (int n0 = 0; n0 < segtot; n0 += 32) {
+            const int n = total + n0 + lane;
+            int j = 0;
+            for (int q = 1; q < nseg; ++q)
+                if (__shfl_sync(0xffffffffu, first, q) <= n) j = q;
+            const int fj = __shfl_sync(0xffffffffu, first, j);
+            const int rsj = __shfl_sync(0xffffffffu, rs, j), lenj = __shfl_sync(0xffffffffu, len, j);
+            if (n0 + lane < segtot && n < chunk_cap) {
+                const int aj = seg0 + j;
+                const int r = rsj + (n - fj) * rows_a;
+                chunk[n] = make_int4(aj, r - aj * I, min(rows_a, rsj + lenj - r), 0);
+            }
+        }
+        total += segtot;
+    }
+    const int nb = (nrows_b + rows_b - 1) / rows_b;
+    for (int i = lane; i < n_act * nb; i += 32) {
+        const int a = i / nb, j = i - a * nb;
+        if (total + i < chunk_cap) chunk[total + i] = make_int4(a, j * rows_b, min(rows_b, nrows_b - j * rows_b), 1);
+    }
+    if (lane == 0) {
+        misc[4] = min(total, chunk_cap);
+        misc[5] = min(total + n_act * nb, chunk_cap);
+    }
+}
+
+__device__ __noinline__ void dc_issue_chunk(int ci, int nchunks_a, int b0, uint8_t *ring, int stage,
+                                            const int4 *chunk, const DevExpert *dpair, const int *plist,
+                                            const int *aoff, uint64_t *full, int *misc) {
+    const int s = ci % DC_NSTAGE;
+    uint8_t *dst = ring + (size_t)s * stage;
+    const int4 ch = chunk[ci];
+    const DevExpert &X = dpair[plist[aoff[ch.x]]];
+    if (ci < nchunks_a) {
+        const uint32_t bg = (uint32_t)(ch.z * X.gate.stride), bu = (uint32_t)(ch.z * X.up.stride);
+        mbar_expect_tx(&full[s], bg + bu);
+        bulk_g2s(dst, X.gate.data + (size_t)ch.y * X.gate.stride, bg, &full[s]);
+        bulk_g2s(dst + bg, X.up.data + (size_t)ch.y * X.up.stride, bu, &full[s]);
+    } else {
+        const uint32_t bd = (uint32_t)(ch.z * X.down.stride);
+        mbar_expect_tx(&full[s], bd);
+        bulk_g2s(dst, X.down.data + (size_t)(b0 + ch.y) * X.down.stride, bd, &full[s]);
+    }
+    *reinterpret_cast<volatile int *>(&misc[16 + s]) = ci;
 }
 
 // ---------------------------------------------------------------- the kernel
@@ -341,18 +499,23 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int T = A.T, k = A.k, E = A.E, H = A.H, I = A.I, P = T * k;
     const DcLayout L = dc_layout(T, k, E, H, I, G, A.stage, A.chunk_cap);
-    const int NS = L.ns, C = L.C, H64 = H / 64, U = I / 32;
+    const int NS = L.ns, NSE = 32 * L.ns, H64 = H / 64, U = I / 32;
 
     uint8_t *ring = smem + L.ring;
+    // the raw activation rows occupy the ring's last slots during the prologue
+    const int nraw = (T * H * 2 + A.stage - 1) / A.stage;
+    uint8_t *xraw = ring + (size_t)DC_NSTAGE * A.stage - (size_t)T * H * 2;
     uint32_t *xs = reinterpret_cast<uint32_t *>(smem + L.xs);     // per token: [8][H/64] uint4 (half2 words)
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);       // [T][H/64][2]
     float *xsc = reinterpret_cast<float *>(smem + L.xsc);
     unsigned *xmax = reinterpret_cast<unsigned *>(smem + L.xmax);
     float *ybuf = reinterpret_cast<float *>(smem + L.ybuf);       // [P][rb]
     float *hsm = reinterpret_cast<float *>(smem + L.hsm);         // [P][I/32][36] when staged
-    float *ckey = reinterpret_cast<float *>(smem + L.ckey);       // [T][C]
-    int *cidx = reinterpret_cast<int *>(smem + L.cidx);
-    float *slm = reinterpret_cast<float *>(smem + L.sm);          // [T][NS] slice max
+    float *rowk = reinterpret_cast<float *>(smem + L.rowk);       // [T][NS*32] logits (-inf if not finite)
+    float2 *smax = reinterpret_cast<float2 *>(smem + L.smax);     // [T][NS] slice best (key, index bits)
+    float2 *surv = reinterpret_cast<float2 *>(smem + L.surv);     // [T][DC_SURV] survivors (key, index bits)
+    int *scnt = reinterpret_cast<int *>(smem + L.scnt);           // [T] survivor counts
+    float2 *tau = reinterpret_cast<float2 *>(smem + L.tau);       // [T] the k-th best slice best
     float *sls = reinterpret_cast<float *>(smem + L.ss);          // [T][NS] slice sum exp(l - max)
     float *selk = reinterpret_cast<float *>(smem + L.selk);       // [P] selected logits
     int *ids = reinterpret_cast<int *>(smem + L.ids);
@@ -364,35 +527,40 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     DevExpert *dpair = reinterpret_cast<DevExpert *>(smem + L.dpair);   // descriptor of each pair's expert
     int4 *chunk = reinterpret_cast<int4 *>(smem + L.chunks);   // (a, first row, rows): gate/up, then down
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
-    int *misc = reinterpret_cast<int *>(smem + L.misc);   // [0] n_act [1] abort [2] flags [3] issued [4] nchunks_a [5] nchunks [6] n_kept
+    // [0] n_act [1] abort [2] flags [4] nchunks_a [5] nchunks [6] n_kept [7] chunks issued
+    // before the ring's raw-activation slots are free [16 + s] the last chunk issued into
+    // ring slot s (-1: none)
+    int *misc = reinterpret_cast<int *>(smem + L.misc);
     unsigned long long *barrier = reinterpret_cast<unsigned long long *>(A.sync + 8);
 
     // The layer's inputs may come from the previous kernel in the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // barrier generation of this launch (no CTA of it has passed the barrier
-    // yet); first used in the gate/up phase, so the load latency is hidden
-    const unsigned long long gen = ld_acquire_u64(barrier) / (unsigned long long)G;
 
     if (tid == 0) {
-        for (int s = 0; s < DC_NSTAGE; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
+        for (int s = 0; s < DC_NSTAGE; ++s) mbar_init(&full[s], 1);
         fence_mbar_init();
-        for (int i = 0; i < 8; ++i) misc[i] = 0;
+        for (int i = 0; i < 16; ++i) misc[i] = 0;
+        for (int i = 16; i < 16 + DC_NSTAGE; ++i) misc[i] = -1;
     }
-    for (int t = tid; t < T; t += DC_THREADS) xmax[t] = 0u;
-    for (int i = tid; i < T * C; i += DC_THREADS) {      // candidate padding
-        ckey[i] = -INFINITY;
-        cidx[i] = 0x7fffffff;
+    for (int t = tid; t < T; t += DC_THREADS) {
+        xmax[t] = 0u;
+        scnt[t] = 0;
     }
     __syncthreads();
+    // barrier count before this launch's arrivals: fewer than G of them can
+    // precede this read, so count / G is this launch's generation. A relaxed
+    // load issued beside the logit and activation loads, so that its latency
+    // overlaps theirs (the next CTA barrier waits for all of them); first
+    // used at the grid barrier.
+    unsigned long long gen_count = 0;
+    if (tid == 0) gen_count = ld_relaxed_u64(barrier);
 
     // ---- 1. activation maxima (16-byte loads of 8 bf16; the raw rows are kept
-    // in the ring, which is unused until the producer starts) and one sorted
-    // 32-logit slice of one token row per warp. Each warp's first logit load
-    // is issued before the activation loads so the two latencies overlap.
+    // in the ring's last slots, which are filled last) and, per warp,
+    // the best logit of one 32-logit slice of one token row (under the
+    // selection order: larger logit, then lower expert index). Each warp's
+    // first logit load is issued before the activation loads so the two
+    // latencies overlap.
     float lv0 = -INFINITY;
     if (warp < T * NS) {
         const int t = warp / NS, e = 32 * (warp - t * NS) + lane;
@@ -401,7 +569,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     for (int i = tid; i < T * (H / 8); i += DC_THREADS) {
         const int t = i / (H / 8);
         const uint4 q = reinterpret_cast<const uint4 *>(A.x)[i];
-        reinterpret_cast<uint4 *>(ring)[i] = q;
+        reinterpret_cast<uint4 *>(xraw)[i] = q;
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         float m = 0.0f;
 #pragma unroll
@@ -414,87 +582,120 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         const int e = 32 * w + lane;
         const float v = task == warp ? lv0 : (e < E ? A.logits[(size_t)t * E + e] : -INFINITY);
         const bool fin = isfinite(v);
-        float key = fin ? v : -INFINITY;
-        int idx = e < E ? e : 0x7fffffff;
+        const float key = fin ? v : -INFINITY;
         if (__any_sync(0xffffffffu, e < E && !fin) && lane == 0)
             atomicOr(reinterpret_cast<unsigned *>(&misc[2]), (unsigned)MOE_FLAG_NONFINITE_LOGIT);
-        const float m = warp_max(key);
-        const float s = warp_sum((m > -INFINITY && key > -INFINITY) ? expf(key - m) : 0.0f);
-        if (lane == 0) {
-            slm[t * NS + w] = m;
-            sls[t * NS + w] = s;
+        rowk[t * NSE + e] = key;
+        float bk = key;
+        int bi = e < E ? e : 0x7fffffff;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            const float ok = __shfl_xor_sync(0xffffffffu, bk, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (topk_beats(ok, oi, bk, bi)) {
+                bk = ok;
+                bi = oi;
+            }
         }
-        warp_sort_desc(key, idx);
-        if (lane < k) {
-            ckey[t * C + w * k + lane] = key;
-            cidx[t * C + w * k + lane] = idx;
+        if (!A.renorm) {   // the slice's sum of exp(l - max) for the full-softmax denominator
+            const float s = warp_sum((bk > -INFINITY && key > -INFINITY) ? expf(key - bk) : 0.0f);
+            if (lane == 0) sls[t * NS + w] = s;
         }
+        if (lane == 0) smax[t * NS + w] = make_float2(bk, __int_as_float(bi));
     }
     __syncthreads();
 
-    // ---- 2. warp t < T: top-k of row t. The k-th best slice maximum tau is a
-    // lower bound of the row's k-th best logit, so only candidates that tau
-    // does not beat are ranked. Then the router weights, the kept flags and
-    // the (asynchronous) fetch of the selected experts' descriptors.
-    // Warps >= T meanwhile convert the activations.
+    // ---- 2. top-k. The k-th best slice best tau (per row) is a lower bound
+    // of the row's k-th best logit: only logits that tau does not beat can be
+    // selected, usually a few more than k. (a) warp t < T finds tau of row t
+    // by counting, (b) every warp lists the survivors of its slices, (c) warp
+    // t ranks the survivors of row t by counting (ranks are unique: the
+    // order is total) and keeps ranks < k. Rows with more survivors than the
+    // list holds are ranked over the whole row.
     if (warp < T) {
         const int t = warp;
-        float hk = lane < NS ? ckey[t * C + lane * k] : -INFINITY;
-        int hi = lane < NS ? cidx[t * C + lane * k] : 0x7fffffff;
-        warp_sort_desc(hk, hi);
-        float tk = -INFINITY;
-        int ti = 0x7fffffff;
-        if (NS >= k) {
-            tk = __shfl_sync(0xffffffffu, hk, k - 1);
-            ti = __shfl_sync(0xffffffffu, hi, k - 1);
-        }
-        float *sk = ckey + t * C;   // survivors compacted in place, in chunks of 32
-        int *si = cidx + t * C;
-        int M = 0;
-        for (int c0 = 0; c0 < C; c0 += 32) {
-            const int ci = c0 + lane;
-            const float kk = ci < C ? sk[ci] : -INFINITY;
-            const int ii = ci < C ? si[ci] : 0x7fffffff;
-            const bool surv = ci < C && ii < E && !topk_beats(tk, ti, kk, ii);
-            const unsigned b = __ballot_sync(0xffffffffu, surv);
-            __syncwarp();
-            if (surv) {
-                const int dst = M + __popc(b & ((1u << lane) - 1u));
-                sk[dst] = kk;
-                si[dst] = ii;
-            }
-            M += __popc(b);
-            __syncwarp();
-        }
-        for (int m = lane; m < M; m += 32) {
-            const float kk = sk[m];
-            const int ii = si[m];
+        bool found = false;
+        for (int l = lane; l < NS; l += 32) {
+            const float2 me = smax[t * NS + l];
             int rank = 0;
-            for (int o = 0; o < M; ++o) rank += topk_beats(sk[o], si[o], kk, ii) ? 1 : 0;
-            if (rank < k) {
-                ids[t * k + rank] = ii;
-                selk[t * k + rank] = kk;
+#pragma unroll 4
+            for (int j = 0; j < NS; ++j) {
+                const float2 o = smax[t * NS + j];
+                rank += topk_beats(o.x, __float_as_int(o.y), me.x, __float_as_int(me.y)) ? 1 : 0;
+            }
+            if (rank == k - 1) {
+                tau[t] = me;
+                found = true;
+            }
+        }
+        if (!__any_sync(0xffffffffu, found) && lane == 0)   // fewer than k slices: every logit survives
+            tau[t] = make_float2(-INFINITY, __int_as_float(0x7fffffff));
+    }
+    __syncthreads();
+    for (int task = warp; task < T * NS; task += DC_WARPS) {
+        const int t = task / NS, e = 32 * (task - t * NS) + lane;
+        const float key = rowk[t * NSE + e];
+        const float2 tt = tau[t];
+        const bool sv = e < E && !topk_beats(tt.x, __float_as_int(tt.y), key, e);
+        const unsigned b = __ballot_sync(0xffffffffu, sv);
+        int base = 0;
+        if (lane == 0 && b) base = atomicAdd(&scnt[t], __popc(b));
+        base = __shfl_sync(0xffffffffu, base, 0) + __popc(b & ((1u << lane) - 1u));
+        if (sv && base < DC_SURV) surv[t * DC_SURV + base] = make_float2(key, __int_as_float(e));
+    }
+    __syncthreads();
+
+    // (c), then the kept flags and the (asynchronous) fetch of the selected
+    // experts' descriptors; the router weights are needed only by the
+    // combine. Warps >= T meanwhile convert the activations.
+    // warp 0: sorts the (expert, pair) keys of the kept pairs (at most 64: two
+    // per lane; one per lane, in 16 or 32 lanes, for up to 32 pairs), which
+    // yields the active experts in ascending order and each expert's pairs in
+    // ascending pair order; returns the number of active experts
+    auto bucket_sorted = [&]() -> int { return dc_bucket_sorted(P, keep, ids, plist, act, aoff, misc); };
+    auto route_weights = [&](int t) { dc_route_weights(t, k, NS, A.renorm, selk, smax, sls, wts); };
+    // the chunk table (warp 0): see below
+    auto build_chunks = [&](int n_act) { dc_build_chunks(n_act, I, H, c, G, A.rows_a, A.rows_b, A.chunk_cap, chunk, misc); };
+    // one thread (lane ci % 16 of warp 0) issues the bulk copies of chunk ci
+    // into ring slot ci % 16
+    auto issue_chunk = [&](int ci, int nchunks_a, int b0) {
+        dc_issue_chunk(ci, nchunks_a, b0, ring, A.stage, chunk, dpair, plist, aoff, full, misc);
+    };
+
+    if (warp < T) {
+        const int t = warp;
+        const int M = scnt[t];
+        if (M <= DC_SURV) {
+            for (int m = lane; m < M; m += 32) {
+                const float2 me = surv[t * DC_SURV + m];
+                const int mi = __float_as_int(me.y);
+                int rank = 0;
+#pragma unroll 4
+                for (int o = 0; o < M; ++o) {
+                    const float2 ot = surv[t * DC_SURV + o];
+                    rank += topk_beats(ot.x, __float_as_int(ot.y), me.x, mi) ? 1 : 0;
+                }
+                if (rank < k) {
+                    ids[t * k + rank] = mi;
+                    selk[t * k + rank] = me.x;
+                }
+            }
+        } else {
+            const float2 tt = tau[t];
+            for (int e = lane; e < E; e += 32) {
+                const float key = rowk[t * NSE + e];
+                if (topk_beats(tt.x, __float_as_int(tt.y), key, e)) continue;
+                int rank = 0;
+                for (int o = 0; o < E; ++o) rank += topk_beats(rowk[t * NSE + o], o, key, e) ? 1 : 0;
+                if (rank < k) {
+                    ids[t * k + rank] = e;
+                    selk[t * k + rank] = key;
+                }
             }
         }
         __syncwarp();
-        const float m = selk[t * k];                     // the row's largest logit (or -inf)
-        const bool any_finite = m > -INFINITY;
-        const float kj = lane < k ? selk[t * k + lane] : -INFINITY;
-        const float ex = (lane < k && any_finite && kj > -INFINITY) ? expf(kj - m) : 0.0f;
-        float denom;
-        if (A.renorm) {
-            denom = warp_sum(ex);
-        } else {
-            float s = 0.0f;
-            for (int w = lane; w < NS; w += 32) {
-                const float mw = slm[t * NS + w];
-                if (any_finite && mw > -INFINITY) s += sls[t * NS + w] * expf(mw - m);
-            }
-            denom = warp_sum(s);
-        }
         if (lane < k) {
             const int p = t * k + lane;
-            wts[p] = denom > 0.0f ? ex / denom : 0.0f;
             const int e = ids[p];
             bool kp = e >= A.lo && e < A.hi;
             if (kp && A.fmt_mask != 0xffffffffu) kp = (A.fmt_mask >> A.table[e].gate.fmt) & 1u;
@@ -520,188 +721,134 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             }
             cp_async_commit();
         }
+        if (T > 1) {
+            route_weights(t);
+            cp_async_wait_all();   // descriptors: warp 0 issues copies after the next barrier
+        }
     } else {
-        // activations -> fp16 (per-token power-of-two scale), ordered as the
-        // Q4_K decoder pairs codes with, stored [v][group] for conflict-free reads
-        for (int task = tid - 32 * T; task < T * H64; task += DC_THREADS - 32 * T) {
-            const int t = task / H64, G64 = task - t * H64;
+        // activations -> int16 (per-token power-of-two scale: max |x| in
+        // [2^14, 2^15)), in the order the Q4_K dot pairs codes with, stored
+        // [v][group] for conflict-free reads. Four lanes per 64-column group:
+        // lane q takes columns 8q..8q+7 and 32+8q..32+8q+7 (output words 2q
+        // and 2q+1); the group's two exact activation sums are combined over
+        // the four lanes.
+        const int ntask = 4 * T * H64;
+        for (int base = (warp - T) * 32; base < ntask; base += (DC_WARPS - T) * 32) {
+            const int task = base + lane;
+            const bool ok = task < ntask;
+            const int g = ok ? task >> 2 : 0, q = task & 3;
+            const int t = g / H64, G64 = g - t * H64;
             const int sg = pow2_shift(__uint_as_float(xmax[t]));
             const float up = exp2i(sg);
-            const uint4 *src = reinterpret_cast<const uint4 *>(ring) + (size_t)t * (H / 8) + 8 * G64;
-            float xf[64];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-                const uint4 q = src[v];
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            const uint4 *src = reinterpret_cast<const uint4 *>(xraw) + (size_t)t * (H / 8) + 8 * G64;
+            float xa[8], xb[8];
+            {
+                const uint4 qa = src[q], qb = src[4 + q];
+                const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    xf[8 * v + 2 * i] = __uint_as_float(w[i] << 16) * up;
-                    xf[8 * v + 2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u) * up;
+                    xa[2 * i] = __uint_as_float(wa[i] << 16) * up;
+                    xa[2 * i + 1] = __uint_as_float(wa[i] & 0xffff0000u) * up;
+                    xb[2 * i] = __uint_as_float(wb[i] << 16) * up;
+                    xb[2 * i + 1] = __uint_as_float(wb[i] & 0xffff0000u) * up;
                 }
             }
             uint4 *dst = reinterpret_cast<uint4 *>(xs + (size_t)t * H / 2);
-            float sa = 0.0f, sb = 0.0f;
+            int ia[8], ib[8];
 #pragma unroll
-            for (int mm = 0; mm < 8; ++mm) {
-                const int i = 4 * mm;
-                const uint32_t w0 = pack_half2(xf[i], xf[i + 2]), w1 = pack_half2(xf[32 + i], xf[32 + i + 2]);
-                const uint32_t w2 = pack_half2(xf[i + 1], xf[i + 3]), w3 = pack_half2(xf[32 + i + 1], xf[32 + i + 3]);
-                dst[mm * H64 + G64] = make_uint4(w0, w1, w2, w3);
-                sa += half_lo(w0) + half_hi(w0) + half_lo(w2) + half_hi(w2);
-                sb += half_lo(w1) + half_hi(w1) + half_lo(w3) + half_hi(w3);
+            for (int i = 0; i < 8; ++i) {
+                ia[i] = max(-32767, min(32767, __float2int_rn(xa[i])));
+                ib[i] = max(-32767, min(32767, __float2int_rn(xb[i])));
             }
-            xsum[((size_t)t * H64 + G64) * 2 + 0] = sa;
-            xsum[((size_t)t * H64 + G64) * 2 + 1] = sb;
-            if (G64 == 0) xsc[t] = exp2i(-sg);
+            int sa = 0, sb = 0;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int i = 4 * h2;
+                const uint32_t w0 = ((uint32_t)ia[i] & 0xffffu) | ((uint32_t)ia[i + 1] << 16);
+                const uint32_t w1 = ((uint32_t)ia[i + 2] & 0xffffu) | ((uint32_t)ia[i + 3] << 16);
+                const uint32_t w2 = ((uint32_t)ib[i] & 0xffffu) | ((uint32_t)ib[i + 1] << 16);
+                const uint32_t w3 = ((uint32_t)ib[i + 2] & 0xffffu) | ((uint32_t)ib[i + 3] << 16);
+                if (ok) dst[(2 * q + h2) * H64 + G64] = make_uint4(w0, w1, w2, w3);
+                sa += ia[i] + ia[i + 1] + ia[i + 2] + ia[i + 3];
+                sb += ib[i] + ib[i + 1] + ib[i + 2] + ib[i + 3];
+            }
+            sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+            sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+            if (ok && q == 0) {
+                xsum[((size_t)t * H64 + G64) * 2 + 0] = (float)sa;
+                xsum[((size_t)t * H64 + G64) * 2 + 1] = (float)sb;
+                if (G64 == 0) xsc[t] = exp2i(-sg);
+            }
         }
     }
-    __syncthreads();
 
-    // ---- 3. bucketing: warp 0 sorts the (expert, pair) keys of the kept pairs
-    // (at most 64: two per lane), which yields the active experts in ascending
-    // order and each expert's pairs in ascending pair order
-    if (warp == 0) {
-        constexpr int SENT = 0x7fffffff;
-        int key[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int p = lane + 32 * r;
-            key[r] = (p < P && keep[p]) ? ((ids[p] << 8) | p) : SENT;
-        }
-#pragma unroll
-        for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll
-            for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                if (stride == 32) {
-                    const int lo = min(key[0], key[1]), hi = max(key[0], key[1]);   // size == 64: ascending
-                    key[0] = lo;
-                    key[1] = hi;
-                } else {
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const int i = lane + 32 * r;
-                        const int other = __shfl_xor_sync(0xffffffffu, key[r], stride);
-                        const bool asc = (i & size) == 0;
-                        const bool lower = (lane & stride) == 0;
-                        key[r] = (lower == asc) ? min(key[r], other) : max(key[r], other);
-                    }
-                }
-            }
-        }
-        // element i = lane + 32 r holds key[r]; starts of expert runs
-        const int prev0 = __shfl_up_sync(0xffffffffu, key[0], 1);
-        const int prev1 = __shfl_up_sync(0xffffffffu, key[1], 1);
-        const int last0 = __shfl_sync(0xffffffffu, key[0], 31);
-        const int pk[2] = {lane == 0 ? -1 : prev0, lane == 0 ? last0 : prev1};
-        bool start[2], valid[2];
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            valid[r] = key[r] != SENT;
-            start[r] = valid[r] && (pk[r] < 0 || (pk[r] >> 8) != (key[r] >> 8));
-        }
-        const unsigned s0 = __ballot_sync(0xffffffffu, start[0]), s1 = __ballot_sync(0xffffffffu, start[1]);
-        const unsigned v0 = __ballot_sync(0xffffffffu, valid[0]), v1 = __ballot_sync(0xffffffffu, valid[1]);
-        const int n_kept = __popc(v0) + __popc(v1), n_act = __popc(s0) + __popc(s1);
-        const unsigned below = (1u << lane) - 1u;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int i = lane + 32 * r;
-            if (valid[r]) plist[i] = key[r] & 0xff;
-            if (start[r]) {
-                const int a = r == 0 ? __popc(s0 & below) : __popc(s0) + __popc(s1 & below);
-                act[a] = key[r] >> 8;
-                aoff[a] = i;
-            }
+    // ---- 3. bucketing, then the chunk table, both by warp 0.
+    // One token: its selected experts are distinct, so the active experts are
+    // taken in rank order, one pair each, without a sort (the published
+    // routing is sorted at the end); warp 0 then issues the copies of the
+    // ring slots that the raw activations do not occupy, and computes the
+    // router weights while they are in flight.
+    if (T == 1 && warp == 0) {
+        cp_async_wait_all();
+        __syncwarp();
+        const bool kp = lane < k && keep[lane];
+        const unsigned b = __ballot_sync(0xffffffffu, kp);
+        const int n_act = __popc(b);
+        if (kp) {
+            const int a = __popc(b & ((1u << lane) - 1u));
+            act[a] = ids[lane];
+            aoff[a] = a;
+            plist[a] = lane;
         }
         if (lane == 0) {
-            aoff[n_act] = n_kept;
+            aoff[n_act] = n_act;
             misc[0] = n_act;
-            misc[6] = n_kept;
+            misc[6] = n_act;
         }
+        __syncwarp();
+        build_chunks(n_act);
+        __syncwarp();
+        {
+            const int na = misc[4], nc = misc[5];
+            const int b0 = (int)((unsigned)H * c / G);
+            const int n0 = min(nc, DC_NSTAGE - nraw);
+            if (lane < n0) issue_chunk(lane, na, b0);   // lane j: chunk j, ring slot j
+            if (lane == 0) misc[7] = n0;
+        }
+        route_weights(0);
     }
     __syncthreads();
-    const int n_act = misc[0];
-    // this CTA's share: gate/up row pairs [a_begin, a_end) over (active expert, row)
-    const int NA = n_act * I;
-    const int a_begin = (int)((unsigned)NA * c / G), a_end = (int)((unsigned)NA * (c + 1) / G);
-    const int b0 = (int)((unsigned)H * c / G), b1 = (int)((unsigned)H * (c + 1) / G);
-    const int nrows_b = b1 - b0;
-    if (warp == 0) {
-        // the chunk table: gate/up chunks of at most rows_a row pairs, never
-        // crossing an expert (lane j: the j-th expert segment of the share);
-        // then, per active expert, the CTA's down rows in chunks of rows_b
-        const int a_first = a_begin / I, a_last = a_end > a_begin ? (a_end - 1) / I : a_first - 1;
-        int total = 0;
-        for (int seg0 = a_first; seg0 <= a_last; seg0 += 32) {
-            const int a = seg0 + lane;
-            int len = 0, rs = 0;
-            if (a <= a_last) {
-                rs = max(a_begin, a * I);
-                len = min(a_end, (a + 1) * I) - rs;
-            }
-            const int nch = (len + A.rows_a - 1) / A.rows_a;
-            int inc = nch;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += v;
-            }
-            int n = total + inc - nch;
-            for (int j = 0; j < nch && n < A.chunk_cap; ++j, ++n) {
-                const int r = rs + j * A.rows_a;
-                chunk[n] = make_int4(a, r - a * I, min(A.rows_a, rs + len - r), 0);
-            }
-            total += __shfl_sync(0xffffffffu, inc, 31);
-        }
-        const int nb = (nrows_b + A.rows_b - 1) / A.rows_b;
-        for (int i = lane; i < n_act * nb; i += 32) {
-            const int a = i / nb, j = i - a * nb;
-            if (total + i < A.chunk_cap) chunk[total + i] = make_int4(a, j * A.rows_b, min(A.rows_b, nrows_b - j * A.rows_b), 1);
-        }
-        if (lane == 0) {
-            misc[4] = min(total, A.chunk_cap);
-            misc[5] = min(total + n_act * nb, A.chunk_cap);
-        }
+    // Several tokens: the sorted bucketing, then the chunk table.
+    if (T > 1 && warp == 0) {
+        const int n_act = bucket_sorted();
+        build_chunks(n_act);
+        __syncwarp();
+        const int n0 = min(misc[5], DC_NSTAGE - nraw);
+        if (lane < n0) issue_chunk(lane, misc[4], (int)((unsigned)H * c / G));
+        if (lane == 0) misc[7] = n0;
     }
     cp_async_wait_all();
     __syncthreads();
     const int nchunks_a = misc[4], nchunks = misc[5];
+    const int b0 = (int)((unsigned)H * c / G), b1 = (int)((unsigned)H * (c + 1) / G);
+    const int nrows_b = b1 - b0;
     // the next kernel in the stream may begin its launch; it waits for this
     // grid's completion before reading anything this grid writes
     asm volatile("griddepcontrol.launch_dependents;");
 
-    if (warp == DC_CW) {
-        // ---------------- producer: one thread streams the CTA's rows
-        if (lane == 0) {
-            for (int ci = 0; ci < nchunks; ++ci) {
-                const int s = ci % DC_NSTAGE;
-                if (ci >= DC_NSTAGE && !mbar_wait(&empty[s], (uint32_t)((ci / DC_NSTAGE) - 1) & 1u)) {
-                    set_abort(misc, A.status);
-                    break;
-                }
-                uint8_t *dst = ring + (size_t)s * A.stage;
-                const int4 ch = chunk[ci];
-                const DevExpert &X = dpair[plist[aoff[ch.x]]];
-                if (ci < nchunks_a) {
-                    const uint32_t bg = (uint32_t)(ch.z * X.gate.stride), bu = (uint32_t)(ch.z * X.up.stride);
-                    mbar_expect_tx(&full[s], bg + bu);
-                    bulk_g2s(dst, X.gate.data + (size_t)ch.y * X.gate.stride, bg, &full[s]);
-                    bulk_g2s(dst + bg, X.up.data + (size_t)ch.y * X.up.stride, bu, &full[s]);
-                } else {
-                    const uint32_t bd = (uint32_t)(ch.z * X.down.stride);
-                    mbar_expect_tx(&full[s], bd);
-                    bulk_g2s(dst, X.down.data + (size_t)(b0 + ch.y) * X.down.stride, bd, &full[s]);
-                }
-                *reinterpret_cast<volatile int *>(&misc[3]) = ci + 1;   // chunks issued
-            }
-        }
-        return;
+    // the ring slots that held the raw activations are free now
+    if (warp == 0) {
+        const int n_early = misc[7];
+        if (lane >= n_early && lane < min(nchunks, DC_NSTAGE)) issue_chunk(lane, nchunks_a, b0);
     }
 
-    // ---------------- consumers, in rounds of up to 16 chunks (the ring): the
-    // round's work items are spread over all 16 warps; a consumer barrier ends
-    // the round and then its slots are released, so no warp ever waits on a
-    // slot more than one phase ahead.
+    // ---------------- the warps consume in rounds of up to 16 chunks (the
+    // ring): a round's work items are spread over all 16 warps; a barrier ends
+    // the round, and then lane s of warp 0 refills the slots the round used
+    // (chunk ci + 16 after chunk ci), so no wait is ever more than one phase
+    // ahead.
     // T = 1: every gate/up row meets the same activations; keep them in registers
     uint32_t xv1[32];
     float XA1 = 0.0f, XB1 = 0.0f;
@@ -719,58 +866,68 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         XA1 = xsum[lane * 2 + 0];
         XB1 = xsum[lane * 2 + 1];
     }
-    for (int cr = 0; cr < nchunks_a; cr += DC_NSTAGE) {
-        const int cend = min(cr + DC_NSTAGE, nchunks_a);
-        for (int f = cr * A.rows_a + warp; f < cend * A.rows_a; f += DC_CW) {
-            const int ci = f / A.rows_a, row = f - ci * A.rows_a;
-            const int4 ch = chunk[ci];
-            const int n = ch.z, r0 = ch.y;
-            if (row >= n) continue;
-            const int s = ci % DC_NSTAGE;
-            if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
-                if (lane == 0) set_abort(misc, A.status);
-                break;
-            }
-            const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
-            const DevExpert &X = dpair[plist[q0]];
-            const uint8_t *stage = ring + (size_t)s * A.stage;
-            const uint8_t *grow = stage + row * (int)X.gate.stride;
-            const uint8_t *urow = stage + n * (int)X.gate.stride + row * (int)X.up.stride;
-            for (int qi = 0; qi < ne; ++qi) {
-                const int p = plist[q0 + qi], t = p / k;
-                float part[2] = {0.0f, 0.0f};
-                if (x_hoist) {
-                    if (lane < H64) {
-                        part[0] = q4k_dot64(grow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
-                        part[1] = q4k_dot64(urow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
-                    }
-                } else {
-                    const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs + (size_t)t * H / 2);
-                    for (int G64 = lane; G64 < H64; G64 += 32) {
-                        uint32_t xv[32];
-#pragma unroll
-                        for (int v = 0; v < 8; ++v) {
-                            const uint4 q = xv4[v * H64 + G64];
-                            xv[4 * v + 0] = q.x;
-                            xv[4 * v + 1] = q.y;
-                            xv[4 * v + 2] = q.z;
-                            xv[4 * v + 3] = q.w;
-                        }
-                        const float XA = xsum[((size_t)t * H64 + G64) * 2 + 0];
-                        const float XB = xsum[((size_t)t * H64 + G64) * 2 + 1];
-                        part[0] += q4k_dot64(grow + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
-                        part[1] += q4k_dot64(urow + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
-                    }
+    // the gate/up rounds, compiled once with the activations hoisted into
+    // registers (one token) and once general, so that the loop that runs is
+    // compact in the instruction cache
+    const int ra_log = 31 - __clz(A.rows_a);   // rows_a is a power of two
+    auto phase_a = [&](auto hoist) {
+        constexpr bool HOIST = decltype(hoist)::value;
+        for (int cr = 0; cr < nchunks_a; cr += DC_NSTAGE) {
+            const int cend = min(cr + DC_NSTAGE, nchunks_a);
+            for (int f = cr * A.rows_a + warp; f < cend * A.rows_a; f += DC_CW) {
+                const int ci = f >> ra_log, row = f & (A.rows_a - 1);
+                const int4 ch = chunk[ci];
+                const int n = ch.z, r0 = ch.y;
+                if (row >= n) continue;
+                const int s = ci % DC_NSTAGE;
+                if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+                    if (lane == 0) set_abort(misc, A.status);
+                    break;
                 }
-                // gate total in lanes 0..15, up total in lanes 16..31
-                const float tot = warp_reduce2(part) * xsc[t];
-                const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
-                if (lane == 0) A.h[(size_t)p * I + r0 + row] = silu_f32(tot) * upv;
+                const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
+                const DevExpert &X = dpair[plist[q0]];
+                const uint8_t *stage = ring + (size_t)s * A.stage;
+                const uint8_t *grow = stage + row * (int)X.gate.stride;
+                const uint8_t *urow = stage + n * (int)X.gate.stride + row * (int)X.up.stride;
+                for (int qi = 0; qi < ne; ++qi) {
+                    const int p = plist[q0 + qi], t = HOIST ? 0 : p / k;
+                    float part[2] = {0.0f, 0.0f};
+                    if constexpr (HOIST) {
+                        if (lane < H64) {
+                            part[0] = q4k_dot64(grow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
+                            part[1] = q4k_dot64(urow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
+                        }
+                    } else {
+                        const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs + (size_t)t * H / 2);
+                        for (int G64 = lane; G64 < H64; G64 += 32) {
+                            uint32_t xv[32];
+    #pragma unroll
+                            for (int v = 0; v < 8; ++v) {
+                                const uint4 q = xv4[v * H64 + G64];
+                                xv[4 * v + 0] = q.x;
+                                xv[4 * v + 1] = q.y;
+                                xv[4 * v + 2] = q.z;
+                                xv[4 * v + 3] = q.w;
+                            }
+                            const float XA = xsum[((size_t)t * H64 + G64) * 2 + 0];
+                            const float XB = xsum[((size_t)t * H64 + G64) * 2 + 1];
+                            part[0] += q4k_dot64(grow + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
+                            part[1] += q4k_dot64(urow + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
+                        }
+                    }
+                    // gate total in lanes 0..15, up total in lanes 16..31
+                    const float tot = warp_reduce2(part) * xsc[t];
+                    const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
+                    if (lane == 0) A.h[(size_t)p * I + r0 + row] = silu_f32(tot) * upv;
+                }
             }
+            consumer_sync();
+            if (warp == 0 && lane < cend - cr && cr + lane + DC_NSTAGE < nchunks &&
+                !*reinterpret_cast<volatile int *>(&misc[1]))
+                issue_chunk(cr + lane + DC_NSTAGE, nchunks_a, b0);
         }
-        consumer_sync();
-        if (tid < cend - cr) mbar_arrive(&empty[(cr + tid) % DC_NSTAGE]);
-    }
+    };
+    if (x_hoist) phase_a(std::true_type{}); else phase_a(std::false_type{});
 
     // ---- grid barrier: every CTA's h and |h| maxima are complete and visible
     consumer_sync();
@@ -778,6 +935,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         // the consumer barrier orders every warp's h stores before this
         // release; the other CTAs' acquire of the counter then sees them
         red_release_add(barrier, 1ull);
+        const unsigned long long gen = gen_count / (unsigned long long)G;
         const unsigned long long target = (gen + 1ull) * (unsigned long long)G;
         uint32_t it = 0;
         while (ld_acquire_u64(barrier) < target) {
@@ -798,13 +956,24 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         // every kept pair's h -> shared memory, coalesced (16-byte loads by
         // consecutive threads), at a 36-float block pitch so that the 16-byte
         // reads of one block per lane below are free of bank conflicts
+        // (four loads in flight per thread: one L2 round trip for typical sizes)
         const int n4 = I / 4;
-        for (int f = tid; f < P * n4; f += DC_CW * 32) {
-            const int p = f / n4, i4 = f - p * n4;
-            if (!keep[p]) continue;
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(A.h + (size_t)p * I) + i4);
-            const int i = 4 * i4;
-            *reinterpret_cast<float4 *>(hsm + ((size_t)p * (I / 32) + (i >> 5)) * 36 + (i & 31)) = v;
+        constexpr int NB = 4;
+        for (int f0 = tid; f0 < P * n4; f0 += NB * DC_CW * 32) {
+            float4 v[NB];
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int f = f0 + u * DC_CW * 32;
+                const int p = f / n4;
+                if (f < P * n4 && keep[p]) v[u] = __ldcg(reinterpret_cast<const float4 *>(A.h + (size_t)p * I) + (f - p * n4));
+            }
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int f = f0 + u * DC_CW * 32;
+                const int p = f / n4, i = 4 * (f - p * n4);
+                if (f < P * n4 && keep[p])
+                    *reinterpret_cast<float4 *>(hsm + ((size_t)p * (I / 32) + (i >> 5)) * 36 + (i & 31)) = v[u];
+            }
         }
         consumer_sync();
     }
@@ -869,7 +1038,9 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 }
             }
             consumer_sync();
-            if (tid < cend - cr) mbar_arrive(&empty[(cr + tid) % DC_NSTAGE]);
+            if (warp == 0 && lane < cend - cr && cr + lane + DC_NSTAGE < nchunks &&
+                !*reinterpret_cast<volatile int *>(&misc[1]))
+                issue_chunk(cr + lane + DC_NSTAGE, nchunks_a, b0);
         }
     }
     consumer_sync();
@@ -889,8 +1060,14 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         A.out[(size_t)t * H + b0 + rr] = acc;
     }
 
-    // CTA 0 publishes the routing results to the workspace
+    // CTA 0 publishes the routing results to the workspace (for one token the
+    // bucketing, used in rank order so far, is sorted first)
     if (c == 0) {
+        if (T == 1) {
+            if (warp == 0) bucket_sorted();
+            consumer_sync();
+        }
+        const int n_act = misc[0];
         const int n_kept = misc[6];
         for (int p = tid; p < P; p += DC_CW * 32) {
             A.ids_out[p] = ids[p];
@@ -943,7 +1120,8 @@ DcPlan decode_fused_plan(int T, int k, int E, int H, int I, int G, int64_t gu_st
     const int64_t rowpair = 2 * gu_stride;
     const int rb = (H + G - 1) / G;
     for (int stage = DC_STAGE_MAX; stage >= 2048; stage -= 512) {
-        const int rows_a = (int)std::min<int64_t>(DC_ROWS_A, stage / rowpair);
+        int rows_a = (int)std::min<int64_t>(DC_ROWS_A, stage / rowpair);
+        while (rows_a & (rows_a - 1)) --rows_a;   // a power of two: items split by shifts
         const int rows_b = (int)std::min<int64_t>(rb, stage / dn_stride);
         if (rows_a < 1 || rows_b < 1) return pl;
         const int P = T * k;

@@ -300,6 +300,30 @@ def test_fused_decode_filters_and_reproducible(M):
     assert ws.read_status() & M.FLAG_NONFINITE_LOGIT
 
 
+@pytest.mark.parametrize("mode", ["halves", "equal", "two_values"])
+def test_fused_decode_tied_logits(M, mode):
+    """Tied router logits: the lower expert index wins, as in the oracle.
+    Coarse logits leave few candidates per slice; all-equal logits leave
+    every candidate (the counting-rank path of the kernel's top-k)."""
+    cfg = synth.LayerConfig("tie", 96, 8, 256, 64, 3, "q4k", True, 31)
+    L = synth.make_layer(cfg, 0)
+    if mode == "halves":
+        L.logits = (np.round(L.logits * 2) / 2).astype(np.float32)
+    elif mode == "equal":
+        L.logits = np.full_like(L.logits, 0.25)
+    else:
+        L.logits = np.where(L.logits > 0.5, 1.0, -1.0).astype(np.float32)
+    out, table, ws = run_path(M, L, M.PATH_FUSED)
+    ref = offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k)
+    assert_parity(out, ref, f"fused tied logits ({mode})")
+    from oracle import router as orouter
+    rid, rw, _ = orouter.route_topk(L.logits, cfg.k)
+    R = ws.routing()
+    np.testing.assert_array_equal(R["ids"].cpu().numpy(), rid)
+    np.testing.assert_allclose(R["weights"].cpu().numpy(), rw, rtol=4e-6, atol=0)
+    assert ws.read_status() == 0
+
+
 def test_fused_path_rejects_ineligible(M):
     L = synth.make_layer(small_cfg(tiers="mixed", T=3, seed=5), 0)
     experts, x, logits = host_layer_to_device(L)
