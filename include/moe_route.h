@@ -220,8 +220,8 @@ size_t moe_ffn_workspace_size_for_path(const moe_weight_table *W, int32_t T, int
  * requested path cannot run this layer. Host-only. */
 int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_options *opt);
 
-/* Zero a workspace's status word and grid-barrier counter (once, before its
- * first forward).
+/* Zero a workspace (all ws_bytes, among them the status word and the fused
+ * kernel's grid-barrier counter) once, before its first forward.
  * ws: device, at least moe_ffn_workspace_size bytes. */
 int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 

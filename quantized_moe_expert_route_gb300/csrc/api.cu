@@ -251,7 +251,7 @@ size_t moe_ffn_workspace_size_for_path(const moe_weight_table *W, int32_t T, int
 
 int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
     if (!ws || ws_bytes < SYNC_BYTES) return MOE_ERR_INVALID_ARG;
-    cudaError_t err = cudaMemsetAsync(ws, 0, SYNC_BYTES, stream);
+    cudaError_t err = cudaMemsetAsync(ws, 0, ws_bytes, stream);
     return err == cudaSuccess ? MOE_OK : cuda_fail(err);
 }
 

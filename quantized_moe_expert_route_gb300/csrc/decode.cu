@@ -23,7 +23,7 @@
 //      16 warps have finished a round of chunks. The warps decode the stages
 //      and write h = silu(W_gate x) * (W_up x) (fp32) to global memory.
 //   3. A bounded grid barrier (cooperative launch: all CTAs co-resident)
-//      separates gate/up from down.
+//      separates gate/up from down; then each CTA reads every pair's h.
 //   4. Each CTA owns a slice of output rows for every routed expert, so the
 //      router-weighted combine runs in-CTA in ascending slot order.
 //
@@ -51,11 +51,11 @@ constexpr int DC_MAX_PAIRS = 64;                 // T * k
 constexpr int DC_ROWS_A = 4;                     // max gate/up row pairs per chunk
 constexpr int DC_SURV = 64;                      // top-k survivors ranked from the short list
 
-constexpr size_t DC_HSM_MAX = 48 * 1024;          // largest h staged in shared memory, bytes
-__host__ __device__ inline bool dc_stage_h(int P, int I) { return (size_t)P * I * 4 <= DC_HSM_MAX; }
+constexpr unsigned long long DC_WAIT_NS = 2000000000ull;   // bound of the wait for other CTAs' h
+constexpr int DC_HQW = 20;                       // words per staged h block: 16 int16 pairs, the scale, pad
 
 struct DcLayout {
-    size_t ring, xs, xsum, xsc, xmax, hsm, ybuf, rowk, smax, surv, scnt, tau, ss, selk, ids, wts, keep, act, aoff,
+    size_t ring, xs, xsum, xsc, xmax, hq, ybuf, rowk, smax, surv, scnt, tau, ss, selk, ids, wts, keep, act, aoff,
         plist,
         dpair, chunks, full, misc, total;
     int rb, ns;
@@ -77,10 +77,10 @@ __host__ __device__ inline DcLayout dc_layout(int T, int k, int E, int H, int I,
     L.xsum = take((size_t)T * (H / 64) * 2 * 4);
     L.xsc = take((size_t)T * 4);
     L.xmax = take((size_t)T * 4);
-    // h of every pair staged in shared memory after the barrier (32-column
-    // blocks at a 36-float pitch) when it is small; else read from L2 per lane
-    L.hsm = take(dc_stage_h(T * k, I) ? (size_t)T * k * (I / 32) * 36 * 4 : 0);
-    L.ybuf = take((size_t)P * L.rb * 4);
+    // h of every pair, staged after gate/up as int16 with one power-of-two
+    // scale per 32-column block; the down outputs per K part (8 blocks)
+    L.hq = take((size_t)P * (I / 32) * DC_HQW * 4);
+    L.ybuf = take((size_t)((I / 32 + 7) / 8) * P * L.rb * 4);
     L.rowk = take((size_t)T * L.ns * 32 * 4);
     L.smax = take((size_t)T * L.ns * 8);
     L.surv = take((size_t)T * DC_SURV * 8);
@@ -112,7 +112,7 @@ struct DcArgs {
     float *h;                       // [T*k][I] fp32, pair p = t*k + j
     int32_t *ids_out, *offsets_out, *active_out, *pairs_out, *pos_out;
     float *wts_out;
-    unsigned char *sync;            // zero-initialised sync region: barrier counter, |h| maxima
+    unsigned char *sync;            // workspace state: the launch counter at offset 8
     uint32_t *status;
     int stage;                      // bytes per ring slot
     int rows_a, rows_b;             // gate/up row pairs per chunk, down rows per chunk
@@ -124,18 +124,6 @@ struct DcArgs {
 
 __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xffff))); }
 __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
-
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
-    unsigned long long v;
-    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-    return v;
-}
 
 __device__ __forceinline__ void consumer_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(DC_CW * 32) : "memory");
@@ -181,8 +169,24 @@ __device__ __forceinline__ void cp_async8(void *dst, const void *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-__device__ __forceinline__ void red_release_add(unsigned long long *p, unsigned long long v) {
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_add_u64(unsigned long long *p, unsigned long long v) {
     asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
 }
 
 
@@ -252,54 +256,54 @@ __device__ __forceinline__ float q4k_dot64(const uint8_t *blk, int g, const uint
 }
 
 
-// On an abort, thread 0 waits (bounded) for the bulk copies the producer
-// issued into stages nobody will consume, so none lands after the CTA exits.
-// (Each slot's latest issue completes after the slot's earlier ones.)
-// 32 activations of one block -> int16 pairs scaled by 2^sigma (block max
-// |v| * 2^sigma in [2^13, 2^14), so no value can round past 2^15) and the
-// inverse scale; exponent arithmetic on the float bits (no library calls). A
-// block with a non-finite value gets a NaN inverse scale.
-__device__ __forceinline__ float quant_i16x32(const float v[32], uint32_t q[16]) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
-    const int be = (int)((__float_as_uint(m) >> 23) & 0xffu);   // biased exponent: m in [2^(be-127), 2^(be-126))
-    if (be == 255) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = 0u;
-        return __int_as_float(0x7fc00000);
-    }
-    // m * 2^sg in [2^13, 2^14): sg = 140 - be, kept where both scales are normal
-    const int sg = m > 0.0f ? max(-100, min(100, 140 - be)) : 0;
-    const float up = __uint_as_float((uint32_t)(127 + sg) << 23);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int lo = __float2int_rn(v[2 * i] * up), hi = __float2int_rn(v[2 * i + 1] * up);
-        q[i] = ((uint32_t)lo & 0xffffu) | ((uint32_t)hi << 16);
-    }
-    return __uint_as_float((uint32_t)(127 - sg) << 23);
+// One lane's down-projection partial over up to 8 consecutive Q8_0 blocks
+// (one 272-byte period of a row: 8 x 34 bytes = 17 x 16 bytes, so that it
+// starts and ends 16-byte aligned) against staged int16 h. Block b's scale is
+// half-word 17 b of the period and its code pairs are half-words 17 b + 1 ...
+// 17 b + 16: the codes enter dp2a undecoded, taking the low or high half of
+// each word as the half-word's parity says (all offsets are compile-time
+// constants). hb: DC_HQW words per block, 16 int16 pairs then the fp32
+// scale 2^-sigma. Returns sum_b d_b * 2^-sigma_b * sum_i q_bi h_bi.
+__device__ __forceinline__ uint32_t u4_word(const uint4 &v, int c) {
+    return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
 }
-
-// Q8_0 block (fp16 scale, then 32 int8 codes; any 2-byte alignment) dotted
-// with 32 int16 activations: exact int32 products and sums (two per dp2a).
-__device__ __forceinline__ float q8_0_dot32_i16(const uint8_t *blk, const uint32_t hq[16]) {
-    const float d = half_bits_to_f32(*reinterpret_cast<const uint16_t *>(blk));
-    const uintptr_t qa = reinterpret_cast<uintptr_t>(blk + 2);
-    const uint32_t *w4 = reinterpret_cast<const uint32_t *>(qa & ~(uintptr_t)3);
-    const uint32_t sh = (uint32_t)(qa & 3) * 8;
-    int acc0 = 0, acc1 = 0;
-    uint32_t prev = w4[0];
+__device__ __forceinline__ float q8_0_period_dot(const uint8_t *wrow, const uint32_t *hb, int nb) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(wrow);
+    uint4 Q[17];
+    float acc = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t next = w4[j + 1];
-        const uint32_t w = __funnelshift_r(prev, next, sh);   // codes 4j .. 4j+3
-        prev = next;
-        asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(acc0) : "r"(hq[2 * j]), "r"(w));
-        asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(acc1) : "r"(hq[2 * j + 1]), "r"(w));
+    for (int b = 0; b < 8; ++b) {
+        if (b >= nb) break;
+        const int khi = ((17 * b + 16) >> 1) >> 2;
+        const int kfirst = b == 0 ? 0 : (((17 * (b - 1) + 16) >> 1) >> 2) + 1;
+#pragma unroll
+        for (int kk = kfirst; kk <= khi; ++kk) Q[kk] = src[kk];
+        const uint4 *h4 = reinterpret_cast<const uint4 *>(hb + b * DC_HQW);
+        uint32_t hv[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 q = h4[v];
+            hv[4 * v] = q.x;
+            hv[4 * v + 1] = q.y;
+            hv[4 * v + 2] = q.z;
+            hv[4 * v + 3] = q.w;
+        }
+        const float hinv = __uint_as_float(hb[b * DC_HQW + 16]);
+        const int wd = (17 * b) >> 1;
+        const uint32_t dw = u4_word(Q[wd >> 2], wd & 3);
+        const float d = half_bits_to_f32((uint16_t)((b & 1) ? (dw >> 16) : (dw & 0xffffu)));
+        int s0 = 0, s1 = 0;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const int hw = 17 * b + 1 + m, w = hw >> 1;
+            const uint32_t word = u4_word(Q[w >> 2], w & 3);
+            int &sm = (m & 1) ? s1 : s0;
+            sm = (hw & 1) ? dp2a_hi(hv[m], word, sm) : dp2a_lo(hv[m], word, sm);
+        }
+        acc = fmaf((float)(s0 + s1), d * hinv, acc);
     }
-    return d * (float)(acc0 + acc1);
+    return acc;
 }
-
 
 // Before an aborting CTA exits (after a CTA barrier, so no copy is issued
 // any more): wait (bounded) for the bulk copy last issued into each ring
@@ -509,8 +513,8 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     float *xsum = reinterpret_cast<float *>(smem + L.xsum);       // [T][H/64][2]
     float *xsc = reinterpret_cast<float *>(smem + L.xsc);
     unsigned *xmax = reinterpret_cast<unsigned *>(smem + L.xmax);
-    float *ybuf = reinterpret_cast<float *>(smem + L.ybuf);       // [P][rb]
-    float *hsm = reinterpret_cast<float *>(smem + L.hsm);         // [P][I/32][36] when staged
+    float *ybuf = reinterpret_cast<float *>(smem + L.ybuf);       // [K parts][P][rb] partial down outputs
+    uint32_t *hq = reinterpret_cast<uint32_t *>(smem + L.hq);     // [P][I/32][DC_HQW] h as int16 + scale
     float *rowk = reinterpret_cast<float *>(smem + L.rowk);       // [T][NS*32] logits (-inf if not finite)
     float2 *smax = reinterpret_cast<float2 *>(smem + L.smax);     // [T][NS] slice best (key, index bits)
     float2 *surv = reinterpret_cast<float2 *>(smem + L.surv);     // [T][DC_SURV] survivors (key, index bits)
@@ -531,7 +535,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     // before the ring's raw-activation slots are free [16 + s] the last chunk issued into
     // ring slot s (-1: none)
     int *misc = reinterpret_cast<int *>(smem + L.misc);
-    unsigned long long *barrier = reinterpret_cast<unsigned long long *>(A.sync + 8);
+    unsigned long long *barrier_ctr = reinterpret_cast<unsigned long long *>(A.sync + 8);
 
     // The layer's inputs may come from the previous kernel in the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -547,13 +551,14 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         scnt[t] = 0;
     }
     __syncthreads();
-    // barrier count before this launch's arrivals: fewer than G of them can
-    // precede this read, so count / G is this launch's generation. A relaxed
-    // load issued beside the logit and activation loads, so that its latency
-    // overlaps theirs (the next CTA barrier waits for all of them); first
-    // used at the grid barrier.
+    // the grid barrier's count before this launch's arrivals: each CTA
+    // arrives once, after its prologue, so fewer than G of this launch's
+    // arrivals can precede this read (a launch starts after the previous one
+    // completes) and count / G is the launch's generation. Loaded beside the
+    // logit and activation loads, so that the latencies overlap.
+    // Read (and later used) by the thread that arrives at the barrier only.
     unsigned long long gen_count = 0;
-    if (tid == 0) gen_count = ld_relaxed_u64(barrier);
+    if (tid == 32 * (DC_CW - 1)) gen_count = ld_relaxed_u64(barrier_ctr);
 
     // ---- 1. activation maxima (16-byte loads of 8 bf16; the raw rows are kept
     // in the ring's last slots, which are filled last) and, per warp,
@@ -929,17 +934,18 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     };
     if (x_hoist) phase_a(std::true_type{}); else phase_a(std::false_type{});
 
-    // ---- grid barrier: every CTA's h and |h| maxima are complete and visible
+    // ---- grid barrier: every CTA's h is complete and visible. Warp 0 issues
+    // the ring's bulk copies (a thread's fence may wait for its copies in
+    // flight), so warp 15 arrives (a release add: the CTA barrier orders the
+    // other warps' h stores before it) and polls (bounded).
     consumer_sync();
-    if (tid == 0) {
-        // the consumer barrier orders every warp's h stores before this
-        // release; the other CTAs' acquire of the counter then sees them
-        red_release_add(barrier, 1ull);
-        const unsigned long long gen = gen_count / (unsigned long long)G;
-        const unsigned long long target = (gen + 1ull) * (unsigned long long)G;
-        uint32_t it = 0;
-        while (ld_acquire_u64(barrier) < target) {
-            if (++it > WAIT_LIMIT) {
+    if (tid == 32 * (DC_CW - 1)) {
+        red_release_add_u64(barrier_ctr, 1ull);
+        // G arrivals past this launch's generation
+        const unsigned long long target = (gen_count / (unsigned long long)G + 1ull) * (unsigned long long)G;
+        const unsigned long long t_start = globaltimer_ns();
+        while (ld_acquire_u64(barrier_ctr) < target) {
+            if (globaltimer_ns() - t_start > DC_WAIT_NS) {
                 set_abort(misc, A.status);
                 break;
             }
@@ -950,91 +956,87 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         drain_copies(full, misc);
         return;
     }
-
-    const bool hstaged = dc_stage_h(P, I);
-    if (nrows_b > 0 && hstaged) {
-        // every kept pair's h -> shared memory, coalesced (16-byte loads by
-        // consecutive threads), at a 36-float block pitch so that the 16-byte
-        // reads of one block per lane below are free of bank conflicts
-        // (four loads in flight per thread: one L2 round trip for typical sizes)
-        const int n4 = I / 4;
+    // ---- h of every pair -> shared memory as int16 with a power-of-two scale
+    // per 32-column block (max |h| * 2^sigma in [2^13, 2^14)): eight
+    // consecutive threads load one block with coalesced 16-byte loads from L2
+    // (four in flight per thread), share its maximum and write 16 int16
+    // pairs and 2^-sigma.
+    if (nrows_b > 0) {
+        const int n4 = I / 4, tot4 = P * n4;
         constexpr int NB = 4;
-        for (int f0 = tid; f0 < P * n4; f0 += NB * DC_CW * 32) {
+        for (int f0 = tid; f0 - tid < tot4; f0 += NB * DC_THREADS) {
             float4 v[NB];
 #pragma unroll
             for (int u = 0; u < NB; ++u) {
-                const int f = f0 + u * DC_CW * 32;
+                const int f = f0 + u * DC_THREADS;
                 const int p = f / n4;
-                if (f < P * n4 && keep[p]) v[u] = __ldcg(reinterpret_cast<const float4 *>(A.h + (size_t)p * I) + (f - p * n4));
+                v[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                if (f < tot4 && keep[p]) v[u] = __ldcg(reinterpret_cast<const float4 *>(A.h + (size_t)p * I) + (f - p * n4));
             }
 #pragma unroll
             for (int u = 0; u < NB; ++u) {
-                const int f = f0 + u * DC_CW * 32;
-                const int p = f / n4, i = 4 * (f - p * n4);
-                if (f < P * n4 && keep[p])
-                    *reinterpret_cast<float4 *>(hsm + ((size_t)p * (I / 32) + (i >> 5)) * 36 + (i & 31)) = v[u];
+                const int f = f0 + u * DC_THREADS;
+                float m = fmaxf(fmaxf(fabsf(v[u].x), fabsf(v[u].y)), fmaxf(fabsf(v[u].z), fabsf(v[u].w)));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+                if (f >= tot4) continue;
+                const int p = f / n4, i4 = f - p * n4;
+                uint32_t *dst = hq + ((size_t)p * U + (i4 >> 3)) * DC_HQW;
+                const int be = (int)((__float_as_uint(m) >> 23) & 0xffu);   // m in [2^(be-127), 2^(be-126))
+                if (be == 255) {   // inf or nan in the block: it propagates
+                    *reinterpret_cast<uint2 *>(dst + 2 * (i4 & 7)) = make_uint2(0u, 0u);
+                    if ((i4 & 7) == 0) dst[16] = 0x7fc00000u;
+                    continue;
+                }
+                const int sg = m > 0.0f ? max(-100, min(100, 140 - be)) : 0;
+                const float up = __uint_as_float((uint32_t)(127 + sg) << 23);
+                const int q0 = __float2int_rn(v[u].x * up), q1 = __float2int_rn(v[u].y * up);
+                const int q2 = __float2int_rn(v[u].z * up), q3 = __float2int_rn(v[u].w * up);
+                *reinterpret_cast<uint2 *>(dst + 2 * (i4 & 7)) =
+                    make_uint2(((uint32_t)q0 & 0xffffu) | ((uint32_t)q1 << 16), ((uint32_t)q2 & 0xffffu) | ((uint32_t)q3 << 16));
+                if ((i4 & 7) == 0) dst[16] = (uint32_t)(127 - sg) << 23;   // 2^-sigma
             }
         }
-        consumer_sync();
+    }
+    consumer_sync();
+    if (*reinterpret_cast<volatile int *>(&misc[1])) {
+        drain_copies(full, misc);
+        return;
     }
     if (nrows_b > 0) {
         // ---- down: this CTA's output rows [b0, b1) of every routed expert.
-        // Work item = (chunk, pair of rows); each warp takes a contiguous run of
-        // a round's items. Lane u < U owns the u-th 32-column block: its 32 h
-        // values (fp32, written by every CTA before the barrier, read through
-        // L2) become int16 with a per-block power-of-two scale and stay in
-        // registers while the warp's items use the same pair; the Q8_0 codes
-        // then enter dp2a (int16 x int8, exact int32 sums) undecoded.
-        const int bpc = (A.rows_b + 1) / 2;
+        // A unit is (down chunk, group of 16 rows, K part of 8 blocks); each
+        // half-warp takes one, lane r its row r, over every pair of the
+        // chunk's expert. The row's 8 blocks are one aligned 272-byte period
+        // read with 16-byte loads (rows of a half-warp fall in distinct
+        // banks); h is read by broadcast. The partial per K part lands in
+        // ybuf and the combine adds the parts in order.
+        const int KP = (U + 7) >> 3, NGR = (A.rows_b + 15) >> 4, upc = NGR * KP;
+        const int r = lane & 15, hw = lane >> 4;
         for (int cr = nchunks_a; cr < nchunks; cr += DC_NSTAGE) {
             const int cend = min(cr + DC_NSTAGE, nchunks);
-            const int nit = (cend - cr) * bpc;
-            const int f0 = (cr - nchunks_a) * bpc + warp * nit / DC_CW;
-            const int f1 = (cr - nchunks_a) * bpc + (warp + 1) * nit / DC_CW;
-            int hp = -1;
-            uint32_t hq[16];
-            float hinv = 0.0f;
-            for (int f = f0; f < f1; ++f) {
-                const int ci = nchunks_a + f / bpc, rb = 2 * (f % bpc);
+            const int nunits = (cend - cr) * upc;
+            for (int uid = 2 * warp + hw; uid < nunits; uid += 2 * DC_CW) {
+                const int ci = cr + uid / upc, rem = uid - (ci - cr) * upc;
+                const int rg = rem / KP, kp = rem - rg * KP;
                 const int4 ch = chunk[ci];
-                const int nr = ch.z;
-                if (rb >= nr) continue;
+                const int nr = ch.z, row = 16 * rg + r;
+                if (16 * rg >= nr) continue;
                 const int s = ci % DC_NSTAGE;
                 if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
-                    if (lane == 0) set_abort(misc, A.status);
+                    set_abort(misc, A.status);
                     break;
                 }
+                if (row >= nr) continue;
                 const int q0 = aoff[ch.x], ne = aoff[ch.x + 1] - q0;
                 const DevMatrix &D = dpair[plist[q0]].down;
-                const uint8_t *stage = ring + (size_t)s * A.stage;
-                const int sd = (int)D.stride, rbase = ch.y;
+                const uint8_t *wrow = ring + (size_t)s * A.stage + (size_t)row * D.stride + 272 * kp;
+                const int nb = min(8, U - 8 * kp);
                 for (int qi = 0; qi < ne; ++qi) {
                     const int p = plist[q0 + qi];
-                    if (p != hp) {
-                        hp = p;
-                        if (lane < U) {
-                            float hf[32];
-                            const float4 *src = hstaged
-                                ? reinterpret_cast<const float4 *>(hsm + ((size_t)p * U + lane) * 36)
-                                : reinterpret_cast<const float4 *>(A.h + (size_t)p * I + 32 * lane);
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                const float4 q = hstaged ? src[v] : __ldcg(src + v);
-                                hf[4 * v] = q.x;
-                                hf[4 * v + 1] = q.y;
-                                hf[4 * v + 2] = q.z;
-                                hf[4 * v + 3] = q.w;
-                            }
-                            hinv = quant_i16x32(hf, hq);
-                        }
-                    }
-                    float part[2] = {0.0f, 0.0f};
-                    if (lane < U) {
-                        part[0] = q8_0_dot32_i16(stage + (size_t)rb * sd + 34 * lane, hq) * hinv;
-                        if (rb + 1 < nr) part[1] = q8_0_dot32_i16(stage + (size_t)(rb + 1) * sd + 34 * lane, hq) * hinv;
-                    }
-                    const float tot = warp_reduce2(part);   // row rb in lanes 0..15, row rb + 1 in 16..31
-                    if ((lane & 15) == 0 && rb + (lane >> 4) < nr) ybuf[p * L.rb + rbase + rb + (lane >> 4)] = tot;
+                    const float y = q8_0_period_dot(wrow, hq + ((size_t)p * U + 8 * kp) * DC_HQW, nb);
+                    ybuf[(kp * P + p) * L.rb + ch.y + row] = y;
                 }
             }
             consumer_sync();
@@ -1049,8 +1051,19 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         return;
     }
 
-    // ---- combine in ascending slot order
-    for (int i = tid; i < T * nrows_b; i += DC_CW * 32) {
+    // ---- the down outputs: K parts added in order (one thread per output),
+    // then the combine in ascending slot order
+    const int KP = (U + 7) >> 3;
+    if (KP > 1) {
+        for (int i = tid; i < P * nrows_b; i += DC_THREADS) {
+            const int p = i / nrows_b, rr = i - p * nrows_b;
+            float y = ybuf[p * L.rb + rr];
+            for (int kp = 1; kp < KP; ++kp) y += ybuf[(kp * P + p) * L.rb + rr];
+            ybuf[p * L.rb + rr] = y;
+        }
+        consumer_sync();
+    }
+    for (int i = tid; i < T * nrows_b; i += DC_THREADS) {
         const int t = i / nrows_b, rr = i - t * nrows_b;
         float acc = 0.0f;
         for (int j = 0; j < k; ++j) {

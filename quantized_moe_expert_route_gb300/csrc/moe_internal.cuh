@@ -21,9 +21,8 @@ struct DevExpert {
     DevMatrix gate, up, down;
 };
 
-// Bytes at the start of a workspace that must be zero before its first use:
-// the device status word (offset 0), the fused kernel's grid-barrier counter
-// (offset 8) and its per-pair |h| maxima (offset 256).
+// Bytes at the start of a workspace that hold its device state: the status
+// word (offset 0) and the fused kernel's grid-barrier counter (offset 8).
 constexpr size_t SYNC_BYTES = 1024;
 
 // Bucketing of more than BUCKET_MANY pairs runs over ranges of BUCKET_RANGE

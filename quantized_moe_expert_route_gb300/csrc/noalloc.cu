@@ -50,10 +50,10 @@ extern "C" int moe_ffn_forward_noalloc(const moe_weight_table *W, const uint16_t
     if (need > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
     void *scratch = nullptr;
     if (scratch_address(&scratch) != 0) return MOE_ERR_CUDA;
-    // Only the first moe::SYNC_BYTES of the scratch must start at zero (the
-    // status word and the fused kernel's barrier counter and |h| maxima; every
-    // other region is written before it is read). Calls share the array, so
-    // that part is cleared on each call.
-    if (cudaMemsetAsync(scratch, 0, moe::SYNC_BYTES, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // The array starts zeroed (a static device array). Each call clears the
+    // status word (offset 0); the fused kernel's grid-barrier counter (offset
+    // 8) only grows, its generation is count / gridDim. Every other region is
+    // written before it is read.
+    if (cudaMemsetAsync(scratch, 0, 8, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return moe_ffn_forward(W, x, logits, T, k, opt, out, scratch, MOE_NOALLOC_SCRATCH_BYTES, stream);
 }
