@@ -813,14 +813,63 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             misc[6] = n_act;
         }
         __syncwarp();
-        build_chunks(n_act);
-        __syncwarp();
+        // the chunk table (the same chunks as in the general case below), each
+        // lane computing its entries directly; the first ring fill is issued
+        // as the entries are made (lane j: chunk j, ring slot j)
         {
-            const int na = misc[4], nc = misc[5];
-            const int b0 = (int)((unsigned)H * c / G);
+            const int NA = n_act * I;
+            const int a_begin = (int)((unsigned)NA * c / G), a_end = (int)((unsigned)NA * (c + 1) / G);
+            const int b0 = (int)((unsigned)H * c / G), nrows_b = (int)((unsigned)H * (c + 1) / G) - b0;
+            const int a_first = a_begin / I, a_last = a_end > a_begin ? (a_end - 1) / I : a_first - 1;
+            const int ra = A.rows_a, rlog = 31 - __clz(ra);
+            int total_a = 0;
+            for (int a = a_first; a <= a_last; ++a) {
+                const int rs = max(a_begin, a * I), len = min(a_end, (a + 1) * I) - rs;
+                total_a += (len + ra - 1) >> rlog;
+            }
+            const int nb = (nrows_b + A.rows_b - 1) / A.rows_b;
+            const int na = min(total_a, A.chunk_cap), nc = min(total_a + n_act * nb, A.chunk_cap);
             const int n0 = min(nc, DC_NSTAGE - nraw);
-            if (lane < n0) issue_chunk(lane, na, b0);   // lane j: chunk j, ring slot j
-            if (lane == 0) misc[7] = n0;
+            for (int j = lane; j < nc; j += 32) {
+                int4 d;
+                if (j < total_a) {
+                    int jj = j, a = a_first;
+                    for (;; ++a) {
+                        const int rs = max(a_begin, a * I), len = min(a_end, (a + 1) * I) - rs;
+                        const int nch = (len + ra - 1) >> rlog;
+                        if (jj < nch) {
+                            d = make_int4(a, rs - a * I + (jj << rlog), min(ra, len - (jj << rlog)), 0);
+                            break;
+                        }
+                        jj -= nch;
+                    }
+                } else {
+                    const int jd = j - total_a, a = jd / nb, jb = jd - a * nb;
+                    d = make_int4(a, jb * A.rows_b, min(A.rows_b, nrows_b - jb * A.rows_b), 1);
+                }
+                chunk[j] = d;
+                if (j < n0) {
+                    uint64_t *bar = &full[j];
+                    uint8_t *dst = ring + (size_t)j * A.stage;
+                    const DevExpert &X = dpair[plist[aoff[d.x]]];
+                    if (j < na) {
+                        const uint32_t bg = (uint32_t)(d.z * X.gate.stride), bu = (uint32_t)(d.z * X.up.stride);
+                        mbar_expect_tx(bar, bg + bu);
+                        bulk_g2s(dst, X.gate.data + (size_t)d.y * X.gate.stride, bg, bar);
+                        bulk_g2s(dst + bg, X.up.data + (size_t)d.y * X.up.stride, bu, bar);
+                    } else {
+                        const uint32_t bd = (uint32_t)(d.z * X.down.stride);
+                        mbar_expect_tx(bar, bd);
+                        bulk_g2s(dst, X.down.data + (size_t)(b0 + d.y) * X.down.stride, bd, bar);
+                    }
+                    misc[16 + j] = j;
+                }
+            }
+            if (lane == 0) {
+                misc[4] = na;
+                misc[5] = nc;
+                misc[7] = n0;
+            }
         }
         route_weights(0);
     }
@@ -939,6 +988,63 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     // flight), so warp 15 arrives (a release add: the CTA barrier orders the
     // other warps' h stores before it) and polls (bounded).
     consumer_sync();
+    if (c == 0 && warp < DC_CW - 1) {
+        // CTA 0's warps 0..14 publish the routing while warp 15 waits at the
+        // barrier. For one token the bucketing was used in rank order; the
+        // published one is sorted here (into scratch, the rank-order arrays
+        // are still in use).
+        constexpr int SENT = 0x7fffffff;
+        constexpr int PUB = 32 * (DC_CW - 1);
+        int *sexp = reinterpret_cast<int *>(surv);   // sorted active experts (prologue scratch)
+        if (T == 1) {
+            if (warp == 0) {
+                int key = (lane < P && keep[lane]) ? ((ids[lane] << 8) | lane) : SENT;
+                key = P <= 16 ? warp_sort_asc<16>(key) : warp_sort_asc<32>(key);
+                if (P <= 16 && lane >= 16) key = SENT;
+                const bool valid = key != SENT;
+                const int nk = __popc(__ballot_sync(0xffffffffu, valid));
+                if (valid) {
+                    A.pairs_out[lane] = key & 0xff;
+                    A.pos_out[key & 0xff] = lane;
+                    A.active_out[1 + lane] = key >> 8;
+                    sexp[lane] = key >> 8;
+                }
+                if (lane == 0) {
+                    A.active_out[0] = nk;
+                    misc[11] = nk;
+                }
+            }
+            asm volatile("bar.sync 2, %0;" ::"n"(PUB) : "memory");
+            const int nk = misc[11];
+            for (int e = tid; e <= E; e += PUB) {   // pairs of experts below e (one pair per expert)
+                int cnt = 0;
+                for (int i = 0; i < nk; ++i) cnt += sexp[i] < e ? 1 : 0;
+                A.offsets_out[e] = cnt;
+            }
+        } else {
+            const int n_act = misc[0], n_kept = misc[6];
+            for (int e = tid; e <= E; e += PUB) {
+                int lo = 0, hi = n_act;          // first active expert >= e
+                while (lo < hi) {
+                    const int mid = (lo + hi) >> 1;
+                    if (act[mid] < e) lo = mid + 1; else hi = mid;
+                }
+                A.offsets_out[e] = aoff[lo];
+            }
+            for (int a = tid; a < n_act; a += PUB) A.active_out[1 + a] = act[a];
+            if (tid == 0) A.active_out[0] = n_act;
+            for (int q = tid; q < n_kept; q += PUB) {
+                A.pairs_out[q] = plist[q];
+                A.pos_out[plist[q]] = q;
+            }
+        }
+        for (int p = tid; p < P; p += PUB) {
+            A.ids_out[p] = ids[p];
+            A.wts_out[p] = wts[p];
+            if (!keep[p]) A.pos_out[p] = -1;
+        }
+        if (tid == 0 && misc[2]) atomicOr(A.status, (uint32_t)misc[2]);
+    }
     if (tid == 32 * (DC_CW - 1)) {
         red_release_add_u64(barrier_ctr, 1ull);
         // G arrivals past this launch's generation
@@ -1071,37 +1177,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             if (keep[p]) acc = fmaf(wts[p], ybuf[p * L.rb + rr], acc);
         }
         A.out[(size_t)t * H + b0 + rr] = acc;
-    }
-
-    // CTA 0 publishes the routing results to the workspace (for one token the
-    // bucketing, used in rank order so far, is sorted first)
-    if (c == 0) {
-        if (T == 1) {
-            if (warp == 0) bucket_sorted();
-            consumer_sync();
-        }
-        const int n_act = misc[0];
-        const int n_kept = misc[6];
-        for (int p = tid; p < P; p += DC_CW * 32) {
-            A.ids_out[p] = ids[p];
-            A.wts_out[p] = wts[p];
-            if (!keep[p]) A.pos_out[p] = -1;
-        }
-        for (int e = tid; e <= E; e += DC_CW * 32) {
-            int lo = 0, hi = n_act;          // first active expert >= e
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (act[mid] < e) lo = mid + 1; else hi = mid;
-            }
-            A.offsets_out[e] = aoff[lo];
-        }
-        for (int a = tid; a < n_act; a += DC_CW * 32) A.active_out[1 + a] = act[a];
-        if (tid == 0) A.active_out[0] = n_act;
-        for (int q = tid; q < n_kept; q += DC_CW * 32) {
-            A.pairs_out[q] = plist[q];
-            A.pos_out[plist[q]] = q;
-        }
-        if (tid == 0 && misc[2]) atomicOr(A.status, (uint32_t)misc[2]);
     }
 }
 
