@@ -202,21 +202,6 @@ __device__ __forceinline__ float warp_reduce2(const float v[2]) {
 }
 
 
-// Sums of 4 per-lane values over the warp: value j ends in lanes 8j .. 8j+7.
-__device__ __forceinline__ float warp_reduce4(const float a[4]) {
-    const bool b16 = threadIdx.x & 16, b8 = threadIdx.x & 8;
-    const float c0 = (b16 ? a[2] : a[0]) + __shfl_xor_sync(0xffffffffu, b16 ? a[0] : a[2], 16);
-    const float c1 = (b16 ? a[3] : a[1]) + __shfl_xor_sync(0xffffffffu, b16 ? a[1] : a[3], 16);
-    float y = (b8 ? c1 : c0) + __shfl_xor_sync(0xffffffffu, b8 ? c0 : c1, 8);
-    y += __shfl_xor_sync(0xffffffffu, y, 4);
-    y += __shfl_xor_sync(0xffffffffu, y, 2);
-    y += __shfl_xor_sync(0xffffffffu, y, 1);
-    return y;
-}
-
-// silu(z) with the fast exponential and division (a few ulp)
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
-
 // Scales and mins of Q4_K sub-blocks 2g and 2g+1 from the 12 scale bytes
 // (three little-endian words), without branches: bytes j' = 2 (g & 1) and
 // j' + 1 of each word; for g >= 2 the low four bits come from s[8..11] and
@@ -943,56 +928,6 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         constexpr bool HOIST = decltype(hoist)::value;
         for (int cr = 0; cr < nchunks_a; cr += DC_NSTAGE) {
             const int cend = min(cr + DC_NSTAGE, nchunks_a);
-            if constexpr (HOIST) {
-                // one token: every expert has one pair. Two items (row pairs) per
-                // pass share one 4-value reduction and overlap their dots.
-                const int fend = cend * A.rows_a;
-                for (int f = cr * A.rows_a + warp; f < fend; f += 2 * DC_CW) {
-                    int ci[2], row[2];
-                    int4 ch[2];
-                    bool ok[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int fu = f + u * DC_CW;
-                        ci[u] = fu >> ra_log;
-                        row[u] = fu & (A.rows_a - 1);
-                        ok[u] = fu < fend;
-                        ch[u] = ok[u] ? chunk[ci[u]] : make_int4(0, 0, 0, 0);
-                        ok[u] = ok[u] && row[u] < ch[u].z;
-                    }
-                    bool fail = false;
-#pragma unroll
-                    for (int u = 0; u < 2; ++u)
-                        if (ok[u] && !mbar_wait(&full[ci[u] % DC_NSTAGE], (uint32_t)(ci[u] / DC_NSTAGE) & 1u)) fail = true;
-                    if (fail) {
-                        if (lane == 0) set_abort(misc, A.status);
-                        break;
-                    }
-                    float part[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    int pp[2] = {0, 0};
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        if (!ok[u]) continue;
-                        const int q0 = aoff[ch[u].x];
-                        pp[u] = plist[q0];
-                        const DevExpert &X = dpair[pp[u]];
-                        const uint8_t *stage = ring + (size_t)(ci[u] % DC_NSTAGE) * A.stage;
-                        const uint8_t *grow = stage + row[u] * (int)X.gate.stride;
-                        const uint8_t *urow = stage + ch[u].z * (int)X.gate.stride + row[u] * (int)X.up.stride;
-                        if (lane < H64) {
-                            part[2 * u] = q4k_dot64(grow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
-                            part[2 * u + 1] = q4k_dot64(urow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
-                        }
-                    }
-                    // gate / up of item 0 in lanes 0..7 / 8..15, of item 1 in 16..23 / 24..31
-                    const float tot = warp_reduce4(part) * xsc[0];
-                    const float upv = __shfl_down_sync(0xffffffffu, tot, 8);
-                    const bool hi = lane & 16;
-                    if ((lane & 15) == 0 && (hi ? ok[1] : ok[0]))
-                        A.h[(size_t)(hi ? pp[1] : pp[0]) * I + (hi ? ch[1].y + row[1] : ch[0].y + row[0])] =
-                            silu_fast(tot) * upv;
-                }
-            } else
             for (int f = cr * A.rows_a + warp; f < cend * A.rows_a; f += DC_CW) {
                 const int ci = f >> ra_log, row = f & (A.rows_a - 1);
                 const int4 ch = chunk[ci];
@@ -1009,9 +944,14 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 const uint8_t *grow = stage + row * (int)X.gate.stride;
                 const uint8_t *urow = stage + n * (int)X.gate.stride + row * (int)X.up.stride;
                 for (int qi = 0; qi < ne; ++qi) {
-                    const int p = plist[q0 + qi], t = p / k;
+                    const int p = plist[q0 + qi], t = HOIST ? 0 : p / k;
                     float part[2] = {0.0f, 0.0f};
-                    {
+                    if constexpr (HOIST) {
+                        if (lane < H64) {
+                            part[0] = q4k_dot64(grow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
+                            part[1] = q4k_dot64(urow + 144 * (lane >> 2), lane & 3, xv1, XA1, XB1);
+                        }
+                    } else {
                         const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs + (size_t)t * H / 2);
                         for (int G64 = lane; G64 < H64; G64 += 32) {
                             uint32_t xv[32];
