@@ -497,11 +497,14 @@ __device__ __noinline__ void dc_issue_chunk(int ci, int nchunks_a, int b0, uint8
 }
 
 // ---------------------------------------------------------------- the kernel
+// ONE: one token with H <= 2048 (the activations fit a lane's registers);
+// compiled separately so that this kernel's code holds only its own path.
+template <bool ONE>
 __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int G = gridDim.x, c = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int T = A.T, k = A.k, E = A.E, H = A.H, I = A.I, P = T * k;
+    const int T = ONE ? 1 : A.T, k = A.k, E = A.E, H = A.H, I = A.I, P = T * k;
     const DcLayout L = dc_layout(T, k, E, H, I, G, A.stage, A.chunk_cap);
     const int NS = L.ns, NSE = 32 * L.ns, H64 = H / 64, U = I / 32;
 
@@ -726,7 +729,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             }
             cp_async_commit();
         }
-        if (T > 1) {
+        if constexpr (!ONE) {
             route_weights(t);
             cp_async_wait_all();   // descriptors: warp 0 issues copies after the next barrier
         }
@@ -795,7 +798,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     // routing is sorted at the end); warp 0 then issues the copies of the
     // ring slots that the raw activations do not occupy, and computes the
     // router weights while they are in flight.
-    if (T == 1 && warp == 0) {
+    if (ONE && warp == 0) {
         cp_async_wait_all();
         __syncwarp();
         const bool kp = lane < k && keep[lane];
@@ -875,7 +878,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     }
     __syncthreads();
     // Several tokens: the sorted bucketing, then the chunk table.
-    if (T > 1 && warp == 0) {
+    if (!ONE && warp == 0) {
         const int n_act = bucket_sorted();
         build_chunks(n_act);
         __syncwarp();
@@ -906,8 +909,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     // T = 1: every gate/up row meets the same activations; keep them in registers
     uint32_t xv1[32];
     float XA1 = 0.0f, XB1 = 0.0f;
-    const bool x_hoist = T == 1 && H64 <= 32;
-    if (x_hoist && lane < H64) {
+    if (ONE && lane < H64) {
         const uint4 *xv4 = reinterpret_cast<const uint4 *>(xs);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
@@ -981,7 +983,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 issue_chunk(cr + lane + DC_NSTAGE, nchunks_a, b0);
         }
     };
-    if (x_hoist) phase_a(std::true_type{}); else phase_a(std::false_type{});
+    phase_a(std::integral_constant<bool, ONE>{});
 
     // ---- grid barrier: every CTA's h is complete and visible. Warp 0 issues
     // the ring's bulk copies (a thread's fence may wait for its copies in
@@ -996,7 +998,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         constexpr int SENT = 0x7fffffff;
         constexpr int PUB = 32 * (DC_CW - 1);
         int *sexp = reinterpret_cast<int *>(surv);   // sorted active experts (prologue scratch)
-        if (T == 1) {
+        if constexpr (ONE) {
             if (warp == 0) {
                 int key = (lane < P && keep[lane]) ? ((ids[lane] << 8) | lane) : SENT;
                 key = P <= 16 ? warp_sort_asc<16>(key) : warp_sort_asc<32>(key);
@@ -1016,8 +1018,10 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
             }
             asm volatile("bar.sync 2, %0;" ::"n"(PUB) : "memory");
             const int nk = misc[11];
+#pragma unroll 1
             for (int e = tid; e <= E; e += PUB) {   // pairs of experts below e (one pair per expert)
                 int cnt = 0;
+#pragma unroll 1
                 for (int i = 0; i < nk; ++i) cnt += sexp[i] < e ? 1 : 0;
                 A.offsets_out[e] = cnt;
             }
@@ -1038,6 +1042,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 A.pos_out[plist[q]] = q;
             }
         }
+#pragma unroll 1
         for (int p = tid; p < P; p += PUB) {
             A.ids_out[p] = ids[p];
             A.wts_out[p] = wts[p];
@@ -1257,12 +1262,15 @@ cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *
         int optin = 0;
         err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
         if (err != cudaSuccess) return err;
-        cudaFuncAttributes fa;
-        err = cudaFuncGetAttributes(&fa, decode_fused_kernel);
-        if (err != cudaSuccess) return err;
-        err = cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   optin - (int)fa.sharedSizeBytes);
-        if (err != cudaSuccess) return err;
+        for (int one = 0; one < 2; ++one) {
+            const void *fn = one ? reinterpret_cast<const void *>(&decode_fused_kernel<true>)
+                                 : reinterpret_cast<const void *>(&decode_fused_kernel<false>);
+            cudaFuncAttributes fa;
+            err = cudaFuncGetAttributes(&fa, fn);
+            if (err != cudaSuccess) return err;
+            err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+            if (err != cudaSuccess) return err;
+        }
         if (dev < 64) g_attr_done[dev] = true;
     }
     DcArgs A;
@@ -1316,7 +1324,8 @@ cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel, A);
+    if (T == 1 && H / 64 <= 32) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, A);
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, A);
 }
 
 }  // namespace moe
