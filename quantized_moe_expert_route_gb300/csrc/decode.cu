@@ -125,7 +125,13 @@ struct DcArgs {
 __device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xffff))); }
 __device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
 
+// Named barriers are written as inline PTX. bar.sync is .aligned (all
+// threads of a warp execute it together), and nothing makes the compiler
+// reconverge a warp before inline assembly, so a warp whose lanes may have
+// diverged (one lane polling, a few lanes issuing copies) is reconverged
+// with __syncwarp() first.
 __device__ __forceinline__ void consumer_sync() {
+    __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"n"(DC_CW * 32) : "memory");
 }
 
@@ -978,18 +984,33 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 }
             }
             consumer_sync();
-            if (warp == 0 && lane < cend - cr && cr + lane + DC_NSTAGE < nchunks &&
+            // the last round's refills wait until warp 15 has arrived at the
+            // grid barrier (below)
+            if (warp == 0 && cr + DC_NSTAGE < nchunks_a && lane < cend - cr && cr + lane + DC_NSTAGE < nchunks &&
                 !*reinterpret_cast<volatile int *>(&misc[1]))
                 issue_chunk(cr + lane + DC_NSTAGE, nchunks_a, b0);
         }
     };
     phase_a(std::integral_constant<bool, ONE>{});
 
-    // ---- grid barrier: every CTA's h is complete and visible. Warp 0 issues
-    // the ring's bulk copies (a thread's fence may wait for its copies in
-    // flight), so warp 15 arrives (a release add: the CTA barrier orders the
-    // other warps' h stores before it) and polls (bounded).
+    // ---- grid barrier: every CTA's h is complete and visible. Warp 15
+    // arrives (a release add: the CTA barrier orders the other warps' h
+    // stores before it) and polls (bounded). Its fence waits for memory
+    // operations still in flight, bulk copies included (it took about 1,700
+    // cycles with the last refills just issued, 1,100 without), so warp 0
+    // issues the last gate/up round's refills only after the arrival, on
+    // named barrier 3 (warps 0 and 15).
     consumer_sync();
+    if (warp == 0) {
+        __syncwarp();
+        asm volatile("bar.sync 3, 64;" ::: "memory");
+        if (nchunks_a > 0) {
+            const int cr = ((nchunks_a - 1) / DC_NSTAGE) * DC_NSTAGE;
+            const int cend = min(cr + DC_NSTAGE, nchunks_a);
+            if (lane < cend - cr && cr + lane + DC_NSTAGE < nchunks && !*reinterpret_cast<volatile int *>(&misc[1]))
+                issue_chunk(cr + lane + DC_NSTAGE, nchunks_a, b0);
+        }
+    }
     if (c == 0 && warp < DC_CW - 1) {
         // CTA 0's warps 0..14 publish the routing while warp 15 waits at the
         // barrier. For one token the bucketing was used in rank order; the
@@ -1016,6 +1037,7 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                     misc[11] = nk;
                 }
             }
+            __syncwarp();
             asm volatile("bar.sync 2, %0;" ::"n"(PUB) : "memory");
             const int nk = misc[11];
 #pragma unroll 1
@@ -1050,8 +1072,12 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
         }
         if (tid == 0 && misc[2]) atomicOr(A.status, (uint32_t)misc[2]);
     }
+    if (warp == DC_CW - 1) {
+        if (lane == 0) red_release_add_u64(barrier_ctr, 1ull);
+        __syncwarp();
+        asm volatile("bar.arrive 3, 64;" ::: "memory");   // the whole warp: warp 0 may refill now
+    }
     if (tid == 32 * (DC_CW - 1)) {
-        red_release_add_u64(barrier_ctr, 1ull);
         // G arrivals past this launch's generation
         const unsigned long long target = (gen_count / (unsigned long long)G + 1ull) * (unsigned long long)G;
         const unsigned long long t_start = globaltimer_ns();

@@ -505,13 +505,17 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 // AND of `pred` over the 128 epilogue threads (warps 0-3), with a barrier.
 __device__ __forceinline__ bool epi_all(bool pred) {
     uint32_t r;
+    __syncwarp();   // the barrier is .aligned: reconverge the warp first
     asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, 1, 128, p; selp.u32 %0, 1, 0, q; }"
                  : "=r"(r)
                  : "r"((uint32_t)pred)
                  : "memory");
     return r != 0;
 }
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_sync() {
+    __syncwarp();   // the barrier is .aligned: reconverge the warp first
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
 
 // A steps per B stage for a unit of n rows (Npad = n rounded up to 16): 4 if
 // four Npad-row tiles fit a stage, else 2. Either divides an event.
