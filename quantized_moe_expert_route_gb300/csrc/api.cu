@@ -16,9 +16,9 @@ size_t bucket_smem_bytes(int E);
 size_t gateup_smem_bytes(int H, int64_t wstride);
 size_t down_smem_bytes(int I, int64_t wstride);
 cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
-                             int64_t dn_stride, const int32_t *offsets, const int32_t *pairs, const int32_t *active,
-                             const int32_t *pos, const float *wts, const uint16_t *x, float *h, float *y, float *out,
-                             uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
+                             int64_t dn_stride, uint32_t down_formats, const int32_t *offsets, const int32_t *pairs,
+                             const int32_t *active, const int32_t *pos, const float *wts, const uint16_t *x, float *h,
+                             float *y, float *out, uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
 bool decode_fused_eligible(int T, int k, int E, int H, int I, uint32_t gateup_formats, uint32_t down_formats,
                            int64_t gu_stride, int64_t dn_stride);
 cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *W, int T, int k, int E, int H, int I,
@@ -313,8 +313,8 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
                              W->down_formats, T, k, E, H, I, offsets, active, pos, wts, x,
                              h, y, base, tc_ws_layout(T, k, E, H, I), out, status, events, stream);
     else
-        err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, offsets, pairs,
-                               active, pos, wts, x, h, y, out, status, events, stream);
+        err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, W->down_formats,
+                               offsets, pairs, active, pos, wts, x, h, y, out, status, events, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     return MOE_OK;
 }

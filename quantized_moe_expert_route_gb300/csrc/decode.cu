@@ -37,6 +37,7 @@
 #include <type_traits>
 
 #include "moe_internal.cuh"
+#include "dot16.cuh"
 
 namespace moe {
 
@@ -122,9 +123,6 @@ struct DcArgs {
     long long ustep[3];
 };
 
-__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xffff))); }
-__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
-
 // Named barriers are written as inline PTX. bar.sync is .aligned (all
 // threads of a warp execute it together), and nothing makes the compiler
 // reconverge a warp before inline assembly, so a warp whose lanes may have
@@ -134,16 +132,6 @@ __device__ __forceinline__ void consumer_sync() {
     __syncwarp();
     asm volatile("bar.sync 1, %0;" ::"n"(DC_CW * 32) : "memory");
 }
-
-// Power-of-two scale for fp16: returns sigma with max * 2^sigma in [2^14, 2^15)
-// (0 for max == 0), clamped so that 2^sigma and 2^-sigma are normal floats.
-__device__ __forceinline__ int pow2_shift(float maxabs) {
-    if (!(maxabs > 0.0f)) return 0;
-    const int e = (int)((__float_as_uint(maxabs) >> 23) & 0xff);
-    int s = 141 - e;
-    return s < -126 ? -126 : (s > 126 ? 126 : s);
-}
-__device__ __forceinline__ float exp2i(int s) { return __uint_as_float((uint32_t)(127 + s) << 23); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -196,70 +184,6 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 
 
-// Sums of 2 per-lane values over the warp: value 0 ends in lanes 0..15, value 1 in 16..31.
-__device__ __forceinline__ float warp_reduce2(const float v[2]) {
-    const bool b16 = threadIdx.x & 16;
-    float y = (b16 ? v[1] : v[0]) + __shfl_xor_sync(0xffffffffu, b16 ? v[0] : v[1], 16);
-    y += __shfl_xor_sync(0xffffffffu, y, 8);
-    y += __shfl_xor_sync(0xffffffffu, y, 4);
-    y += __shfl_xor_sync(0xffffffffu, y, 2);
-    y += __shfl_xor_sync(0xffffffffu, y, 1);
-    return y;
-}
-
-
-// Scales and mins of Q4_K sub-blocks 2g and 2g+1 from the 12 scale bytes
-// (three little-endian words), without branches: bytes j' = 2 (g & 1) and
-// j' + 1 of each word; for g >= 2 the low four bits come from s[8..11] and
-// the top two from bits 6-7 of s[0..3] (scales) and s[4..7] (mins).
-__device__ __forceinline__ void q4k_pair_scales(int g, uint32_t s03, uint32_t s47, uint32_t s811, float &sc0,
-                                                float &sc1, float &m0, float &m1) {
-    const int sh = (g & 1) * 16;
-    const uint32_t a = (s03 >> sh) & 0xFFFFu, m = (s47 >> sh) & 0xFFFFu, h = (s811 >> sh) & 0xFFFFu;
-    const uint32_t sc_lo = a & 0x3F3Fu, mn_lo = m & 0x3F3Fu;
-    const uint32_t sc_hi = (h & 0x0F0Fu) | ((a >> 2) & 0x3030u);
-    const uint32_t mn_hi = ((h >> 4) & 0x0F0Fu) | ((m >> 2) & 0x3030u);
-    const uint32_t scp = g < 2 ? sc_lo : sc_hi, mnp = g < 2 ? mn_lo : mn_hi;
-    sc0 = (float)(scp & 0xFFu);
-    sc1 = (float)(scp >> 8);
-    m0 = (float)(mnp & 0xFFu);
-    m1 = (float)(mnp >> 8);
-}
-
-__device__ __forceinline__ int dp2a_lo(uint32_t a, uint32_t b, int c) {
-    asm("dp2a.lo.s32.s32 %0, %1, %2, %0;" : "+r"(c) : "r"(a), "r"(b));
-    return c;
-}
-__device__ __forceinline__ int dp2a_hi(uint32_t a, uint32_t b, int c) {
-    asm("dp2a.hi.s32.s32 %0, %1, %2, %0;" : "+r"(c) : "r"(a), "r"(b));
-    return c;
-}
-
-// One lane's share of a Q4_K row dot product: the 64 weights of pair g of
-// super-block blk (sub-blocks 2g, 2g+1) times 64 int16 activations xq (two
-// per word: xq[4m], xq[4m+1] hold sub-block 2g's weights 4m..4m+3 and
-// xq[4m+2], xq[4m+3] sub-block 2g+1's), with XA, XB the sums of those
-// activations per sub-block. The 4-bit codes enter dp2a as bytes, so the
-// products and sums per sub-block are exact integers. Returns sum_i w_i x_i.
-__device__ __forceinline__ float q4k_dot64(const uint8_t *blk, int g, const uint32_t xq[32], float XA, float XB) {
-    const uint4 hdr = *reinterpret_cast<const uint4 *>(blk);
-    const uint4 c0 = *reinterpret_cast<const uint4 *>(blk + 16 + 32 * g);
-    const uint4 c1 = *reinterpret_cast<const uint4 *>(blk + 32 + 32 * g);
-    const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    int sA0 = 0, sA1 = 0, sB0 = 0, sB1 = 0;
-#pragma unroll
-    for (int m = 0; m < 8; ++m) {
-        const uint32_t lo = cw[m] & 0x0F0F0F0Fu, hi = (cw[m] >> 4) & 0x0F0F0F0Fu;
-        sA0 = dp2a_lo(xq[4 * m + 0], lo, sA0);
-        sA1 = dp2a_hi(xq[4 * m + 1], lo, sA1);
-        sB0 = dp2a_lo(xq[4 * m + 2], hi, sB0);
-        sB1 = dp2a_hi(xq[4 * m + 3], hi, sB1);
-    }
-    float sc0, sc1, m0, m1;
-    q4k_pair_scales(g, hdr.y, hdr.z, hdr.w, sc0, sc1, m0, m1);
-    const float d = half_lo(hdr.x), dmin = half_hi(hdr.x);
-    return d * (sc0 * (float)(sA0 + sA1) + sc1 * (float)(sB0 + sB1)) - dmin * (m0 * XA + m1 * XB);
-}
 
 
 // One lane's down-projection partial over up to 8 consecutive Q8_0 blocks

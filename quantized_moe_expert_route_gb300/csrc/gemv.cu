@@ -398,9 +398,18 @@ size_t gateup_smem_bytes(int H, int64_t wstride) {
 size_t down_smem_bytes(int I, int64_t wstride) { return (size_t)(DN_ROWS * wstride) + (size_t)GV_NT * I * 4; }
 
 cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
-                             int64_t dn_stride, const int32_t *offsets, const int32_t *pairs, const int32_t *active,
-                             const int32_t *pos, const float *wts, const uint16_t *x, float *h, float *y, float *out,
-                             uint32_t *status, cudaEvent_t const *events, cudaStream_t s) {
+                             int64_t dn_stride, uint32_t down_formats, const int32_t *offsets, const int32_t *pairs,
+                             const int32_t *active, const int32_t *pos, const float *wts, const uint16_t *x, float *h,
+                             float *y, float *out, uint32_t *status, cudaEvent_t const *events, cudaStream_t s) {
+    // decode batches of up to 16 rows: the streaming kernels (stream.cu)
+    if (T > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+        const SgPlan p = stream_plan(T, k, E, H, I, down_formats, gu_stride, dn_stride);
+        if (p.ok) {
+            cudaError_t err = launch_stream_path(table, p, T, k, E, H, I, offsets, pairs, active, x, h, y, status, events, s);
+            if (err != cudaSuccess) return err;
+            return launch_combine(T, k, H, pos, wts, y, out, s);
+        }
+    }
     static bool attr_done[64] = {};
     int dev = current_device();
     if (dev >= 64 || !attr_done[dev]) {

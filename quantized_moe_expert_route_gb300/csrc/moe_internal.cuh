@@ -105,6 +105,19 @@ int sm_count();
 cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float *wts, const float *y, float *out,
                            cudaStream_t s);
 
+// Streaming grouped GEMV for decode batches (stream.cu): the launch plan
+// (ok == false if the kernels cannot run the layer) and the launcher of its
+// gate/up and down kernels (the combine is launched separately).
+struct SgPlan {
+    bool ok;
+    int cr, ns, stage, nexp, nsb, stageb, nq;
+    size_t smem_a, smem_b;
+};
+SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t down_formats, int64_t gu_stride, int64_t dn_stride);
+cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, int k, int E, int H, int I,
+                               const int32_t *offsets, const int32_t *pairs, const int32_t *active, const uint16_t *x,
+                               float *h, float *y, uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
+
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

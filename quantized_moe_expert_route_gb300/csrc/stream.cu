@@ -1,0 +1,753 @@
+// Streaming grouped GEMV for decode batches of up to 16 token rows, any mix of
+// the gate/up formats (Q8_0, Q4_K, Q6_K, MXFP4) and Q8_0 or MXFP4 down.
+//
+// The grouped multi-session decode of "多卡 CUDA 张量并行：DwarfStar 如何在 8 张
+// L40S 上跑出 120 t/s" (section 120 t/s 的秘密) reads each selected expert's
+// weights once for all the rows that picked it; the tiered mul_mat_id of "三张
+// RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南" (section
+// 优化策略三) serves each expert in its own format. Here two persistent kernels
+// (one CTA per SM, 16 warps) stream the weights:
+//
+//   gate/up: the active experts' gate/up rows are split evenly over the CTAs
+//     in chunks of 1, 2 or 4 row pairs. Warp w < 15 consumes the CTA's
+//     chunks w, w + 15, ... from a ring of shared-memory slots that TMA bulk
+//     copies fill; one thread of warp 15 refills each slot with the chunk NS
+//     ahead as soon as the slot's chunk is consumed, so no CTA-wide barrier
+//     stands in the loop and no consumer waits on a copy it issued. A warp
+//     holds its slot while it computes, so the chunk size is chosen to leave
+//     about as many slots in flight (HBM latency x bandwidth per SM) as are
+//     being computed. For every row pair and every
+//     token of the chunk's expert the warp forms both dot products (lane =
+//     64-column group, int16 activations, dp2a on the codes) and writes
+//     h = silu(W_gate x) (W_up x) in fp32.
+//   down: the active experts' down rows are split the same way in chunks of
+//     4 rows (8 lanes per row); each CTA first stages the h rows of the
+//     pairs of its experts as int16 with a power-of-two scale per 32-block,
+//     then writes y = W_down h in fp32 per pair; the combine kernel adds the
+//     k rows of a token in slot order.
+//
+// The down kernel is launched with programmatic dependent launch: it reads
+// its experts and issues its first weight copies while the gate/up kernel
+// finishes, and waits for it only before reading h.
+#include <algorithm>
+
+#include "moe_internal.cuh"
+#include "dot16.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int SG_THREADS = 512;
+constexpr int SG_WARPS = SG_THREADS / 32;
+constexpr int SG_CONS = SG_WARPS - 1;   // consumer warps; lane 0 of the last warp refills the ring
+constexpr int SG_MAX_SLOTS = 64;
+constexpr int SG_MAX_T = 16;
+constexpr int SG_DN_ROWS = 4;   // down rows per chunk: 8 lanes per row
+constexpr int SG_HQW = 20;      // words per staged 32-block of h: 16 int16 pairs, 2^-sigma, padding to 16 bytes
+
+struct SgExp {
+    DevMatrix a, b;   // gate, up (gate/up kernel) or down, unused (down kernel)
+    int e, q0, n, pad;
+};
+
+struct SgArgs {
+    const DevExpert *table;
+    const int32_t *offsets, *pairs, *active;
+    const uint16_t *x;   // bf16 [T, H]
+    float *h;            // fp32 [kept pairs, I], bucket order
+    float *y;            // fp32 [kept pairs, H], bucket order
+    uint32_t *status;
+    int T, k, H, I, E;
+    int cr, ns, stage, nexp;   // gate/up: row pairs per chunk, ring slots, slot bytes, experts per CTA (bound)
+    int nsb, stageb, nq;       // down: ring slots, slot bytes, staged pairs per CTA (bound)
+};
+
+__device__ __forceinline__ void sg_flag(uint32_t *status, uint32_t f) {
+    if (status) atomicOr(status, f);
+}
+
+// A slot's chunks j, j + ns, j + 2 ns, ... complete its mbarrier's phases
+// 0, 1, 2, ...; a parity wait is only meaningful once the slot's previous
+// phase has completed (a wait on the parity of a phase two ahead of the
+// current one returns at once). Chunk j is issued only after chunk j - ns was
+// consumed, so a consumer first waits (bounded) until the slot's issue record
+// shows chunk j, then on the parity.
+__device__ __forceinline__ bool sg_wait_chunk(uint64_t *full, const int *last, int s, int j, int ns) {
+    const volatile int *l = last + s;
+    for (uint32_t i = 0; *l != j; ++i) {
+        if (i >= WAIT_LIMIT) return false;
+        __nanosleep(32);
+    }
+    return mbar_wait(&full[s], (uint32_t)(j / ns) & 1u);
+}
+
+// The ring's producer (warp 15): lane l < SG_PL issues the chunks
+// j = ns + l, ns + l + SG_PL, ... in order, each into slot j % ns once that
+// slot's previous chunk has been consumed (used[s] names the last chunk
+// consumed from slot s). With ns a multiple of SG_PL every slot is served by
+// one lane, and the lanes' copies go out together. False if a wait gave up.
+constexpr int SG_PL = 8;
+template <class Issue>
+__device__ bool sg_produce(int ns, int n, const int *used, Issue issue) {
+    const int lane = threadIdx.x & 31;
+    int next = ns + lane;
+    uint32_t idle = 0;
+    for (;;) {
+        const bool want = lane < SG_PL && next < n;
+        if (!__any_sync(0xffffffffu, want)) return true;
+        const bool ready = want && *reinterpret_cast<const volatile int *>(used + next % ns) == next - ns;
+        if (ready) {
+            issue(next);
+            next += SG_PL;
+        }
+        if (__any_sync(0xffffffffu, ready)) {
+            idle = 0;
+        } else {
+            if (++idle >= WAIT_LIMIT) return false;
+            __nanosleep(64);
+        }
+    }
+}
+
+// Waits (bounded, thread 0) for the last copy issued into every slot, so that
+// no copy lands in the shared memory of an exited CTA.
+__device__ void sg_drain(uint64_t *full, const int *last, int ns) {
+    for (int s = 0; s < ns; ++s)
+        if (last[s] >= 0) mbar_wait(&full[s], (uint32_t)(last[s] / ns) & 1u);
+}
+
+// One 64-column group of CR rows of gate and of up against one token.
+template <int FMT, int CR>
+__device__ __forceinline__ void sg_rows(const uint8_t *g0, int gs, const uint8_t *u0, int us, int G64,
+                                        const uint32_t xv[32], int4 X16, float ag[CR], float au[CR]) {
+    const float XA = (float)(X16.x + X16.y), XB = (float)(X16.z + X16.w);
+#pragma unroll
+    for (int r = 0; r < CR; ++r) {
+        const uint8_t *gr = g0 + r * gs, *ur = u0 + r * us;
+        if constexpr (FMT == MOE_Q4_K) {
+            ag[r] += q4k_dot64(gr + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
+            au[r] += q4k_dot64(ur + 144 * (G64 >> 2), G64 & 3, xv, XA, XB);
+        } else if constexpr (FMT == MOE_Q8_0) {
+            ag[r] += q8_0_dot64(gr, G64, xv);
+            au[r] += q8_0_dot64(ur, G64, xv);
+        } else if constexpr (FMT == MOE_Q6_K) {
+            ag[r] += q6k_dot64(gr, G64, xv, X16);
+            au[r] += q6k_dot64(ur, G64, xv, X16);
+        } else {
+            ag[r] += mxfp4_dot64(gr, G64, xv);
+            au[r] += mxfp4_dot64(ur, G64, xv);
+        }
+    }
+}
+
+// One chunk of the gate/up kernel: CR row pairs of one expert, every token of
+// the expert. The slot holds the CR gate rows, then the CR up rows.
+template <int FMT, int CR>
+__device__ void sg_gateup_chunk(const SgArgs &A, const SgExp &X, const int *tok, const uint8_t *st, int r0,
+                                const uint4 *xs4, const int4 *x16, const float *xsc) {
+    const int lane = threadIdx.x & 31, H64 = A.H / 64;
+    const int gs = (int)X.a.stride, us = (int)X.b.stride;
+    const uint8_t *u0 = st + CR * gs;
+    for (int qi = 0; qi < X.n; ++qi) {
+        // an expert has at most T pairs unless a token repeats it
+        const int t = qi < A.T ? tok[qi] : A.pairs[X.q0 + qi] / A.k;
+        float ag[CR], au[CR];
+#pragma unroll
+        for (int r = 0; r < CR; ++r) ag[r] = au[r] = 0.0f;
+        for (int G64 = lane; G64 < H64; G64 += 32) {
+            uint32_t xv[32];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const uint4 q = xs4[((size_t)t * 8 + v) * H64 + G64];
+                xv[4 * v + 0] = q.x;
+                xv[4 * v + 1] = q.y;
+                xv[4 * v + 2] = q.z;
+                xv[4 * v + 3] = q.w;
+            }
+            sg_rows<FMT, CR>(st, gs, u0, us, G64, xv, x16[(size_t)t * H64 + G64], ag, au);
+        }
+        const float s = xsc[t];
+#pragma unroll
+        for (int r = 0; r < CR; ++r) {
+            const float v2[2] = {ag[r], au[r]};
+            const float tot = warp_reduce2(v2) * s;   // gate in lanes 0..15, up in 16..31
+            const float upv = __shfl_down_sync(0xffffffffu, tot, 16);
+            if (lane == 0) A.h[(size_t)(X.q0 + qi) * A.I + r0 + r] = silu_f32(tot) * upv;
+        }
+    }
+}
+
+template <int CR>
+__device__ __forceinline__ void sg_gateup_dispatch(const SgArgs &A, const SgExp &X, const int *tok, const uint8_t *st,
+                                                   int r0, const uint4 *xs4, const int4 *x16, const float *xsc) {
+    switch (X.a.fmt) {
+        case MOE_Q4_K: sg_gateup_chunk<MOE_Q4_K, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+        case MOE_Q8_0: sg_gateup_chunk<MOE_Q8_0, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+        case MOE_Q6_K: sg_gateup_chunk<MOE_Q6_K, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+        case MOE_MXFP4: sg_gateup_chunk<MOE_MXFP4, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+        default: break;
+    }
+}
+
+// Shared memory of the gate/up kernel after the ring (ring first, so that the
+// 4-byte reads that run up to 7 bytes past a row stay inside the allocation).
+struct SgLayoutA {
+    size_t xs, x16, xsc, xsg, full, last, used, ex, tok, cost, total;
+};
+__host__ __device__ inline SgLayoutA sg_layout_a(int T, int H, int E, int ns, int stage, int nexp) {
+    SgLayoutA L;
+    size_t o = align_up((size_t)ns * stage + 16, 128);
+    L.xs = o;
+    o += (size_t)T * H * 2;
+    L.x16 = o;
+    o += (size_t)T * (H / 64) * 16;
+    L.xsc = o;
+    o = align_up(o + (size_t)T * 4, 16);
+    L.xsg = o;
+    o = align_up(o + (size_t)T * 4, 16);
+    L.full = o;
+    o += (size_t)SG_MAX_SLOTS * 8;
+    L.last = o;
+    o += (size_t)SG_MAX_SLOTS * 4;
+    L.used = o;
+    o += (size_t)SG_MAX_SLOTS * 4;
+    L.ex = align_up(o, 16);
+    o = L.ex + (size_t)nexp * sizeof(SgExp);
+    L.tok = o;
+    o += (size_t)nexp * T * 4;
+    L.cost = align_up(o, 16);
+    o = L.cost + (size_t)(E + 1) * 4;
+    L.total = align_up(o, 128);
+    return L;
+}
+
+struct SgLayoutB {
+    size_t hq, full, last, used, ex, cost, total;
+};
+__host__ __device__ inline SgLayoutB sg_layout_b(int I, int E, int nsb, int stageb, int nq, int nexp) {
+    SgLayoutB L;
+    size_t o = align_up((size_t)nsb * stageb + 16, 128);
+    L.hq = o;
+    o += (size_t)nq * (I / 32) * SG_HQW * 4;
+    L.full = align_up(o, 8);
+    o = L.full + (size_t)SG_MAX_SLOTS * 8;
+    L.last = o;
+    o += (size_t)SG_MAX_SLOTS * 4;
+    L.used = o;
+    o += (size_t)SG_MAX_SLOTS * 4;
+    L.ex = align_up(o, 16);
+    o = L.ex + (size_t)nexp * sizeof(SgExp);
+    L.cost = align_up(o, 16);
+    o = L.cost + (size_t)(E + 1) * 4;
+    L.total = align_up(o, 128);
+    return L;
+}
+
+// The CTA's share of the chunk list [n_act experts x cpe chunks]: [c0, c1),
+// its experts a0 .. a0 + na - 1 (indices into the active list). The list is
+// split by cost, not by length: a chunk of expert a costs n_a + 1, its rows
+// times the expert's n_a pairs of dot products plus one for streaming the
+// rows, so the CTAs holding the rows of experts that many tokens picked get
+// fewer of them. S: shared scratch of n_act + 1 ints (the prefix costs).
+__device__ void sg_range(const SgArgs &A, int n_act, int cpe, int *S, int &c0, int &nloc, int &a0, int &na) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    for (int a = tid; a < n_act; a += SG_THREADS) {
+        const int e = A.active[1 + a];
+        S[a] = cpe * (A.offsets[e + 1] - A.offsets[e] + 1);
+    }
+    __syncthreads();
+    if (tid < 32) {   // exclusive prefix sums in place, S[n_act] = total
+        const int per = (n_act + 31) / 32, b = min(n_act, lane * per), e = min(n_act, b + per);
+        int sum = 0;
+        for (int a = b; a < e; ++a) sum += S[a];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int a = b; a < e; ++a) {
+            const int w = S[a];
+            S[a] = run;
+            run += w;
+        }
+        if (lane == 31) S[n_act] = incl;
+    }
+    __syncthreads();
+    // the first chunk that starts at or after cost t
+    auto chunk_at = [&](long long t) -> int {
+        int lo = 0, hi = n_act;   // largest a with S[a] <= t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (S[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        if (lo >= n_act) return n_act * cpe;
+        const int w = (S[lo + 1] - S[lo]) / cpe;
+        const long long k = (t - S[lo] + w - 1) / w;
+        return lo * cpe + (k < cpe ? (int)k : cpe);
+    };
+    const long long tot = S[n_act];
+    const int G = gridDim.x, c = blockIdx.x;
+    c0 = chunk_at(tot * c / G);
+    const int c1 = chunk_at(tot * (c + 1) / G);
+    nloc = c1 - c0;
+    a0 = nloc > 0 ? c0 / cpe : 0;
+    na = nloc > 0 ? (c1 - 1) / cpe - a0 + 1 : 0;
+}
+
+__global__ void __launch_bounds__(SG_THREADS, 1) sg_gateup_kernel(SgArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int T = A.T, H = A.H, H64 = H / 64;
+    const SgLayoutA L = sg_layout_a(T, H, A.E, A.ns, A.stage, A.nexp);
+    uint8_t *ring = smem;
+    uint4 *xs4 = reinterpret_cast<uint4 *>(smem + L.xs);   // [T][8][H/64]
+    int4 *x16 = reinterpret_cast<int4 *>(smem + L.x16);    // [T][H/64] activation sums per 16
+    float *xsc = reinterpret_cast<float *>(smem + L.xsc);  // [T] 2^-sigma
+    int *xsg = reinterpret_cast<int *>(smem + L.xsg);      // [T] sigma
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
+    int *last = reinterpret_cast<int *>(smem + L.last);    // last chunk issued into each slot
+    int *used = reinterpret_cast<int *>(smem + L.used);    // last chunk consumed from each slot
+    SgExp *ex = reinterpret_cast<SgExp *>(smem + L.ex);
+    int *tok = reinterpret_cast<int *>(smem + L.tok);      // [nexp][T] tokens of each expert's pairs
+
+    // the routing comes from the previous kernels in the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int n_act = A.active[0], cpe = A.I / A.cr;
+    int c0, nloc, a0, na;
+    sg_range(A, n_act, cpe, reinterpret_cast<int *>(smem + L.cost), c0, nloc, a0, na);
+    if (na > A.nexp) {   // beyond the planned bound (cannot happen): skip, flagged
+        if (tid == 0) sg_flag(A.status, MOE_FLAG_WAIT_TIMEOUT);
+        return;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < A.ns; ++s) {
+            mbar_init(&full[s], 1);
+            last[s] = -1;
+            used[s] = -1;
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane < na) {
+        const int e = A.active[1 + a0 + lane];
+        SgExp X;
+        X.a = A.table[e].gate;
+        X.b = A.table[e].up;
+        X.e = e;
+        X.q0 = A.offsets[e];
+        X.n = A.offsets[e + 1] - X.q0;
+        X.pad = 0;
+        ex[lane] = X;
+    }
+    __syncthreads();
+    auto issue = [&](int j) {   // local chunk j into slot j % ns (one thread)
+        const int gc = c0 + j, la = gc / cpe - a0, r0 = (gc - (gc / cpe) * cpe) * A.cr, s = j % A.ns;
+        const SgExp &X = ex[la];
+        const uint32_t bg = (uint32_t)(A.cr * X.a.stride), bu = (uint32_t)(A.cr * X.b.stride);
+        uint8_t *dst = ring + (size_t)s * A.stage;
+        mbar_expect_tx(&full[s], bg + bu);
+        bulk_g2s(dst, X.a.data + (size_t)r0 * X.a.stride, bg, &full[s]);
+        bulk_g2s(dst + bg, X.b.data + (size_t)r0 * X.b.stride, bu, &full[s]);
+        *reinterpret_cast<volatile int *>(&last[s]) = j;
+    };
+    if (lane == 0)
+        for (int j = warp; j < min(A.ns, nloc); j += SG_WARPS) issue(j);
+    for (int i = tid; i < na * T; i += SG_THREADS) {
+        const int la = i / T, qi = i - la * T;
+        tok[i] = qi < ex[la].n ? A.pairs[ex[la].q0 + qi] / A.k : 0;
+    }
+    // activations: per-token power-of-two scale (max |x| in [2^14, 2^15))
+    for (int t = warp; t < T; t += SG_WARPS) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(A.x + (size_t)t * H);
+        float m = 0.0f;
+        for (int i = lane; i < H / 8; i += 32) {
+            const uint4 q = src[i];
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xffff0000u))));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            const int sg = pow2_shift(m);
+            xsg[t] = sg;
+            xsc[t] = exp2i(-sg);
+        }
+    }
+    __syncthreads();
+    // int16 activations in the dot layout: four lanes per 64-column group, lane
+    // q takes columns 8q .. 8q+7 of part A and of part B (uint4 words 2q, 2q+1)
+    {
+        const int ntask = 4 * T * H64;
+        for (int base = warp * 32; base < ntask; base += SG_THREADS) {
+            const int task = base + lane;
+            const bool ok = task < ntask;
+            const int g = ok ? task >> 2 : 0, q = task & 3;
+            const int t = g / H64, G64 = g - t * H64;
+            const float up = exp2i(xsg[t]);
+            const uint4 *src = reinterpret_cast<const uint4 *>(A.x + (size_t)t * H) + 8 * G64;
+            const uint4 qa = src[q], qb = src[4 + q];
+            const uint32_t wa[4] = {qa.x, qa.y, qa.z, qa.w}, wb[4] = {qb.x, qb.y, qb.z, qb.w};
+            int ia[8], ib[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ia[2 * i] = max(-32767, min(32767, __float2int_rn(__uint_as_float(wa[i] << 16) * up)));
+                ia[2 * i + 1] = max(-32767, min(32767, __float2int_rn(__uint_as_float(wa[i] & 0xffff0000u) * up)));
+                ib[2 * i] = max(-32767, min(32767, __float2int_rn(__uint_as_float(wb[i] << 16) * up)));
+                ib[2 * i + 1] = max(-32767, min(32767, __float2int_rn(__uint_as_float(wb[i] & 0xffff0000u) * up)));
+            }
+            int sa = 0, sb = 0;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int i = 4 * h2;
+                const uint32_t w0 = ((uint32_t)ia[i] & 0xffffu) | ((uint32_t)ia[i + 1] << 16);
+                const uint32_t w1 = ((uint32_t)ia[i + 2] & 0xffffu) | ((uint32_t)ia[i + 3] << 16);
+                const uint32_t w2 = ((uint32_t)ib[i] & 0xffffu) | ((uint32_t)ib[i + 1] << 16);
+                const uint32_t w3 = ((uint32_t)ib[i + 2] & 0xffffu) | ((uint32_t)ib[i + 3] << 16);
+                if (ok) xs4[((size_t)t * 8 + 2 * q + h2) * H64 + G64] = make_uint4(w0, w1, w2, w3);
+                sa += ia[i] + ia[i + 1] + ia[i + 2] + ia[i + 3];
+                sb += ib[i] + ib[i + 1] + ib[i + 2] + ib[i + 3];
+            }
+            // lanes q = 0, 1 cover columns 0..15 of each part, q = 2, 3 columns 16..31
+            sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+            sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+            const int sa_hi = __shfl_down_sync(0xffffffffu, sa, 2), sb_hi = __shfl_down_sync(0xffffffffu, sb, 2);
+            if (ok && q == 0) x16[(size_t)t * H64 + G64] = make_int4(sa, sa_hi, sb, sb_hi);
+        }
+    }
+    __syncthreads();
+    // the down kernel may begin its launch (it waits for this grid before reading h)
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    bool ok = true;
+    if (warp < SG_CONS) {
+        for (int j = warp; j < nloc; j += SG_CONS) {
+            const int s = j % A.ns;
+            const int gc = c0 + j, la = gc / cpe - a0, r0 = (gc - (gc / cpe) * cpe) * A.cr;
+            if (!sg_wait_chunk(full, last, s, j, A.ns)) {
+                ok = false;
+                break;
+            }
+            const uint8_t *st = ring + (size_t)s * A.stage;
+            const SgExp &X = ex[la];
+            const int *tk = tok + la * T;
+            if (A.cr == 4) sg_gateup_dispatch<4>(A, X, tk, st, r0, xs4, x16, xsc);
+            else if (A.cr == 2) sg_gateup_dispatch<2>(A, X, tk, st, r0, xs4, x16, xsc);
+            else sg_gateup_dispatch<1>(A, X, tk, st, r0, xs4, x16, xsc);
+            __syncwarp();
+            if (lane == 0) *reinterpret_cast<volatile int *>(&used[s]) = j;
+        }
+    } else {
+        ok = sg_produce(A.ns, nloc, used, issue);
+    }
+    if (!ok && lane == 0) sg_flag(A.status, MOE_FLAG_WAIT_TIMEOUT);
+    __syncwarp();
+    __syncthreads();
+    if (tid == 0) sg_drain(full, last, A.ns);
+}
+
+// Down: one 32-block b of a row against staged h (16 int16 pairs, 2^-sigma).
+template <int FMT>
+__device__ __forceinline__ float sg_down_block(const uint8_t *wrow, int b, const uint32_t *hb) {
+    uint32_t hv[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 q = reinterpret_cast<const uint4 *>(hb)[v];
+        hv[4 * v] = q.x;
+        hv[4 * v + 1] = q.y;
+        hv[4 * v + 2] = q.z;
+        hv[4 * v + 3] = q.w;
+    }
+    const float hs = __uint_as_float(hb[16]);
+    int s = 0;
+    if constexpr (FMT == MOE_Q8_0) {
+        // 34 bytes per block: fp16 d, then 32 int8 codes from byte 2
+        const uint8_t *blk = wrow + 34 * b;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 2);
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        const uint32_t sh = 8 * (uint32_t)(a & 3);
+        uint32_t W[9];
+#pragma unroll
+        for (int i = 0; i < 9; ++i) W[i] = w[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t c = __funnelshift_r(W[i], W[i + 1], sh);
+            s = dp2a_lo(hv[2 * i], c, s);
+            s = dp2a_hi(hv[2 * i + 1], c, s);
+        }
+        return __half2float(__ushort_as_half((uint16_t)ld_u16(blk))) * hs * (float)s;
+    } else {
+        // MXFP4, 17 bytes per block: E8M0 e, then 16 code bytes
+        const uint8_t *blk = wrow + 17 * b;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 1);
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        const uint32_t sh = 8 * (uint32_t)(a & 3);
+        uint32_t W[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) W[i] = w[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t c = __funnelshift_r(W[i], W[i + 1], sh);
+            const uint32_t lo = e2m1x2_bytes(c & 0x0F0F0F0Fu), hi = e2m1x2_bytes((c >> 4) & 0x0F0F0F0Fu);
+            s = dp2a_lo(hv[2 * i], lo, s);
+            s = dp2a_hi(hv[2 * i + 1], lo, s);
+            s = dp2a_lo(hv[8 + 2 * i], hi, s);
+            s = dp2a_hi(hv[8 + 2 * i + 1], hi, s);
+        }
+        return e8m0_half_scale(blk[0]) * hs * (float)s;
+    }
+}
+
+template <int FMT>
+__device__ void sg_down_chunk(const SgArgs &A, const SgExp &X, const uint8_t *st, int r0, const uint32_t *hq,
+                              int qbase) {
+    const int lane = threadIdx.x & 31, row = lane >> 3, qd = lane & 7, U = A.I / 32;
+    const uint8_t *wrow = st + (size_t)row * X.a.stride;
+    for (int qi = 0; qi < X.n; ++qi) {
+        const int q = X.q0 + qi;
+        const uint32_t *hrow = hq + (size_t)(q - qbase) * U * SG_HQW;
+        float acc = 0.0f;
+        for (int b = qd; b < U; b += 8) acc += sg_down_block<FMT>(wrow, b, hrow + b * SG_HQW);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        if (qd == 0) A.y[(size_t)q * A.H + r0 + row] = acc;
+    }
+}
+
+__global__ void __launch_bounds__(SG_THREADS, 1) sg_down_kernel(SgArgs A) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int U = A.I / 32;
+    const SgLayoutB L = sg_layout_b(A.I, A.E, A.nsb, A.stageb, A.nq, A.nexp);
+    uint8_t *ring = smem;
+    uint32_t *hq = reinterpret_cast<uint32_t *>(smem + L.hq);   // [staged pairs][U][SG_HQW]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
+    int *last = reinterpret_cast<int *>(smem + L.last);
+    int *used = reinterpret_cast<int *>(smem + L.used);
+    SgExp *ex = reinterpret_cast<SgExp *>(smem + L.ex);
+
+    // The routing was complete before the gate/up kernel began (it waited for
+    // it), and this kernel starts after that kernel's trigger: the experts and
+    // the first weight copies need no wait.
+    const int n_act = A.active[0], cpe = A.H / SG_DN_ROWS;
+    int c0, nloc, a0, na;
+    sg_range(A, n_act, cpe, reinterpret_cast<int *>(smem + L.cost), c0, nloc, a0, na);
+    if (na > A.nexp) {
+        if (tid == 0) sg_flag(A.status, MOE_FLAG_WAIT_TIMEOUT);
+        return;
+    }
+    if (tid == 0) {
+        for (int s = 0; s < A.nsb; ++s) {
+            mbar_init(&full[s], 1);
+            last[s] = -1;
+            used[s] = -1;
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane < na) {
+        const int e = A.active[1 + a0 + lane];
+        SgExp X;
+        X.a = A.table[e].down;
+        X.b = X.a;
+        X.e = e;
+        X.q0 = A.offsets[e];
+        X.n = A.offsets[e + 1] - X.q0;
+        X.pad = 0;
+        ex[lane] = X;
+    }
+    __syncthreads();
+    auto issue = [&](int j) {
+        const int gc = c0 + j, la = gc / cpe - a0, r0 = (gc - (gc / cpe) * cpe) * SG_DN_ROWS, s = j % A.nsb;
+        const SgExp &X = ex[la];
+        const uint32_t bd = (uint32_t)(SG_DN_ROWS * X.a.stride);
+        mbar_expect_tx(&full[s], bd);
+        bulk_g2s(ring + (size_t)s * A.stageb, X.a.data + (size_t)r0 * X.a.stride, bd, &full[s]);
+        *reinterpret_cast<volatile int *>(&last[s]) = j;
+    };
+    if (lane == 0)
+        for (int j = warp; j < min(A.nsb, nloc); j += SG_WARPS) issue(j);
+
+    // h of the gate/up kernel
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int qbase = na > 0 ? ex[0].q0 : 0;
+    const int nql = na > 0 ? ex[na - 1].q0 + ex[na - 1].n - qbase : 0;   // the experts' pairs are contiguous
+    bool ok = nql <= A.nq;
+    if (ok) {
+        // eight threads per 32-block: four values each, a shared maximum, then
+        // 16 int16 pairs and 2^-sigma with max |h| 2^sigma in [2^13, 2^14)
+        const int ntask = nql * U * 8;
+        for (int base = warp * 32; base < ntask; base += SG_THREADS) {
+            const int task = base + lane;
+            const bool in = task < ntask;
+            const int blk = in ? task >> 3 : 0, part = task & 7;
+            const int qq = blk / U, b = blk - qq * U;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (in) v = __ldcg(reinterpret_cast<const float4 *>(A.h + (size_t)(qbase + qq) * A.I + 32 * b) + part);
+            float m = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+            if (!in) continue;
+            uint32_t *dst = hq + (size_t)blk * SG_HQW;
+            const int be = (int)((__float_as_uint(m) >> 23) & 0xffu);
+            if (be == 255) {   // inf or nan in the block: it propagates
+                *reinterpret_cast<uint2 *>(dst + 2 * part) = make_uint2(0u, 0u);
+                if (part == 0) dst[16] = 0x7fc00000u;
+                continue;
+            }
+            const int sg = m > 0.0f ? max(-100, min(100, 140 - be)) : 0;
+            const float up = __uint_as_float((uint32_t)(127 + sg) << 23);
+            const int q0 = __float2int_rn(v.x * up), q1 = __float2int_rn(v.y * up);
+            const int q2 = __float2int_rn(v.z * up), q3 = __float2int_rn(v.w * up);
+            *reinterpret_cast<uint2 *>(dst + 2 * part) =
+                make_uint2(((uint32_t)q0 & 0xffffu) | ((uint32_t)q1 << 16), ((uint32_t)q2 & 0xffffu) | ((uint32_t)q3 << 16));
+            if (part == 0) dst[16] = (uint32_t)(127 - sg) << 23;
+        }
+    }
+    __syncthreads();
+    if (ok && warp < SG_CONS) {
+        for (int j = warp; j < nloc; j += SG_CONS) {
+            const int s = j % A.nsb;
+            const int gc = c0 + j, la = gc / cpe - a0, r0 = (gc - (gc / cpe) * cpe) * SG_DN_ROWS;
+            if (!sg_wait_chunk(full, last, s, j, A.nsb)) {
+                ok = false;
+                break;
+            }
+            const SgExp &X = ex[la];
+            const uint8_t *st = ring + (size_t)s * A.stageb;
+            if (X.a.fmt == MOE_Q8_0) sg_down_chunk<MOE_Q8_0>(A, X, st, r0, hq, qbase);
+            else sg_down_chunk<MOE_MXFP4>(A, X, st, r0, hq, qbase);
+            __syncwarp();
+            if (lane == 0) *reinterpret_cast<volatile int *>(&used[s]) = j;
+        }
+    } else if (ok) {
+        ok = sg_produce(A.nsb, nloc, used, issue);
+    }
+    if (!ok && lane == 0) sg_flag(A.status, MOE_FLAG_WAIT_TIMEOUT);
+    __syncwarp();
+    __syncthreads();
+    if (tid == 0) sg_drain(full, last, A.nsb);
+}
+
+int optin_smem() {
+    static int cached[64] = {};
+    const int dev = current_device();
+    if (dev < 64 && cached[dev]) return cached[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    if (dev < 64) cached[dev] = v;
+    return v;
+}
+
+}  // namespace
+
+SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t down_formats, int64_t gu_stride, int64_t dn_stride) {
+    SgPlan p{};
+    p.ok = false;
+    const int G = sm_count(), optin = optin_smem();
+    if (G <= 0 || optin <= 0) return p;
+    if (T < 1 || T > SG_MAX_T || H % 64 != 0 || I % 32 != 0 || H % SG_DN_ROWS != 0) return p;
+    if ((down_formats & ~((1u << MOE_Q8_0) | (1u << MOE_MXFP4))) != 0) return p;
+    if (gu_stride <= 0 || dn_stride <= 0 || gu_stride % 16 != 0 || dn_stride % 16 != 0) return p;
+    const int P = T * k, nmax = std::min(P, E);
+    // experts one CTA's share can touch: an expert costs at least 2 per
+    // chunk, the whole list at most 2 P per chunk row, so a share holds at
+    // most P / G whole experts plus the two it starts and ends in
+    p.nexp = std::max(nmax, P) / G + 2;
+    // gate/up: each of the 15 consumer warps holds one slot while it
+    // computes, so the slots beyond 15 are the copies in flight: the largest chunk (4, 2 or 1
+    // row pairs) that gives at least 32 slots, else the largest with 24
+    const size_t fixed_a = sg_layout_a(T, H, E, 0, 0, p.nexp).total;
+    if ((size_t)optin <= fixed_a + 16) return p;
+    const size_t budget_a = (size_t)optin - fixed_a - 16;
+    for (int min_ns : {32, 24}) {
+        for (int cr : {4, 2, 1}) {
+            if (I % cr != 0) continue;
+            const size_t stage = (size_t)2 * cr * gu_stride;
+            const size_t ns = std::min<size_t>(SG_MAX_SLOTS, budget_a / stage) / SG_PL * SG_PL;
+            if (ns >= (size_t)min_ns) {
+                p.cr = cr;
+                p.stage = (int)stage;
+                p.ns = (int)ns;
+                break;
+            }
+        }
+        if (p.cr) break;
+    }
+    if (p.cr == 0) return p;
+    p.smem_a = sg_layout_a(T, H, E, p.ns, p.stage, p.nexp).total;
+    // down: 4 rows per chunk, at least 24 slots
+    p.nq = std::min(P, p.nexp * T + 2 * P / G + 1);   // pairs of the experts of one share
+    p.stageb = (int)(SG_DN_ROWS * dn_stride);
+    const size_t fixed_b = sg_layout_b(I, E, 0, 0, p.nq, p.nexp).total;
+    if ((size_t)optin <= fixed_b + 16) return p;
+    p.nsb = (int)(std::min<size_t>(SG_MAX_SLOTS, ((size_t)optin - fixed_b - 16) / p.stageb) / SG_PL * SG_PL);
+    if (p.nsb < 24) return p;
+    p.smem_b = sg_layout_b(I, E, p.nsb, p.stageb, p.nq, p.nexp).total;
+    p.ok = p.smem_a <= (size_t)optin && p.smem_b <= (size_t)optin;
+    return p;
+}
+
+cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, int k, int E, int H, int I,
+                               const int32_t *offsets, const int32_t *pairs, const int32_t *active, const uint16_t *x,
+                               float *h, float *y, uint32_t *status, cudaEvent_t const *events, cudaStream_t s) {
+    static bool attr_done[64] = {};
+    const int dev = current_device();
+    if (dev >= 64 || !attr_done[dev]) {
+        cudaError_t err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_gateup_kernel));
+        if (err == cudaSuccess) err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_down_kernel));
+        if (err != cudaSuccess) return err;
+        if (dev < 64) attr_done[dev] = true;
+    }
+    SgArgs A{};
+    A.table = table;
+    A.offsets = offsets;
+    A.pairs = pairs;
+    A.active = active;
+    A.x = x;
+    A.h = h;
+    A.y = y;
+    A.status = status;
+    A.T = T;
+    A.k = k;
+    A.H = H;
+    A.I = I;
+    A.E = E;
+    A.cr = p.cr;
+    A.ns = p.ns;
+    A.stage = p.stage;
+    A.nexp = p.nexp;
+    A.nsb = p.nsb;
+    A.stageb = p.stageb;
+    A.nq = p.nq;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(sm_count());
+    cfg.blockDim = dim3(SG_THREADS);
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t err;
+    if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
+    cfg.dynamicSmemBytes = p.smem_a;
+    err = cudaLaunchKernelEx(&cfg, sg_gateup_kernel, A);
+    if (err != cudaSuccess) return err;
+    // a profiling event between the kernels would serialise them; both are
+    // recorded after the down kernel
+    cfg.dynamicSmemBytes = p.smem_b;
+    err = cudaLaunchKernelEx(&cfg, sg_down_kernel, A);
+    if (err != cudaSuccess) return err;
+    if (events) {
+        if ((err = record_event(events[1], s)) != cudaSuccess) return err;
+        if ((err = record_event(events[2], s)) != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace moe

@@ -210,16 +210,21 @@ def test_zero_tokens(M):
 
 
 # --------------------------------------------------------------- full size
-def full_layer_parity(M, name, tokens_to_check=None, layer=0):
+def full_layer_parity(M, name, tokens_to_check=None, layer=0, paths=(None,)):
+    """AUTO (None) and any explicitly requested paths against one oracle result."""
     from synth import gpu as sgpu
     cfg = synth.CONFIGS[name]
     DL = sgpu.make_device_layer(cfg, layer)
     table = M.WeightTable(DL.experts, cfg.hidden, cfg.inter)
-    out = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k).cpu().numpy()
+    outs = {}
+    for path in paths:
+        opt = None if path is None else M.make_options(n_experts=cfg.n_experts, path=path)
+        outs[path] = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k, options=opt).cpu().numpy()
     lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
     tok = list(range(cfg.tokens)) if tokens_to_check is None else tokens_to_check
     ref = offn.moe_ffn(lazy, DL.x_host, DL.logits_host, cfg.k, tokens=tok, gate_formats=lazy.gate_formats())
-    assert_parity(out[tok], ref, name)
+    for path, out in outs.items():
+        assert_parity(out[tok], ref, f"{name} path {path}")
     del table, DL
     torch.cuda.empty_cache()
 
@@ -230,11 +235,11 @@ def test_full_decode1(M):
 
 
 def test_full_decode16(M):
-    full_layer_parity(M, "decode16", tokens_to_check=[0, 5, 15])
+    full_layer_parity(M, "decode16", tokens_to_check=[0, 5, 15], paths=(None, M.PATH_GEMV))
 
 
 def test_full_mtp6(M):
-    full_layer_parity(M, "mtp6")
+    full_layer_parity(M, "mtp6", paths=(None, M.PATH_GEMV))
 
 
 def test_full_prefill_sampled(M):
@@ -346,6 +351,22 @@ def test_gemv_path_small(M, tiers, T, H, I):
     opt = M.make_options(n_experts=cfg.n_experts, path=M.PATH_GEMV)
     out, *_ = run_layer(M, L, options=opt)
     assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), f"gemv {tiers} T={T}")
+
+
+@pytest.mark.parametrize("tiers,T,H,I", [("q8_0", 2, 256, 64), ("q4k", 5, 512, 96), ("mixed", 16, 256, 64),
+                                         ("mixed", 6, 512, 160), ("q4k", 8, 4096, 64), ("q8_0", 16, 2048, 32),
+                                         ("mixed", 1, 1024, 32)])
+def test_stream_kernels_small(M, tiers, T, H, I):
+    """The streaming decode kernels of the GEMV path (up to 16 rows): chunks of
+    1, 2 and 4 row pairs, 1 and 2 column groups per lane, one-block rows,
+    every gate/up format and both down formats."""
+    cfg = synth.LayerConfig("sg", 16, 4, H, I, T, tiers, True, 700 + T + H + I)
+    L = synth.make_layer(cfg, 0)
+    opt = M.make_options(n_experts=cfg.n_experts, path=M.PATH_GEMV)
+    out, table, x, logits = run_layer(M, L, options=opt)
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), f"stream {tiers} T={T} H={H} I={I}")
+    again = M.ffn_forward(table, x, logits, cfg.k, options=opt)
+    assert np.array_equal(again.cpu().numpy(), out)
 
 
 def test_full_decode1_gemv_path(M):
