@@ -423,8 +423,12 @@ def run_ours(args, world, rank, local, cpu_proc):
     gu_bytes = float(np.mean(per_layer_gu_bytes)) + T * H * 2 + mean_pairs * I * 4
     dn_bytes = float(np.mean(per_layer_dn_bytes)) + mean_pairs * I * 4 + mean_pairs * H * 4
     path = M.ffn_path(tables[0], T, k, opts_plain)
-    gu_name, dn_name = (("tc_gemm_kernel<gate/up>", "tc_hprep_kernel + tc_gemm_kernel<down>")
-                        if path == M.PATH_TENSOR else ("gateup_gemv_kernel", "down_gemv_kernel"))
+    if path == M.PATH_TENSOR:
+        gu_name, dn_name = "tc_gemm_kernel<gate/up>", "tc_hprep_kernel + tc_gemm_kernel<down>"
+    elif M.gemv_kernels(tables[0], T, k) == M.GEMV_STREAMING:
+        gu_name, dn_name = "sg_gateup_kernel", "sg_down_kernel"
+    else:
+        gu_name, dn_name = "gateup_gemv_kernel", "down_gemv_kernel"
     if path == M.PATH_TENSOR:
         # the h conversion runs between the two timing events of the down projection
         dn_bytes += mean_pairs * I * 2

@@ -220,6 +220,16 @@ size_t moe_ffn_workspace_size_for_path(const moe_weight_table *W, int32_t T, int
  * requested path cannot run this layer. Host-only. */
 int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_options *opt);
 
+/* Which kernels the grouped GEMV path (MOE_PATH_GEMV) runs for these
+ * arguments: MOE_GEMV_STREAMING (persistent gate/up and down kernels that
+ * stream the routed experts' rows through a shared-memory ring; decode
+ * batches of 1..16 rows with Q8_0 or MXFP4 down and an activation pointer
+ * aligned to 16 bytes at the forward) or MOE_GEMV_TILED (one CTA per expert
+ * tile; any other layer). -1 if the arguments are invalid. Host-only. */
+#define MOE_GEMV_TILED 0
+#define MOE_GEMV_STREAMING 1
+int moe_ffn_gemv_kernels(const moe_weight_table *W, int32_t T, int32_t k);
+
 /* Zero a workspace (all ws_bytes, among them the status word and the fused
  * kernel's grid-barrier counter) once, before its first forward.
  * ws: device, at least moe_ffn_workspace_size bytes. */

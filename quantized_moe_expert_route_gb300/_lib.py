@@ -22,13 +22,14 @@ BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17}
 MOE_OK = 0
 MOE_TABLE_PREPARED = 0x4D4F4554
 PATH_AUTO, PATH_GEMV, PATH_TENSOR, PATH_FUSED = 0, 1, 2, 3
+GEMV_TILED, GEMV_STREAMING = 0, 1
 FLAG_NONFINITE_LOGIT, FLAG_BAD_ID, FLAG_DUPLICATE_ID, FLAG_WAIT_TIMEOUT = 1, 2, 4, 8
 
 EXPORTED = [
     "moe_strerror", "moe_last_cuda_error", "moe_table_device_bytes", "moe_table_prepare",
     "moe_route_topk", "moe_bucket", "moe_ffn_workspace_size", "moe_ffn_workspace_init",
     "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc",
-    "moe_ffn_path", "moe_ffn_workspace_size_for_path",
+    "moe_ffn_path", "moe_ffn_gemv_kernels", "moe_ffn_workspace_size_for_path",
 ]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -96,6 +97,8 @@ def load() -> ctypes.CDLL:
     L.moe_ffn_workspace_views.argtypes = [ctypes.POINTER(WeightTableC), i32, i32, vp, pp, pp, pp, pp, pp, pp]
     L.moe_ffn_path.argtypes = [ctypes.POINTER(WeightTableC), i32, i32, ctypes.POINTER(Options)]
     L.moe_ffn_path.restype = ctypes.c_int
+    L.moe_ffn_gemv_kernels.argtypes = [ctypes.POINTER(WeightTableC), i32, i32]
+    L.moe_ffn_gemv_kernels.restype = ctypes.c_int
     L.moe_ffn_forward_noalloc.argtypes = [ctypes.POINTER(WeightTableC), vp, vp, i32, i32, ctypes.POINTER(Options),
                                           vp, vp]
     for name in ("moe_table_prepare", "moe_route_topk", "moe_bucket", "moe_ffn_workspace_init",
@@ -235,6 +238,11 @@ def ffn_path(table: "WeightTable", T: int, k: int, options: Optional[Options] = 
     """The path moe_ffn_forward takes (PATH_GEMV / PATH_TENSOR / PATH_FUSED), -1 if none."""
     opt = ctypes.byref(options) if options is not None else None
     return load().moe_ffn_path(ctypes.byref(table.c), T, k, opt)
+
+
+def gemv_kernels(table: "WeightTable", T: int, k: int) -> int:
+    """GEMV_STREAMING or GEMV_TILED: the kernels the grouped GEMV path runs; -1 if invalid."""
+    return load().moe_ffn_gemv_kernels(ctypes.byref(table.c), T, k)
 
 
 def make_options(renormalize: bool = True, format_mask: int = 0xFFFFFFFF, expert_lo: int = 0,

@@ -79,12 +79,16 @@ int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
     const bool fused_ok = decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
                                                 W->down_formats, W->max_gateup_stride, W->max_down_stride);
     const bool tc_ok = W->tc_maps == 1 && tc_path_eligible(W->hidden, W->inter);
+    const bool stream_ok = stream_plan(T, k, W->n_experts, W->hidden, W->inter, W->down_formats,
+                                       W->max_gateup_stride, W->max_down_stride).ok;
     switch (requested) {
         case MOE_PATH_AUTO:
-            // measured on GB300: the fused kernel where it applies, else the
-            // tensor path (16-row decode 225 us vs 700 us, 6-row mixed 152 vs
-            // 303, 2048-row prefill 1.2 ms vs 74 ms per layer), else GEMV
-            return fused_ok ? MOE_PATH_FUSED : tc_ok ? MOE_PATH_TENSOR : MOE_PATH_GEMV;
+            // measured on GB300 per layer: the fused kernel where it applies;
+            // else the streaming GEMV kernels for decode batches (16-row
+            // decode 144 us vs 225 us on the tensor path, 6-row mixed tiers
+            // 123 vs 151); else the tensor path (2048-row prefill 1.2 ms vs
+            // 74 ms with the tiled GEMV kernels); else GEMV
+            return fused_ok ? MOE_PATH_FUSED : stream_ok ? MOE_PATH_GEMV : tc_ok ? MOE_PATH_TENSOR : MOE_PATH_GEMV;
         case MOE_PATH_GEMV: return MOE_PATH_GEMV;
         case MOE_PATH_TENSOR: return tc_ok ? MOE_PATH_TENSOR : -1;
         case MOE_PATH_FUSED: return fused_ok ? MOE_PATH_FUSED : -1;
@@ -317,6 +321,14 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
                                offsets, pairs, active, pos, wts, x, h, y, out, status, events, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     return MOE_OK;
+}
+
+int moe_ffn_gemv_kernels(const moe_weight_table *W, int32_t T, int32_t k) {
+    if (!W || W->prepared != MOE_TABLE_PREPARED || T < 0 || k <= 0 || k > W->n_experts) return -1;
+    return stream_plan(T > 0 ? T : 1, k, W->n_experts, W->hidden, W->inter, W->down_formats, W->max_gateup_stride,
+                       W->max_down_stride).ok
+               ? MOE_GEMV_STREAMING
+               : MOE_GEMV_TILED;
 }
 
 int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_options *opt) {

@@ -738,15 +738,13 @@ cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, i
     cfg.dynamicSmemBytes = p.smem_a;
     err = cudaLaunchKernelEx(&cfg, sg_gateup_kernel, A);
     if (err != cudaSuccess) return err;
-    // a profiling event between the kernels would serialise them; both are
-    // recorded after the down kernel
+    // with timing events the down kernel's early start (its prologue under
+    // the gate/up kernel's tail) is given up for a clean split
+    if (events && (err = record_event(events[1], s)) != cudaSuccess) return err;
     cfg.dynamicSmemBytes = p.smem_b;
     err = cudaLaunchKernelEx(&cfg, sg_down_kernel, A);
     if (err != cudaSuccess) return err;
-    if (events) {
-        if ((err = record_event(events[1], s)) != cudaSuccess) return err;
-        if ((err = record_event(events[2], s)) != cudaSuccess) return err;
-    }
+    if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
     return cudaSuccess;
 }
 

@@ -338,8 +338,10 @@ def test_fused_path_rejects_ineligible(M):
     with pytest.raises(M.MoeError) as ei:
         M.ffn_forward(table, x, logits, L.cfg.k, options=opt)
     assert ei.value.code == 8
-    # AUTO takes the tensor path for this shape (H % 128 == 0, I % 64 == 0)
-    assert M.ffn_path(table, 3, L.cfg.k) == M.PATH_TENSOR
+    # AUTO takes the streaming GEMV kernels for this decode batch
+    assert M.ffn_path(table, 3, L.cfg.k) == M.PATH_GEMV
+    assert M.gemv_kernels(table, 3, L.cfg.k) == M.GEMV_STREAMING
+    assert M.gemv_kernels(table, 17, L.cfg.k) == M.GEMV_TILED
 
 
 @pytest.mark.parametrize("tiers,T,H,I", [("q8_0", 1, 256, 64), ("q4k", 3, 256, 64), ("mixed", 7, 256, 64),
