@@ -131,11 +131,12 @@ typedef struct {
 } moe_weight_table;
 
 /* Paths for moe_options.path. */
-#define MOE_PATH_AUTO 0        /* FUSED where it applies, else TENSOR where it applies, else GEMV
-                                  (see moe_ffn_path) */
+#define MOE_PATH_AUTO 0        /* FUSED where it applies, else GEMV where its streaming kernels
+                                  apply (moe_ffn_gemv_kernels), else TENSOR where it applies,
+                                  else GEMV (see moe_ffn_path) */
 #define MOE_PATH_GEMV 1        /* grouped GEMV kernels (route, bucket, gate/up, down, combine); any layer */
 #define MOE_PATH_TENSOR 2      /* tcgen05 grouped GEMMs with TMEM-resident dequantised weights
-                                  (prefill chunks and multi-row decode):
+                                  (prefill chunks):
                                   H % 128 == 0, I % 64 == 0, any format mix. Each weight is
                                   represented in fp16, so it must lie within fp16 range
                                   (|w| <= 65504; quantized LLM weights are O(1)). */
