@@ -659,12 +659,15 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t down_formats, int
     // most P / G whole experts plus the two it starts and ends in
     p.nexp = std::max(nmax, P) / G + 2;
     // gate/up: each of the 15 consumer warps holds one slot while it
-    // computes, so the slots beyond 15 are the copies in flight: the largest chunk (4, 2 or 1
-    // row pairs) that gives at least 32 slots, else the largest with 24
+    // computes, so the slots beyond 15 are the copies in flight: the largest
+    // chunk (4, 2 or 1 row pairs) that gives at least 24 slots (the 6-row
+    // mixed-tier layer: 121 us with 2-pair chunks in 24 slots, 123 us with
+    // 1-pair chunks in 56)
     const size_t fixed_a = sg_layout_a(T, H, E, 0, 0, p.nexp).total;
     if ((size_t)optin <= fixed_a + 16) return p;
     const size_t budget_a = (size_t)optin - fixed_a - 16;
-    for (int min_ns : {32, 24}) {
+    {
+        const int min_ns = 24;
         for (int cr : {4, 2, 1}) {
             if (I % cr != 0) continue;
             const size_t stage = (size_t)2 * cr * gu_stride;
@@ -676,7 +679,6 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t down_formats, int
                 break;
             }
         }
-        if (p.cr) break;
     }
     if (p.cr == 0) return p;
     p.smem_a = sg_layout_a(T, H, E, p.ns, p.stage, p.nexp).total;
