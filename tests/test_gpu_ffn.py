@@ -407,3 +407,23 @@ def test_uniform_layout_matches_descriptor_table(M):
     lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
     ref = offn.moe_ffn(lazy, DL.x_host, DL.logits_host, cfg.k, gate_formats=lazy.gate_formats())
     assert_parity(a.cpu().numpy(), ref, "uniform layout")
+
+
+@pytest.mark.parametrize("tiers,T,path", [("q4k", 1, "FUSED"), ("mixed", 6, "GEMV"), ("mixed", 40, "TENSOR")])
+def test_timing_events_leave_results_unchanged(M, tiers, T, path):
+    """The profiling events (before gate/up, between gate/up and down, after
+    down) are recorded on every path and change nothing in the result."""
+    cfg = synth.LayerConfig("ev", 16, 4, 512, 128, T, tiers, True, 880 + T)
+    L = synth.make_layer(cfg, 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, cfg.hidden, cfg.inter)
+    p = getattr(M, "PATH_" + path)
+    assert M.ffn_path(table, T, cfg.k, M.make_options(n_experts=cfg.n_experts, path=p)) == p
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    plain = M.ffn_forward(table, x, logits, cfg.k, options=M.make_options(n_experts=cfg.n_experts, path=p))
+    timed = M.ffn_forward(table, x, logits, cfg.k,
+                          options=M.make_options(n_experts=cfg.n_experts, path=p, timing_events=ev))
+    torch.cuda.synchronize()
+    assert torch.equal(plain, timed)
+    assert ev[0].elapsed_time(ev[1]) >= 0.0 and ev[1].elapsed_time(ev[2]) >= 0.0
+    assert_parity(timed.cpu().numpy(), offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), f"events {path}")
