@@ -55,3 +55,8 @@ def test_host_validation_without_gpu(libs):
     assert route.moe_route_topk(None, 1, 2048, 4, 1, None, None, None, None) == 8
     route.moe_bucket.restype = ctypes.c_int
     assert route.moe_bucket(None, 1, 0, 4, 0, 4, None, None, None, None, None, None) == 1
+    # the path and GEMV-kernel queries refuse a missing table on the host
+    route.moe_ffn_path.restype = ctypes.c_int
+    assert route.moe_ffn_path(None, 1, 1, None) == -1
+    route.moe_ffn_gemv_kernels.restype = ctypes.c_int
+    assert route.moe_ffn_gemv_kernels(None, 1, 1) == -1
