@@ -8,18 +8,19 @@
 // 优化策略三) serves each expert in its own format. Here two persistent kernels
 // (one CTA per SM, 16 warps) stream the weights:
 //
-//   gate/up: the active experts' gate/up rows are split evenly over the CTAs
-//     in chunks of 1, 2 or 4 row pairs. Warp w < 15 consumes the CTA's
+//   gate/up: the active experts' gate/up rows, in chunks of 1, 2 or 4 row
+//     pairs, are split over the CTAs by cost (rows times the expert's tokens,
+//     plus the streaming), not by length. Warp w < 15 consumes the CTA's
 //     chunks w, w + 15, ... from a ring of shared-memory slots that TMA bulk
-//     copies fill; one thread of warp 15 refills each slot with the chunk NS
+//     copies fill; lanes 0-7 of warp 15 refill each slot with the chunk NS
 //     ahead as soon as the slot's chunk is consumed, so no CTA-wide barrier
 //     stands in the loop and no consumer waits on a copy it issued. A warp
 //     holds its slot while it computes, so the chunk size is chosen to leave
-//     about as many slots in flight (HBM latency x bandwidth per SM) as are
-//     being computed. For every row pair and every
-//     token of the chunk's expert the warp forms both dot products (lane =
-//     64-column group, int16 activations, dp2a on the codes) and writes
-//     h = silu(W_gate x) (W_up x) in fp32.
+//     slots in flight (HBM latency x bandwidth per SM) beyond those being
+//     computed. For every row pair and every token of the chunk's expert the
+//     warp forms both dot products (lane = 64-column group, int16
+//     activations, dp2a on the codes) and writes h = silu(W_gate x) (W_up x)
+//     in fp32.
 //   down: the active experts' down rows are split the same way in chunks of
 //     4 rows (8 lanes per row); each CTA first stages the h rows of the
 //     pairs of its experts as int16 with a power-of-two scale per 32-block,
