@@ -26,7 +26,8 @@ Modules:
     formats  block decoders (Q8_0, Q4_K, Q6_K, MXFP4) -> dense fp64 matrices
     router   softmax / top-k with the lower-index tie-break
     bucket   per-expert pair lists (counts, exclusive prefix sum, stable scatter)
-    ffn      the layer, plus an independent brute-force dense evaluation
+    ffn      the layer (pair by pair, and expert by expert with bounded memory for
+             full-size layers), plus an independent brute-force dense evaluation
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 against hand-built blocks, closed forms, library routines (scipy softmax, numpy

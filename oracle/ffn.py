@@ -97,6 +97,55 @@ def moe_ffn(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, renormalize
     return out
 
 
+def _expert_job(job):
+    """(experts, e, xr [n, H] fp64) -> y [n, H]: expert e on the rows xr."""
+    experts, e, xr = job
+    ex = experts[e]
+    Wg, Wu, Wd = dense(ex["gate"]), dense(ex["up"]), dense(ex["down"])
+    release = getattr(experts, "release", None)
+    if release is not None:
+        release(e)
+    return expert_forward(Wg, Wu, Wd, xr)[3]
+
+
+def moe_ffn_by_expert(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, renormalize: bool = True,
+                      expert_lo: int = 0, expert_hi: Optional[int] = None, format_mask: int = 0xFFFFFFFF,
+                      tokens: Optional[Sequence[int]] = None,
+                      gate_formats: Optional[Sequence[int]] = None, map_fn=map):
+    """The same layer output as ``moe_ffn``, evaluated one expert at a time:
+    every routed pair of the wanted tokens is grouped by its expert, each
+    expert's matrices are decoded once, applied to all of its rows, and
+    dropped, so memory stays at one expert's dense matrices (per worker)
+    whatever the layer size. The combine is the same ascending-slot sum.
+    ``map_fn`` maps the per-expert jobs (``map``, or a process pool's map; the
+    jobs carry ``experts`` and must then be picklable)."""
+    x = bf16_bits_to_f64(x_bf16)
+    T, H = x.shape
+    E = len(experts)
+    ids, w, _ = router.route_topk(logits, k, renormalize)
+    if gate_formats is None:
+        gate_formats = [experts[e]["gate"].fmt for e in range(E)]
+    _, _, pos, _, _ = bucket_mod.bucket(ids, E, expert_lo, expert_hi, format_mask, gate_formats)
+    tok = list(range(T)) if tokens is None else [int(t) for t in tokens]
+    by_expert: Dict[int, list] = {}
+    for t in sorted(set(tok)):
+        for j in range(k):
+            if pos[t * k + j] >= 0:
+                by_expert.setdefault(int(ids[t, j]), []).append((t, j))
+    order = sorted(by_expert)
+    jobs = [(experts, e, x[[t for t, _ in by_expert[e]]]) for e in order]
+    y = {}
+    for e, ye in zip(order, map_fn(_expert_job, jobs)):
+        for (t, j), row in zip(by_expert[e], ye):
+            y[(t, j)] = row
+    out = np.zeros((len(tok), H), dtype=np.float64)
+    for row, t in enumerate(tok):
+        for j in range(k):                      # ascending slot order
+            if (t, j) in y:
+                out[row] += w[t, j] * y[(t, j)]
+    return out
+
+
 def moe_ffn_bruteforce(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int,
                        renormalize: bool = True) -> np.ndarray:
     """Independent second evaluation for small layers: every expert on every

@@ -362,6 +362,16 @@ class LazyExperts:
     def gate_formats(self) -> List[int]:
         return [f[0] for f in self.fmts]
 
+    def release(self, e: int) -> None:
+        """Forget expert e's generated bytes (it is regenerated on next access)."""
+        self._cache.pop(int(e), None)
+
+    def __getstate__(self):
+        # pickled without the generated bytes (they are regenerated on access)
+        d = dict(self.__dict__)
+        d["_cache"] = {}
+        return d
+
 
 def expert_bytes(fmts: Tuple[int, int], hidden: int, inter: int) -> int:
     """Unpadded quantized bytes of one expert (gate + up + down)."""

@@ -152,3 +152,122 @@ def test_planted_transpose_fails_closed_form():
     out = ffn.moe_ffn(experts, bf16_bits(x), np.zeros((1, 1), np.float32), k=1)[0]
     np.testing.assert_allclose(out, right, rtol=1e-14)
     assert np.abs(out - wrong).max() > 1e-3
+
+
+# --------------------------------------------------------------- bf16 activations
+# bf16 bit patterns with their values written out by hand: sign, 8 exponent
+# bits (bias 127), 7 fraction bits.
+BF16_LITERALS = [
+    (0x3F80, 1.0),                          # 0 01111111 0000000
+    (0xC040, -3.0),                         # 1 10000000 1000000 = -1.5 * 2
+    (0x4049, 3.140625),                     # 0 10000000 1001001 = 2 * (1 + 73/128)
+    (0x3E80, 0.25),                         # 0 01111101 0000000
+    (0x0001, 2.0 ** -133),                  # smallest subnormal: 2^-126 * 2^-7
+    (0x0080, 2.0 ** -126),                  # smallest normal
+    (0x7F7F, (2.0 - 2.0 ** -7) * 2.0 ** 127),   # largest finite
+    (0x8000, -0.0),
+    (0x7F80, float("inf")),
+    (0xFF80, float("-inf")),
+]
+
+
+def test_bf16_bits_literal_values():
+    bits = np.array([b for b, _ in BF16_LITERALS], np.uint16)
+    got = ffn.bf16_bits_to_f64(bits)
+    for (b, v), g in zip(BF16_LITERALS, got):
+        assert g == v, (hex(b), g, v)
+        assert np.signbit(g) == np.signbit(v), hex(b)
+    nan = ffn.bf16_bits_to_f64(np.array([0x7FC0], np.uint16))[0]
+    assert np.isnan(nan)
+    # shape is kept: a [T, H] matrix of bits decodes element by element
+    m = ffn.bf16_bits_to_f64(bits[:4].reshape(2, 2))
+    assert m.shape == (2, 2) and m[1, 0] == 3.140625
+
+
+def test_bf16_planted_shift_fails():
+    """A decoder shifting by 15 instead of 16 must miss the literal values."""
+    def wrong(xb):
+        u = np.asarray(xb, dtype=np.uint16).astype(np.uint32) << np.uint32(15)
+        return u.view(np.float32).astype(np.float64)
+    bits = np.array([b for b, _ in BF16_LITERALS[:7]], np.uint16)
+    vals = np.array([v for _, v in BF16_LITERALS[:7]])
+    assert np.any(wrong(bits) != vals)
+    assert np.all(ffn.bf16_bits_to_f64(bits) == vals)
+
+
+# --------------------------------------------------------------- one-hot activations
+def _golden_block(name):
+    import os
+    from tests.test_oracle_formats import load_golden
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
+    return load_golden(here)
+
+
+def _scaled_rows(fmt, block, n_rows, scale_offsets):
+    """n_rows copies of a one-block row whose fp16 scales at scale_offsets are
+    multiplied by 2^(r % 4) (exact: the exponent field goes up by r % 4), so
+    row r's weights are the block's weights times 2^(r % 4)."""
+    stride = synth.padded_stride(fmt, 256)
+    data = np.zeros((n_rows, stride), np.uint8)
+    for r in range(n_rows):
+        b = block.copy()
+        for off in scale_offsets:
+            h = int(b[off]) | (int(b[off + 1]) << 8)
+            h += (r % 4) << 10
+            b[off], b[off + 1] = h & 0xFF, h >> 8
+        data[r, :b.shape[0]] = b
+    return MatrixBytes(fmt, n_rows, 256, stride, data.reshape(-1))
+
+
+@pytest.mark.parametrize("name,scale_offsets", [("q4_k_block.txt", (0, 2)), ("q6_k_block.txt", (208,))])
+def test_one_hot_x_gives_weight_column(name, scale_offsets):
+    """x = e_i (a one-hot bf16 row) through a layer of one expert: the gate
+    output is column i of W_gate, whose entries are the golden block's
+    hand-computed weight i times 2^(r % 4); with up = gate and a down matrix
+    that copies h_r to out_r (r < 32), out_r = silu(c_r) * c_r."""
+    fmt, block, expected = _golden_block(name)
+    I, H = 32, 256
+    G = _scaled_rows(fmt, block, I, scale_offsets)
+    D = np.zeros((H, I), np.int64)
+    D[np.arange(I), np.arange(I)] = 1
+    experts = [{"gate": G, "up": G, "down": q8_0_matrix(D)}]
+    for i, w_i in expected:
+        c = np.array([w_i * 2.0 ** (r % 4) for r in range(I)])
+        x = np.zeros((1, H), np.uint16)
+        x[0, i] = 0x3F80                                   # bf16 1.0
+        g, u, h, y = ffn.expert_forward(ffn.dense(G), ffn.dense(G), ffn.dense(experts[0]["down"]),
+                                        ffn.bf16_bits_to_f64(x))
+        np.testing.assert_array_equal(g[0], c)
+        out = ffn.moe_ffn(experts, x, np.zeros((1, 1), np.float32), k=1)[0]
+        with np.errstate(over="ignore"):                   # exp(-c) = inf for c << 0: silu -> -0
+            expect = c * c / (1.0 + np.exp(-c))
+        np.testing.assert_allclose(out[:I], expect, rtol=1e-14, atol=0)
+        assert np.all(out[I:] == 0)
+
+
+# --------------------------------------------------------------- expert-by-expert evaluation
+@pytest.mark.parametrize("kw", [{}, {"renormalize": False}, {"tokens": [4, 0, 2]},
+                                {"expert_lo": 3, "expert_hi": 11}, {"format_mask": 1 << synth.Q4_K}])
+def test_by_expert_matches_per_pair(kw):
+    L = small_layer(E=16, k=4, T=6, seed=9)
+    gf = [ex["gate"].fmt for ex in L.experts]
+    a = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, L.cfg.k, gate_formats=gf, **kw)
+    b = ffn.moe_ffn_by_expert(L.experts, L.x_bf16, L.logits, L.cfg.k, gate_formats=gf, **kw)
+    np.testing.assert_allclose(b, a, rtol=1e-12, atol=1e-12 * max(np.abs(a).max(), 1e-300))
+
+
+def test_by_expert_lazy_experts_and_pool():
+    """Lazily generated experts (released after use), mapped over a spawned
+    process pool, give the per-pair result."""
+    import multiprocessing as mp
+    cfg = synth.LayerConfig("t", 12, 3, 256, 64, 5, "mixed", True, 41)
+    L = synth.make_layer(cfg, 0, with_weights=False)
+    lazy = synth.LazyExperts(cfg, L.seed, L.fmts)
+    ref = ffn.moe_ffn(synth.make_layer(cfg, 0).experts, L.x_bf16, L.logits, cfg.k)
+    got = ffn.moe_ffn_by_expert(lazy, L.x_bf16, L.logits, cfg.k, gate_formats=lazy.gate_formats())
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert not lazy._cache                                # every expert was released
+    with mp.get_context("spawn").Pool(2) as pool:
+        got2 = ffn.moe_ffn_by_expert(lazy, L.x_bf16, L.logits, cfg.k, gate_formats=lazy.gate_formats(),
+                                     map_fn=pool.map)
+    np.testing.assert_array_equal(got2, got)
