@@ -258,7 +258,8 @@ int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, voi
                             int32_t **pos);
 
 /* Read and clear the device status flags of a workspace (moe_device_flags).
- * Synchronises `stream`. *status_out is a host pointer. */
+ * ws = NULL reads those of moe_ffn_forward_noalloc's scratch array on the
+ * current device. Synchronises `stream`. *status_out is a host pointer. */
 int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream);
 
 /* Size of the device scratch array that moe_ffn_forward_noalloc uses. */
@@ -272,16 +273,20 @@ int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream);
  * (4 MiB) inside this library, held by every GPU that loads the library until
  * the process exits; no workspace argument, and no allocation of any kind.
  * The source pages have no counterpart of this entry point.
- *   - Sizes: accepted when moe_ffn_workspace_size(W, T, k) <= 4 MiB (e.g. up to
- *     25 tokens at E = 512, k = 10, H = 2048, I = 640, where rows beyond the
- *     fused kernel's reach take the tensor path); larger sizes return
- *     MOE_ERR_UNSUPPORTED before anything is enqueued.
+ *   - Sizes: accepted when the workspace of the path the call takes
+ *     (moe_ffn_workspace_size_for_path with opt->path, AUTO by default) fits in
+ *     4 MiB: e.g. up to 25 tokens at E = 512, k = 10, H = 2048, I = 640, where
+ *     AUTO sends one token to the fused kernel and up to 16 rows to the
+ *     streaming GEMV kernels, and a requested tensor path up to about 20
+ *     tokens; larger sizes return MOE_ERR_UNSUPPORTED before anything is
+ *     enqueued.
  *   - The first call on a device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents:
  *     calls whose work overlaps on the GPU (different streams, or several host
  *     threads) race and corrupt each other's results; order them on one
- *     stream. Device status flags are cleared at each call and not reported.
+ *     stream. Device status flags accumulate in the array until read with
+ *     moe_ffn_read_status(NULL, ...).
  * Other arguments, errors and ownership as for moe_ffn_forward. */
 int moe_ffn_forward_noalloc(const moe_weight_table *W, const uint16_t *x, const float *logits, int32_t T,
                             int32_t k, const moe_options *opt, float *out, moe_stream_t stream);

@@ -307,3 +307,12 @@ def ffn_forward_noalloc(table: WeightTable, x_bf16: torch.Tensor, logits: torch.
     _check("moe_ffn_forward_noalloc", load().moe_ffn_forward_noalloc(
         ctypes.byref(table.c), _ptr(x_bits), _ptr(logits), T, k, opt, _ptr(out), _stream(stream)))
     return out
+
+
+def noalloc_read_status(stream=None) -> int:
+    """Read and clear the device status flags (FLAG_*) that calls of
+    ffn_forward_noalloc accumulated in the library's array on the current
+    device (moe_ffn_read_status with a NULL workspace). Synchronises."""
+    v = ctypes.c_uint32(0)
+    _check("moe_ffn_read_status", load().moe_ffn_read_status(None, ctypes.byref(v), _stream(stream)))
+    return v.value

@@ -35,6 +35,7 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
                            const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
                            const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
                            cudaStream_t s);
+int noalloc_scratch_address(void **out);
 }  // namespace moe
 
 using namespace moe;
@@ -354,7 +355,8 @@ int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, voi
 }
 
 int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream) {
-    if (!ws || !status_out) return MOE_ERR_INVALID_ARG;
+    if (!status_out) return MOE_ERR_INVALID_ARG;
+    if (!ws && noalloc_scratch_address(&ws) != 0) return MOE_ERR_CUDA;   // the noalloc entry point's array
     cudaError_t err = cudaMemcpyAsync(status_out, ws, sizeof(uint32_t), cudaMemcpyDeviceToHost, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     err = cudaMemsetAsync(ws, 0, sizeof(uint32_t), stream);

@@ -10,50 +10,59 @@
 // arrays, the SwiGLU intermediate and the per-pair down outputs) in a
 // file-scope device array of fixed size instead. The source pages have no
 // counterpart of this entry point; it is a property of this library only.
+#include <atomic>
+
 #include "moe_internal.cuh"
 
 namespace {
 
 // The scratch: every GPU that loads this library holds these bytes until the
-// process exits.
+// process exits. A static device array starts zeroed.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
 constexpr int MAX_DEVICES = 64;
-void *g_scratch_ptr[MAX_DEVICES] = {};
+std::atomic<void *> g_scratch_ptr[MAX_DEVICES];
+
+}  // namespace
+
+namespace moe {
 
 // Device address of the scratch on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device with that device current.
-int scratch_address(void **out) {
+// per device with that device current (threads that race on the first lookup
+// store the same value).
+int noalloc_scratch_address(void **out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return (int)err;
     if (dev < 0 || dev >= MAX_DEVICES) return (int)cudaErrorInvalidDevice;
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
+    void *p = g_scratch_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
         err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (err != cudaSuccess) return (int)err;
-        g_scratch_ptr[dev] = p;
+        g_scratch_ptr[dev].store(p, std::memory_order_release);
     }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return 0;
 }
 
-}  // namespace
+}  // namespace moe
 
 extern "C" int moe_ffn_forward_noalloc(const moe_weight_table *W, const uint16_t *x, const float *logits,
                                        int32_t T, int32_t k, const moe_options *opt, float *out,
                                        moe_stream_t stream) {
     if (!W) return MOE_ERR_INVALID_ARG;
-    const size_t need = moe_ffn_workspace_size(W, T, k);
-    if (need == 0) return MOE_ERR_INVALID_ARG;
+    if (opt && opt->struct_size != sizeof(moe_options)) return MOE_ERR_INVALID_ARG;
+    // sized for the path the forward will take (a requested tensor path needs
+    // more than AUTO's); 0 means invalid arguments or a path that cannot run
+    // the layer, which moe_ffn_forward rejects before enqueuing anything
+    const size_t need = moe_ffn_workspace_size_for_path(W, T, k, opt ? opt->path : MOE_PATH_AUTO);
     if (need > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
     void *scratch = nullptr;
-    if (scratch_address(&scratch) != 0) return MOE_ERR_CUDA;
-    // The array starts zeroed (a static device array). Each call clears the
-    // status word (offset 0); the fused kernel's grid-barrier counter (offset
-    // 8) only grows, its generation is count / gridDim. Every other region is
-    // written before it is read.
-    if (cudaMemsetAsync(scratch, 0, 8, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (moe::noalloc_scratch_address(&scratch) != 0) return MOE_ERR_CUDA;
+    // Offset 0 holds the device status flags (sticky until read with
+    // moe_ffn_read_status(NULL, ...)); offset 8 the fused kernel's grid-barrier
+    // counter, which only grows (its generation is count / gridDim, the same
+    // grid on every launch). Every other region is written before it is read.
     return moe_ffn_forward(W, x, logits, T, k, opt, out, scratch, MOE_NOALLOC_SCRATCH_BYTES, stream);
 }

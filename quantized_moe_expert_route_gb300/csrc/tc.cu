@@ -47,11 +47,7 @@ constexpr int TC_EVSLOTS = TC_ASTAGES / TC_AEV;
 constexpr int TC_BSTAGES = 3;                // B stages in shared memory
 constexpr int TC_BSTAGE_BYTES = 2 * TC_NCHUNK * 128;   // 32 KB: up to 4 A steps of <= 64 rows
 constexpr int TC_BOX_ROWS = 16;              // rows per activation TMA box
-#ifndef TC_DG_OVERRIDE
 constexpr int TC_DG = TC_KR / TC_KA;         // dequantising warpgroups
-#else
-constexpr int TC_DG = TC_DG_OVERRIDE;
-#endif
 constexpr int TC_PPG = (TC_KR / TC_KA) / TC_DG;   // 64-K pieces per group per raw stage
 constexpr int TC_DQ0 = 4;                    // warps 0-3 epilogue, 4..19 dequant
 constexpr int TC_PROD = TC_DQ0 + 4 * TC_DG;  // 20: weight producer (TMA)
