@@ -2,6 +2,9 @@
 device, compare with the oracle. Imported by test modules only."""
 from __future__ import annotations
 
+import contextlib
+import os
+
 import numpy as np
 import torch
 
@@ -53,3 +56,45 @@ def assert_parity(gpu: np.ndarray, ref: np.ndarray, what: str = ""):
         return
     assert rel <= REL_L2_TOL, f"{what}: rel-L2 {rel:.3e} > {REL_L2_TOL}"
     assert mx <= MAX_ABS_RMS_TOL * rms, f"{what}: max abs {mx:.3e} > {MAX_ABS_RMS_TOL} * rms {rms:.3e}"
+
+
+# ------------------------------------------------------------------ full-size oracle
+_ORACLE_CACHE = {}
+
+
+@contextlib.contextmanager
+def oracle_pool():
+    """A spawned process pool for the oracle's per-expert jobs (spawned, so it
+    is safe after CUDA work in this process), one BLAS thread per worker."""
+    import multiprocessing as mp
+    keys = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")
+    old = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ[k] = "1"
+    try:
+        pool = mp.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    try:
+        yield pool
+    finally:
+        pool.close()
+        pool.join()
+
+
+def oracle_full_layer(cfg: synth.LayerConfig, DL, tokens=None) -> np.ndarray:
+    """The oracle's output of a device-filled layer (synth.gpu.DeviceLayer) for
+    `tokens` (default: all), expert by expert over a process pool; cached per
+    (config, seed, tokens) for the session."""
+    from oracle import ffn as offn
+    key = (cfg.name, DL.seed, None if tokens is None else tuple(tokens))
+    if key not in _ORACLE_CACHE:
+        lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
+        with oracle_pool() as pool:
+            _ORACLE_CACHE[key] = offn.moe_ffn_by_expert(lazy, DL.x_host, DL.logits_host, cfg.k, tokens=tokens,
+                                                        gate_formats=lazy.gate_formats(), map_fn=pool.map)
+    return _ORACLE_CACHE[key]
