@@ -7,13 +7,18 @@ independent layers (different seeds, so the selected experts' weights stream
 from HBM rather than L2), replayed as one CUDA graph. Inputs are seeded
 synthetic data; the weights are written on the device by the seeded filler.
 
-Prints one JSON line. `value` is MoE-layer tokens/s (token-layers per second,
-i.e. T / per-layer time, summed over ranks); `e2e` is the same metric through
-the public API with pinned host buffers copied in and out every layer;
-`roofline` is the dominant kernel's algorithmic bytes per launch over its
-event-timed duration against the measured HBM copy bandwidth;
-`cpu_baseline` is the fp64 oracle on the host, single-threaded, on a bounded
-sample of the same workload.
+Prints one JSON line. The headline workload (``--config``, default the
+2048-token mixed-tier prefill chunk, the largest single-GPU configuration) is
+timed over exactly ``--steps`` steps. `value` is MoE-layer tokens/s
+(token-layers per second, i.e. T / per-layer time, summed over ranks); `e2e`
+is the same metric through the public API with pinned host buffers copied in
+and out every layer; `roofline` is the dominant kernel's algorithmic bytes
+per launch over its event-timed duration against the measured HBM copy
+bandwidth; `cpu_baseline` is the fp64 oracle on the host cores (all cores,
+and single-threaded in `cpu_baseline.single_thread`) on a bounded sample of
+the same workload. `per_config` carries the same measurements for the decode
+workloads (1-token, 16-row, 6-row mixed-tier), each timed for at least
+``--min-seconds``.
 
 --impl reference runs the oracle as the reference arm (there is no runnable
 reference implementation: the source pages ship no code).
@@ -46,10 +51,14 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--config", default="decode1", help="tiny|decode1|decode16|mtp6|prefill2048")
+    p.add_argument("--config", default="prefill2048", help="tiny|decode1|decode16|mtp6|prefill2048")
+    p.add_argument("--per-config", default="decode1,decode16,mtp6",
+                   help="comma-separated workloads measured after the headline ('none': skip)")
+    p.add_argument("--min-seconds", type=float, default=1.0, help="timed region of each per-config workload")
     p.add_argument("--layers", type=int, default=48)
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    p.add_argument("--cpu-budget", type=float, default=12.0,
+                   help="seconds of oracle work for each cpu_baseline leg (single thread, all cores)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--path", type=int, default=0, help="0 auto, 1 grouped GEMV, 2 tensor cores, 3 fused decode")
@@ -58,9 +67,13 @@ def parse_args(argv=None):
 
 # ----------------------------------------------------------------------------
 # oracle worker (host CPU baseline / reference arm); runs in a subprocess
-# started before any CUDA work, with BLAS limited to one thread
+# started before any CUDA work. mode "serial": the per-pair evaluation with
+# BLAS on one thread; mode "pool": the expert-by-expert evaluation over a
+# spawned process pool of every host core (one BLAS thread per worker).
 # ----------------------------------------------------------------------------
 def oracle_worker(spec: dict) -> dict:
+    import multiprocessing as mp
+
     import numpy as np
     import synth
     from oracle import ffn as offn
@@ -68,42 +81,78 @@ def oracle_worker(spec: dict) -> dict:
 
     cfg = synth.CONFIGS[spec["config"]]
     budget = float(spec["budget_s"])
-    pairs_per_sample = spec.get("pairs_per_sample")      # None: whole layers
-    # Untimed: inputs, routing and the routed experts' bytes (the oracle's
-    # input); timed: the oracle's arithmetic (decode + routed FFN).
-    t_work, token_layers, samples, layer = 0.0, 0.0, [], 0
-    while t_work < budget and layer < 1000:
+    n_tok = min(cfg.tokens, int(spec.get("tokens_per_sample") or cfg.tokens))
+    pool = mp.get_context("spawn").Pool(os.cpu_count() or 1) if spec["mode"] == "pool" else None
+    cores = (os.cpu_count() or 1) if pool else 1
+    # Untimed: the layer's inputs, routing and the routed experts' bytes (the
+    # oracle's input); timed: the oracle's arithmetic (decode + routed FFN).
+    t_work, token_layers, layer = 0.0, 0, 0
+    steps = []
+    n_samples = int(spec.get("samples") or 0)
+    while (t_work < budget if not n_samples else layer < n_samples) and layer < 1000:
         L = synth.make_layer(cfg, layer % 48, with_weights=False)
         lazy = synth.LazyExperts(cfg, L.seed, L.fmts)
-        ids, _, _ = orouter.route_topk(L.logits, cfg.k)
-        T = cfg.tokens
-        if pairs_per_sample is None:
-            toks = list(range(T))
+        # a different window of tokens per layer sample
+        t0_tok = (layer * 97) % max(1, cfg.tokens - n_tok + 1)
+        toks = list(range(t0_tok, t0_tok + n_tok))
+        if pool is None:
+            ids, _, _ = orouter.route_topk(L.logits, cfg.k)
+            for e in np.unique(ids[toks]):
+                lazy[int(e)]
+            t0 = time.perf_counter()
+            offn.moe_ffn(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks, gate_formats=lazy.gate_formats())
         else:
-            toks = list(range(min(T, max(1, pairs_per_sample // cfg.k))))
-        for e in np.unique(ids[toks]):
-            lazy[int(e)]
-        t0 = time.perf_counter()
-        offn.moe_ffn(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks, gate_formats=lazy.gate_formats())
+            t0 = time.perf_counter()
+            offn.moe_ffn_by_expert(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks,
+                                   gate_formats=lazy.gate_formats(), map_fn=pool.map)
         dt = time.perf_counter() - t0
+        steps.append(dt)
         t_work += dt
         token_layers += len(toks)
-        samples.append(dt)
         layer += 1
-    return {"value": token_layers / t_work, "token_layers": token_layers, "seconds": t_work,
-            "layers": layer, "tokens_per_layer": len(toks)}
+    if pool is not None:
+        pool.close()
+        pool.join()
+    return {"value": token_layers / t_work, "token_layers": token_layers, "seconds": t_work, "layers": layer,
+            "tokens_per_layer": n_tok, "cores": cores, "step_seconds": steps}
 
 
-def run_oracle_subprocess(spec: dict, threads: int = 1) -> dict:
+def run_oracle_subprocess(spec: dict) -> dict:
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
-        env[v] = str(threads)
+        env[v] = "1"
     env["MOE_BENCH_ORACLE_WORKER"] = json.dumps(spec)
     r = subprocess.run([sys.executable, os.path.abspath(__file__)], env=env, capture_output=True, text=True,
                        timeout=1800)
     if r.returncode != 0:
         raise RuntimeError(f"oracle worker failed: {r.stderr[-2000:]}")
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# tokens per oracle sample, a window of the layer's tokens: each token costs
+# about ten expert decodes (plus ~40 MFLOP of fp64 per pair), so one thread
+# takes 2 tokens per sample and the pool 48 (whole layers up to 16 rows)
+def oracle_sample_tokens(cfg, mode: str) -> int:
+    return min(cfg.tokens, 2 if mode == "serial" else 48)
+
+
+def cpu_baseline(config: str, budget: float) -> dict:
+    import synth
+    cfg = synth.CONFIGS[config]
+    legs = {}
+    for mode in ("pool", "serial"):
+        n_tok = oracle_sample_tokens(cfg, mode)
+        res = run_oracle_subprocess({"config": config, "budget_s": budget, "mode": mode,
+                                     "tokens_per_sample": n_tok})
+        what = ("expert by expert over a spawned pool, one BLAS thread per process" if mode == "pool"
+                else "pair by pair, BLAS limited to 1 thread")
+        legs[mode] = {"value": res["value"], "unit": UNIT, "cores": res["cores"], "kind": "oracle",
+                      "sample": f"{config}: {res['layers']} layer samples of {res['tokens_per_layer']} token(s) "
+                                f"(all their routed experts), {res['seconds']:.1f} s of fp64 oracle arithmetic, "
+                                f"{what}"}
+    line = dict(legs["pool"])
+    line["single_thread"] = legs["serial"]
+    return line
 
 
 # ----------------------------------------------------------------------------
@@ -246,39 +295,41 @@ def run_reference(args, world, rank):
         return None
     import synth
     cfg = synth.CONFIGS[args.config]
-    n_steps = args.steps + args.warmup
-    # each step: a bounded sample of (token, slot) pairs, sized so the whole
-    # run stays within ~150 s of oracle work
-    probe = run_oracle_subprocess({"config": args.config, "budget_s": 0.5, "pairs_per_sample": cfg.k})
-    per_pair = probe["seconds"] / max(probe["token_layers"] * cfg.k, 1)
-    pairs = int(max(cfg.k, min(cfg.tokens * cfg.k, 150.0 / n_steps / max(per_pair, 1e-6))))
-    res = run_oracle_subprocess({"config": args.config, "budget_s": 150.0 * args.steps / n_steps,
-                                 "pairs_per_sample": pairs})
-    sample = (f"{args.config}: {res['layers']} layer samples of {res['tokens_per_layer']} token(s) "
-              f"(x {cfg.k} experts), {res['seconds']:.1f} s of oracle arithmetic")
-    v = res["value"]
+    n_tok = cfg.tokens if cfg.tokens <= 16 else 16
+    res = run_oracle_subprocess({"config": args.config, "budget_s": 0.0, "mode": "pool",
+                                 "tokens_per_sample": n_tok, "samples": args.warmup + args.steps})
+    timed = res["step_seconds"][args.warmup:]
+    secs = sum(timed)
+    v = n_tok * len(timed) / secs
+    sample = (f"{args.config}: each step one layer sample of {n_tok} token(s) (all their routed experts), "
+              f"{len(timed)} timed steps after {args.warmup} warm-up, {secs:.1f} s of fp64 oracle arithmetic, "
+              f"expert by expert over a spawned pool of {res['cores']} processes")
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.config},
-            "cpu_baseline": {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(len(timed), 1) * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_name(cfg, getattr(args, "layers", 48))},
+            "cpu_baseline": {"value": v, "unit": UNIT, "cores": res["cores"], "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     return line
 
 
-def run_ours(args, world, rank, local, cpu_proc):
+def workload_name(cfg, NL: int) -> str:
+    return (f"{cfg.name}: E{cfg.n_experts} k{cfg.k} H{cfg.hidden} I{cfg.inter} T{cfg.tokens} ({cfg.tiers} tiers), "
+            f"{NL} stacked layers per step")
+
+
+def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=None):
+    """Build the workload's stacked layers, time `steps` steps (or as many as
+    fill `min_seconds`) of the CUDA graph, then the profiling and end-to-end
+    regions; returns the JSON fields of the workload. Frees its device memory."""
     import numpy as np
     import torch
 
     import synth
     from synth import gpu as sgpu
-    import __graft_entry__
-    __graft_entry__.build()
-    import quantized_moe_expert_route_gb300 as M
 
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    cfg = synth.CONFIGS[args.config]
+    cfg = synth.CONFIGS[name]
     T, E, k, H, I = cfg.tokens, cfg.n_experts, cfg.k, cfg.hidden, cfg.inter
     NL = args.layers
 
@@ -340,6 +391,14 @@ def run_ours(args, world, rank, local, cpu_proc):
     for _ in range(args.warmup):
         run(False)
     torch.cuda.synchronize()
+    if steps is None:
+        # as many steps as fill min_seconds, from the period of a few
+        t0 = time.perf_counter()
+        for _ in range(3):
+            run(False)
+        torch.cuda.synchronize()
+        per = (time.perf_counter() - t0) / 3
+        steps = max(3, int(min_seconds / max(per, 1e-6)) + 1)
 
     props = torch.cuda.get_device_properties(dev)
     gpu_id = str(getattr(props, "uuid", local))
@@ -355,7 +414,7 @@ def run_ours(args, world, rank, local, cpu_proc):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.mark_start()
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         run(False)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -363,19 +422,15 @@ def run_ours(args, world, rank, local, cpu_proc):
     barrier(world)
     elapsed = allreduce_max(e0.elapsed_time(e1) / 1e3, world)
 
-    # ---- timed region 2: same steps with event nodes around the mat-mul kernels
+    # ---- timed region 2: event nodes around the mat-mul kernels of every layer
     gu_ms, dn_ms = [], []
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    prof_steps = max(1, min(args.steps, 50))
+    prof_steps = max(1, min(steps, 20))
     for _ in range(prof_steps):
         run(True)
         stream.synchronize()
         for l in range(NL):
             gu_ms.append(ev[l][0].elapsed_time(ev[l][1]))
             dn_ms.append(ev[l][1].elapsed_time(ev[l][2]))
-    t1.record(stream)
-    torch.cuda.synchronize()
     clk = clocks.stop()
 
     # ---- e2e: public API with pinned host buffers, copies inside the region
@@ -384,25 +439,25 @@ def run_ours(args, world, rank, local, cpu_proc):
     out_pin = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in layers]
     x_dev = [torch.empty((T, H), dtype=torch.int16, device=dev) for _ in layers]
     lg_dev = [torch.empty((T, E), dtype=torch.float32, device=dev) for _ in layers]
-    n_e2e = max(1, min(args.e2e_steps, args.steps))
+    n_e2e = max(1, min(args.e2e_steps, steps))
+
+    def e2e_step():
+        for l in range(NL):
+            x_dev[l].copy_(x_pin[l], non_blocking=True)
+            lg_dev[l].copy_(lg_pin[l], non_blocking=True)
+            M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
+            out_pin[l].copy_(outs[l], non_blocking=True)
+
     with torch.cuda.stream(stream):
         for _ in range(2):
-            for l in range(NL):
-                x_dev[l].copy_(x_pin[l], non_blocking=True)
-                lg_dev[l].copy_(lg_pin[l], non_blocking=True)
-                M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
-                out_pin[l].copy_(outs[l], non_blocking=True)
+            e2e_step()
     stream.synchronize()
     barrier(world)
     h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         h0.record(stream)
         for _ in range(n_e2e):
-            for l in range(NL):
-                x_dev[l].copy_(x_pin[l], non_blocking=True)
-                lg_dev[l].copy_(lg_pin[l], non_blocking=True)
-                M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
-                out_pin[l].copy_(outs[l], non_blocking=True)
+            e2e_step()
         h1.record(stream)
     stream.synchronize()
     e2e_elapsed = allreduce_max(h0.elapsed_time(h1) / 1e3, world)
@@ -411,9 +466,9 @@ def run_ours(args, world, rank, local, cpu_proc):
     bad = sum(ws.read_status() for ws in wss)
 
     hbm_peak, peak_kind = measured_peaks()
-    token_layers = T * NL * args.steps * world
+    token_layers = T * NL * steps * world
     value = token_layers / elapsed
-    per_layer_s = elapsed / (args.steps * NL)
+    per_layer_s = elapsed / (steps * NL)
     mean_expert_bytes = float(np.mean(per_layer_expert_bytes))
     layer_bytes = mean_expert_bytes + io_bytes
     gu_avg, dn_avg = statistics.mean(gu_ms) / 1e3, statistics.mean(dn_ms) / 1e3
@@ -456,14 +511,9 @@ def run_ours(args, world, rank, local, cpu_proc):
         tensor_pipe = {"flops_per_layer": flops, "achieved_tflops": tf, "peak_tflops": pk["bf16_tflops"],
                        "frac": tf / pk["bf16_tflops"], "peak_kind": "measured bf16 dense burst",
                        "window": "gate/up GEMM + h conversion + down GEMM"}
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded SplitMix64 weights written on the device; bf16 N(0,1) activations; "
-                "Zipf-biased fp32 logits)",
-        "config": {"workload": f"{args.config}: E{E} k{k} H{H} I{I} T{T} ({cfg.tiers} tiers), "
-                               f"{NL} stacked layers per step",
+    res = {
+        "value": value, "steps": steps, "ms_per_step": elapsed / steps * 1e3,
+        "config": {"workload": workload_name(cfg, NL),
                    "tokens": T, "layers_per_step": NL, "graph": not args.no_graph,
                    "l2": f"inputs exceed L2: {NL} distinct layers, {NL * mean_expert_bytes / 1e9:.2f} GB of "
                          f"routed expert weights per step vs {props.L2_cache_size / 1e6:.0f} MB L2",
@@ -474,7 +524,7 @@ def run_ours(args, world, rank, local, cpu_proc):
                            "achieved": layer_bytes / per_layer_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
                            "frac": layer_bytes / per_layer_s / 1e9 / hbm_peak, "peak_kind": peak_kind},
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": kernel_traffic(kname, args.config),
+                     "frac": achieved / hbm_peak, "traffic": kernel_traffic(kname, name),
                      "bytes_per_launch": kbytes, "launch_us": kdur * 1e6, "peak_kind": peak_kind,
                      "launch_timing": ("timed-region period per launch" if path == M.PATH_FUSED
                                        else "event nodes around each kernel"),
@@ -483,13 +533,44 @@ def run_ours(args, world, rank, local, cpu_proc):
         "tensor_pipe": tensor_pipe,
         "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
-        "gpu_launches": KERNELS_PER_LAYER[path] * NL * args.steps,
+        "gpu_launches": KERNELS_PER_LAYER[path] * NL * steps,
         "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
                  M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
         "clocks": clk,
         "device_status_flags": bad,
-        "gpu": props.name,
     }
+    del graphs, layers, tables, wss, outs, x_pin, lg_pin, out_pin, x_dev, lg_dev
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import quantized_moe_expert_route_gb300 as M
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    head = measure_workload(M, args.config, args, world, rank, local, steps=args.steps)
+    line = {"metric": METRIC, "value": head.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64 weights written on the device; bf16 N(0,1) activations; "
+                    "Zipf-biased fp32 logits)"}
+    head.pop("steps")
+    line.update(head)
+    line["gpu"] = torch.cuda.get_device_properties(dev).name
+    others = [c for c in args.per_config.split(",") if c and c != "none" and c != args.config]
+    if world == 1 and others:
+        per = {}
+        for c in others:
+            r = measure_workload(M, c, args, world, rank, local, min_seconds=args.min_seconds)
+            r["timed_seconds"] = r["ms_per_step"] * r["steps"] / 1e3
+            per[c] = r
+        line["per_config"] = per
     return line
 
 
@@ -508,11 +589,8 @@ def main():
     # CPU baseline first (before any CUDA work in this process), rank 0, N = 1
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res = run_oracle_subprocess({"config": args.config, "budget_s": args.cpu_budget})
-        cpu = {"value": res["value"], "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{args.config}: {res['layers']} whole layers ({res['tokens_per_layer']} token(s) each), "
-                         f"{res['seconds']:.1f} s of fp64 oracle arithmetic, BLAS limited to 1 thread"}
-    line = run_ours(args, world, rank, local, None)
+        cpu = cpu_baseline(args.config, args.cpu_budget)
+    line = run_ours(args, world, rank, local)
     if rank == 0:
         line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
