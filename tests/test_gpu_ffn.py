@@ -220,7 +220,8 @@ def full_layer_parity(M, name, tokens_to_check=None, layer=0, paths=(None,)):
     outs = {}
     for path in paths:
         opt = None if path is None else M.make_options(n_experts=cfg.n_experts, path=path)
-        outs[path] = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k, options=opt).cpu().numpy()
+        ws = M.Workspace(table, cfg.tokens, cfg.k, path=path or 0)
+        outs[path] = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k, ws=ws, options=opt).cpu().numpy()
     tok = list(range(cfg.tokens)) if tokens_to_check is None else tokens_to_check
     ref = oracle_full_layer(cfg, DL, None if tokens_to_check is None else tok)
     for path, out in outs.items():
