@@ -157,23 +157,38 @@ __device__ __forceinline__ uint64_t global_ns() {
 // as the phase completes, so waiting warps do not spin on the issue slots.
 constexpr uint32_t TC_SUSPEND_NS = 20000;
 
-// Bounded parity wait (TC_WAIT_NS, or WAIT_LIMIT polls) that also gives up
-// once another role has aborted.
-__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
-    const uint32_t addr = smem_addr(bar);
+__device__ __forceinline__ bool try_wait_parity(uint32_t addr, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// The polling loop of a bounded parity wait (TC_WAIT_NS, or WAIT_LIMIT
+// polls) that also gives up once another role has aborted; `suspend` polls
+// with a suspend-time hint. Out of line: every role's waits share one copy of
+// the code, which keeps the kernel small enough for the instruction caches.
+__device__ __noinline__ bool tc_wait_slow(uint32_t addr, uint32_t parity, volatile int *abort_flag, bool suspend) {
     uint64_t t0 = 0;
+    const uint32_t check = suspend ? 15u : 1023u;
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         uint32_t done;
-        asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
-            : "=r"(done)
-            : "r"(addr), "r"(parity), "r"(TC_SUSPEND_NS)
-            : "memory");
+        if (suspend)
+            asm volatile(
+                "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
+                : "=r"(done)
+                : "r"(addr), "r"(parity), "r"(TC_SUSPEND_NS)
+                : "memory");
+        else
+            done = try_wait_parity(addr, parity);
         if (done) return true;
-        if ((i & 15u) == 15u) {
+        if ((i & check) == check) {
             if (*abort_flag) return false;
             const uint64_t now = global_ns();
-            if (i == 15u)
+            if (i == check)
                 t0 = now;
             else if (now - t0 > TC_WAIT_NS)
                 return false;
@@ -181,29 +196,17 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile
     }
     return false;
 }
+// Bounded parity wait for roles that may wait long (producers, dequantisers,
+// epilogue): polls with a suspend hint.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
+    const uint32_t addr = smem_addr(bar);
+    return try_wait_parity(addr, parity) || tc_wait_slow(addr, parity, abort_flag, true);
+}
 // The same without a suspend hint, for the MMA issuer: its waits are short and
 // on the critical path.
 __device__ __forceinline__ bool tc_spin(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     const uint32_t addr = smem_addr(bar);
-    uint64_t t0 = 0;
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-        uint32_t done;
-        asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-            : "=r"(done)
-            : "r"(addr), "r"(parity)
-            : "memory");
-        if (done) return true;
-        if ((i & 1023u) == 1023u) {
-            if (*abort_flag) return false;
-            const uint64_t now = global_ns();
-            if (i == 1023u)
-                t0 = now;
-            else if (now - t0 > TC_WAIT_NS)
-                return false;
-        }
-    }
-    return false;
+    return try_wait_parity(addr, parity) || tc_wait_slow(addr, parity, abort_flag, false);
 }
 
 __device__ __forceinline__ void tc_fail(volatile int *abort_flag, uint32_t *status) {
@@ -279,6 +282,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
 // Instruction descriptor, kind::f16: fp32 D, fp16 A and B, both K-major, M = 128.
 __host__ __device__ constexpr uint32_t idesc_f16(int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
+}
+
+// Hint: bring `bytes` (a multiple of 16) at `src` (16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
@@ -420,17 +428,32 @@ __device__ __forceinline__ void dq_q6k(uint32_t blk, int g, uint32_t (&r)[32]) {
 __device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t x) {
     return ((x & 0x00070007u) << 9) | ((x & 0x00080008u) << 12);
 }
-// The same pair for any scale byte, through fp32 (E8M0 255 is NaN).
-__device__ __forceinline__ uint32_t mxfp4_pair_slow(uint32_t x, uint32_t e) {
-    float v[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const uint32_t c = (x >> (16 * i)) & 0xf, ex = (c >> 1) & 3, mb = c & 1;
-        const float mag = ex == 0 ? 0.5f * (float)mb : ldexpf(1.0f + 0.5f * (float)mb, (int)ex - 1);
-        const float sc = e == 255 ? __int_as_float(0x7fc00000) : ldexpf(1.0f, (int)e - 127);
-        v[i] = ((c & 8) ? -mag : mag) * sc;
+// fp16 pair (2^k, 2^k) for -24 <= k <= 15 (subnormal below -14).
+__device__ __forceinline__ uint32_t pow2_half2(int k) {
+    const uint32_t h = k >= -14 ? (uint32_t)(k + 15) << 10 : 0x0200u >> (-15 - k);
+    return h * 0x10001u;
+}
+// The two fp16 factors SA, SB with (v * 2^-14) * SA * SB = v * 2^(e-127) for an
+// E2M1 value v, such that the first product is exact and only the second
+// rounds (one rounding in all): e in [99, 128] takes SA = 2^(e-113), SB = 1;
+// larger e takes SA = 2^15 and the rest in SB (results beyond fp16 range
+// overflow, as any weight outside it would); e < 99 gives |w| < 2^-26, which
+// rounds to 0; e = 255 (NaN in E8M0) gives NaN.
+__device__ __forceinline__ void mxfp4_scales(uint32_t e, uint32_t &SA, uint32_t &SB) {
+    const int k = (int)e - 113;
+    if (e == 255u) {
+        SA = 0x7e007e00u;
+        SB = 0x3c003c00u;
+    } else if (k > 15) {
+        SA = pow2_half2(15);
+        SB = pow2_half2(min(k - 15, 15));
+    } else if (k >= -14) {
+        SA = pow2_half2(k);
+        SB = 0x3c003c00u;
+    } else {
+        SA = 0u;
+        SB = 0x3c003c00u;
     }
-    return half2_bits(__float2half_rn(v[0]), __float2half_rn(v[1]));
 }
 // MXFP4: piece g = blocks 2g and 2g+1 of the stage (17 bytes each) at byte
 // 34g of `blk`; element i < 16 of a block is the low nibble of qs[i], element
@@ -448,13 +471,13 @@ __device__ __forceinline__ void dq_mxfp4(uint32_t blk, int g, uint32_t (&r)[32])
     }
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
-        const bool fast = e[b] >= 99 && e[b] <= 128;   // 2^(e-113) is a normal fp16
-        const uint32_t S2 = ((e[b] - 98u) << 10) * 0x10001u;
+        uint32_t SA, SB;
+        mxfp4_scales(e[b], SA, SB);
 #pragma unroll
         for (int jj = 0; jj < 16; ++jj) {
             const uint32_t t = prmt(qs[b][(jj & 7) >> 1], 0u, (jj & 1) ? 0x4342u : 0x4140u);
             const uint32_t x = (jj >= 8 ? (t >> 4) : t) & 0x000F000Fu;
-            r[16 * b + jj] = fast ? hmul2(e2m1_pair_bits(x), S2) : mxfp4_pair_slow(x, e[b]);
+            r[16 * b + jj] = hmul2(hmul2(e2m1_pair_bits(x), SA), SB);
         }
     }
 }
@@ -529,7 +552,7 @@ __device__ __forceinline__ void red_release_shared(uint32_t *p, uint32_t v) {
     asm volatile("red.release.cta.shared.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
 // Spin until the counter reaches `target` (wrapping compare); bounded like tc_spin.
-__device__ __forceinline__ bool counter_spin(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
+__device__ __noinline__ bool counter_spin_slow(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
     uint64_t t0 = 0;
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         if ((int32_t)(ld_acquire_shared(p) - target) >= 0) return true;
@@ -543,6 +566,9 @@ __device__ __forceinline__ bool counter_spin(const uint32_t *p, uint32_t target,
         }
     }
     return false;
+}
+__device__ __forceinline__ bool counter_spin(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
+    return (int32_t)(ld_acquire_shared(p) - target) >= 0 || counter_spin_slow(p, target, abort_flag);
 }
 
 template <bool GATEUP>
@@ -602,14 +628,29 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const int G = gridDim.x;
 
     if (warp == TC_PROD) {
-        // ---- weight producer: per raw stage one 2-D TMA box per matrix (two for Q8_0)
+        // ---- weight producer: per raw stage one 2-D TMA box per matrix (two for Q8_0).
+        // A unit's weight rows are contiguous in memory (R rows of each matrix),
+        // while a raw stage takes a 256-wide K slice of every row: the rows are
+        // prefetched into L2 as whole contiguous blocks one unit ahead, so DRAM
+        // streams them sequentially and the boxes are served from L2.
         if (lane == 0) {
             uint32_t rg = 0;
             bool ok = true;
+            auto prefetch_unit = [&](const Unit &x) {
+                const DevExpert &ex = A.table[x.e];
+                const DevMatrix &m0 = GATEUP ? ex.gate : ex.down;
+                const uint32_t bytes = (uint32_t)(R * m0.stride);
+                prefetch_l2(m0.data + (size_t)R * x.s * m0.stride, bytes);
+                if (GATEUP) prefetch_l2(ex.up.data + (size_t)R * x.s * ex.up.stride, (uint32_t)(R * ex.up.stride));
+            };
             Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, true) : Unit{};
+            if (blockIdx.x < n_units) prefetch_unit(nxt);
             for (int u = blockIdx.x; u < n_units && ok; u += G) {
                 const Unit cu = nxt;
-                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, true);
+                if (u + G < n_units) {
+                    nxt = load_unit<GATEUP>(A, u + G, true);
+                    prefetch_unit(nxt);
+                }
                 const int W = raw_w(cu.fmt), nbox = raw_nbox(cu.fmt);
                 const uint32_t bytes = (uint32_t)(NMAT * nbox * R * W);
                 const CUtensorMap *m0 = A.wmaps + 3 * cu.e + (GATEUP ? 0 : 2);
