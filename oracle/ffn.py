@@ -39,7 +39,9 @@ def silu(z: np.ndarray) -> np.ndarray:
 
 
 def dense(m) -> np.ndarray:
-    return formats.dequant_matrix(m.fmt, m.rows, m.cols, m.stride, m.data)
+    """A matrix (attributes fmt, rows, cols, stride, data; IQ3_XXS matrices also
+    carry their grid) -> fp64 [rows, cols]."""
+    return formats.dequant_matrix(m.fmt, m.rows, m.cols, m.stride, m.data, getattr(m, "grid", None))
 
 
 class DenseCache:

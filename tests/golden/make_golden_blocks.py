@@ -104,15 +104,126 @@ def mxfp4_block(e):
     return b, expected, rule
 
 
-def write(name, fmt, block, expected, rule):
+# The IQ4 codebook as the format defines it (value of code 0..15), typed in.
+IQ4 = [-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113]
+
+
+def iq4_nl_block():
+    # d = 0.5 (0x3800); qs[i] = i | ((15 - i) << 4): weight i has code i,
+    # weight 16+i has code 15-i. w = 0.5 * IQ4[code].
+    b = [0x00, 0x38] + [i | ((15 - i) << 4) for i in range(16)]
+    expected = [
+        (0, -63.5),    # code 0: 0.5 * -127
+        (7, -5.0),     # code 7: 0.5 * -10
+        (8, 0.5),      # code 8: 0.5 * 1
+        (15, 56.5),    # code 15: 0.5 * 113
+        (16, 56.5),    # high nibble of qs[0] = 15
+        (20, 19.0),    # high nibble of qs[4] = 11: 0.5 * 38
+        (31, -63.5),   # high nibble of qs[15] = 0
+    ]
+    rule = "d = 0.5; qs[i] = i | ((15 - i) << 4): weight i has code i, weight 16+i code 15-i"
+    return b, expected, rule
+
+
+def iq4_xs_block():
+    # d = 0.25 (0x3400). Sub-block scales ls = 32 33 31 40 0 63 16 48, i.e.
+    # ls - 32 = 0 1 -1 8 -32 31 -16 16.
+    #   scales_l (low nibbles, sub-block 2k in the low half of byte k):
+    #     [0x10, 0x8F, 0xF0, 0x00]   (32&15=0, 33&15=1 | 31&15=15, 40&15=8 | 0, 63&15=15 | 16&15=0, 48&15=0)
+    #   scales_h (bits 2b..2b+1 = ls_b >> 4): 2 2 1 2 0 3 1 3
+    #     = 2 + 2*4 + 1*16 + 2*64 + 0*256 + 3*1024 + 1*4096 + 3*16384 = 56474 = 0xDC9A -> bytes 9A DC
+    # qs[16b + j] = j | (((j + b) & 15) << 4): weight 32b+j has code j,
+    # weight 32b+16+j has code (j + b) & 15.
+    qs = [j | (((j + b) & 15) << 4) for b in range(8) for j in range(16)]
+    b = [0x00, 0x34, 0x9A, 0xDC, 0x10, 0x8F, 0xF0, 0x00] + qs
+    expected = [
+        (0, 0.0),        # b0: ls - 32 = 0
+        (32, -31.75),    # b1 j0: 0.25 * 1 * IQ4[0] = -127/4
+        (48, -26.0),     # b1 high j0: code 1: 0.25 * 1 * -104
+        (69, 8.75),      # b2 j5: 0.25 * -1 * IQ4[5] = -0.25 * -35
+        (111, 226.0),    # b3 j15: 0.25 * 8 * 113
+        (114, -70.0),    # b3 high j2: code 5: 2 * -35
+        (137, -104.0),   # b4 j9: 0.25 * -32 * 13
+        (186, 875.75),   # b5 high j10: code 15: 0.25 * 31 * 113
+        (195, 260.0),    # b6 j3: 0.25 * -16 * -65
+        (255, -88.0),    # b7 high j15: code (15 + 7) & 15 = 6: 0.25 * 16 * -22
+    ]
+    rule = ("d = 0.25; ls = 32 33 31 40 0 63 16 48; qs[16b+j] = j | (((j + b) & 15) << 4)")
+    return b, expected, rule
+
+
+def iq3_grid():
+    # A test grid (the format's own grid is an input of the decoder): byte 0 of
+    # entry i is 4 + 8 * (i & 7), byte 1 is 4 + 8 * ((i >> 3) & 7), byte 2 is
+    # 4 + 8 * ((i >> 6) & 3), byte 3 is 62.
+    return [(4 + 8 * (i & 7)) | ((4 + 8 * ((i >> 3) & 7)) << 8) | ((4 + 8 * ((i >> 6) & 3)) << 16) | (62 << 24)
+            for i in range(256)]
+
+
+def iq3_xxs_block():
+    # d = 1.0 (0x3C00). Grid indices q[k] = (37 k + 5) & 255. Sub-block b's
+    # word: sign indices s_l = (5 (4b + l)) & 127 in bits 7l.., scale 2b in
+    # bits 28..31, so its scale is (0.5 + 2b) / 2 = 0.25 + b.
+    q = [(37 * k + 5) & 255 for k in range(64)]
+    words = []
+    for blk in range(8):
+        a = (2 * blk) << 28
+        for l in range(4):
+            a |= ((5 * (4 * blk + l)) & 127) << (7 * l)
+        words += [a & 255, (a >> 8) & 255, (a >> 16) & 255, (a >> 24) & 255]
+    b = [0x00, 0x3C] + q + words
+    expected = [
+        # b0 (scale 0.25), group 0: sign index 0 -> all positive; q0 = 5, q1 = 42
+        (0, 11.0),     # grid[5] byte 0 = 4 + 8*5 = 44
+        (1, 1.0),      # grid[5] byte 1 = 4
+        (3, 15.5),     # byte 3 = 62
+        (4, 5.0),      # grid[42] byte 0 = 4 + 8*2 = 20
+        (5, 11.0),     # grid[42] byte 1 = 4 + 8*5 = 44
+        # b0 group 1: sign index 5 = 0b101 (two bits, even): weights 0 and 2 negative; q2 = 79
+        (8, -15.0),    # grid[79] byte 0 = 4 + 8*7 = 60
+        (9, 3.0),      # byte 1 = 4 + 8*1 = 12
+        (10, -3.0),    # byte 2 = 4 + 8*1 = 12, negative
+        (11, 15.5),
+        # b0 group 3: sign index 15 (four bits, even): weights 0-3 negative; q7 = 8 (weights 4-7)
+        (28, 1.0),     # grid[8] byte 0 = 4
+        (29, 3.0),     # grid[8] byte 1 = 12
+        # b1 (scale 1.25), group 0: sign index 20 = 0b10100: weights 2 and 4 negative; q8 = 45, q9 = 82
+        (32, 55.0),    # grid[45] byte 0 = 44
+        (34, -5.0),    # grid[45] byte 2 = 4, negative
+        (36, -25.0),   # grid[82] byte 0 = 20, negative
+        (37, 25.0),    # grid[82] byte 1 = 20
+        (38, 15.0),    # grid[82] byte 2 = 12
+        (39, 77.5),    # byte 3 = 62
+        # b1 group 1: sign index 25 = 0b11001 (three bits, odd): bit 7 set; weights 0, 3, 4, 7
+        # negative; q10 = 119, q11 = 156
+        (40, -75.0),   # grid[119] byte 0 = 60, negative
+        (41, 65.0),    # grid[119] byte 1 = 4 + 8*6 = 52
+        (43, -77.5),   # byte 3 = 62, negative
+        (44, -45.0),   # grid[156] byte 0 = 4 + 8*4 = 36, negative
+        (45, 35.0),    # grid[156] byte 1 = 4 + 8*3 = 28
+        (47, -77.5),   # byte 3 = 62, negative (the implied eighth sign)
+        # b7 (scale 7.25), group 0: sign index 140 & 127 = 12 = 0b1100: weights 2, 3 negative; q56 = 29
+        (224, 319.0),  # grid[29] byte 0 = 44
+        (226, -29.0),  # byte 2 = 4
+        (227, -449.5),  # byte 3 = 62
+    ]
+    rule = ("d = 1.0; q[k] = (37k + 5) & 255; sub-block b: sign indices (5(4b + l)) & 127, scale 2b; "
+            "grid entry i bytes 4+8(i&7), 4+8((i>>3)&7), 4+8((i>>6)&3), 62")
+    return b, expected, rule
+
+
+def write(name, fmt, block, expected, rule, grid=None):
     path = os.path.join(HERE, name)
     with open(path, "w") as f:
         f.write(f"# Hand-built {fmt} block. Construction: {rule}\n")
         f.write("# Expected weights hand-computed from the block layout (see make_golden_blocks.py).\n")
-        f.write("# Layout reading: GGUF block layouts (Q8_0/Q4_K/Q6_K), OCP MX v1.0 (MXFP4); format names from\n")
-        f.write("# '三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南', 优化策略二.\n")
+        f.write("# Layout reading: GGUF block layouts (Q8_0/Q4_K/Q6_K/IQ4_NL/IQ4_XS/IQ3_XXS), OCP MX v1.0\n")
+        f.write("# (MXFP4); format names from '三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南',\n")
+        f.write("# 优化策略二.\n")
         f.write(f"format {fmt}\n")
         f.write("bytes " + " ".join(f"{x:02x}" for x in block) + "\n")
+        if grid is not None:
+            f.write("grid " + " ".join(f"{x:08x}" for x in grid) + "\n")
         for i, v in expected:
             f.write(f"w {i} {v!r}\n")
 
@@ -124,3 +235,6 @@ if __name__ == "__main__":
     write("q6_k_block.txt", "Q6_K", *q6_k_block())
     write("mxfp4_e127_block.txt", "MXFP4", *mxfp4_block(127))
     write("mxfp4_e128_block.txt", "MXFP4", *mxfp4_block(128))
+    write("iq4_nl_block.txt", "IQ4_NL", *iq4_nl_block())
+    write("iq4_xs_block.txt", "IQ4_XS", *iq4_xs_block())
+    write("iq3_xxs_block.txt", "IQ3_XXS", *iq3_xxs_block(), grid=iq3_grid())

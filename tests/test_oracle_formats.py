@@ -16,11 +16,12 @@ import pytest
 
 from oracle import formats
 
-FMT = {"Q8_0": formats.Q8_0, "Q4_K": formats.Q4_K, "Q6_K": formats.Q6_K, "MXFP4": formats.MXFP4}
+FMT = {"Q8_0": formats.Q8_0, "Q4_K": formats.Q4_K, "Q6_K": formats.Q6_K, "MXFP4": formats.MXFP4,
+       "IQ4_NL": formats.IQ4_NL, "IQ4_XS": formats.IQ4_XS, "IQ3_XXS": formats.IQ3_XXS}
 
 
-def load_golden(path):
-    fmt, data, exp = None, None, []
+def load_golden(path, with_grid=False):
+    fmt, data, exp, grid = None, None, [], None
     with open(path) as f:
         for line in f:
             if line.startswith("#") or not line.strip():
@@ -30,22 +31,24 @@ def load_golden(path):
                 fmt = FMT[p[1]]
             elif p[0] == "bytes":
                 data = np.array([int(x, 16) for x in p[1:]], dtype=np.uint8)
+            elif p[0] == "grid":
+                grid = np.array([int(x, 16) for x in p[1:]], dtype=np.int64)
             elif p[0] == "w":
                 exp.append((int(p[1]), float(p[2])))
-    return fmt, data, exp
+    return (fmt, data, exp, grid) if with_grid else (fmt, data, exp)
 
 
 def golden_files(golden_dir):
     files = sorted(glob.glob(os.path.join(golden_dir, "*_block.txt")))
-    assert len(files) >= 6
+    assert len(files) >= 9
     return files
 
 
 def check_golden(decoders, golden_dir):
     for path in golden_files(golden_dir):
-        fmt, data, exp = load_golden(path)
+        fmt, data, exp, grid = load_golden(path, with_grid=True)
         assert data.shape[0] == formats.BLOCK_BYTES[fmt]
-        w = decoders[fmt](data[None, :])[0]
+        w = decoders[fmt](data[None, :], grid)[0] if fmt == formats.IQ3_XXS else decoders[fmt](data[None, :])[0]
         for i, v in exp:
             if w[i] != v:
                 return False, (os.path.basename(path), i, w[i], v)
@@ -142,6 +145,94 @@ def val_mxfp4(e, codes):
     return 2.0 ** (e - 127) * sign * mag[codes & 7]
 
 
+IQ4_VALUES = np.array([-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113], dtype=np.float64)
+
+
+def enc_iq4_nl(d, codes):
+    b = np.zeros(18, dtype=np.uint8)
+    b[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    b[2:18] = codes[:16] | (codes[16:] << 4)
+    return b
+
+
+def enc_iq4_xs(d, ls, codes):
+    """ls int [8] (0..63); codes int [256] (0..15)."""
+    b = np.zeros(136, dtype=np.uint8)
+    b[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    sh = 0
+    for j in range(8):
+        sh |= (int(ls[j]) >> 4) << (2 * j)
+        b[4 + j // 2] |= (int(ls[j]) & 15) << (4 * (j % 2))
+    b[2], b[3] = sh & 255, sh >> 8
+    for j in range(8):
+        for i in range(16):
+            b[8 + 16 * j + i] = codes[32 * j + i] | (codes[32 * j + 16 + i] << 4)
+    return b
+
+
+def enc_iq3_xxs(d, q, signs7, scales4):
+    """q int [64] grid indices; signs7 int [8, 4] (0..127); scales4 int [8] (0..15)."""
+    b = np.zeros(98, dtype=np.uint8)
+    b[0:2] = np.frombuffer(np.float16(d).tobytes(), np.uint8)
+    b[2:66] = q
+    for j in range(8):
+        a = int(scales4[j]) << 28
+        for l in range(4):
+            a |= int(signs7[j, l]) << (7 * l)
+        b[66 + 4 * j: 70 + 4 * j] = np.frombuffer(np.uint32(a).tobytes(), np.uint8)
+    return b
+
+
+def val_iq3_xxs(d, q, signs7, scales4, grid):
+    d = float(np.float16(d))
+    out = np.zeros(256)
+    for j in range(8):
+        sc = d * (0.5 + scales4[j]) / 2
+        for l in range(4):
+            s = int(signs7[j, l])
+            sbits = s | ((bin(s).count("1") & 1) << 7)
+            for t in range(8):
+                entry = int(grid[q[8 * j + 2 * l + t // 4]])
+                mag = (entry >> (8 * (t % 4))) & 255
+                out[32 * j + 8 * l + t] = sc * mag * (-1.0 if (sbits >> t) & 1 else 1.0)
+    return out
+
+
+def test_iq4_roundtrips():
+    rng = np.random.default_rng(6)
+    for _ in range(20):
+        codes = rng.integers(0, 16, 32)
+        d = rng.uniform(1e-3, 1.0)
+        np.testing.assert_array_equal(formats.dequant_iq4_nl(enc_iq4_nl(d, codes)[None])[0],
+                                      float(np.float16(d)) * IQ4_VALUES[codes])
+        ls = rng.integers(0, 64, 8)
+        codes = rng.integers(0, 16, 256)
+        w = formats.dequant_iq4_xs(enc_iq4_xs(d, ls, codes)[None])[0]
+        np.testing.assert_array_equal(w, float(np.float16(d)) * (ls[np.arange(256) // 32] - 32) * IQ4_VALUES[codes])
+
+
+def test_iq3_xxs_roundtrip():
+    rng = np.random.default_rng(7)
+    for _ in range(10):
+        grid = rng.integers(0, 2 ** 32, 256, dtype=np.int64)
+        q = rng.integers(0, 256, 64)
+        signs7 = rng.integers(0, 128, (8, 4))
+        scales4 = rng.integers(0, 16, 8)
+        d = rng.uniform(1e-3, 1.0)
+        w = formats.dequant_iq3_xxs(enc_iq3_xxs(d, q, signs7, scales4)[None], grid)[0]
+        np.testing.assert_array_equal(w, val_iq3_xxs(d, q, signs7, scales4, grid))
+    # the eighth sign is implied: every group has an even number of negative weights
+    grid = np.full(256, 0x01010101, dtype=np.int64)
+    blk = enc_iq3_xxs(1.0, rng.integers(0, 256, 64), rng.integers(0, 128, (8, 4)), np.zeros(8, np.int64))
+    w = formats.dequant_iq3_xxs(blk[None], grid)[0].reshape(32, 8)
+    assert np.all((w < 0).sum(axis=1) % 2 == 0)
+
+
+def test_iq3_xxs_needs_its_grid():
+    with pytest.raises(ValueError):
+        formats.decode_blocks(formats.IQ3_XXS, np.zeros((1, 98), np.uint8))
+
+
 def test_q4_k_roundtrip():
     rng = np.random.default_rng(2)
     for _ in range(20):
@@ -222,7 +313,46 @@ def _q8_0_wrong_offset(blk):
     return d[..., None] * q
 
 
+def _iq4_nl_linear(blk):
+    # a linear 4-bit code (q - 8) * 16 instead of the codebook
+    d = formats._f16(blk[..., 0:2])
+    qs = blk[..., 2:18].astype(np.int64)
+    codes = np.concatenate([qs & 15, qs >> 4], axis=-1)
+    return d[..., None] * (codes - 8) * 16.0
+
+
+def _iq4_xs_unsigned_scale(blk):
+    # the sub-block scale d * ls instead of d * (ls - 32)
+    d = formats._f16(blk[..., 0:2])
+    ls = formats.iq4_xs_scales(blk)
+    qs = blk[..., 8:136].astype(np.int64)
+    out = np.empty(blk.shape[:-1] + (256,))
+    for b in range(8):
+        byte = qs[..., 16 * b: 16 * b + 16]
+        scale = (d * ls[..., b])[..., None]
+        out[..., 32 * b: 32 * b + 16] = scale * formats.IQ4_CODEBOOK[byte & 15]
+        out[..., 32 * b + 16: 32 * b + 32] = scale * formats.IQ4_CODEBOOK[byte >> 4]
+    return out
+
+
+def _iq3_xxs_no_parity(blk, grid):
+    # the eighth sign of each group taken as positive instead of from the parity
+    w = formats.dequant_iq3_xxs(blk, grid).copy()
+    g = w.reshape(w.shape[:-1] + (32, 8))
+    g[..., 7] = np.abs(g[..., 7])
+    return g.reshape(w.shape)
+
+
+def _iq3_xxs_scale_half(blk, grid):
+    # scale d * (0.5 + s) without the final halving
+    return 2 * formats.dequant_iq3_xxs(blk, grid)
+
+
 @pytest.mark.parametrize("fmt,bad", [
+    (formats.IQ4_NL, _iq4_nl_linear),
+    (formats.IQ4_XS, _iq4_xs_unsigned_scale),
+    (formats.IQ3_XXS, _iq3_xxs_no_parity),
+    (formats.IQ3_XXS, _iq3_xxs_scale_half),
     (formats.Q4_K, _q4_k_no_min),
     (formats.Q4_K, _q4_k_swapped_nibbles),
     (formats.Q6_K, _q6_k_scale_per_32),
