@@ -67,15 +67,34 @@ typedef enum {
 } moe_device_flags;
 
 /* Weight block formats (little-endian; fp16 = IEEE binary16).
- *  Q8_0  : 34 B / 32 weights : fp16 d, int8 q[32];                 w = d*q
- *  Q4_K  : 144 B / 256       : fp16 d, fp16 dmin, 12 B packed 6-bit
- *                              (scale, min) x 8, 128 B 4-bit codes; w = d*sc*q - dmin*m
- *  Q6_K  : 210 B / 256       : 128 B low nibbles, 64 B high 2-bit pairs,
- *                              int8 scale x 16, fp16 d (last);      w = d*scale*(q - 32)
- *  MXFP4 : 17 B / 32         : E8M0 scale e, 16 B E2M1 codes;       w = 2^(e-127) * E2M1
- * These are the public GGUF layouts (Q8_0, Q4_K, Q6_K) and the OCP MX v1.0
- * encoding (MXFP4); the pages name the formats but print no layout. */
-typedef enum { MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_Q6_K = 3, MOE_MXFP4 = 4 } moe_format;
+ *  Q8_0    : 34 B / 32 weights : fp16 d, int8 q[32];                 w = d*q
+ *  Q4_K    : 144 B / 256       : fp16 d, fp16 dmin, 12 B packed 6-bit
+ *                                (scale, min) x 8, 128 B 4-bit codes; w = d*sc*q - dmin*m
+ *  Q6_K    : 210 B / 256       : 128 B low nibbles, 64 B high 2-bit pairs,
+ *                                int8 scale x 16, fp16 d (last);      w = d*scale*(q - 32)
+ *  MXFP4   : 17 B / 32         : E8M0 scale e, 16 B E2M1 codes;       w = 2^(e-127) * E2M1
+ *  IQ4_NL  : 18 B / 32         : fp16 d, 16 B 4-bit codes (low nibbles = weights 0..15);
+ *                                w = d * NL[code], NL = -127 -104 -83 -65 -49 -35 -22 -10
+ *                                1 13 25 38 53 69 89 113
+ *  IQ4_XS  : 136 B / 256       : fp16 d, uint16 high scale bits, 4 B low scale
+ *                                nibbles, 128 B codes; sub-block b of 32:
+ *                                w = d * (ls_b - 32) * NL[code]
+ *  IQ3_XXS : 98 B / 256        : fp16 d, 64 B grid indices, 8 x uint32 (4-bit
+ *                                scale s, four 7-bit sign indices) per
+ *                                sub-block of 32; w = d * (0.5 + s) / 2 *
+ *                                magnitude from the grid * sign (the eighth
+ *                                sign of a group of 8 is its parity)
+ * These are the public GGUF layouts (Q8_0, Q4_K, Q6_K, IQ4_NL, IQ4_XS, IQ3_XXS)
+ * and the OCP MX v1.0 encoding (MXFP4); the pages name the formats (the tiers
+ * of "三张 RTX 3090 …", section 优化策略二: Q6_K/Q8_0, IQ4_XS/IQ4_NL,
+ * IQ3_XXS/MXFP4) but print no layout. IQ3_XXS needs the 256-entry grid of
+ * four magnitude bytes per entry that its model file was made with, passed in
+ * moe_weight_table.iq3_grid. IQ formats run on the tensor-core and the tiled
+ * grouped GEMV paths. */
+typedef enum {
+    MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_Q6_K = 3, MOE_MXFP4 = 4,
+    MOE_IQ4_NL = 5, MOE_IQ4_XS = 6, MOE_IQ3_XXS = 7
+} moe_format;
 
 /* Limits of this build. */
 #define MOE_MAX_EXPERTS 1024
@@ -128,6 +147,9 @@ typedef struct {
     int32_t tc_maps;           /* 1 when the tensor path's per-matrix TMA descriptors were built */
     moe_expert uniform_base;
     int64_t uniform_step[3];
+    /* ---- filled by the caller ---- */
+    const void *iq3_grid;      /* device uint32 [256], 16-byte aligned: the IQ3_XXS grid
+                                  (required if any matrix is IQ3_XXS, else may be NULL) */
 } moe_weight_table;
 
 /* Paths for moe_options.path. */
@@ -261,6 +283,33 @@ int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, voi
  * ws = NULL reads those of moe_ffn_forward_noalloc's scratch array on the
  * current device. Synchronises `stream`. *status_out is a host pointer. */
 int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream);
+
+/* Bound (ns) on every device-side wait of the layer's kernels for data or for
+ * other threads (ring slots, mbarriers, the fused kernel's grid barrier) on
+ * the current device; 0 restores the default of 2 s (a layer takes well
+ * under a millisecond). A wait that exceeds it gives up: the kernel sets
+ * MOE_FLAG_WAIT_TIMEOUT in the status word, skips the rest of its work, waits
+ * (with a separate, long poll bound) for its own bulk copies and MMAs still in
+ * flight, releases its tensor memory and returns, so the context stays usable;
+ * that call's output is then incomplete. Meant for tests of this path and for
+ * callers that want an earlier deadline. A blocking copy to the device (it
+ * synchronises with the legacy default stream); not during stream capture.
+ * This follows no passage of the pages: it is the library's failure
+ * detection. Errors: CUDA. */
+int moe_set_wait_timeout_ns(uint64_t ns);
+
+/* Expert sharding across GPUs ("多卡 CUDA 张量并行：DwarfStar 如何在 8 张 L40S 上跑出
+ * 120 t/s", section "8 张卡是怎么配对的": the routed experts are split 50/50
+ * across a pair of GPUs and the router is replicated). Each rank runs
+ * moe_ffn_forward over the same x and logits with its expert range
+ * (moe_options.expert_lo/expert_hi) and gets a partial out[T, H]; after the
+ * partials of all ranks are gathered, this sums them:
+ *     out[i] = ((parts[0][i] + parts[1][i]) + parts[2][i]) + ...
+ * one fp32 add at a time in ascending part (rank) order, so every rank gets
+ * bit-identical results. parts: device fp32 [n_parts][count] (contiguous);
+ * out: device fp32 [count] (may alias parts[0]). n_parts >= 1, count >= 0.
+ * Errors: INVALID_ARG, CUDA. */
+int moe_sum_partials(const float *parts, int32_t n_parts, int64_t count, float *out, moe_stream_t stream);
 
 /* Size of the device scratch array that moe_ffn_forward_noalloc uses. */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -20,7 +20,7 @@ extern "C" {
 typedef struct CUstream_st *moe_stream_t;
 
 /* One matrix to fill: `rows` rows of `cols` weights in block format `format`
- * (1 Q8_0, 2 Q4_K, 3 Q6_K, 4 MXFP4), row stride `row_stride_bytes`, drawn from
+ * (1 Q8_0, 2 Q4_K, 3 Q6_K, 4 MXFP4, 5 IQ4_NL, 6 IQ4_XS, 7 IQ3_XXS), row stride `row_stride_bytes`, drawn from
  * the SplitMix64 sequence with key `key`. Padding bytes are written as 0. */
 typedef struct {
     void *data;               /* device, rows * row_stride_bytes bytes */

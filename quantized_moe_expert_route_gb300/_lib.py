@@ -15,9 +15,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe_route.so")
 
-Q8_0, Q4_K, Q6_K, MXFP4 = 1, 2, 3, 4
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17}
+Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS = 1, 2, 3, 4, 5, 6, 7
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32, IQ4_NL: 32, IQ4_XS: 256, IQ3_XXS: 256}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17, IQ4_NL: 18, IQ4_XS: 136, IQ3_XXS: 98}
 
 MOE_OK = 0
 MOE_TABLE_PREPARED = 0x4D4F4554
@@ -29,7 +29,8 @@ EXPORTED = [
     "moe_strerror", "moe_last_cuda_error", "moe_table_device_bytes", "moe_table_prepare",
     "moe_route_topk", "moe_bucket", "moe_ffn_workspace_size", "moe_ffn_workspace_init",
     "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc",
-    "moe_ffn_path", "moe_ffn_gemv_kernels", "moe_ffn_workspace_size_for_path",
+    "moe_ffn_path", "moe_ffn_gemv_kernels", "moe_ffn_workspace_size_for_path", "moe_sum_partials",
+    "moe_set_wait_timeout_ns",
 ]
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
@@ -57,7 +58,7 @@ class WeightTableC(ctypes.Structure):
                 ("down_formats", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
                 ("max_down_stride", ctypes.c_int64), ("uniform_layout", ctypes.c_int32),
                 ("tc_maps", ctypes.c_int32), ("uniform_base", Expert),
-                ("uniform_step", ctypes.c_int64 * 3)]
+                ("uniform_step", ctypes.c_int64 * 3), ("iq3_grid", ctypes.c_void_p)]
 
 
 class Options(ctypes.Structure):
@@ -101,8 +102,11 @@ def load() -> ctypes.CDLL:
     L.moe_ffn_gemv_kernels.restype = ctypes.c_int
     L.moe_ffn_forward_noalloc.argtypes = [ctypes.POINTER(WeightTableC), vp, vp, i32, i32, ctypes.POINTER(Options),
                                           vp, vp]
+    L.moe_sum_partials.argtypes = [vp, i32, ctypes.c_int64, vp, vp]
+    L.moe_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
     for name in ("moe_table_prepare", "moe_route_topk", "moe_bucket", "moe_ffn_workspace_init",
-                 "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc"):
+                 "moe_ffn_forward", "moe_ffn_read_status", "moe_ffn_workspace_views", "moe_ffn_forward_noalloc",
+                 "moe_sum_partials", "moe_set_wait_timeout_ns"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -140,7 +144,10 @@ class WeightTable:
     is a tuple (format, rows, cols, row_stride_bytes, uint8 CUDA tensor). The
     tensors are kept alive by this object."""
 
-    def __init__(self, experts: Sequence[dict], hidden: int, inter: int, stream=None):
+    def __init__(self, experts: Sequence[dict], hidden: int, inter: int, stream=None,
+                 grid: Optional[torch.Tensor] = None):
+        """experts: per expert {"gate"|"up"|"down": (fmt, rows, cols, stride, uint8 CUDA tensor)};
+        grid: the IQ3_XXS grid (256 x 32-bit CUDA tensor), needed when a matrix is IQ3_XXS."""
         L = load()
         E = len(experts)
         self.n_experts, self.hidden, self.inter = E, hidden, inter
@@ -154,6 +161,12 @@ class WeightTable:
                 setattr(arr[e], name, Matrix(fmt, rows, cols, 0, stride, data.data_ptr()))
         self._arr = arr
         self.c = WeightTableC(E, hidden, inter, 0, ctypes.cast(arr, ctypes.POINTER(Expert)))
+        if grid is not None:
+            if grid.numel() != 256 or grid.element_size() != 4:
+                raise ValueError("grid must hold 256 32-bit entries")
+            _dev(grid, "grid")
+            self._keep.append(grid)
+            self.c.iq3_grid = grid.data_ptr()
         nbytes = L.moe_table_device_bytes(E)
         if nbytes == 0:
             raise ValueError(f"bad expert count {E}")
@@ -316,3 +329,21 @@ def noalloc_read_status(stream=None) -> int:
     v = ctypes.c_uint32(0)
     _check("moe_ffn_read_status", load().moe_ffn_read_status(None, ctypes.byref(v), _stream(stream)))
     return v.value
+
+
+def sum_partials(parts: torch.Tensor, out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """parts fp32 [n, ...] (CUDA, contiguous) -> out fp32 [...] = sum over n in
+    ascending order, one fp32 add at a time (moe_sum_partials)."""
+    _dev(parts, "parts", torch.float32)
+    n = parts.shape[0]
+    out = out if out is not None else torch.empty(parts.shape[1:], dtype=torch.float32, device=parts.device)
+    _dev(out, "out", torch.float32)
+    _check("moe_sum_partials", load().moe_sum_partials(_ptr(parts), n, parts[0].numel(), _ptr(out),
+                                                        _stream(stream)))
+    return out
+
+
+def set_wait_timeout_ns(ns: int = 0) -> None:
+    """Bound (ns) on the kernels' device-side waits (0: the default, 2 s);
+    see moe_set_wait_timeout_ns."""
+    _check("moe_set_wait_timeout_ns", load().moe_set_wait_timeout_ns(int(ns)))

@@ -16,9 +16,10 @@ size_t bucket_smem_bytes(int E);
 size_t gateup_smem_bytes(int H, int64_t wstride);
 size_t down_smem_bytes(int I, int64_t wstride);
 cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
-                             int64_t dn_stride, uint32_t down_formats, const int32_t *offsets, const int32_t *pairs,
-                             const int32_t *active, const int32_t *pos, const float *wts, const uint16_t *x, float *h,
-                             float *y, float *out, uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
+                             int64_t dn_stride, uint32_t gu_formats, uint32_t down_formats, const uint32_t *grid,
+                             const int32_t *offsets, const int32_t *pairs, const int32_t *active, const int32_t *pos,
+                             const float *wts, const uint16_t *x, float *h, float *y, float *out, uint32_t *status,
+                             cudaEvent_t const *events, cudaStream_t s);
 bool decode_fused_eligible(int T, int k, int E, int H, int I, uint32_t gateup_formats, uint32_t down_formats,
                            int64_t gu_stride, int64_t dn_stride);
 cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *W, int T, int k, int E, int H, int I,
@@ -30,12 +31,16 @@ bool tc_path_eligible(int H, int I);
 size_t tc_weight_map_bytes(int E);
 bool tc_encode_weight_maps(const moe_weight_table *W, void *out);
 cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t gu_formats, uint32_t dn_formats,
-                           int T, int k, int E,
+                           const uint32_t *grid, int T, int k, int E,
                            int H, int I, const int32_t *offsets, const int32_t *active, const int32_t *pos,
                            const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
                            const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
                            cudaStream_t s);
 int noalloc_scratch_address(void **out);
+cudaError_t set_wait_ns_stream(unsigned long long ns);
+cudaError_t set_wait_ns_gemv(unsigned long long ns);
+cudaError_t set_wait_ns_decode(unsigned long long ns);
+cudaError_t set_wait_ns_tc(unsigned long long ns);
 }  // namespace moe
 
 using namespace moe;
@@ -65,7 +70,7 @@ bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 size_t map_offset(int E) { return align_up((size_t)E * sizeof(DevExpert), 128); }
 
 int check_matrix(const moe_matrix &m, int rows, int cols) {
-    if (m.format < MOE_Q8_0 || m.format > MOE_MXFP4) return MOE_ERR_BAD_FORMAT;
+    if (m.format < MOE_Q8_0 || m.format > MOE_IQ3_XXS) return MOE_ERR_BAD_FORMAT;
     if (m.rows != rows || m.cols != cols) return MOE_ERR_BAD_SHAPE;
     const int be = BLOCK_ELEMS[m.format], bb = BLOCK_BYTES[m.format];
     if (cols % be != 0) return MOE_ERR_BAD_SHAPE;
@@ -80,7 +85,7 @@ int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
     const bool fused_ok = decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
                                                 W->down_formats, W->max_gateup_stride, W->max_down_stride);
     const bool tc_ok = W->tc_maps == 1 && tc_path_eligible(W->hidden, W->inter);
-    const bool stream_ok = stream_plan(T, k, W->n_experts, W->hidden, W->inter, W->down_formats,
+    const bool stream_ok = stream_plan(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats, W->down_formats,
                                        W->max_gateup_stride, W->max_down_stride).ok;
     switch (requested) {
         case MOE_PATH_AUTO:
@@ -174,6 +179,8 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     }
     if (gateup_smem_bytes(H, gu_max) > SMEM_LIMIT || down_smem_bytes(I, dn_max) > SMEM_LIMIT)
         return MOE_ERR_UNSUPPORTED;
+    // IQ3_XXS weights are read through the caller's 256-entry grid
+    if ((present & (1u << MOE_IQ3_XXS)) && (!W->iq3_grid || !aligned(W->iq3_grid, 16))) return MOE_ERR_INVALID_ARG;
     cudaError_t err = cudaMemcpyAsync(device_buf, dev.data(), (size_t)E * sizeof(DevExpert), cudaMemcpyHostToDevice,
                                       stream);
     if (err != cudaSuccess) return cuda_fail(err);
@@ -315,18 +322,21 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     if (err != cudaSuccess) return cuda_fail(err);
     if (path == MOE_PATH_TENSOR)
         err = launch_tc_path(table, static_cast<const char *>(W->device_table) + map_offset(E), W->gateup_formats,
-                             W->down_formats, T, k, E, H, I, offsets, active, pos, wts, x,
+                             W->down_formats, static_cast<const uint32_t *>(W->iq3_grid), T, k, E, H, I, offsets,
+                             active, pos, wts, x,
                              h, y, base, tc_ws_layout(T, k, E, H, I), out, status, events, stream);
     else
-        err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, W->down_formats,
-                               offsets, pairs, active, pos, wts, x, h, y, out, status, events, stream);
+        err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, W->gateup_formats,
+                               W->down_formats, static_cast<const uint32_t *>(W->iq3_grid), offsets, pairs, active,
+                               pos, wts, x, h, y, out, status, events, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     return MOE_OK;
 }
 
 int moe_ffn_gemv_kernels(const moe_weight_table *W, int32_t T, int32_t k) {
     if (!W || W->prepared != MOE_TABLE_PREPARED || T < 0 || k <= 0 || k > W->n_experts) return -1;
-    return stream_plan(T > 0 ? T : 1, k, W->n_experts, W->hidden, W->inter, W->down_formats, W->max_gateup_stride,
+    return stream_plan(T > 0 ? T : 1, k, W->n_experts, W->hidden, W->inter, W->gateup_formats, W->down_formats,
+                       W->max_gateup_stride,
                        W->max_down_stride).ok
                ? MOE_GEMV_STREAMING
                : MOE_GEMV_TILED;
@@ -363,6 +373,15 @@ int moe_ffn_read_status(void *ws, uint32_t *status_out, moe_stream_t stream) {
     if (err != cudaSuccess) return cuda_fail(err);
     err = cudaStreamSynchronize(stream);
     return err == cudaSuccess ? MOE_OK : cuda_fail(err);
+}
+
+int moe_set_wait_timeout_ns(uint64_t ns) {
+    const unsigned long long v = ns ? (unsigned long long)ns : DEFAULT_WAIT_NS;
+    cudaError_t err;
+    if ((err = set_wait_ns_stream(v)) != cudaSuccess || (err = set_wait_ns_gemv(v)) != cudaSuccess ||
+        (err = set_wait_ns_decode(v)) != cudaSuccess || (err = set_wait_ns_tc(v)) != cudaSuccess)
+        return cuda_fail(err);
+    return MOE_OK;
 }
 
 }  // extern "C"

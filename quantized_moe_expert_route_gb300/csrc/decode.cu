@@ -52,7 +52,6 @@ constexpr int DC_MAX_PAIRS = 64;                 // T * k
 constexpr int DC_ROWS_A = 4;                     // max gate/up row pairs per chunk
 constexpr int DC_SURV = 64;                      // top-k survivors ranked from the short list
 
-constexpr unsigned long long DC_WAIT_NS = 2000000000ull;   // bound of the wait for other CTAs' h
 constexpr int DC_HQW = 20;                       // words per staged h block: 16 int16 pairs, the scale, pad
 
 struct DcLayout {
@@ -866,7 +865,8 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 const int n = ch.z, r0 = ch.y;
                 if (row >= n) continue;
                 const int s = ci % DC_NSTAGE;
-                if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+                if (*reinterpret_cast<volatile int *>(&misc[1]) ||
+                    !mbar_wait_timed(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
                     if (lane == 0) set_abort(misc, A.status);
                     break;
                 }
@@ -1004,9 +1004,9 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
     if (tid == 32 * (DC_CW - 1)) {
         // G arrivals past this launch's generation
         const unsigned long long target = (gen_count / (unsigned long long)G + 1ull) * (unsigned long long)G;
-        const unsigned long long t_start = globaltimer_ns();
+        const unsigned long long t_start = globaltimer_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
         while (ld_acquire_u64(barrier_ctr) < target) {
-            if (globaltimer_ns() - t_start > DC_WAIT_NS) {
+            if (globaltimer_ns() - t_start > bound) {
                 set_abort(misc, A.status);
                 break;
             }
@@ -1085,7 +1085,8 @@ __global__ void __launch_bounds__(DC_THREADS, 1) decode_fused_kernel(DcArgs A) {
                 const int nr = ch.z, row = 16 * rg + r;
                 if (16 * rg >= nr) continue;
                 const int s = ci % DC_NSTAGE;
-                if (!mbar_wait(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
+                if (*reinterpret_cast<volatile int *>(&misc[1]) ||
+                    !mbar_wait_timed(&full[s], (uint32_t)(ci / DC_NSTAGE) & 1u)) {
                     set_abort(misc, A.status);
                     break;
                 }
@@ -1277,5 +1278,8 @@ cudaError_t launch_decode_fused(const DevExpert *table, const moe_weight_table *
     if (T == 1 && H / 64 <= 32) return cudaLaunchKernelEx(&cfg, decode_fused_kernel<true>, A);
     return cudaLaunchKernelEx(&cfg, decode_fused_kernel<false>, A);
 }
+
+// This file's copy of the wait bound (moe_set_wait_timeout_ns).
+cudaError_t set_wait_ns_decode(unsigned long long ns) { return set_tu_wait_ns(ns); }
 
 }  // namespace moe

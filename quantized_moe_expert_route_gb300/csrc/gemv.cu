@@ -136,6 +136,77 @@ __device__ __forceinline__ void decode_unit<MOE_MXFP4>(const uint8_t *row, int u
     U.m = 0.0f;
 }
 
+// The non-linear codebook of IQ4_NL / IQ4_XS: value of code 0..15 as a signed
+// byte, four codes per word (code 4w + i in byte i of word w):
+//   -127 -104 -83 -65 | -49 -35 -22 -10 | 1 13 25 38 | 53 69 89 113.
+__device__ __forceinline__ int iq4_value(uint32_t c) {
+    const uint32_t w0 = (c & 8) ? 0x26190D01u : 0xBFAD9881u;
+    const uint32_t w1 = (c & 8) ? 0x71594535u : 0xF6EADDCFu;
+    uint32_t b;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(b) : "r"(w0), "r"(w1), "r"(c & 7u));
+    return (int)(int8_t)(b & 0xffu);
+}
+
+// IQ4_NL: 18 B = fp16 d | 16 B codes; weight i < 16 low nibble of byte 2 + i,
+// 16 + i its high nibble; w = d * codebook[code].
+template <>
+__device__ __forceinline__ void decode_unit<MOE_IQ4_NL>(const uint8_t *row, int u, Unit &U) {
+    const uint8_t *b = row + 18 * u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t q = b[2 + i];
+        U.c[i] = (float)iq4_value(q & 15);
+        U.c[16 + i] = (float)iq4_value(q >> 4);
+    }
+    U.s_lo = U.s_hi = half_bits_to_f32(ld16(b));
+    U.m = 0.0f;
+}
+
+// IQ4_XS: 136 B per 256 = fp16 d | uint16 high scale bits | 4 B low scale
+// nibbles | 128 B codes. Unit u is sub-block j = u % 8: scale
+// d * (ls_j - 32), ls_j = nibble (j % 2) of byte 4 + j / 2 | bits 2j.. of the
+// uint16 << 4; codes 16 j .. +15 low nibbles then high nibbles.
+template <>
+__device__ __forceinline__ void decode_unit<MOE_IQ4_XS>(const uint8_t *row, int u, Unit &U) {
+    const int sb = u >> 3, j = u & 7;
+    const uint8_t *b = row + 136 * sb;
+    const uint32_t sh = ld16(b + 2);
+    const int ls = ((b[4 + (j >> 1)] >> (4 * (j & 1))) & 15) | (((sh >> (2 * j)) & 3) << 4);
+    const uint8_t *qs = b + 8 + 16 * j;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t q = qs[i];
+        U.c[i] = (float)iq4_value(q & 15);
+        U.c[16 + i] = (float)iq4_value(q >> 4);
+    }
+    U.s_lo = U.s_hi = half_bits_to_f32(ld16(b)) * (float)(ls - 32);
+    U.m = 0.0f;
+}
+
+// IQ3_XXS: 98 B per 256 = fp16 d | 64 grid-index bytes | 8 words. Unit u is
+// sub-block j = u % 8, word a = word j: scale d * (0.5 + (a >> 28)) / 2;
+// group l (weights 8l .. 8l+7) takes magnitudes from grid[q[8j + 2l]] (4) and
+// grid[q[8j + 2l + 1]] (4), signs from the 7-bit index (a >> 7l) & 127 plus
+// the parity bit for the eighth.
+__device__ __forceinline__ void decode_iq3_unit(const uint8_t *row, int u, const uint32_t *grid, Unit &U) {
+    const int sb = u >> 3, j = u & 7;
+    const uint8_t *b = row + 98 * sb;
+    const uint32_t a = (uint32_t)ld16(b + 66 + 4 * j) | ((uint32_t)ld16(b + 68 + 4 * j) << 16);
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+        const uint32_t s7 = (a >> (7 * l)) & 127u;
+        const uint32_t signs = s7 | ((__popc(s7) & 1u) << 7);
+        const uint32_t g0 = __ldg(grid + b[2 + 8 * j + 2 * l]), g1 = __ldg(grid + b[3 + 8 * j + 2 * l]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            const float mag = (float)(((t < 4 ? g0 : g1) >> (8 * (t & 3))) & 255u);
+            U.c[8 * l + t] = ((signs >> t) & 1u) ? -mag : mag;
+        }
+    }
+    U.s_lo = U.s_hi = half_bits_to_f32(ld16(b)) * (0.5f + (float)(a >> 28)) * 0.5f;
+    U.m = 0.0f;
+}
+
 // acc += dot(w, x) for one 32-weight unit; x in shared memory (fp32).
 __device__ __forceinline__ float unit_dot(const Unit &U, const float *x) {
     float lo = 0.0f, hi = 0.0f, sx = 0.0f;
@@ -153,12 +224,15 @@ __device__ __forceinline__ float unit_dot(const Unit &U, const float *x) {
 // Row-dot of GV_SLICES threads: thread `slice` takes units slice, slice + 8, ...
 template <int FMT>
 __device__ __forceinline__ void row_dot(const uint8_t *row, int units, int slice, const float *xs, int xstride,
-                                        int nt, float acc[GV_NT]) {
+                                        int nt, float acc[GV_NT], const uint32_t *grid) {
 #pragma unroll
     for (int t = 0; t < GV_NT; ++t) acc[t] = 0.0f;
     for (int u = slice; u < units; u += GV_SLICES) {
         Unit U;
-        decode_unit<FMT>(row, u, U);
+        if constexpr (FMT == MOE_IQ3_XXS)
+            decode_iq3_unit(row, u, grid, U);
+        else
+            decode_unit<FMT>(row, u, U);
 #pragma unroll
         for (int t = 0; t < GV_NT; ++t)
             if (t < nt) acc[t] += unit_dot(U, xs + t * xstride + 32 * u);
@@ -176,7 +250,7 @@ __device__ __forceinline__ void row_dot(const uint8_t *row, int units, int slice
 // thread 0 waits once more (bounded) so no copy is left landing in a CTA that
 // has exited.
 __device__ __forceinline__ bool tile_ready(uint64_t *bar, uint32_t *status) {
-    const bool ok = mbar_wait(bar, 0);
+    const bool ok = mbar_wait_timed(bar, 0);
     if (__syncthreads_and(ok)) return true;
     if (threadIdx.x == 0) {
         atomicOr(status, (uint32_t)MOE_FLAG_WAIT_TIMEOUT);
@@ -194,6 +268,7 @@ struct GvArgs {
     float *y;            // fp32 [pairs, H] in bucket order
     uint32_t *status;
     int64_t wstride;     // smem bytes reserved per weight row (max stride)
+    const uint32_t *grid;   // IQ3_XXS grid (256 words) or null
 };
 
 template <int FMT>
@@ -235,7 +310,7 @@ __device__ void gateup_tile(const GvArgs &A, const DevMatrix &G, const DevMatrix
             // recompute the last row and discard it
             const int rr = row < nrows ? row : nrows - 1;
             const uint8_t *rp = (mat ? wu + rr * Uw.stride : wg + rr * G.stride);
-            row_dot<FMT>(rp, units, slice, xs, A.H, nt, acc);
+            row_dot<FMT>(rp, units, slice, xs, A.H, nt, acc, A.grid);
             if (slice == 0 && row < nrows)
 #pragma unroll
                 for (int t = 0; t < GV_NT; ++t) gu[(mat * GU_ROWS + row) * GV_NT + t] = acc[t];
@@ -271,6 +346,9 @@ __global__ void __launch_bounds__(GV_THREADS) gateup_gemv_kernel(GvArgs A) {
         case MOE_Q4_K: gateup_tile<MOE_Q4_K>(A, G, Uw, e, r0, nrows, smem, &bar); break;
         case MOE_Q6_K: gateup_tile<MOE_Q6_K>(A, G, Uw, e, r0, nrows, smem, &bar); break;
         case MOE_MXFP4: gateup_tile<MOE_MXFP4>(A, G, Uw, e, r0, nrows, smem, &bar); break;
+        case MOE_IQ4_NL: gateup_tile<MOE_IQ4_NL>(A, G, Uw, e, r0, nrows, smem, &bar); break;
+        case MOE_IQ4_XS: gateup_tile<MOE_IQ4_XS>(A, G, Uw, e, r0, nrows, smem, &bar); break;
+        case MOE_IQ3_XXS: gateup_tile<MOE_IQ3_XXS>(A, G, Uw, e, r0, nrows, smem, &bar); break;
         default: break;
     }
 }
@@ -301,7 +379,7 @@ __device__ void down_tile(const GvArgs &A, const DevMatrix &D, int e, int r0, in
         float acc[GV_NT];
         {
             const int rr = row < nrows ? row : nrows - 1;
-            row_dot<FMT>(wd + rr * D.stride, units, slice, hs, A.I, nt, acc);
+            row_dot<FMT>(wd + rr * D.stride, units, slice, hs, A.I, nt, acc, A.grid);
             if (slice == 0 && row < nrows)
                 for (int t = 0; t < nt; ++t) A.y[(size_t)(q0 + t0 + t) * A.H + r0 + row] = acc[t];
         }
@@ -330,6 +408,9 @@ __global__ void __launch_bounds__(GV_THREADS) down_gemv_kernel(GvArgs A) {
         case MOE_Q4_K: down_tile<MOE_Q4_K>(A, D, e, r0, nrows, smem, &bar); break;
         case MOE_Q6_K: down_tile<MOE_Q6_K>(A, D, e, r0, nrows, smem, &bar); break;
         case MOE_MXFP4: down_tile<MOE_MXFP4>(A, D, e, r0, nrows, smem, &bar); break;
+        case MOE_IQ4_NL: down_tile<MOE_IQ4_NL>(A, D, e, r0, nrows, smem, &bar); break;
+        case MOE_IQ4_XS: down_tile<MOE_IQ4_XS>(A, D, e, r0, nrows, smem, &bar); break;
+        case MOE_IQ3_XXS: down_tile<MOE_IQ3_XXS>(A, D, e, r0, nrows, smem, &bar); break;
         default: break;
     }
 }
@@ -398,12 +479,13 @@ size_t gateup_smem_bytes(int H, int64_t wstride) {
 size_t down_smem_bytes(int I, int64_t wstride) { return (size_t)(DN_ROWS * wstride) + (size_t)GV_NT * I * 4; }
 
 cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H, int I, int64_t gu_stride,
-                             int64_t dn_stride, uint32_t down_formats, const int32_t *offsets, const int32_t *pairs,
-                             const int32_t *active, const int32_t *pos, const float *wts, const uint16_t *x, float *h,
-                             float *y, float *out, uint32_t *status, cudaEvent_t const *events, cudaStream_t s) {
+                             int64_t dn_stride, uint32_t gu_formats, uint32_t down_formats, const uint32_t *grid,
+                             const int32_t *offsets, const int32_t *pairs, const int32_t *active, const int32_t *pos,
+                             const float *wts, const uint16_t *x, float *h, float *y, float *out, uint32_t *status,
+                             cudaEvent_t const *events, cudaStream_t s) {
     // decode batches of up to 16 rows: the streaming kernels (stream.cu)
     if (T > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
-        const SgPlan p = stream_plan(T, k, E, H, I, down_formats, gu_stride, dn_stride);
+        const SgPlan p = stream_plan(T, k, E, H, I, gu_formats, down_formats, gu_stride, dn_stride);
         if (p.ok) {
             cudaError_t err = launch_stream_path(table, p, T, k, E, H, I, offsets, pairs, active, x, h, y, status, events, s);
             if (err != cudaSuccess) return err;
@@ -420,7 +502,7 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
     }
     const int max_active = T * k < E ? T * k : E;
     if (T > 0 && max_active > 0) {
-        GvArgs A{table, H, I, k, offsets, pairs, active, x, h, y, status, gu_stride};
+        GvArgs A{table, H, I, k, offsets, pairs, active, x, h, y, status, gu_stride, grid};
         cudaError_t err;
         if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
         dim3 g1((I + GU_ROWS - 1) / GU_ROWS, max_active);
@@ -442,5 +524,8 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
     }
     return cudaSuccess;
 }
+
+// This file's copy of the wait bound (moe_set_wait_timeout_ns).
+cudaError_t set_wait_ns_gemv(unsigned long long ns) { return set_tu_wait_ns(ns); }
 
 }  // namespace moe

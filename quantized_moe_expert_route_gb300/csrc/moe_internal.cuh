@@ -90,11 +90,22 @@ inline TcLayout tc_ws_layout(int T, int k, int E, int H, int I) {
     return C;
 }
 
-constexpr int BLOCK_ELEMS[5] = {0, 32, 256, 256, 32};
-constexpr int BLOCK_BYTES[5] = {0, 34, 144, 210, 17};
+constexpr int BLOCK_ELEMS[8] = {0, 32, 256, 256, 32, 32, 256, 256};
+constexpr int BLOCK_BYTES[8] = {0, 34, 144, 210, 17, 18, 136, 98};
 
 // Bounded waits: a wait that exceeds this many polls sets MOE_FLAG_WAIT_TIMEOUT.
 constexpr uint32_t WAIT_LIMIT = 1u << 26;
+
+// The time bound (ns) of the kernels' waits for data or for other threads
+// (ring slots, barriers); the waits for a CTA's own copies in flight before
+// it exits (drains) keep the poll bound above. Default 2 s: a whole layer
+// takes well under a millisecond. Each translation unit has its own copy
+// (no relocatable device code); moe_set_wait_timeout_ns sets all of them.
+constexpr unsigned long long DEFAULT_WAIT_NS = 2000000000ull;
+static __device__ unsigned long long g_wait_ns = DEFAULT_WAIT_NS;
+static inline cudaError_t set_tu_wait_ns(unsigned long long ns) {
+    return cudaMemcpyToSymbol(g_wait_ns, &ns, sizeof(ns));
+}
 
 // Host helpers shared by the launchers (gemv.cu, decode.cu).
 cudaError_t record_event(cudaEvent_t ev, cudaStream_t s);   // event (graph node when capturing)
@@ -113,7 +124,8 @@ struct SgPlan {
     int cr, ns, stage, nexp, nsb, stageb, nq;
     size_t smem_a, smem_b;
 };
-SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t down_formats, int64_t gu_stride, int64_t dn_stride);
+SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint32_t down_formats, int64_t gu_stride,
+                   int64_t dn_stride);
 cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, int k, int E, int H, int I,
                                const int32_t *offsets, const int32_t *pairs, const int32_t *active, const uint16_t *x,
                                float *h, float *y, uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
@@ -150,6 +162,40 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
         if (done) return true;
     }
     return false;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Returns true once the phase with the given parity has completed; false
+// after g_wait_ns (or WAIT_LIMIT polls). For waits on data or on other
+// threads; drains use mbar_wait.
+static __device__ __noinline__ bool mbar_wait_timed_slow(uint32_t addr, uint32_t parity) {
+    const unsigned long long t0 = now_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t done;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(done)
+            : "r"(addr), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (now_ns() - t0 > bound) return false;
+    }
+    return false;
+}
+__device__ __forceinline__ bool mbar_wait_timed(uint64_t *bar, uint32_t parity) {
+    const uint32_t addr = smem_addr(bar);
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    return done || mbar_wait_timed_slow(addr, parity);
 }
 
 // 1-D bulk copy global -> shared (TMA engine). dst, src 16-byte aligned,

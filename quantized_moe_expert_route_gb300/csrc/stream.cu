@@ -76,11 +76,14 @@ __device__ __forceinline__ void sg_flag(uint32_t *status, uint32_t f) {
 // shows chunk j, then on the parity.
 __device__ __forceinline__ bool sg_wait_chunk(uint64_t *full, const int *last, int s, int j, int ns) {
     const volatile int *l = last + s;
-    for (uint32_t i = 0; *l != j; ++i) {
-        if (i >= WAIT_LIMIT) return false;
-        __nanosleep(32);
+    if (*l != j) {
+        const unsigned long long t0 = now_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
+        for (uint32_t i = 0; *l != j; ++i) {
+            if (i >= WAIT_LIMIT || now_ns() - t0 > bound) return false;
+            __nanosleep(32);
+        }
     }
-    return mbar_wait(&full[s], (uint32_t)(j / ns) & 1u);
+    return mbar_wait_timed(&full[s], (uint32_t)(j / ns) & 1u);
 }
 
 // The ring's producer (warp 15): lane l < SG_PL issues the chunks
@@ -94,6 +97,8 @@ __device__ bool sg_produce(int ns, int n, const int *used, Issue issue) {
     const int lane = threadIdx.x & 31;
     int next = ns + lane;
     uint32_t idle = 0;
+    const unsigned long long bound = *(volatile unsigned long long *)&g_wait_ns;
+    unsigned long long t_idle = 0;
     for (;;) {
         const bool want = lane < SG_PL && next < n;
         if (!__any_sync(0xffffffffu, want)) return true;
@@ -105,7 +110,9 @@ __device__ bool sg_produce(int ns, int n, const int *used, Issue issue) {
         if (__any_sync(0xffffffffu, ready)) {
             idle = 0;
         } else {
-            if (++idle >= WAIT_LIMIT) return false;
+            const unsigned long long t = now_ns();
+            if (idle == 0) t_idle = t;
+            if (++idle >= WAIT_LIMIT || t - t_idle > bound) return false;
             __nanosleep(64);
         }
     }
@@ -646,13 +653,15 @@ int optin_smem() {
 
 }  // namespace
 
-SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t down_formats, int64_t gu_stride, int64_t dn_stride) {
+SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint32_t down_formats, int64_t gu_stride,
+                   int64_t dn_stride) {
     SgPlan p{};
     p.ok = false;
     const int G = sm_count(), optin = optin_smem();
     if (G <= 0 || optin <= 0) return p;
     if (T < 1 || T > SG_MAX_T || H % 64 != 0 || I % 32 != 0 || H % SG_DN_ROWS != 0) return p;
     if ((down_formats & ~((1u << MOE_Q8_0) | (1u << MOE_MXFP4))) != 0) return p;
+    if ((gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K) | (1u << MOE_Q6_K) | (1u << MOE_MXFP4))) != 0) return p;
     if (gu_stride <= 0 || dn_stride <= 0 || gu_stride % 16 != 0 || dn_stride % 16 != 0) return p;
     const int P = T * k, nmax = std::min(P, E);
     // experts one CTA's share can touch: an expert costs at least 2 per
@@ -750,5 +759,8 @@ cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, i
     if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
     return cudaSuccess;
 }
+
+// This file's copy of the wait bound (moe_set_wait_timeout_ns).
+cudaError_t set_wait_ns_stream(unsigned long long ns) { return set_tu_wait_ns(ns); }
 
 }  // namespace moe

@@ -67,12 +67,17 @@ constexpr uint32_t TC_MAGIC = 0x64006400u;    // fp16 pair (1024, 1024)
 // Raw stage geometry per format (index = moe_format): a stage holds, for each
 // weight row, the blocks of 256 K as TMA boxes of RAW_W bytes (widened to
 // 16-byte boundaries); Q8_0's 272 bytes take two boxes, 128 bytes apart.
-__host__ __device__ constexpr int raw_w(int f) { return f == MOE_Q6_K ? 240 : 144; }
+__host__ __device__ constexpr int raw_w(int f) { return f == MOE_Q6_K ? 240 : f == MOE_IQ3_XXS ? 112 : 144; }
 __host__ __device__ constexpr int raw_nbox(int f) { return f == MOE_Q8_0 ? 2 : 1; }
-__host__ __device__ constexpr int blk_elems(int f) { return f == MOE_Q4_K || f == MOE_Q6_K ? 256 : 32; }
-__host__ __device__ constexpr int blk_bytes(int f) {
-    return f == MOE_Q8_0 ? 34 : f == MOE_Q4_K ? 144 : f == MOE_Q6_K ? 210 : 17;
+__host__ __device__ constexpr int blk_elems(int f) {
+    return f == MOE_Q4_K || f == MOE_Q6_K || f == MOE_IQ4_XS || f == MOE_IQ3_XXS ? 256 : 32;
 }
+__host__ __device__ constexpr int blk_bytes(int f) {
+    return f == MOE_Q8_0 ? 34 : f == MOE_Q4_K ? 144 : f == MOE_Q6_K ? 210 : f == MOE_MXFP4 ? 17
+         : f == MOE_IQ4_NL ? 18 : f == MOE_IQ4_XS ? 136 : 98;
+}
+constexpr uint32_t TC_IQ_FORMATS = (1u << MOE_IQ4_NL) | (1u << MOE_IQ4_XS) | (1u << MOE_IQ3_XXS);
+constexpr int TC_GRID_BYTES = 1024;          // the IQ3_XXS grid in shared memory (IQ variant)
 
 static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
 static_assert(TC_DG * TC_PPG == TC_KR / TC_KA, "groups x pieces cover a raw stage");
@@ -93,6 +98,7 @@ struct TcArgs {
     uint32_t *hmax;            // gate/up: max |h| bits per bucket row
     float *y;                  // down: y [rows][H] fp32, bucket order
     uint32_t *status;
+    const uint32_t *grid;      // IQ3_XXS grid (256 words) or null
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -144,9 +150,6 @@ __device__ __forceinline__ void lds_words(uint32_t addr, uint32_t (&w)[N]) {
 __device__ __forceinline__ void mbar_arrive_cta(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
-// A wait that lasts this long (ns) has failed: a whole layer takes well under
-// a millisecond.
-constexpr uint64_t TC_WAIT_NS = 2000000000ull;
 
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
@@ -167,31 +170,28 @@ __device__ __forceinline__ bool try_wait_parity(uint32_t addr, uint32_t parity) 
     return done != 0;
 }
 
-// The polling loop of a bounded parity wait (TC_WAIT_NS, or WAIT_LIMIT
+// The polling loop of a bounded parity wait (g_wait_ns, or WAIT_LIMIT
 // polls) that also gives up once another role has aborted; `suspend` polls
 // with a suspend-time hint. Out of line: every role's waits share one copy of
 // the code, which keeps the kernel small enough for the instruction caches.
 __device__ __noinline__ bool tc_wait_slow(uint32_t addr, uint32_t parity, volatile int *abort_flag, bool suspend) {
-    uint64_t t0 = 0;
-    const uint32_t check = suspend ? 15u : 1023u;
+    const uint64_t t0 = global_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
+    const uint32_t check = suspend ? 0u : 1023u;
+    const uint32_t hint = bound < TC_SUSPEND_NS ? (uint32_t)bound : TC_SUSPEND_NS;
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         uint32_t done;
         if (suspend)
             asm volatile(
                 "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
                 : "=r"(done)
-                : "r"(addr), "r"(parity), "r"(TC_SUSPEND_NS)
+                : "r"(addr), "r"(parity), "r"(hint)
                 : "memory");
         else
             done = try_wait_parity(addr, parity);
         if (done) return true;
         if ((i & check) == check) {
             if (*abort_flag) return false;
-            const uint64_t now = global_ns();
-            if (i == check)
-                t0 = now;
-            else if (now - t0 > TC_WAIT_NS)
-                return false;
+            if (global_ns() - t0 > bound) return false;
         }
     }
     return false;
@@ -482,6 +482,103 @@ __device__ __forceinline__ void dq_mxfp4(uint32_t blk, int g, uint32_t (&r)[32])
     }
 }
 
+// ---- the IQ formats (IQ variant of the kernel)
+// Signed bytes of four IQ4 codes (nibbles 0..3 of sel16) from the non-linear
+// codebook -127 -104 -83 -65 -49 -35 -22 -10 1 13 25 38 53 69 89 113 (four
+// codes per word, code 4w + i in byte i): a byte permute in each half of the
+// book, then a byte mask from bit 3 of each code (prmt sign-replicate).
+__device__ __forceinline__ uint32_t iq4_lookup4(uint32_t sel16) {
+    const uint32_t s7 = sel16 & 0x7777u;
+    const uint32_t lo = prmt(0xBFAD9881u, 0xF6EADDCFu, s7);
+    const uint32_t hi = prmt(0x26190D01u, 0x71594535u, s7);
+    const uint32_t m = prmt(0u, 0x80808080u, ((sel16 >> 1) & 0x4444u) | 0x8888u);
+    return (hi & m) | (lo & ~m);
+}
+// Codes of bytes 0..3 of w, low nibbles (hi = false) or high nibbles, as a
+// 16-bit selector with code i in nibble i.
+__device__ __forceinline__ uint32_t nibble_sel(uint32_t w, bool hi) {
+    const uint32_t v = hi ? (w >> 4) : w;
+    const uint32_t x = (v & 0x000F000Fu) | ((v >> 4) & 0x00F000F0u);
+    return prmt(x, 0u, 0x0020u);
+}
+// Four signed bytes -> two fp16 pairs (exact), times D (one rounding).
+__device__ __forceinline__ void i8x4_to_half(uint32_t c, uint32_t D, uint32_t &p0, uint32_t &p1) {
+    c ^= 0x80808080u;
+    p0 = hmul2(hadd2(prmt(c, 0x64646464u, 0x5140u), TC_NEG1152), D);
+    p1 = hmul2(hadd2(prmt(c, 0x64646464u, 0x7362u), TC_NEG1152), D);
+}
+// 32 IQ4 codes (16 code bytes w[0..3]: weights 0..15 low nibbles, 16..31
+// high nibbles) times scale pair D -> 16 fp16 pairs in K order at r[o..o+15].
+__device__ __forceinline__ void iq4_32(const uint32_t (&w)[4], uint32_t D, uint32_t (&r)[32], int o) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        i8x4_to_half(iq4_lookup4(nibble_sel(w[k], false)), D, r[o + 2 * k], r[o + 2 * k + 1]);
+        i8x4_to_half(iq4_lookup4(nibble_sel(w[k], true)), D, r[o + 8 + 2 * k], r[o + 8 + 2 * k + 1]);
+    }
+}
+// IQ4_NL: piece g = blocks 2g, 2g+1 of the stage (18 bytes each: fp16 d,
+// 16 code bytes). w = d * codebook[code].
+__device__ __forceinline__ void dq_iq4nl(uint32_t blk, int g, uint32_t (&r)[32]) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const uint32_t p = blk + 36 * g + 18 * b;
+        uint32_t dw[1], w[4];
+        lds_words<1>(p, dw);
+        lds_words<4>(p + 2, w);
+        iq4_32(w, (dw[0] & 0xffffu) * 0x10001u, r, 16 * b);
+    }
+}
+// IQ4_XS: super-block at `blk` (8-byte aligned); piece g = sub-blocks 2g,
+// 2g+1: code bytes [8 + 32g, +32), scales d * (ls - 32) with ls from the
+// 6-bit fields (low nibble in byte 4 + j/2, high bits j of the uint16 at 2).
+__device__ __forceinline__ void dq_iq4xs(uint32_t blk, int g, uint32_t (&r)[32]) {
+    uint32_t h[2], w[8];
+    lds_words<2>(blk, h);
+    lds_words<8>(blk + 8 + 32 * g, w);
+    const float d = __half2float(__ushort_as_half((uint16_t)(h[0] & 0xffffu)));
+    const uint32_t sh = h[0] >> 16;
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * g + jj;
+        const int ls = (int)((h[1] >> (8 * (j >> 1) + 4 * (j & 1))) & 15u) | (int)(((sh >> (2 * j)) & 3u) << 4);
+        const uint32_t D = splat_half(__float2half_rn(d * (float)(ls - 32)));
+        const uint32_t ww[4] = {w[4 * jj], w[4 * jj + 1], w[4 * jj + 2], w[4 * jj + 3]};
+        iq4_32(ww, D, r, 16 * jj);
+    }
+}
+// IQ3_XXS: super-block at `blk` (2-byte aligned); piece g = sub-blocks 2g,
+// 2g+1: grid indices [2 + 16g, +16), words [66 + 8g, +8); scale
+// d * (0.5 + (a >> 28)) / 2; group l of 8 weights takes its magnitudes from
+// two grid entries (grid_s, shared memory) and its signs from the 7-bit
+// index (a >> 7l) & 127 with the parity as the eighth.
+__device__ __forceinline__ void dq_iq3xxs(uint32_t blk, int g, const uint32_t *grid_s, uint32_t (&r)[32]) {
+    uint32_t dw[1], q[4], a[2];
+    lds_words<1>(blk, dw);
+    lds_words<4>(blk + 2 + 16 * g, q);
+    lds_words<2>(blk + 66 + 8 * g, a);
+    const float d = __half2float(__ushort_as_half((uint16_t)(dw[0] & 0xffffu)));
+    constexpr uint32_t NEG1024 = 0xE400E400u;   // fp16 pair (-1024, -1024)
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj) {
+        const uint32_t S = splat_half(__float2half_rn(d * (0.5f + (float)(a[jj] >> 28)) * 0.5f));
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            const uint32_t s7 = (a[jj] >> (7 * l)) & 127u;
+            const uint32_t sb = s7 | ((__popc(s7) & 1u) << 7);
+            const uint32_t qw = q[2 * jj + (l >> 1)];
+            const uint32_t e0 = grid_s[(qw >> (16 * (l & 1))) & 0xffu];
+            const uint32_t e1 = grid_s[(qw >> (16 * (l & 1) + 8)) & 0xffu];
+#pragma unroll
+            for (int t = 0; t < 8; t += 2) {
+                const uint32_t e = t < 4 ? e0 : e1;
+                const uint32_t m = hadd2(prmt(e, 0x64646464u, (t & 2) ? 0x7362u : 0x5140u), NEG1024);
+                const uint32_t sg = ((sb << (15 - t)) & 0x8000u) | ((sb << (30 - t)) & 0x80000000u);
+                r[16 * jj + 4 * l + (t >> 1)] = hmul2(m, S ^ sg);
+            }
+        }
+    }
+}
+
 // Raw stage rs of a weight row: the byte offset (within the row) of the first
 // block of K range [256 rs, ...), the 16-byte-aligned x of its TMA box and the
 // lead of the block inside the box.
@@ -492,9 +589,9 @@ __host__ __device__ __forceinline__ void raw_x(int fmt, int rs, int &x0, int &le
 }
 
 // ------------------------------------------------------------------ the grouped GEMM
-size_t tc_smem_bytes(int slot_bytes, int RS) {
+size_t tc_smem_bytes(int slot_bytes, int RS, bool iq = false) {
     return 1024 + (size_t)TC_BSTAGES * TC_BSTAGE_BYTES + (size_t)RS * slot_bytes + TC_UBUF_FLOATS * 4 +
-           TC_NBARS * 8 + 64;
+           TC_NBARS * 8 + 64 + (iq ? TC_GRID_BYTES : 0);
 }
 
 struct Unit {
@@ -553,16 +650,12 @@ __device__ __forceinline__ void red_release_shared(uint32_t *p, uint32_t v) {
 }
 // Spin until the counter reaches `target` (wrapping compare); bounded like tc_spin.
 __device__ __noinline__ bool counter_spin_slow(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
-    uint64_t t0 = 0;
+    const uint64_t t0 = global_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         if ((int32_t)(ld_acquire_shared(p) - target) >= 0) return true;
         if ((i & 1023u) == 1023u) {
             if (*abort_flag) return false;
-            const uint64_t now = global_ns();
-            if (i == 1023u)
-                t0 = now;
-            else if (now - t0 > TC_WAIT_NS)
-                return false;
+            if (global_ns() - t0 > bound) return false;
         }
     }
     return false;
@@ -571,7 +664,7 @@ __device__ __forceinline__ bool counter_spin(const uint32_t *p, uint32_t target,
     return (int32_t)(ld_acquire_shared(p) - target) >= 0 || counter_spin_slow(p, target, abort_flag);
 }
 
-template <bool GATEUP>
+template <bool GATEUP, bool IQ>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const TcArgs A) {
     extern __shared__ __align__(16) uint8_t tc_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -587,6 +680,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     uint32_t *a_ready = raw_info + TC_RS_MAX;   // [TC_EVSLOTS]: dequant warps done, 16 per use
     uint32_t *tmem_slot = a_ready + TC_EVSLOTS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    uint32_t *grid_s = reinterpret_cast<uint32_t *>(bars + TC_NBARS) + 16;   // IQ variant: after the 64-byte misc area
+    if (IQ && A.grid)
+        for (int i = threadIdx.x; i < 256; i += TC_THREADS) grid_s[i] = A.grid[i];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int R = GATEUP ? 64 : 128;          // weight rows per matrix box
@@ -813,8 +909,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         dq_q8_0(gp < 2 ? base + 68 * gp : base + (uint32_t)(R * W) + 68 * gp - 128, r);
                     else if (fmt == MOE_Q6_K)
                         dq_q6k(base, gp, r);
-                    else
+                    else if (!IQ || fmt == MOE_MXFP4)
                         dq_mxfp4(base, gp, r);
+                    else if (fmt == MOE_IQ4_NL)
+                        dq_iq4nl(base, gp, r);
+                    else if (fmt == MOE_IQ4_XS)
+                        dq_iq4xs(base, gp, r);
+                    else
+                        dq_iq3xxs(base, gp, grid_s, r);
                     tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + es * (TC_AEV * 32) + gp * 32, r);
                 }
                 }
@@ -1074,7 +1176,7 @@ bool encode_act_map(CUtensorMap *map, const void *base, int rows, int cols) {
 int raw_slot_bytes(uint32_t fmask, bool gateup) {
     const int R = gateup ? 64 : 128, nmat = gateup ? 2 : 1;
     int sb = 0;
-    for (int f = MOE_Q8_0; f <= MOE_MXFP4; ++f)
+    for (int f = MOE_Q8_0; f <= MOE_IQ3_XXS; ++f)
         if (fmask & (1u << f)) sb = std::max(sb, nmat * raw_nbox(f) * R * raw_w(f));
     return sb;
 }
@@ -1086,18 +1188,20 @@ int smem_optin() {
     if (dev < 64 && g_tc_smem_optin[dev]) return g_tc_smem_optin[dev];
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-    if (cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess)
+    if (cudaFuncSetAttribute(tc_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess)
         return 0;
     if (dev < 64) g_tc_smem_optin[dev] = v;
     return v;
 }
 
 // Raw ring depth that fits next to the fixed shared memory; 0 if < 2.
-int raw_stages(int slot_bytes) {
+int raw_stages(int slot_bytes, bool iq) {
     const int optin = smem_optin();
     if (optin <= 0 || slot_bytes <= 0) return 0;
-    const long room = (long)optin - (long)tc_smem_bytes(slot_bytes, 0);
+    const long room = (long)optin - (long)tc_smem_bytes(slot_bytes, 0, iq);
     long rs = room / slot_bytes;
     if (rs > TC_RS_MAX) rs = TC_RS_MAX;
     return rs >= 2 ? (int)rs : 0;
@@ -1134,7 +1238,7 @@ bool tc_encode_weight_maps(const moe_weight_table *W, void *out) {
 }
 
 cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t gu_formats, uint32_t dn_formats,
-                           int T, int k, int E,
+                           const uint32_t *grid, int T, int k, int E,
                            int H, int I, const int32_t *offsets, const int32_t *active, const int32_t *pos,
                            const float *wts, const uint16_t *x, float *h32, float *y, char *ws_base,
                            const TcLayout &C, float *out, uint32_t *status, cudaEvent_t const *events,
@@ -1142,7 +1246,11 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
     if (T <= 0) return cudaSuccess;
     const int P = T * k;
     const int sb1 = raw_slot_bytes(gu_formats, true), sb2 = raw_slot_bytes(dn_formats, false);
-    const int rs1 = raw_stages(sb1), rs2 = raw_stages(sb2);
+    // layers with IQ formats take the kernel variant with their decoders (and
+    // the IQ3_XXS grid in shared memory); the others keep the smaller code
+    const bool iq = ((gu_formats | dn_formats) & TC_IQ_FORMATS) != 0;
+    if (iq && ((gu_formats | dn_formats) & (1u << MOE_IQ3_XXS)) && !grid) return cudaErrorInvalidValue;
+    const int rs1 = raw_stages(sb1, iq), rs2 = raw_stages(sb2, iq);
     const CUtensorMap *maps = static_cast<const CUtensorMap *>(wmaps);
     const int G = sm_count();
     if (!rs1 || !rs2 || G <= 0) return cudaErrorInvalidConfiguration;
@@ -1162,19 +1270,28 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
 
-    TcArgs a1{table, maps, chunks, n_chunks, H, I / 64, H, I, sb1, rs1, xinv, h32, hmax, nullptr, status};
-    tc_gemm_kernel<true><<<G, TC_THREADS, tc_smem_bytes(sb1, rs1), s>>>(xmap, a1);
+    TcArgs a1{table, maps, chunks, n_chunks, H, I / 64, H, I, sb1, rs1, xinv, h32, hmax, nullptr, status, grid};
+    if (iq)
+        tc_gemm_kernel<true, true><<<G, TC_THREADS, tc_smem_bytes(sb1, rs1, true), s>>>(xmap, a1);
+    else
+        tc_gemm_kernel<true, false><<<G, TC_THREADS, tc_smem_bytes(sb1, rs1), s>>>(xmap, a1);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[1], s)) != cudaSuccess) return err;
 
     tc_hprep_kernel<<<(P + PREP_THREADS / 32 - 1) / (PREP_THREADS / 32), PREP_THREADS, 0, s>>>(h32, hmax, offsets, E,
                                                                                              I, h16, hinv);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    TcArgs a2{table, maps, chunks, n_chunks, I, H / TC_M, H, I, sb2, rs2, hinv, nullptr, nullptr, y, status};
-    tc_gemm_kernel<false><<<G, TC_THREADS, tc_smem_bytes(sb2, rs2), s>>>(hmap, a2);
+    TcArgs a2{table, maps, chunks, n_chunks, I, H / TC_M, H, I, sb2, rs2, hinv, nullptr, nullptr, y, status, grid};
+    if (iq)
+        tc_gemm_kernel<false, true><<<G, TC_THREADS, tc_smem_bytes(sb2, rs2, true), s>>>(hmap, a2);
+    else
+        tc_gemm_kernel<false, false><<<G, TC_THREADS, tc_smem_bytes(sb2, rs2), s>>>(hmap, a2);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
     return launch_combine(T, k, H, pos, wts, y, out, s);
 }
+
+// This file's copy of the wait bound (moe_set_wait_timeout_ns).
+cudaError_t set_wait_ns_tc(unsigned long long ns) { return set_tu_wait_ns(ns); }
 
 }  // namespace moe

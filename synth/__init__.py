@@ -34,6 +34,16 @@ Recipe (all values little-endian):
   r_{24+i//4}, 255) - 127; d = f16(1e-4 + 9e-4 u24(r28)).
 * MXFP4 (17 B): e = 124 + ubelow(low 32 bits of r0, 3); the 16 code bytes are
   the bytes of r1, r2.
+* IQ4_NL (18 B): d = f16(0.002 + 0.018 u24(r0)); the 16 code bytes are the
+  bytes of r1, r2.
+* IQ4_XS (136 B): d = f16(2e-4 + 1e-3 u24(r0)); bytes 2..7 (high scale bits
+  and low scale nibbles) are bytes 0..5 of r1; the 128 code bytes are the
+  bytes of r2..r17.
+* IQ3_XXS (98 B): d = f16(0.001 + 0.009 u24(r0)); the 64 grid-index bytes
+  are the bytes of r1..r8; the 32 scale/sign bytes are the bytes of r9..r12.
+  The layer's grid (256 entries of four magnitude bytes) is drawn once from
+  stream GRID of seed 0: byte j of entry i is ``IQ3_MAGNITUDES[ubelow(16-bit
+  chunk j of draw i, 8)]``.
 * Row padding bytes (``row_stride`` beyond the row's blocks) are zero.
 * Normals: Box-Muller in fp64 on draws (2i, 2i+1):
   ``sqrt(-2 ln u1) cos(2 pi u2)`` with ``u1 = ((r >> 11) + 1) 2**-53``,
@@ -53,10 +63,13 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import numpy as np
 
 # Format tags (the same numeric values as the C ABI's moe_format enum).
-Q8_0, Q4_K, Q6_K, MXFP4 = 1, 2, 3, 4
-FORMAT_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", MXFP4: "MXFP4"}
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17}
+Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS = 1, 2, 3, 4, 5, 6, 7
+FORMAT_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", MXFP4: "MXFP4", IQ4_NL: "IQ4_NL", IQ4_XS: "IQ4_XS",
+                IQ3_XXS: "IQ3_XXS"}
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32, IQ4_NL: 32, IQ4_XS: 256, IQ3_XXS: 256}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17, IQ4_NL: 18, IQ4_XS: 136, IQ3_XXS: 98}
+# the magnitudes the synthetic IQ3_XXS grid draws from
+IQ3_MAGNITUDES = np.array([4, 12, 20, 28, 36, 44, 52, 62], dtype=np.int64)
 
 GAMMA = 0x9E3779B97F4A7C15
 _MASK64 = (1 << 64) - 1
@@ -64,6 +77,7 @@ _MASK64 = (1 << 64) - 1
 STREAM_X = 1
 STREAM_LOGITS = 2
 STREAM_PERM = 3
+STREAM_GRID = 4
 STREAM_WEIGHTS = 16          # + 3 * expert + matrix (0 gate, 1 up, 2 down)
 DRAWS_PER_BLOCK = 32
 
@@ -137,6 +151,7 @@ class MatrixBytes:
     cols: int
     stride: int
     data: np.ndarray  # uint8 [rows * stride]
+    grid: Optional[np.ndarray] = None   # IQ3_XXS: the 256-entry grid (uint32)
 
     @property
     def nbytes_unpadded(self) -> int:
@@ -176,6 +191,17 @@ def gen_blocks(fmt: int, key: int, block_idx: np.ndarray) -> np.ndarray:
         lo32 = (r[:, 0] & np.uint64(0xFFFFFFFF)).astype(np.uint64)
         out[:, 0] = (124 + ((lo32 * np.uint64(3)) >> np.uint64(32))).astype(np.uint8)
         out[:, 1:17] = _bytes_of(r[:, 1:3])
+    elif fmt == IQ4_NL:
+        out[:, 0:2] = _f16_uniform(r[:, 0], 0.002, 0.018).view(np.uint8).reshape(n, 2)
+        out[:, 2:18] = _bytes_of(r[:, 1:3])
+    elif fmt == IQ4_XS:
+        out[:, 0:2] = _f16_uniform(r[:, 0], 2e-4, 1e-3).view(np.uint8).reshape(n, 2)
+        out[:, 2:8] = _bytes_of(r[:, 1:2])[:, 0:6]
+        out[:, 8:136] = _bytes_of(r[:, 2:18])
+    elif fmt == IQ3_XXS:
+        out[:, 0:2] = _f16_uniform(r[:, 0], 0.001, 0.009).view(np.uint8).reshape(n, 2)
+        out[:, 2:66] = _bytes_of(r[:, 1:9])
+        out[:, 66:98] = _bytes_of(r[:, 9:13])
     else:
         raise ValueError(f"unknown format {fmt}")
     return out
@@ -194,6 +220,14 @@ def gen_matrix(fmt: int, rows: int, cols: int, key: int, stride: Optional[int] =
     return MatrixBytes(fmt, rows, cols, stride, data.reshape(-1))
 
 
+def iq3_grid() -> np.ndarray:
+    """The synthetic IQ3_XXS grid (uint32 [256]), the same for every layer."""
+    r = draws(stream_key(0, STREAM_GRID), np.arange(256))
+    idx = _ubelow16(_chunks16(r[:, None]), 8).reshape(256, 4)
+    mag = IQ3_MAGNITUDES[idx]
+    return (mag[:, 0] | (mag[:, 1] << 8) | (mag[:, 2] << 16) | (mag[:, 3] << 24)).astype(np.uint32)
+
+
 def weight_key(seed: int, expert: int, matrix: int) -> int:
     return stream_key(seed, STREAM_WEIGHTS + 3 * expert + matrix)
 
@@ -209,7 +243,7 @@ class LayerConfig:
     hidden: int
     inter: int
     tokens: int
-    tiers: str            # "q8_0" (all Q8_0), "q4k" (Q4_K gate/up + Q8_0 down), "mixed"
+    tiers: str            # "q8_0" (all Q8_0), "q4k" (Q4_K gate/up + Q8_0 down), "mixed", "mixed_iq"
     zipf_bias: bool
     seed_base: int        # layer l uses seed seed_base + l (tiny: seed 0)
 
@@ -220,6 +254,9 @@ CONFIGS: Dict[str, LayerConfig] = {
     "decode16": LayerConfig("decode16", 512, 10, 2048, 640, 16, "q4k", True, 3000),
     "mtp6": LayerConfig("mtp6", 512, 10, 2048, 640, 6, "mixed", True, 4000),
     "prefill2048": LayerConfig("prefill2048", 512, 10, 2048, 640, 2048, "mixed", True, 5000),
+    # the pages' own tier formats: Q6_K/Q8_0, IQ4_XS/IQ4_NL, IQ3_XXS/MXFP4
+    "mtp6_iq": LayerConfig("mtp6_iq", 512, 10, 2048, 640, 6, "mixed_iq", True, 6000),
+    "prefill2048_iq": LayerConfig("prefill2048_iq", 512, 10, 2048, 640, 2048, "mixed_iq", True, 7000),
 }
 
 
@@ -244,7 +281,8 @@ def expert_formats(cfg: LayerConfig, seed: int) -> List[Tuple[int, int]]:
         return [(Q8_0, Q8_0)] * E
     if cfg.tiers == "q4k":
         return [(Q4_K, Q8_0)] * E
-    if cfg.tiers == "mixed":
+    if cfg.tiers in ("mixed", "mixed_iq"):
+        iq = cfg.tiers == "mixed_iq"
         perm = permutation(seed, E)
         a, b = tier_bounds(E)
         fm: List[Tuple[int, int]] = [(0, 0)] * E
@@ -252,9 +290,9 @@ def expert_formats(cfg: LayerConfig, seed: int) -> List[Tuple[int, int]]:
             if rank < a:
                 fm[int(e)] = (Q6_K, Q8_0)
             elif rank < b:
-                fm[int(e)] = (Q4_K, Q8_0)
+                fm[int(e)] = (IQ4_XS, IQ4_NL) if iq else (Q4_K, Q8_0)
             else:
-                fm[int(e)] = (MXFP4, MXFP4)
+                fm[int(e)] = (IQ3_XXS, MXFP4) if iq else (MXFP4, MXFP4)
         return fm
     raise ValueError(cfg.tiers)
 
@@ -269,11 +307,15 @@ def expert_matrices(cfg: LayerConfig, seed: int, expert: int,
         fmts = expert_formats(cfg, seed)[expert]
     gu, dn = fmts
     H, I = cfg.hidden, cfg.inter
-    return {
+    m = {
         "gate": gen_matrix(gu, I, H, weight_key(seed, expert, GATE)),
         "up": gen_matrix(gu, I, H, weight_key(seed, expert, UP)),
         "down": gen_matrix(dn, H, I, weight_key(seed, expert, DOWN)),
     }
+    for v in m.values():
+        if v.fmt == IQ3_XXS:
+            v.grid = iq3_grid()
+    return m
 
 
 # --------------------------------------------------------------------------

@@ -40,8 +40,9 @@ __device__ __forceinline__ uint8_t byte_of(uint64_t r, int i) { return (uint8_t)
 
 __global__ void synth_fill_kernel(const moe_synth_matrix *__restrict__ descs) {
     const moe_synth_matrix M = descs[blockIdx.y];
-    const int be = (M.format == 2 || M.format == 3) ? 256 : 32;
-    const int bb = M.format == 1 ? 34 : M.format == 2 ? 144 : M.format == 3 ? 210 : 17;
+    const int be = (M.format == 2 || M.format == 3 || M.format == 6 || M.format == 7) ? 256 : 32;
+    const int bb = M.format == 1 ? 34 : M.format == 2 ? 144 : M.format == 3 ? 210 : M.format == 4 ? 17
+                 : M.format == 5 ? 18 : M.format == 6 ? 136 : 98;
     const int nb = M.cols / be;
     const int64_t nblocks = (int64_t)M.rows * nb;
     const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -78,12 +79,32 @@ __global__ void synth_fill_kernel(const moe_synth_matrix *__restrict__ descs) {
                 out[192 + 4 * g + c] = (uint8_t)(ubelow16((r >> (16 * c)) & 0xFFFF, 255) - 127);
         }
         put16(out + 208, f16_uniform(draw(key, base + 28), (float)1e-4, (float)9e-4));
-    } else {  // MXFP4
+    } else if (M.format == 4) {  // MXFP4
         uint64_t r0 = draw(key, base + 0);
         out[0] = (uint8_t)(124 + (((r0 & 0xFFFFFFFFull) * 3ull) >> 32));
         for (int g = 0; g < 2; ++g) {
             uint64_t r = draw(key, base + 1 + g);
             for (int c = 0; c < 8; ++c) out[1 + 8 * g + c] = byte_of(r, c);
+        }
+    } else if (M.format == 5) {  // IQ4_NL (fp16 d at an even offset of the 16-aligned row: 18 j is even)
+        put16(out, f16_uniform(draw(key, base + 0), (float)0.002, (float)0.018));
+        for (int g = 0; g < 2; ++g) {
+            uint64_t r = draw(key, base + 1 + g);
+            for (int c = 0; c < 8; ++c) out[2 + 8 * g + c] = byte_of(r, c);
+        }
+    } else if (M.format == 6) {  // IQ4_XS
+        put16(out, f16_uniform(draw(key, base + 0), (float)2e-4, (float)1e-3));
+        const uint64_t r1 = draw(key, base + 1);
+        for (int c = 0; c < 6; ++c) out[2 + c] = byte_of(r1, c);
+        for (int g = 0; g < 16; ++g) {
+            uint64_t r = draw(key, base + 2 + g);
+            for (int c = 0; c < 8; ++c) out[8 + 8 * g + c] = byte_of(r, c);
+        }
+    } else {  // IQ3_XXS
+        put16(out, f16_uniform(draw(key, base + 0), (float)0.001, (float)0.009));
+        for (int g = 0; g < 12; ++g) {
+            uint64_t r = draw(key, base + 1 + g);
+            for (int c = 0; c < 8; ++c) out[2 + 8 * g + c] = byte_of(r, c);
         }
     }
     if (j == nb - 1) {  // zero the row padding

@@ -14,8 +14,8 @@ from typing import Dict, List, Optional, Tuple
 import numpy as np
 import torch
 
-from . import (DOWN, GATE, UP, LayerConfig, expert_formats, gen_logits, gen_x_bf16, layer_seed, padded_stride,
-               row_bytes, weight_key, BLOCK_ELEMS)
+from . import (DOWN, GATE, IQ3_XXS, UP, LayerConfig, expert_formats, gen_logits, gen_x_bf16, iq3_grid, layer_seed,
+               padded_stride, row_bytes, weight_key, BLOCK_ELEMS)
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe_synth.so")
 
@@ -75,6 +75,7 @@ class DeviceLayer:
     x_host: np.ndarray                      # uint16 bf16 bits [T, H]
     logits_host: np.ndarray                 # fp32 [T, E]
     weight_bytes_unpadded: int
+    grid: Optional[torch.Tensor] = None     # IQ3_XXS grid (int32 [256] on the device), if the layer has IQ3_XXS
 
     def expert_bytes(self, e: int) -> int:
         gu, dn = self.fmts[e]
@@ -110,4 +111,7 @@ def make_device_layer(cfg: LayerConfig, layer: int = 0, tokens: Optional[int] = 
     x = torch.from_numpy(x_host.view(np.int16).copy()).to("cuda").view(torch.bfloat16)
     lg = torch.from_numpy(logits_host.copy()).to("cuda")
     unpadded = sum(2 * I * row_bytes(gu, H) + H * row_bytes(dn, I) for gu, dn in fmts)
-    return DeviceLayer(cfg, seed, fmts, storage, experts, x, lg, x_host, logits_host, unpadded)
+    grid = None
+    if any(IQ3_XXS in f for f in fmts):
+        grid = torch.from_numpy(iq3_grid().view(np.int32).copy()).to("cuda")
+    return DeviceLayer(cfg, seed, fmts, storage, experts, x, lg, x_host, logits_host, unpadded, grid)

@@ -91,7 +91,7 @@ def oracle_full_layer(cfg: synth.LayerConfig, DL, tokens=None) -> np.ndarray:
     `tokens` (default: all), expert by expert over a process pool; cached per
     (config, seed, tokens) for the session."""
     from oracle import ffn as offn
-    key = (cfg.name, DL.seed, None if tokens is None else tuple(tokens))
+    key = (cfg.name, DL.seed, DL.x_host.shape[0], None if tokens is None else tuple(tokens))
     if key not in _ORACLE_CACHE:
         lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
         with oracle_pool() as pool:

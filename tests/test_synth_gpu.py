@@ -14,7 +14,8 @@ def test_gpu_filler_matches_numpy():
     ensure_built()
     from synth import gpu as sgpu
     cases = [(synth.Q8_0, 7, 640), (synth.Q8_0, 3, 256), (synth.Q4_K, 5, 2048), (synth.Q6_K, 4, 512),
-             (synth.MXFP4, 6, 640), (synth.MXFP4, 2, 2048)]
+             (synth.MXFP4, 6, 640), (synth.MXFP4, 2, 2048), (synth.IQ4_NL, 5, 640), (synth.IQ4_NL, 3, 96),
+             (synth.IQ4_XS, 4, 2048), (synth.IQ3_XXS, 6, 512)]
     mats, refs = [], []
     for i, (fmt, rows, cols) in enumerate(cases):
         key = synth.stream_key(1234, 40 + i)
@@ -27,10 +28,11 @@ def test_gpu_filler_matches_numpy():
         np.testing.assert_array_equal(t.cpu().numpy(), ref.data)
 
 
-def test_device_layer_matches_lazy_experts():
+@pytest.mark.parametrize("name", ["mtp6", "mtp6_iq"])
+def test_device_layer_matches_lazy_experts(name):
     ensure_built()
     from synth import gpu as sgpu
-    cfg = synth.CONFIGS["mtp6"]
+    cfg = synth.CONFIGS[name]
     DL = sgpu.make_device_layer(cfg, 0)
     lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
     perm = synth.permutation(DL.seed, cfg.n_experts)
@@ -40,3 +42,5 @@ def test_device_layer_matches_lazy_experts():
             m = lazy[e][name]
             assert (fmt, rows, cols, stride) == (m.fmt, m.rows, m.cols, m.stride)
             np.testing.assert_array_equal(view.cpu().numpy(), m.data)
+    if name == "mtp6_iq":
+        np.testing.assert_array_equal(DL.grid.cpu().numpy().view(np.uint32), synth.iq3_grid())
