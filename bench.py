@@ -40,9 +40,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer tokens/s; expert-weight HBM GB/s and % of GB300 roofline"
 UNIT = "tokens/s"
-KERNELS_PER_LAYER = {1: 5,   # GEMV: route, bucket, gate/up, down, combine
-                     2: 7,   # tensor: route, bucket, prep, gate/up GEMM, h conversion, down GEMM, combine
-                     3: 1}   # fused decode: one kernel
+KERNELS_PER_LAYER = {1: 4,   # GEMV: route, gate/up, down, combine (+ bucketing)
+                     2: 6,   # tensor: route, prep, gate/up GEMM, h conversion, down GEMM, combine (+ bucketing)
+                     3: 1}   # fused decode: one kernel (its own routing and bucketing)
+
+
+def launches_per_layer(path: int, pairs: int) -> int:
+    """Our kernel launches per layer: the bucketing is one kernel up to 2,048
+    (token, slot) pairs and three (histograms, scan, scatter) above."""
+    if path == 3:
+        return 1
+    return KERNELS_PER_LAYER[path] + (1 if pairs <= 2048 else 3)
 
 
 def parse_args(argv=None):
@@ -533,7 +541,7 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
         "tensor_pipe": tensor_pipe,
         "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
-        "gpu_launches": KERNELS_PER_LAYER[path] * NL * steps,
+        "gpu_launches": launches_per_layer(path, T * k) * NL * steps,
         "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
                  M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
         "clocks": clk,

@@ -58,7 +58,8 @@ class WeightTableC(ctypes.Structure):
                 ("down_formats", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
                 ("max_down_stride", ctypes.c_int64), ("uniform_layout", ctypes.c_int32),
                 ("tc_maps", ctypes.c_int32), ("uniform_base", Expert),
-                ("uniform_step", ctypes.c_int64 * 3), ("iq3_grid", ctypes.c_void_p)]
+                ("uniform_step", ctypes.c_int64 * 3), ("iq3_grid", ctypes.c_void_p), ("n_cold", ctypes.c_int32),
+                ("reserved2", ctypes.c_int32), ("cold_bytes_max", ctypes.c_int64)]
 
 
 class Options(ctypes.Structure):
@@ -156,7 +157,10 @@ class WeightTable:
         for e, ex in enumerate(experts):
             for name in ("gate", "up", "down"):
                 fmt, rows, cols, stride, data = ex[name]
-                _dev(data, f"expert {e} {name}", torch.uint8)
+                if data.is_cuda:
+                    _dev(data, f"expert {e} {name}", torch.uint8)
+                elif not (data.is_pinned() and data.dtype == torch.uint8 and data.is_contiguous()):
+                    raise ValueError(f"expert {e} {name}: a CUDA tensor, or a pinned host tensor (cold tier)")
                 self._keep.append(data)
                 setattr(arr[e], name, Matrix(fmt, rows, cols, 0, stride, data.data_ptr()))
         self._arr = arr

@@ -26,7 +26,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-r
 LIBS = {
     "moe_route": {
         "out": os.path.join(PKG, "libmoe_route.so"),
-        "srcs": [os.path.join(PKG, "csrc", f) for f in ("api.cu", "route.cu", "bucket.cu", "gemv.cu", "stream.cu", "decode.cu", "tc.cu", "noalloc.cu", "shard.cu")],
+        "srcs": [os.path.join(PKG, "csrc", f) for f in ("api.cu", "route.cu", "bucket.cu", "gemv.cu", "stream.cu", "decode.cu", "tc.cu", "noalloc.cu", "shard.cu", "cold.cu")],
         "deps": [os.path.join(PKG, "csrc", "moe_internal.cuh"), os.path.join(PKG, "csrc", "dot16.cuh"),
                  os.path.join(INCLUDE, "moe_route.h")],
     },

@@ -66,8 +66,30 @@ cudaError_t record_timing_event(cudaEvent_t ev, cudaStream_t s) {
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Offset of the tensor path's weight maps in the prepared device table.
+// Offset of the tensor path's weight maps in the prepared device table, and
+// of the per-expert cold flags after them.
 size_t map_offset(int E) { return align_up((size_t)E * sizeof(DevExpert), 128); }
+size_t cold_offset(int E) { return align_up(map_offset(E) + tc_weight_map_bytes(E), 256); }
+
+// Where a matrix's bytes live: 1 device memory, 0 host memory the GPU can read
+// (pinned or registered; the cold tier), -1 neither. *dptr: the device-side
+// address.
+int locate(const void *p, const void **dptr) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+        *dptr = p;
+        return 1;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer) {
+        *dptr = a.devicePointer;
+        return 0;
+    }
+    return -1;
+}
 
 int check_matrix(const moe_matrix &m, int rows, int cols) {
     if (m.format < MOE_Q8_0 || m.format > MOE_IQ3_XXS) return MOE_ERR_BAD_FORMAT;
@@ -82,9 +104,13 @@ int check_matrix(const moe_matrix &m, int rows, int cols) {
 
 // Resolve the path of a forward; -1 if the requested path cannot run it.
 int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
-    const bool fused_ok = decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
-                                                W->down_formats, W->max_gateup_stride, W->max_down_stride);
-    const bool tc_ok = W->tc_maps == 1 && tc_path_eligible(W->hidden, W->inter);
+    // a table with cold (host-resident) experts runs on the grouped GEMV
+    // kernels, which read the routed cold experts from their staged copy
+    const bool hot_only = W->n_cold == 0;
+    const bool fused_ok = hot_only && decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter,
+                                                            W->gateup_formats, W->down_formats, W->max_gateup_stride,
+                                                            W->max_down_stride);
+    const bool tc_ok = hot_only && W->tc_maps == 1 && tc_path_eligible(W->hidden, W->inter);
     const bool stream_ok = stream_plan(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats, W->down_formats,
                                        W->max_gateup_stride, W->max_down_stride).ok;
     switch (requested) {
@@ -105,7 +131,10 @@ int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
 // Workspace bytes of a forward on `path` (the tensor path adds its regions).
 size_t path_ws_bytes(const moe_weight_table *W, int T, int k, int path) {
     if (path == MOE_PATH_TENSOR) return tc_ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
-    return ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
+    const size_t base = ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
+    if (W->prepared == MOE_TABLE_PREPARED && W->n_cold > 0)
+        return cold_ws_layout(base, T, k, W->n_experts, W->n_cold, W->cold_bytes_max).total;
+    return base;
 }
 
 // Options with defaults filled in; false if they are invalid.
@@ -142,7 +171,7 @@ int moe_last_cuda_error(void) { return g_last_cuda_error; }
 
 size_t moe_table_device_bytes(int32_t n_experts) {
     if (n_experts <= 0 || n_experts > MOE_MAX_EXPERTS) return 0;
-    return align_up(map_offset(n_experts) + tc_weight_map_bytes(n_experts), 256);
+    return align_up(cold_offset(n_experts) + (size_t)n_experts, 256);
 }
 
 int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes, moe_stream_t stream) {
@@ -153,8 +182,10 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     if (H > MOE_MAX_HIDDEN || I > MOE_MAX_INTER) return MOE_ERR_UNSUPPORTED;
     if (device_bytes < moe_table_device_bytes(E) || !aligned(device_buf, 16)) return MOE_ERR_INVALID_ARG;
     std::vector<DevExpert> dev(E);
+    std::vector<uint8_t> cold(E, 0);
     uint32_t present = 0, gu_present = 0, dn_present = 0;
-    int64_t gu_max = 0, dn_max = 0;
+    int64_t gu_max = 0, dn_max = 0, cold_max = 0;
+    int n_cold = 0;
     for (int e = 0; e < E; ++e) {
         const moe_expert &x = W->experts[e];
         int rc;
@@ -170,11 +201,24 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
         dn_max = std::max<int64_t>(dn_max, x.down.row_stride_bytes);
         const moe_matrix *src[3] = {&x.gate, &x.up, &x.down};
         DevMatrix *dst[3] = {&dev[e].gate, &dev[e].up, &dev[e].down};
+        int where[3];
         for (int i = 0; i < 3; ++i) {
-            dst[i]->data = static_cast<const uint8_t *>(src[i]->data);
+            const void *dp = nullptr;
+            where[i] = locate(src[i]->data, &dp);
+            if (where[i] < 0) return MOE_ERR_INVALID_ARG;
+            dst[i]->data = static_cast<const uint8_t *>(dp);
             dst[i]->stride = src[i]->row_stride_bytes;
             dst[i]->fmt = src[i]->format;
             dst[i]->rows = src[i]->rows;
+        }
+        // a cold expert keeps all three matrices in host memory
+        if (where[0] != where[1] || where[0] != where[2]) return MOE_ERR_INVALID_ARG;
+        if (where[0] == 0) {
+            cold[e] = 1;
+            ++n_cold;
+            int64_t b = 0;
+            for (int i = 0; i < 3; ++i) b += (int64_t)align_up((size_t)src[i]->rows * src[i]->row_stride_bytes, 256);
+            cold_max = std::max(cold_max, b);
         }
     }
     if (gateup_smem_bytes(H, gu_max) > SMEM_LIMIT || down_smem_bytes(I, dn_max) > SMEM_LIMIT)
@@ -183,6 +227,9 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     if ((present & (1u << MOE_IQ3_XXS)) && (!W->iq3_grid || !aligned(W->iq3_grid, 16))) return MOE_ERR_INVALID_ARG;
     cudaError_t err = cudaMemcpyAsync(device_buf, dev.data(), (size_t)E * sizeof(DevExpert), cudaMemcpyHostToDevice,
                                       stream);
+    if (err != cudaSuccess) return cuda_fail(err);
+    err = cudaMemcpyAsync(static_cast<char *>(device_buf) + cold_offset(E), cold.data(), (size_t)E,
+                          cudaMemcpyHostToDevice, stream);
     if (err != cudaSuccess) return cuda_fail(err);
     // the tensor path's TMA descriptors of every weight matrix
     std::vector<unsigned char> maps;
@@ -224,6 +271,8 @@ int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes
     W->down_formats = dn_present;
     W->max_gateup_stride = gu_max;
     W->max_down_stride = dn_max;
+    W->n_cold = n_cold;
+    W->cold_bytes_max = cold_max;
     W->prepared = MOE_TABLE_PREPARED;
     return MOE_OK;
 }
@@ -325,10 +374,19 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
                              W->down_formats, static_cast<const uint32_t *>(W->iq3_grid), T, k, E, H, I, offsets,
                              active, pos, wts, x,
                              h, y, base, tc_ws_layout(T, k, E, H, I), out, status, events, stream);
-    else
+    else {
+        if (W->n_cold > 0) {
+            // the routed cold experts' bytes into the workspace, read through a remapped table
+            const ColdLayout CL = cold_ws_layout(L.total, T, k, E, W->n_cold, W->cold_bytes_max);
+            err = launch_cold_staging(table, static_cast<const uint8_t *>(W->device_table) + cold_offset(E), E,
+                                      active, base, CL, stream);
+            if (err != cudaSuccess) return cuda_fail(err);
+            table = reinterpret_cast<const DevExpert *>(base + CL.remap);
+        }
         err = launch_gemv_path(table, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, W->gateup_formats,
                                W->down_formats, static_cast<const uint32_t *>(W->iq3_grid), offsets, pairs, active,
                                pos, wts, x, h, y, out, status, events, stream);
+    }
     if (err != cudaSuccess) return cuda_fail(err);
     return MOE_OK;
 }

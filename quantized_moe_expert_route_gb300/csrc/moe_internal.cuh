@@ -90,6 +90,32 @@ inline TcLayout tc_ws_layout(int T, int k, int E, int H, int I) {
     return C;
 }
 
+// The cold-expert tier (cold.cu): workspace regions after the path's own
+// (remapped descriptor table, copy segments, staging of the routed cold
+// experts' bytes), present when the weight table has cold experts.
+struct ColdSeg {
+    const uint8_t *src;
+    uint8_t *dst;
+    uint64_t bytes;
+};
+struct ColdLayout {
+    size_t remap, segs, n_segs, staging, total;
+};
+inline ColdLayout cold_ws_layout(size_t after, int T, int k, int E, int n_cold, int64_t cold_bytes_max) {
+    ColdLayout C;
+    size_t o = after;
+    auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, 256); return r; };
+    const size_t P = (size_t)T * k, nc = P < (size_t)n_cold ? P : (size_t)n_cold;
+    C.remap = take((size_t)E * sizeof(DevExpert));
+    C.segs = take(3 * nc * sizeof(ColdSeg));
+    C.n_segs = take(4);
+    C.staging = take(nc * (size_t)cold_bytes_max);
+    C.total = o;
+    return C;
+}
+cudaError_t launch_cold_staging(const DevExpert *table, const uint8_t *cold, int E, const int32_t *active,
+                                char *ws_base, const ColdLayout &C, cudaStream_t s);
+
 constexpr int BLOCK_ELEMS[8] = {0, 32, 256, 256, 32, 32, 256, 256};
 constexpr int BLOCK_BYTES[8] = {0, 34, 144, 210, 17, 18, 136, 98};
 

@@ -284,11 +284,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(int N) {
     return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(TC_M >> 4) << 24);
 }
 
-// Hint: bring `bytes` (a multiple of 16) at `src` (16-byte aligned) into L2.
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
@@ -428,32 +423,20 @@ __device__ __forceinline__ void dq_q6k(uint32_t blk, int g, uint32_t (&r)[32]) {
 __device__ __forceinline__ uint32_t e2m1_pair_bits(uint32_t x) {
     return ((x & 0x00070007u) << 9) | ((x & 0x00080008u) << 12);
 }
-// fp16 pair (2^k, 2^k) for -24 <= k <= 15 (subnormal below -14).
-__device__ __forceinline__ uint32_t pow2_half2(int k) {
-    const uint32_t h = k >= -14 ? (uint32_t)(k + 15) << 10 : 0x0200u >> (-15 - k);
-    return h * 0x10001u;
-}
 // The two fp16 factors SA, SB with (v * 2^-14) * SA * SB = v * 2^(e-127) for an
 // E2M1 value v, such that the first product is exact and only the second
 // rounds (one rounding in all): e in [99, 128] takes SA = 2^(e-113), SB = 1;
 // larger e takes SA = 2^15 and the rest in SB (results beyond fp16 range
 // overflow, as any weight outside it would); e < 99 gives |w| < 2^-26, which
-// rounds to 0; e = 255 (NaN in E8M0) gives NaN.
+// rounds to 0; e = 255 (NaN in E8M0) gives NaN. Selects, no branches: the
+// lanes of a warp hold different rows' scales.
 __device__ __forceinline__ void mxfp4_scales(uint32_t e, uint32_t &SA, uint32_t &SB) {
     const int k = (int)e - 113;
-    if (e == 255u) {
-        SA = 0x7e007e00u;
-        SB = 0x3c003c00u;
-    } else if (k > 15) {
-        SA = pow2_half2(15);
-        SB = pow2_half2(min(k - 15, 15));
-    } else if (k >= -14) {
-        SA = pow2_half2(k);
-        SB = 0x3c003c00u;
-    } else {
-        SA = 0u;
-        SB = 0x3c003c00u;
-    }
+    const int ka = min(max(k, -14), 15), kb = min(max(k - 15, 0), 15);
+    SA = ((uint32_t)(ka + 15) << 10) * 0x10001u;
+    SB = ((uint32_t)(kb + 15) << 10) * 0x10001u;
+    SA = k < -14 ? 0u : SA;
+    SA = e == 255u ? 0x7e007e00u : SA;
 }
 // MXFP4: piece g = blocks 2g and 2g+1 of the stage (17 bytes each) at byte
 // 34g of `blk`; element i < 16 of a block is the low nibble of qs[i], element
@@ -724,29 +707,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     const int G = gridDim.x;
 
     if (warp == TC_PROD) {
-        // ---- weight producer: per raw stage one 2-D TMA box per matrix (two for Q8_0).
-        // A unit's weight rows are contiguous in memory (R rows of each matrix),
-        // while a raw stage takes a 256-wide K slice of every row: the rows are
-        // prefetched into L2 as whole contiguous blocks one unit ahead, so DRAM
-        // streams them sequentially and the boxes are served from L2.
+        // ---- weight producer: per raw stage one 2-D TMA box per matrix (two for Q8_0)
         if (lane == 0) {
             uint32_t rg = 0;
             bool ok = true;
-            auto prefetch_unit = [&](const Unit &x) {
-                const DevExpert &ex = A.table[x.e];
-                const DevMatrix &m0 = GATEUP ? ex.gate : ex.down;
-                const uint32_t bytes = (uint32_t)(R * m0.stride);
-                prefetch_l2(m0.data + (size_t)R * x.s * m0.stride, bytes);
-                if (GATEUP) prefetch_l2(ex.up.data + (size_t)R * x.s * ex.up.stride, (uint32_t)(R * ex.up.stride));
-            };
             Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, true) : Unit{};
-            if (blockIdx.x < n_units) prefetch_unit(nxt);
             for (int u = blockIdx.x; u < n_units && ok; u += G) {
                 const Unit cu = nxt;
-                if (u + G < n_units) {
-                    nxt = load_unit<GATEUP>(A, u + G, true);
-                    prefetch_unit(nxt);
-                }
+                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, true);
                 const int W = raw_w(cu.fmt), nbox = raw_nbox(cu.fmt);
                 const uint32_t bytes = (uint32_t)(NMAT * nbox * R * W);
                 const CUtensorMap *m0 = A.wmaps + 3 * cu.e + (GATEUP ? 0 : 2);
@@ -808,7 +776,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         }
     } else if (warp == TC_MMA) {
         // ---- MMA issuer: one thread; per event (raw stage) one wait on the dequantisers'
-        // counter, up to 16 MMAs back to back, one commit
+        // counter, then per B stage (one of 4 A steps, or two of 2 when the chunk has more
+        // than 64 rows) one wait and its MMAs back to back, then one commit
         if (lane == 0) {
             uint32_t ev = 0, bg = 0, uc = 0;
             bool ok = true, issued = false;
@@ -826,8 +795,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                 }
                 tmem_fence_after();
                 const uint32_t dcol = tmem + d * TC_NCHUNK;
-                int sub = 0;
-                uint64_t bdesc = 0;
                 for (int rs = 0; rs < nR; ++rs) {
                     const int na = min(TC_AEV, nA - TC_AEV * rs);
                     const uint32_t slot = ev & (TC_EVSLOTS - 1);
@@ -837,30 +804,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                     }
                     tmem_fence_after();
                     const uint32_t acol0 = tmem + TC_ACOL0 + slot * (TC_AEV * 32);
+                    // the raw stage's B stages: one of 4 A steps (q = 4) or two of 2
+                    for (int h0 = 0; h0 < na; h0 += q) {
+                        const uint32_t bs = bg % TC_BSTAGES;
+                        if (!tc_spin(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tmem_fence_after();
+                        const uint64_t bd = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES));
+                        const int nh = min(q, na - h0);
 #pragma unroll
-                    for (int i = 0; i < TC_AEV; ++i) {
-                        if (i >= na) break;
-                        if (sub == 0) {
-                            const uint32_t bs = bg % TC_BSTAGES;
-                            if (!tc_spin(&b_full[bs], (bg / TC_BSTAGES) & 1, abort_flag)) {
-                                ok = false;
-                                break;
+                        for (int i = 0; i < 4; ++i) {
+                            if (i < nh) {
+                                const uint32_t acol = acol0 + 32 * (h0 + i);
+                                const uint64_t b0 = bd + (uint64_t)(i * sub_step);
+                                mma_f16_ts(dcol, acol, b0, idesc, (rs | h0 | i) != 0);
+                                mma_f16_ts(dcol, acol + 8, b0 + 2, idesc, 1);
+                                mma_f16_ts(dcol, acol + 16, b0 + 4, idesc, 1);
+                                mma_f16_ts(dcol, acol + 24, b0 + 6, idesc, 1);
                             }
-                            tmem_fence_after();
-                            bdesc = smem_desc_sw128(smem_addr(bring + bs * TC_BSTAGE_BYTES));
                         }
-                        const uint32_t acol = acol0 + 32 * i;
-                        mma_f16_ts(dcol, acol, bdesc, idesc, (rs | i) != 0);
-                        mma_f16_ts(dcol, acol + 8, bdesc + 2, idesc, 1);
-                        mma_f16_ts(dcol, acol + 16, bdesc + 4, idesc, 1);
-                        mma_f16_ts(dcol, acol + 24, bdesc + 6, idesc, 1);
-                        issued = true;
-                        bdesc += sub_step;
-                        if (++sub == q || TC_AEV * rs + i == nA - 1) {
-                            mma_commit(&b_empty[bg % TC_BSTAGES]);
-                            ++bg;
-                            sub = 0;
-                        }
+                        issued = true;   // before any later wait can give up: TMEM is freed only after these complete
+                        mma_commit(&b_empty[bs]);
+                        ++bg;
                     }
                     if (!ok) break;
                     mma_commit(&a_empty[slot]);
