@@ -105,7 +105,14 @@ typedef enum {
 /* One quantized matrix: `rows` rows of `cols` weights, blocks along the
  * columns (the reduction axis). Row r starts at data + r * row_stride_bytes.
  * row_stride_bytes >= (cols / block_elems) * block_bytes and a multiple of 16;
- * data is a 16-byte aligned device pointer to rows * row_stride_bytes bytes. */
+ * data is a 16-byte aligned pointer to rows * row_stride_bytes bytes, in
+ * device memory, or, for the experts of the cold tier, in pinned or registered
+ * host memory that the GPU can read (on GB300 the Grace CPU's memory, read
+ * over NVLink-C2C; "三张 RTX 3090 …", section 优化策略一 keeps the coldest experts
+ * in host RAM). An expert's three matrices are all in device memory or all in
+ * host memory. A layer with cold experts runs on the grouped GEMV path: after
+ * routing, the routed cold experts' bytes are copied by the GPU into the
+ * workspace (sized by moe_ffn_workspace_size) and read from there. */
 typedef struct {
     int32_t format;            /* moe_format */
     int32_t rows;
@@ -150,6 +157,10 @@ typedef struct {
     /* ---- filled by the caller ---- */
     const void *iq3_grid;      /* device uint32 [256], 16-byte aligned: the IQ3_XXS grid
                                   (required if any matrix is IQ3_XXS, else may be NULL) */
+    /* ---- written by moe_table_prepare ---- */
+    int32_t n_cold;            /* experts whose weights are in host memory (the cold tier) */
+    int32_t reserved2;
+    int64_t cold_bytes_max;    /* largest cold expert, bytes (256-aligned matrices) */
 } moe_weight_table;
 
 /* Paths for moe_options.path. */
