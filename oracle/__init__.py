@@ -23,7 +23,7 @@ byte layouts, router equations or combine order; the readings taken are listed
 in each module's docstring.
 
 Modules:
-    formats  block decoders (Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS) -> dense fp64 matrices
+    formats  block decoders (Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS, t5_g128) -> dense fp64 matrices
     router   softmax / top-k with the lower-index tie-break
     bucket   per-expert pair lists (counts, exclusive prefix sum, stable scatter)
     ffn      the layer (pair by pair, and expert by expert with bounded memory for

@@ -7,7 +7,11 @@ Q8_0/Q4_K/Q6_K in the GGUF list of "一张 RTX 3090 跑 Llama 70B", section 一)
 print no byte layout. Reading taken: the public GGUF block layouts for
 Q8_0/Q4_K/Q6_K/IQ4_NL/IQ4_XS/IQ3_XXS and the OCP Microscaling (MX) v1.0
 element/scale encoding for MXFP4, little-endian, fp16 = IEEE binary16
-(subnormals included). Each decoder below states its layout. IQ3_XXS maps
+(subnormals included); the ternary t5_g128 format of "RTX 4080 SUPER 原生
+Windows 跑 27B" (section 九.2) is described there only by its packing (five
+base-3 weights per byte, one fp16 scale per 128 weights), and the layout below
+is the plainest one that fits it (scale first, digits least significant
+first). Each decoder below states its layout. IQ3_XXS maps
 8-bit indices through a 256-entry grid of four magnitudes; the grid is an
 input of the decoder (its values are not reproduced here).
 
@@ -18,9 +22,9 @@ from __future__ import annotations
 
 import numpy as np
 
-Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS = 1, 2, 3, 4, 5, 6, 7
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32, IQ4_NL: 32, IQ4_XS: 256, IQ3_XXS: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17, IQ4_NL: 18, IQ4_XS: 136, IQ3_XXS: 98}
+Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS, T5_G128 = 1, 2, 3, 4, 5, 6, 7, 8
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32, IQ4_NL: 32, IQ4_XS: 256, IQ3_XXS: 256, T5_G128: 128}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17, IQ4_NL: 18, IQ4_XS: 136, IQ3_XXS: 98, T5_G128: 28}
 
 # The non-linear 4-bit codebook of IQ4_NL and IQ4_XS: value of code 0..15.
 IQ4_CODEBOOK = np.array([-127, -104, -83, -65, -49, -35, -22, -10, 1, 13, 25, 38, 53, 69, 89, 113],
@@ -217,8 +221,21 @@ def dequant_iq3_xxs(blk: np.ndarray, grid: np.ndarray) -> np.ndarray:
     return out
 
 
+def dequant_t5_g128(blk: np.ndarray) -> np.ndarray:
+    """Ternary t5_g128 ("RTX 4080 SUPER 原生 Windows 跑 27B", section 九.2: ternary
+    codes packed base-3, five weights per byte, and one fp16 scale per 128
+    weights, 1.75 bits per weight), 28 bytes per 128 weights: fp16 scale s at
+    [0:2], 26 code bytes at [2:28]. Weight 5b + i (i < 5) is base-3 digit i
+    of byte 2 + b, least significant first (digit i = floor(v / 3^i) mod 3);
+    the last byte's digits 3 and 4 are unused. w = s * (digit - 1)."""
+    s = _f16(blk[..., 0:2])
+    v = blk[..., 2:28].astype(np.int64)
+    digits = np.stack([(v // 3 ** i) % 3 for i in range(5)], axis=-1).reshape(blk.shape[:-1] + (130,))
+    return s[..., None] * (digits[..., :128] - 1).astype(np.float64)
+
+
 DECODERS = {Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q6_K: dequant_q6_k, MXFP4: dequant_mxfp4,
-            IQ4_NL: dequant_iq4_nl, IQ4_XS: dequant_iq4_xs, IQ3_XXS: dequant_iq3_xxs}
+            IQ4_NL: dequant_iq4_nl, IQ4_XS: dequant_iq4_xs, IQ3_XXS: dequant_iq3_xxs, T5_G128: dequant_t5_g128}
 
 
 def decode_blocks(fmt: int, blocks: np.ndarray, grid=None) -> np.ndarray:

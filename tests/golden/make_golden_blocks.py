@@ -212,12 +212,38 @@ def iq3_xxs_block():
     return b, expected, rule
 
 
+def t5_g128_block():
+    # s = 0.5 (0x3800). Byte b (b < 26) holds weights 5b..5b+4 with base-3
+    # digits (b + i) % 3 for i = 0..4, least significant first; w = 0.5 * (digit - 1).
+    #   byte 0: digits 0 1 2 0 1 -> 0 + 3 + 18 + 0 + 81  = 102 (0x66)
+    #   byte 1: digits 1 2 0 1 2 -> 1 + 6 + 0 + 27 + 162 = 196 (0xC4)
+    #   byte 2: digits 2 0 1 2 0 -> 2 + 0 + 9 + 54 + 0   = 65  (0x41)
+    # and the pattern repeats every three bytes.
+    codes = [[102, 196, 65][b % 3] for b in range(26)]
+    b = [0x00, 0x38] + codes
+    expected = [
+        (0, -0.5),     # byte 0 digit 0 = 0
+        (1, 0.0),      # byte 0 digit 1 = 1
+        (2, 0.5),      # byte 0 digit 2 = 2
+        (4, 0.0),      # byte 0 digit 4 = 1
+        (5, 0.0),      # byte 1 digit 0 = 1
+        (9, 0.5),      # byte 1 digit 4 = 2
+        (64, 0.0),     # byte 12 (like byte 0) digit 4 = 1
+        (100, 0.5),    # byte 20 (like byte 2) digit 0 = 2
+        (126, 0.5),    # byte 25 (like byte 1) digit 1 = 2
+        (127, -0.5),   # byte 25 digit 2 = 0
+    ]
+    rule = "s = 0.5; byte b holds digits (b + i) % 3 for i = 0..4, least significant first"
+    return b, expected, rule
+
+
 def write(name, fmt, block, expected, rule, grid=None):
     path = os.path.join(HERE, name)
     with open(path, "w") as f:
         f.write(f"# Hand-built {fmt} block. Construction: {rule}\n")
         f.write("# Expected weights hand-computed from the block layout (see make_golden_blocks.py).\n")
-        f.write("# Layout reading: GGUF block layouts (Q8_0/Q4_K/Q6_K/IQ4_NL/IQ4_XS/IQ3_XXS), OCP MX v1.0\n")
+        f.write("# Layout reading: GGUF block layouts (Q8_0/Q4_K/Q6_K/IQ4_NL/IQ4_XS/IQ3_XXS), OCP MX v1.0, and the\n")
+        f.write("# base-3 packing of 'RTX 4080 SUPER 原生 Windows 跑 27B', 九.2 (T5_G128)\n")
         f.write("# (MXFP4); format names from '三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南',\n")
         f.write("# 优化策略二.\n")
         f.write(f"format {fmt}\n")
@@ -238,3 +264,4 @@ if __name__ == "__main__":
     write("iq4_nl_block.txt", "IQ4_NL", *iq4_nl_block())
     write("iq4_xs_block.txt", "IQ4_XS", *iq4_xs_block())
     write("iq3_xxs_block.txt", "IQ3_XXS", *iq3_xxs_block(), grid=iq3_grid())
+    write("t5_g128_block.txt", "T5_G128", *t5_g128_block())

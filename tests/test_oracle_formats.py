@@ -17,7 +17,7 @@ import pytest
 from oracle import formats
 
 FMT = {"Q8_0": formats.Q8_0, "Q4_K": formats.Q4_K, "Q6_K": formats.Q6_K, "MXFP4": formats.MXFP4,
-       "IQ4_NL": formats.IQ4_NL, "IQ4_XS": formats.IQ4_XS, "IQ3_XXS": formats.IQ3_XXS}
+       "IQ4_NL": formats.IQ4_NL, "IQ4_XS": formats.IQ4_XS, "IQ3_XXS": formats.IQ3_XXS, "T5_G128": formats.T5_G128}
 
 
 def load_golden(path, with_grid=False):
@@ -228,6 +228,43 @@ def test_iq3_xxs_roundtrip():
     assert np.all((w < 0).sum(axis=1) % 2 == 0)
 
 
+def enc_t5(scale, trits):
+    """trits int [128] in {-1, 0, 1} -> 28 bytes (scale, then five base-3 digits per byte)."""
+    b = np.zeros(28, dtype=np.uint8)
+    b[0:2] = np.frombuffer(np.float16(scale).tobytes(), np.uint8)
+    d = np.concatenate([np.asarray(trits) + 1, np.ones(2, np.int64)])
+    for j in range(26):
+        b[2 + j] = sum(int(d[5 * j + i]) * 3 ** i for i in range(5))
+    return b
+
+
+def test_t5_g128_roundtrip():
+    rng = np.random.default_rng(8)
+    for _ in range(20):
+        trits = rng.integers(-1, 2, 128)
+        s = rng.uniform(0.1, 2.0)
+        np.testing.assert_array_equal(formats.dequant_t5_g128(enc_t5(s, trits)[None])[0],
+                                      float(np.float16(s)) * trits)
+    # every byte value decodes to digits 0..2 (values above 242 included)
+    blk = np.zeros((1, 28), np.uint8)
+    blk[0, 0:2] = np.frombuffer(np.float16(1.0).tobytes(), np.uint8)
+    blk[0, 2:] = 255
+    assert set(np.unique(formats.dequant_t5_g128(blk))) <= {-1.0, 0.0, 1.0}
+
+
+def _t5_msd_first(blk):
+    # digits most significant first
+    s = formats._f16(blk[..., 0:2])
+    v = blk[..., 2:28].astype(np.int64)
+    digits = np.stack([(v // 3 ** (4 - i)) % 3 for i in range(5)], axis=-1).reshape(blk.shape[:-1] + (130,))
+    return s[..., None] * (digits[..., :128] - 1).astype(np.float64)
+
+
+def _t5_no_offset(blk):
+    # the digit itself instead of digit - 1
+    return formats.dequant_t5_g128(blk) + formats._f16(blk[..., 0:2])[..., None]
+
+
 def test_iq3_xxs_needs_its_grid():
     with pytest.raises(ValueError):
         formats.decode_blocks(formats.IQ3_XXS, np.zeros((1, 98), np.uint8))
@@ -349,6 +386,8 @@ def _iq3_xxs_scale_half(blk, grid):
 
 
 @pytest.mark.parametrize("fmt,bad", [
+    (formats.T5_G128, _t5_msd_first),
+    (formats.T5_G128, _t5_no_offset),
     (formats.IQ4_NL, _iq4_nl_linear),
     (formats.IQ4_XS, _iq4_xs_unsigned_scale),
     (formats.IQ3_XXS, _iq3_xxs_no_parity),
