@@ -15,6 +15,13 @@ Readings taken where the pages are silent:
   out[t] = sum over slots j = 0..k-1, in ascending j, of w[t, j] * y_{t,j}.
 * x is the exact bf16 value; every weight is the exact decoded value; all
   arithmetic is fp64.
+* Shared experts ("多卡 CUDA 张量并行：DwarfStar 如何在 8 张 L40S 上跑出
+  120 t/s", memory layout: the model keeps shared experts beside the routed
+  ones, stored there in Q8_0) run on every token with weight 1 and are added
+  after the routed experts: with S shared experts as entries E .. E+S-1 of the
+  expert list, slot k + s of every token holds expert E + s, weight 1, and the
+  ascending-slot sum runs over all k + S slots. The expert-range and format
+  filters apply to them like to any expert.
 
 Experts are given as a list of mappings with keys "gate", "up", "down"; each
 value has attributes fmt, rows, cols, stride and data (uint8 bytes).
@@ -67,22 +74,41 @@ def expert_forward(Wg: np.ndarray, Wu: np.ndarray, Wd: np.ndarray, x: np.ndarray
     return g, u, h, y
 
 
+def token_slots(logits: np.ndarray, k: int, renormalize: bool, n_shared: int):
+    """Every token's slots: (ids [T, k + S], weights [T, k + S]): the router's
+    k experts, then the S shared experts E .. E+S-1 with weight 1."""
+    ids, w, _ = router.route_topk(logits, k, renormalize)
+    if n_shared == 0:
+        return ids, w
+    T, E = logits.shape
+    sid = np.broadcast_to(np.arange(E, E + n_shared, dtype=ids.dtype), (T, n_shared))
+    return np.concatenate([ids, sid], axis=1), np.concatenate([w, np.ones((T, n_shared), w.dtype)], axis=1)
+
+
+def _check_entries(experts, logits, n_shared):
+    if not 0 <= n_shared or len(experts) != logits.shape[1] + n_shared:
+        raise ValueError("the expert list must hold the E routed experts, then the n_shared shared ones")
+
+
 def moe_ffn(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, renormalize: bool = True,
             expert_lo: int = 0, expert_hi: Optional[int] = None, format_mask: int = 0xFFFFFFFF,
             tokens: Optional[Sequence[int]] = None, cache: Optional[DenseCache] = None,
-            gate_formats: Optional[Sequence[int]] = None):
+            gate_formats: Optional[Sequence[int]] = None, n_shared: int = 0):
     """Layer output fp64 [len(tokens) or T, H].
 
     Routing (router.route_topk) and bucketing (bucket.bucket) run on all T
     tokens; ``tokens`` only restricts which output rows are evaluated.
-    ``experts`` may be any indexable of length E (e.g. a lazy generator); only
-    the experts that are routed to are read. ``gate_formats`` (format tag of
-    each expert's gate matrix) is needed by the format filter; by default it is
-    read from every expert."""
+    ``experts`` may be any indexable of length E + n_shared (e.g. a lazy
+    generator): the E routed experts, then the shared ones; only the experts
+    that are routed to are read. ``gate_formats`` (format tag of each expert's
+    gate matrix) is needed by the format filter; by default it is read from
+    every expert."""
     x = bf16_bits_to_f64(x_bf16)
     T, H = x.shape
+    _check_entries(experts, logits, n_shared)
     E = len(experts)
-    ids, w, _ = router.route_topk(logits, k, renormalize)
+    ids, w = token_slots(logits, k, renormalize, n_shared)
+    k = k + n_shared
     if gate_formats is None:
         gate_formats = [experts[e]["gate"].fmt for e in range(E)]
     _, _, pos, _, _ = bucket_mod.bucket(ids, E, expert_lo, expert_hi, format_mask, gate_formats)
@@ -113,7 +139,7 @@ def _expert_job(job):
 def moe_ffn_by_expert(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, renormalize: bool = True,
                       expert_lo: int = 0, expert_hi: Optional[int] = None, format_mask: int = 0xFFFFFFFF,
                       tokens: Optional[Sequence[int]] = None,
-                      gate_formats: Optional[Sequence[int]] = None, map_fn=map):
+                      gate_formats: Optional[Sequence[int]] = None, map_fn=map, n_shared: int = 0):
     """The same layer output as ``moe_ffn``, evaluated one expert at a time:
     every routed pair of the wanted tokens is grouped by its expert, each
     expert's matrices are decoded once, applied to all of its rows, and
@@ -123,8 +149,10 @@ def moe_ffn_by_expert(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, r
     jobs carry ``experts`` and must then be picklable)."""
     x = bf16_bits_to_f64(x_bf16)
     T, H = x.shape
+    _check_entries(experts, logits, n_shared)
     E = len(experts)
-    ids, w, _ = router.route_topk(logits, k, renormalize)
+    ids, w = token_slots(logits, k, renormalize, n_shared)
+    k = k + n_shared
     if gate_formats is None:
         gate_formats = [experts[e]["gate"].fmt for e in range(E)]
     _, _, pos, _, _ = bucket_mod.bucket(ids, E, expert_lo, expert_hi, format_mask, gate_formats)
@@ -149,16 +177,19 @@ def moe_ffn_by_expert(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int, r
 
 
 def moe_ffn_bruteforce(experts, x_bf16: np.ndarray, logits: np.ndarray, k: int,
-                       renormalize: bool = True) -> np.ndarray:
+                       renormalize: bool = True, n_shared: int = 0) -> np.ndarray:
     """Independent second evaluation for small layers: every expert on every
-    token (dense fp64 matrices), then a dense [T, E] routing-weight matrix
-    selects and weights the results. Shares only the decoders and the router
-    with ``moe_ffn``; no bucketing, no per-pair loop."""
+    token (dense fp64 matrices), then a dense [T, E + S] routing-weight matrix
+    selects and weights the results (the shared experts' columns are all
+    ones). Shares only the decoders and the router with ``moe_ffn``; no
+    bucketing, no per-pair loop, no slot list."""
     x = bf16_bits_to_f64(x_bf16)
     T, H = x.shape
+    _check_entries(experts, logits, n_shared)
     E = len(experts)
     ids, w, _ = router.route_topk(logits, k, renormalize)
     R = np.zeros((T, E), dtype=np.float64)
+    R[:, E - n_shared:] = 1.0
     for t in range(T):
         for j in range(k):
             R[t, ids[t, j]] += w[t, j]

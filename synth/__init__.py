@@ -246,6 +246,12 @@ class LayerConfig:
     tiers: str            # "q8_0" (all Q8_0), "q4k" (Q4_K gate/up + Q8_0 down), "mixed", "mixed_iq"
     zipf_bias: bool
     seed_base: int        # layer l uses seed seed_base + l (tiny: seed 0)
+    n_shared: int = 0     # shared experts (Q8_0), entries n_experts .. n_experts + n_shared - 1
+
+    @property
+    def n_entries(self) -> int:
+        """Routed plus shared experts: the length of the layer's expert table."""
+        return self.n_experts + self.n_shared
 
 
 CONFIGS: Dict[str, LayerConfig] = {
@@ -257,6 +263,9 @@ CONFIGS: Dict[str, LayerConfig] = {
     # the pages' own tier formats: Q6_K/Q8_0, IQ4_XS/IQ4_NL, IQ3_XXS/MXFP4
     "mtp6_iq": LayerConfig("mtp6_iq", 512, 10, 2048, 640, 6, "mixed_iq", True, 6000),
     "prefill2048_iq": LayerConfig("prefill2048_iq", 512, 10, 2048, 640, 2048, "mixed_iq", True, 7000),
+    # one Q8_0 shared expert beside the routed ones
+    "decode16_shared": LayerConfig("decode16_shared", 512, 10, 2048, 640, 16, "q4k", True, 8000, 1),
+    "prefill512_shared": LayerConfig("prefill512_shared", 512, 10, 2048, 640, 512, "mixed", True, 9000, 1),
 }
 
 
@@ -275,7 +284,12 @@ def permutation(seed: int, n_experts: int) -> np.ndarray:
 
 
 def expert_formats(cfg: LayerConfig, seed: int) -> List[Tuple[int, int]]:
-    """Per expert id: (gate/up format, down format)."""
+    """Per table entry: (gate/up format, down format); the shared experts,
+    after the routed ones, are Q8_0."""
+    return _routed_formats(cfg, seed) + [(Q8_0, Q8_0)] * cfg.n_shared
+
+
+def _routed_formats(cfg: LayerConfig, seed: int) -> List[Tuple[int, int]]:
     E = cfg.n_experts
     if cfg.tiers == "q8_0":
         return [(Q8_0, Q8_0)] * E
@@ -379,13 +393,13 @@ def make_layer(cfg: LayerConfig, layer: int = 0, with_weights: bool = True,
     fmts = expert_formats(cfg, seed)
     x = gen_x_bf16(seed, T, cfg.hidden)
     logits = gen_logits(seed, T, cfg.n_experts, cfg.zipf_bias)
-    experts = [expert_matrices(cfg, seed, e, fmts[e]) for e in range(cfg.n_experts)] if with_weights else []
+    experts = [expert_matrices(cfg, seed, e, fmts[e]) for e in range(cfg.n_entries)] if with_weights else []
     return SynthLayer(cfg, seed, fmts, x, logits, experts)
 
 
 class LazyExperts:
     """Indexable of a layer's experts that generates (and keeps) an expert's
-    matrices on first access; ``len`` is the expert count."""
+    matrices on first access; ``len`` is the table length (routed + shared)."""
 
     def __init__(self, cfg: LayerConfig, seed: int, fmts: Optional[List[Tuple[int, int]]] = None):
         self.cfg, self.seed = cfg, seed
@@ -393,7 +407,7 @@ class LazyExperts:
         self._cache: Dict[int, Dict[str, MatrixBytes]] = {}
 
     def __len__(self) -> int:
-        return self.cfg.n_experts
+        return self.cfg.n_entries
 
     def __getitem__(self, e: int) -> Dict[str, MatrixBytes]:
         e = int(e)

@@ -91,14 +91,14 @@ def make_device_layer(cfg: LayerConfig, layer: int = 0, tokens: Optional[int] = 
     H, I = cfg.hidden, cfg.inter
     spec = []        # (offset, fmt, rows, cols, stride, key, expert, name)
     off = 0
-    for e in range(cfg.n_experts):
+    for e in range(cfg.n_entries):
         gu, dn = fmts[e]
         for name, mat, fmt, rows, cols in (("gate", GATE, gu, I, H), ("up", UP, gu, I, H), ("down", DOWN, dn, H, I)):
             stride = padded_stride(fmt, cols)
             spec.append((off, fmt, rows, cols, stride, weight_key(seed, e, mat), e, name))
             off += (rows * stride + 255) // 256 * 256
     storage = torch.empty(off, dtype=torch.uint8, device="cuda")
-    experts: List[Dict[str, tuple]] = [dict() for _ in range(cfg.n_experts)]
+    experts: List[Dict[str, tuple]] = [dict() for _ in range(cfg.n_entries)]
     mats = []
     for (o, fmt, rows, cols, stride, key, e, name) in spec:
         view = storage[o:o + rows * stride]

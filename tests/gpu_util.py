@@ -96,5 +96,6 @@ def oracle_full_layer(cfg: synth.LayerConfig, DL, tokens=None) -> np.ndarray:
         lazy = synth.LazyExperts(cfg, DL.seed, DL.fmts)
         with oracle_pool() as pool:
             _ORACLE_CACHE[key] = offn.moe_ffn_by_expert(lazy, DL.x_host, DL.logits_host, cfg.k, tokens=tokens,
-                                                        gate_formats=lazy.gate_formats(), map_fn=pool.map)
+                                                        gate_formats=lazy.gate_formats(), map_fn=pool.map,
+                                                        n_shared=cfg.n_shared)
     return _ORACLE_CACHE[key]

@@ -271,3 +271,98 @@ def test_by_expert_lazy_experts_and_pool():
         got2 = ffn.moe_ffn_by_expert(lazy, L.x_bf16, L.logits, cfg.k, gate_formats=lazy.gate_formats(),
                                      map_fn=pool.map)
     np.testing.assert_array_equal(got2, got)
+
+
+# --------------------------------------------------------------- shared experts
+def _shared_closed_form_layer():
+    """The closed-form pair of routed experts plus one shared expert with
+    gate = I, up = I, down = 3 I: y_shared = 3 silu(x) x on every token."""
+    n = 32
+    P = np.roll(np.eye(n, dtype=np.int64), 5, axis=1)
+    Id = np.eye(n, dtype=np.int64)
+    experts = [
+        {"gate": q8_0_matrix(P), "up": q8_0_matrix(Id), "down": q8_0_matrix(Id)},
+        {"gate": q8_0_matrix(Id), "up": q8_0_matrix(2 * Id), "down": q8_0_matrix(Id)},
+        {"gate": q8_0_matrix(Id), "up": q8_0_matrix(Id), "down": q8_0_matrix(3 * Id)},
+    ]
+    rng = np.random.default_rng(32)
+    xb = bf16_bits(rng.standard_normal((3, n)))
+    logits = np.array([[1.0, 0.25], [-0.5, 0.75], [0.0, 0.0]], np.float32)
+    return experts, xb, logits, P
+
+
+def _shared_expected(xb, logits, P):
+    xq = ffn.bf16_bits_to_f64(xb)
+    l = logits.astype(np.float64)
+    routed, shared = np.empty_like(xq), np.empty_like(xq)
+    for t in range(xq.shape[0]):
+        w0 = np.exp(l[t, 0]) / np.exp(l[t]).sum()
+        routed[t] = w0 * ffn.silu(xq[t] @ P.T) * xq[t] + (1 - w0) * ffn.silu(xq[t]) * 2 * xq[t]
+        shared[t] = 3 * ffn.silu(xq[t]) * xq[t]
+    return routed, shared
+
+
+@pytest.mark.parametrize("evaluate", ["per_pair", "by_expert", "bruteforce"])
+def test_shared_expert_closed_form(evaluate):
+    """A shared expert is added with weight 1 to the routed experts' weighted
+    sum, whatever the router's weights (renormalised or not)."""
+    experts, xb, logits, P = _shared_closed_form_layer()
+    routed, shared = _shared_expected(xb, logits, P)
+    fn = {"per_pair": ffn.moe_ffn, "by_expert": ffn.moe_ffn_by_expert,
+          "bruteforce": ffn.moe_ffn_bruteforce}[evaluate]
+    out = fn(experts, xb, logits, 2, n_shared=1)
+    np.testing.assert_allclose(out, routed + shared, rtol=1e-13, atol=1e-15)
+
+
+def test_shared_expert_filters():
+    """The expert range and the format filter treat the shared expert (entry
+    E) like any other: [0, E) gives the routed part, [E, E + 1) the shared
+    part alone."""
+    experts, xb, logits, P = _shared_closed_form_layer()
+    routed, shared = _shared_expected(xb, logits, P)
+    r = ffn.moe_ffn(experts, xb, logits, 2, n_shared=1, expert_lo=0, expert_hi=2)
+    s = ffn.moe_ffn(experts, xb, logits, 2, n_shared=1, expert_lo=2, expert_hi=3)
+    np.testing.assert_allclose(r, routed, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(s, shared, rtol=1e-13, atol=1e-15)
+    none = ffn.moe_ffn(experts, xb, logits, 2, n_shared=1, format_mask=1 << synth.Q4_K)
+    assert np.all(none == 0)
+
+
+def test_shared_expert_slots():
+    """Slots k .. k+S-1 of every token hold the shared experts E .. E+S-1,
+    weight 1, after the router's k slots."""
+    logits = np.array([[0.5, -1.0, 2.0, 0.0], [1.0, 1.0, 1.0, 1.0]], np.float32)
+    ids, w = ffn.token_slots(logits, 2, True, 2)
+    np.testing.assert_array_equal(ids, [[2, 0, 4, 5], [0, 1, 4, 5]])
+    assert np.all(w[:, 2:] == 1.0)
+    np.testing.assert_allclose(w[:, :2].sum(axis=1), 1.0, rtol=1e-15)
+    with pytest.raises(ValueError):
+        ffn.moe_ffn([None] * 4, np.zeros((2, 32), np.uint16), logits, 2, n_shared=1)
+
+
+def test_shared_planted_renormalised_weight_fails():
+    """Planted mistake: a shared expert that joins the router's softmax (its
+    weight renormalised together with the routed ones) fails the closed form."""
+    experts, xb, logits, P = _shared_closed_form_layer()
+    routed, shared = _shared_expected(xb, logits, P)
+    ids, w = ffn.token_slots(logits, 2, True, 1)
+    w_bad = w / w.sum(axis=1, keepdims=True)
+    xq = ffn.bf16_bits_to_f64(xb)
+    dense = [tuple(ffn.dense(ex[m]) for m in ("gate", "up", "down")) for ex in experts]
+    out = np.zeros_like(xq)
+    for t in range(xq.shape[0]):
+        for j in range(3):
+            out[t] += w_bad[t, j] * ffn.expert_forward(*dense[ids[t, j]], xq[t:t + 1])[3][0]
+    assert not np.allclose(out, routed + shared, rtol=1e-6)
+
+
+def test_shared_layer_matches_brute_force():
+    cfg = synth.LayerConfig("t", 12, 3, 256, 64, 5, "mixed", True, 44, 1)
+    L = synth.make_layer(cfg, 0)
+    assert len(L.experts) == 13 and L.fmts[-1] == (synth.Q8_0, synth.Q8_0)
+    out = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k, n_shared=1)
+    bf = ffn.moe_ffn_bruteforce(L.experts, L.x_bf16, L.logits, cfg.k, n_shared=1)
+    np.testing.assert_allclose(out, bf, rtol=1e-12, atol=1e-12 * np.abs(bf).max())
+    routed = ffn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k, n_shared=1, expert_hi=12)
+    plain = ffn.moe_ffn(L.experts[:12], L.x_bf16, L.logits, cfg.k)
+    np.testing.assert_array_equal(routed, plain)
