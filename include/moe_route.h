@@ -98,7 +98,8 @@ typedef enum {
 
 /* Limits of this build. */
 #define MOE_MAX_EXPERTS 1024
-#define MOE_MAX_K 32
+#define MOE_MAX_K 32           /* k + n_shared <= MOE_MAX_K */
+#define MOE_MAX_SHARED 4
 #define MOE_MAX_HIDDEN 8192
 #define MOE_MAX_INTER 8192
 
@@ -131,13 +132,23 @@ typedef struct {
 #define MOE_TABLE_PREPARED 0x4d4f4554u
 
 /* The per-expert format-tagged weight table of one layer. The caller fills
- * n_experts, hidden, inter and experts; moe_table_prepare fills the rest. */
+ * n_experts, hidden, inter, n_shared and experts; moe_table_prepare fills the
+ * rest.
+ *
+ * Shared experts ("多卡 CUDA 张量并行：DwarfStar 如何在 8 张 L40S 上跑出
+ * 120 t/s", memory layout: the router and the shared experts sit beside the
+ * routed experts; the model there stores them in Q8_0) run for every token
+ * with weight 1, added to the routed experts' weighted sum. They are table
+ * entries E .. E + n_shared - 1 and take the token slots k .. k + n_shared - 1
+ * after the routed ones, so they go through the same bucketing, grouped
+ * kernels and ordered combine; moe_options.expert_lo/hi range over all
+ * E + n_shared entries. */
 typedef struct {
-    int32_t n_experts;         /* E, 1..MOE_MAX_EXPERTS */
+    int32_t n_experts;         /* E: routed experts, 1..MOE_MAX_EXPERTS */
     int32_t hidden;            /* H */
     int32_t inter;             /* I */
-    int32_t reserved;
-    const moe_expert *experts; /* host array [E]; read by moe_table_prepare only */
+    int32_t n_shared;          /* S: shared experts, 0..MOE_MAX_SHARED; E + S <= MOE_MAX_EXPERTS */
+    const moe_expert *experts; /* host array [E + S]; read by moe_table_prepare only */
     /* ---- written by moe_table_prepare ---- */
     void *device_table;        /* device copy of the descriptors */
     uint32_t formats_present;  /* bit (1 << format) for every format in use */
@@ -175,14 +186,14 @@ typedef struct {
                                   (|w| <= 65504; quantized LLM weights are O(1)). */
 #define MOE_PATH_FUSED 3       /* one persistent cooperative kernel per layer for decode rows:
                                   T * k <= 64, Q4_K gate/up and Q8_0 down, H % 64 == 0,
-                                  I % 32 == 0, I <= 1024 */
+                                  I % 32 == 0, I <= 1024, no shared experts, no cold tier */
 
 /* Options of moe_ffn_forward (NULL = defaults). */
 typedef struct {
     uint32_t struct_size;      /* sizeof(moe_options); checked */
     int32_t renormalize;       /* 1 (default): the k selected weights sum to 1; 0: plain softmax values */
     uint32_t format_mask;      /* keep an expert only if bit (1 << its gate format) is set; default all */
-    int32_t expert_lo;         /* keep experts in [expert_lo, expert_hi); default [0, E) */
+    int32_t expert_lo;         /* keep experts in [expert_lo, expert_hi); default [0, E + n_shared) */
     int32_t expert_hi;
     int32_t path;              /* MOE_PATH_* */
     int32_t reserved;          /* 0 */
@@ -200,14 +211,14 @@ const char *moe_strerror(int code);
 /* The last CUDA error seen by this thread (cudaError_t value, 0 if none). */
 int moe_last_cuda_error(void);
 
-/* Bytes of device memory moe_table_prepare needs for `n_experts` experts:
- * the 72-byte descriptors, then 3 x 128-byte TMA tensor maps per expert for
- * the tensor path. */
+/* Bytes of device memory moe_table_prepare needs for `n_experts` table
+ * entries (routed plus shared experts): the 72-byte descriptors, a cold-tier
+ * flag byte and 3 x 128-byte TMA tensor maps per entry for the tensor path. */
 size_t moe_table_device_bytes(int32_t n_experts);
 
 /* Validate W (shapes, formats, strides, alignment) and copy its descriptors
  * into `device_buf` (caller-owned device memory of at least
- * moe_table_device_bytes(W->n_experts) bytes). Synchronises `stream`.
+ * moe_table_device_bytes(W->n_experts + W->n_shared) bytes). Synchronises `stream`.
  * On success sets W->device_table = device_buf, W->prepared and the summary
  * fields. The weight data itself is not read or copied; its device pointers
  * must stay valid while forwards that use W run. Re-prepare after changing
@@ -270,7 +281,9 @@ int moe_ffn_gemv_kernels(const moe_weight_table *W, int32_t T, int32_t k);
 int moe_ffn_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* The whole layer (steps 1-6): router, bucketing, grouped gate/up with the
- * fused SwiGLU, grouped down projection and the slot-ordered combine.
+ * fused SwiGLU, grouped down projection and the slot-ordered combine; with
+ * n_shared > 0 the shared experts ride in the same kernels as slots k.. of
+ * every token (weight 1) and are added after the routed experts.
  * x: device bf16 bits [T, H]; logits: device fp32 [T, E]; out: device fp32
  * [T, H] (fully overwritten; tokens whose pairs are all dropped get 0).
  * ws: device workspace of ws_bytes >= moe_ffn_workspace_size(W, T, k), 256-byte
@@ -283,9 +296,11 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
                     moe_stream_t stream);
 
 /* Device pointers (into ws) of the routing results the last forward with this
- * workspace left: ids [T*k], weights [T*k], offsets [E+1], active [E+1],
- * pairs [T*k] and pos [T*k], with the meaning given at moe_route_topk and
- * moe_bucket. Output pointers may be NULL. Host-only; no CUDA call. */
+ * workspace left: ids [T*K], weights [T*K], offsets [N+1], active [N+1],
+ * pairs [T*K] and pos [T*K] (K = k + n_shared slots per token, the shared
+ * experts in the last n_shared with weight 1; N = E + n_shared), with the
+ * meaning given at moe_route_topk and moe_bucket. Output pointers may be
+ * NULL. Host-only; no CUDA call. */
 int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, void *ws, int32_t **ids,
                             float **weights, int32_t **offsets, int32_t **active, int32_t **pairs,
                             int32_t **pos);

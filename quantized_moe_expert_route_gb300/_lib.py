@@ -52,7 +52,7 @@ class Expert(ctypes.Structure):
 
 class WeightTableC(ctypes.Structure):
     _fields_ = [("n_experts", ctypes.c_int32), ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
-                ("reserved", ctypes.c_int32), ("experts", ctypes.POINTER(Expert)),
+                ("n_shared", ctypes.c_int32), ("experts", ctypes.POINTER(Expert)),
                 ("device_table", ctypes.c_void_p), ("formats_present", ctypes.c_uint32),
                 ("prepared", ctypes.c_uint32), ("gateup_formats", ctypes.c_uint32),
                 ("down_formats", ctypes.c_uint32), ("max_gateup_stride", ctypes.c_int64),
@@ -146,12 +146,17 @@ class WeightTable:
     tensors are kept alive by this object."""
 
     def __init__(self, experts: Sequence[dict], hidden: int, inter: int, stream=None,
-                 grid: Optional[torch.Tensor] = None):
-        """experts: per expert {"gate"|"up"|"down": (fmt, rows, cols, stride, uint8 CUDA tensor)};
-        grid: the IQ3_XXS grid (256 x 32-bit CUDA tensor), needed when a matrix is IQ3_XXS."""
+                 grid: Optional[torch.Tensor] = None, n_shared: int = 0):
+        """experts: per expert {"gate"|"up"|"down": (fmt, rows, cols, stride, uint8 CUDA tensor)},
+        the routed experts followed by the ``n_shared`` shared experts (run on
+        every token with weight 1); grid: the IQ3_XXS grid (256 x 32-bit CUDA
+        tensor), needed when a matrix is IQ3_XXS."""
         L = load()
         E = len(experts)
-        self.n_experts, self.hidden, self.inter = E, hidden, inter
+        if not 0 <= n_shared < E:
+            raise ValueError(f"bad shared-expert count {n_shared} for {E} experts")
+        self.n_entries, self.n_shared = E, n_shared
+        self.n_experts, self.hidden, self.inter = E - n_shared, hidden, inter
         self._keep: List[torch.Tensor] = []
         arr = (Expert * E)()
         for e, ex in enumerate(experts):
@@ -164,7 +169,7 @@ class WeightTable:
                 self._keep.append(data)
                 setattr(arr[e], name, Matrix(fmt, rows, cols, 0, stride, data.data_ptr()))
         self._arr = arr
-        self.c = WeightTableC(E, hidden, inter, 0, ctypes.cast(arr, ctypes.POINTER(Expert)))
+        self.c = WeightTableC(E - n_shared, hidden, inter, n_shared, ctypes.cast(arr, ctypes.POINTER(Expert)))
         if grid is not None:
             if grid.numel() != 256 or grid.element_size() != 4:
                 raise ValueError("grid must hold 256 32-bit entries")
@@ -199,13 +204,14 @@ class Workspace:
 
     def routing(self) -> dict:
         """Views (CUDA tensors) of the routing results of the last forward:
-        ids [T, k], weights [T, k], offsets [E+1], active [E+1], pairs, pos [T*k]."""
+        ids [T, k+S], weights [T, k+S], offsets [E+S+1], active [E+S+1],
+        pairs, pos [T*(k+S)] (S shared experts: slots k.. of every token)."""
         L = load()
         ptrs = [ctypes.c_void_p() for _ in range(6)]
         _check("moe_ffn_workspace_views", L.moe_ffn_workspace_views(
             ctypes.byref(self.table.c), self.T, self.k, _ptr(self.buf), *[ctypes.byref(p) for p in ptrs]))
         base = self.buf.data_ptr()
-        T, k, E = self.T, self.k, self.table.n_experts
+        T, k, E = self.T, self.k + self.table.n_shared, self.table.n_entries
 
         def view(p, n, dtype):
             off = p.value - base
@@ -265,8 +271,10 @@ def gemv_kernels(table: "WeightTable", T: int, k: int) -> int:
 def make_options(renormalize: bool = True, format_mask: int = 0xFFFFFFFF, expert_lo: int = 0,
                  expert_hi: Optional[int] = None, n_experts: int = 0, path: int = PATH_AUTO,
                  timing_events: Optional[Sequence["torch.cuda.Event"]] = None) -> Options:
-    """Options of ffn_forward. ``timing_events``: 3 torch.cuda.Event (enable_timing)
-    recorded before the gate/up kernel, between gate/up and down, after down."""
+    """Options of ffn_forward. ``n_experts``: the table length (WeightTable.n_entries,
+    routed + shared), the default expert_hi. ``timing_events``: 3 torch.cuda.Event
+    (enable_timing) recorded before the gate/up kernel, between gate/up and down,
+    after down."""
     hi = n_experts if expert_hi is None else expert_hi
     o = Options(ctypes.sizeof(Options), int(renormalize), format_mask & 0xFFFFFFFF, expert_lo, hi, path, 0, None)
     if timing_events is not None:

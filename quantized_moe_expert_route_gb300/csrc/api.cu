@@ -8,7 +8,7 @@
 
 namespace moe {
 cudaError_t launch_route_topk(const float *logits, int T, int E, int k, int renorm, int32_t *ids, float *wts,
-                              uint32_t *status, cudaStream_t s);
+                              uint32_t *status, cudaStream_t s, int n_shared = 0);
 cudaError_t launch_bucket(const int32_t *ids, int T, int k, int E, int lo, int hi, uint32_t fmt_mask,
                           const DevExpert *table, int32_t *offsets, int32_t *pairs, int32_t *pos, int32_t *active,
                           uint32_t *status, int32_t *scratch, cudaStream_t s);
@@ -103,15 +103,23 @@ int check_matrix(const moe_matrix &m, int rows, int cols) {
 }
 
 // Resolve the path of a forward; -1 if the requested path cannot run it.
+// Shared experts ride along as entries E .. E + n_shared - 1 of the table and
+// as slots k .. k + n_shared - 1 of every token (weight 1): the kernels after
+// the router see k + n_shared slots over E + n_shared experts.
+int n_all(const moe_weight_table *W) { return W->n_experts + W->n_shared; }
+int k_all(const moe_weight_table *W, int k) { return k + W->n_shared; }
+
 int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
     // a table with cold (host-resident) experts runs on the grouped GEMV
-    // kernels, which read the routed cold experts from their staged copy
+    // kernels, which read the routed cold experts from their staged copy; the
+    // fused kernel routes in-kernel and has no shared-expert slots
     const bool hot_only = W->n_cold == 0;
-    const bool fused_ok = hot_only && decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter,
-                                                            W->gateup_formats, W->down_formats, W->max_gateup_stride,
-                                                            W->max_down_stride);
+    const int kk = k_all(W, k), EE = n_all(W);
+    const bool fused_ok = hot_only && W->n_shared == 0 &&
+                          decode_fused_eligible(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats,
+                                                W->down_formats, W->max_gateup_stride, W->max_down_stride);
     const bool tc_ok = hot_only && W->tc_maps == 1 && tc_path_eligible(W->hidden, W->inter);
-    const bool stream_ok = stream_plan(T, k, W->n_experts, W->hidden, W->inter, W->gateup_formats, W->down_formats,
+    const bool stream_ok = stream_plan(T, kk, EE, W->hidden, W->inter, W->gateup_formats, W->down_formats,
                                        W->max_gateup_stride, W->max_down_stride).ok;
     switch (requested) {
         case MOE_PATH_AUTO:
@@ -130,20 +138,21 @@ int resolve_path(const moe_weight_table *W, int T, int k, int requested) {
 
 // Workspace bytes of a forward on `path` (the tensor path adds its regions).
 size_t path_ws_bytes(const moe_weight_table *W, int T, int k, int path) {
-    if (path == MOE_PATH_TENSOR) return tc_ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
-    const size_t base = ws_layout(T, k, W->n_experts, W->hidden, W->inter).total;
+    const int kk = k_all(W, k), EE = n_all(W);
+    if (path == MOE_PATH_TENSOR) return tc_ws_layout(T, kk, EE, W->hidden, W->inter).total;
+    const size_t base = ws_layout(T, kk, EE, W->hidden, W->inter).total;
     if (W->prepared == MOE_TABLE_PREPARED && W->n_cold > 0)
-        return cold_ws_layout(base, T, k, W->n_experts, W->n_cold, W->cold_bytes_max).total;
+        return cold_ws_layout(base, T, kk, EE, W->n_cold, W->cold_bytes_max).total;
     return base;
 }
 
 // Options with defaults filled in; false if they are invalid.
 bool effective_options(const moe_weight_table *W, const moe_options *opt, moe_options &o) {
-    o = moe_options{sizeof(moe_options), 1, 0xffffffffu, 0, W->n_experts, MOE_PATH_AUTO, 0, nullptr};
+    o = moe_options{sizeof(moe_options), 1, 0xffffffffu, 0, n_all(W), MOE_PATH_AUTO, 0, nullptr};
     if (!opt) return true;
     if (opt->struct_size != sizeof(moe_options)) return false;
     o = *opt;
-    if (o.expert_lo < 0 || o.expert_hi > W->n_experts || o.expert_lo > o.expert_hi) return false;
+    if (o.expert_lo < 0 || o.expert_hi > n_all(W) || o.expert_lo > o.expert_hi) return false;
     if (o.path < MOE_PATH_AUTO || o.path > MOE_PATH_FUSED) return false;
     return true;
 }
@@ -177,7 +186,8 @@ size_t moe_table_device_bytes(int32_t n_experts) {
 int moe_table_prepare(moe_weight_table *W, void *device_buf, size_t device_bytes, moe_stream_t stream) {
     if (!W || !W->experts || !device_buf) return MOE_ERR_INVALID_ARG;
     W->prepared = 0;
-    const int E = W->n_experts, H = W->hidden, I = W->inter;
+    if (W->n_shared < 0 || W->n_shared > MOE_MAX_SHARED || W->n_experts <= 0) return MOE_ERR_INVALID_ARG;
+    const int E = W->n_experts + W->n_shared, H = W->hidden, I = W->inter;   // every table entry
     if (E <= 0 || E > MOE_MAX_EXPERTS || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
     if (H > MOE_MAX_HIDDEN || I > MOE_MAX_INTER) return MOE_ERR_UNSUPPORTED;
     if (device_bytes < moe_table_device_bytes(E) || !aligned(device_buf, 16)) return MOE_ERR_INVALID_ARG;
@@ -320,21 +330,24 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
                     const moe_options *opt, float *out, void *ws, size_t ws_bytes, moe_stream_t stream) {
     if (!W) return MOE_ERR_INVALID_ARG;
     if (W->prepared != MOE_TABLE_PREPARED || !W->device_table) return MOE_ERR_NOT_PREPARED;
-    const int E = W->n_experts, H = W->hidden, I = W->inter;
-    if (T < 0 || k <= 0 || k > E) return MOE_ERR_INVALID_ARG;
-    if (k > MOE_MAX_K || T > MAX_T) return MOE_ERR_UNSUPPORTED;
+    const int ER = W->n_experts, H = W->hidden, I = W->inter;
+    if (T < 0 || k <= 0 || k > ER) return MOE_ERR_INVALID_ARG;
+    if (k > MOE_MAX_K || k + W->n_shared > MOE_MAX_K || T > MAX_T) return MOE_ERR_UNSUPPORTED;
+    // after the router: k + n_shared slots per token over E + n_shared experts
+    const int E = n_all(W), kr = k;
+    k = k_all(W, k);
     if (!ws || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x || !logits || !out)) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!aligned(out, 16))) return MOE_ERR_INVALID_ARG;
     moe_options o;
     if (!effective_options(W, opt, o)) return MOE_ERR_INVALID_ARG;
-    int path = resolve_path(W, T > 0 ? T : 1, k, o.path);
+    int path = resolve_path(W, T > 0 ? T : 1, kr, o.path);
     // the fused and tensor paths read activation rows with 16-byte loads
     if ((path == MOE_PATH_FUSED || path == MOE_PATH_TENSOR) && T > 0 && !aligned(x, 16))
         path = o.path == MOE_PATH_AUTO ? MOE_PATH_GEMV : -1;
     if (path < 0) return MOE_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(T, k, E, H, I);
-    if (ws_bytes < path_ws_bytes(W, T, k, path)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < path_ws_bytes(W, T, kr, path)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     if (T == 0) return MOE_OK;
 
     char *base = static_cast<char *>(ws);
@@ -353,7 +366,7 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
     cudaError_t err;
     if (path == MOE_PATH_FUSED) {
         if (events && (err = record_timing_event(events[0], stream)) != cudaSuccess) return cuda_fail(err);
-        err = launch_decode_fused(table, W, T, k, E, H, I, W->max_gateup_stride, W->max_down_stride, o.renormalize,
+        err = launch_decode_fused(table, W, T, kr, ER, H, I, W->max_gateup_stride, W->max_down_stride, o.renormalize,
                                   o.expert_lo, o.expert_hi, o.format_mask, logits,
                                   x, out, h, ids, wts, offsets, active, pairs, pos,
                                   reinterpret_cast<unsigned char *>(base + L.status), status, stream);
@@ -364,7 +377,7 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
         }
         return MOE_OK;
     }
-    err = launch_route_topk(logits, T, E, k, o.renormalize, ids, wts, status, stream);
+    err = launch_route_topk(logits, T, ER, kr, o.renormalize, ids, wts, status, stream, W->n_shared);
     if (err != cudaSuccess) return cuda_fail(err);
     err = launch_bucket(ids, T, k, E, o.expert_lo, o.expert_hi, o.format_mask, table, offsets, pairs, pos, active,
                         status, reinterpret_cast<int32_t *>(base + L.bscratch), stream);
@@ -393,7 +406,7 @@ int moe_ffn_forward(const moe_weight_table *W, const uint16_t *x, const float *l
 
 int moe_ffn_gemv_kernels(const moe_weight_table *W, int32_t T, int32_t k) {
     if (!W || W->prepared != MOE_TABLE_PREPARED || T < 0 || k <= 0 || k > W->n_experts) return -1;
-    return stream_plan(T > 0 ? T : 1, k, W->n_experts, W->hidden, W->inter, W->gateup_formats, W->down_formats,
+    return stream_plan(T > 0 ? T : 1, k_all(W, k), n_all(W), W->hidden, W->inter, W->gateup_formats, W->down_formats,
                        W->max_gateup_stride,
                        W->max_down_stride).ok
                ? MOE_GEMV_STREAMING
@@ -411,7 +424,7 @@ int moe_ffn_workspace_views(const moe_weight_table *W, int32_t T, int32_t k, voi
                             float **weights, int32_t **offsets, int32_t **active, int32_t **pairs,
                             int32_t **pos) {
     if (!W || !ws || T < 0 || k <= 0 || W->n_experts <= 0 || k > W->n_experts) return MOE_ERR_INVALID_ARG;
-    const WsLayout L = ws_layout(T, k, W->n_experts, W->hidden, W->inter);
+    const WsLayout L = ws_layout(T, k_all(W, k), n_all(W), W->hidden, W->inter);
     char *b = static_cast<char *>(ws);
     if (ids) *ids = reinterpret_cast<int32_t *>(b + L.ids);
     if (weights) *weights = reinterpret_cast<float *>(b + L.wts);

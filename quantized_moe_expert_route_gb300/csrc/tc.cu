@@ -1188,7 +1188,7 @@ bool tc_encode_weight_maps(const moe_weight_table *W, void *out) {
     EncodeTiledFn f = encode_fn();
     if (!f) return false;
     CUtensorMap *maps = static_cast<CUtensorMap *>(out);
-    for (int e = 0; e < W->n_experts; ++e) {
+    for (int e = 0; e < W->n_experts + W->n_shared; ++e) {
         const moe_matrix *m[3] = {&W->experts[e].gate, &W->experts[e].up, &W->experts[e].down};
         for (int i = 0; i < 3; ++i) {
             const cuuint64_t dims[2] = {(cuuint64_t)m[i]->row_stride_bytes, (cuuint64_t)m[i]->rows};

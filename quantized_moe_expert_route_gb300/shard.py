@@ -46,7 +46,9 @@ def gather_partials(partial: torch.Tensor, group=None) -> List[torch.Tensor]:
 class ShardedLayer:
     """One rank's share of an expert-sharded layer. `table` holds this rank's
     experts' weights for [lo, hi) (the other experts' entries are never read:
-    their pairs are dropped before any weight access)."""
+    their pairs are dropped before any weight access). `n_experts` is the
+    table length, routed plus shared experts: the shared experts are the last
+    entries, so the last rank's range computes them, once."""
 
     def __init__(self, table, n_experts: int, rank: int, world: int, group=None):
         self.table, self.group = table, group

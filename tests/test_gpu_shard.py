@@ -45,24 +45,25 @@ def test_sum_partials_ordered(M, n, count, offset):
     np.testing.assert_array_equal(out.cpu().numpy(), ref)
 
 
-def _shard_table(M, experts, lo, hi, hidden, inter):
+def _shard_table(M, experts, lo, hi, hidden, inter, n_shared=0):
     """The table of a rank holding experts [lo, hi): the other entries point
     at expert lo's tensors (placeholders of the right shape, never read)."""
     ph = experts[lo]
     own = [experts[e] if lo <= e < hi else ph for e in range(len(experts))]
-    return M.WeightTable(own, hidden, inter)
+    return M.WeightTable(own, hidden, inter, n_shared=n_shared)
 
 
-@pytest.mark.parametrize("name,world", [("decode16", 2), ("mtp6", 2), ("decode1", 3)])
+@pytest.mark.parametrize("name,world", [("decode16", 2), ("mtp6", 2), ("decode1", 3), ("decode16_shared", 2)])
 def test_shards_sum_to_the_layer(M, name, world):
+    """With a shared expert (the last table entry) the last shard computes it."""
     from synth import gpu as sgpu
     cfg = synth.CONFIGS[name]
     DL = sgpu.make_device_layer(cfg, 5)
     parts = []
     for r in range(world):
-        lo, hi = M.expert_shard(cfg.n_experts, r, world)
-        table = _shard_table(M, DL.experts, lo, hi, cfg.hidden, cfg.inter)
-        opt = M.make_options(n_experts=cfg.n_experts, expert_lo=lo, expert_hi=hi)
+        lo, hi = M.expert_shard(cfg.n_entries, r, world)
+        table = _shard_table(M, DL.experts, lo, hi, cfg.hidden, cfg.inter, cfg.n_shared)
+        opt = M.make_options(n_experts=cfg.n_entries, expert_lo=lo, expert_hi=hi)
         parts.append(M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k, options=opt))
     out = M.sum_partials(torch.stack(parts)).cpu().numpy()
     assert_parity(out, oracle_full_layer(cfg, DL), f"{name} in {world} expert shards")
