@@ -90,10 +90,19 @@ typedef enum {
  * IQ3_XXS/MXFP4) but print no layout. IQ3_XXS needs the 256-entry grid of
  * four magnitude bytes per entry that its model file was made with, passed in
  * moe_weight_table.iq3_grid. IQ formats run on the tensor-core and the tiled
- * grouped GEMV paths. */
+ * grouped GEMV paths.
+ *   MOE_T5_G128 ternary, 128 weights / 28 B: fp16 s, then 26 code bytes;
+ *                                weight 5b + i is base-3 digit i (least
+ *                                significant first) of code byte b (the last
+ *                                byte's digits 3 and 4 unused); w = s * (digit - 1)
+ * The ternary packing is the one "RTX 4080 SUPER 原生 Windows 跑 27B", section
+ * 九.2 gives (five weights per byte, one fp16 scale per 128 weights, 1.75 bits
+ * per weight); the digit order within a byte and the scale's place in front
+ * of the codes are this library's reading. It runs on the tensor-core and the
+ * tiled grouped GEMV paths. */
 typedef enum {
     MOE_Q8_0 = 1, MOE_Q4_K = 2, MOE_Q6_K = 3, MOE_MXFP4 = 4,
-    MOE_IQ4_NL = 5, MOE_IQ4_XS = 6, MOE_IQ3_XXS = 7
+    MOE_IQ4_NL = 5, MOE_IQ4_XS = 6, MOE_IQ3_XXS = 7, MOE_T5_G128 = 8
 } moe_format;
 
 /* Limits of this build. */

@@ -92,7 +92,7 @@ int locate(const void *p, const void **dptr) {
 }
 
 int check_matrix(const moe_matrix &m, int rows, int cols) {
-    if (m.format < MOE_Q8_0 || m.format > MOE_IQ3_XXS) return MOE_ERR_BAD_FORMAT;
+    if (m.format < MOE_Q8_0 || m.format > MOE_T5_G128) return MOE_ERR_BAD_FORMAT;
     if (m.rows != rows || m.cols != cols) return MOE_ERR_BAD_SHAPE;
     const int be = BLOCK_ELEMS[m.format], bb = BLOCK_BYTES[m.format];
     if (cols % be != 0) return MOE_ERR_BAD_SHAPE;

@@ -207,6 +207,35 @@ __device__ __forceinline__ void decode_iq3_unit(const uint8_t *row, int u, const
     U.m = 0.0f;
 }
 
+// T5_G128: 28 B per 128 = fp16 s | 26 code bytes; weight 5c + i is base-3
+// digit i (least significant first) of code byte c; w = s * (digit - 1). Unit
+// u is quarter j = u % 4 of block u / 4: weights 32j .. 32j + 31, which start
+// at digit (32j) % 5 of code byte (32j) / 5 and span at most 8 code bytes.
+// floor(v / 3) = (v * 171) >> 9 for every byte value v.
+template <>
+__device__ __forceinline__ void decode_unit<MOE_T5_G128>(const uint8_t *row, int u, Unit &U) {
+    const uint8_t *b = row + 28 * (u >> 2);
+    const int j = u & 3, first = (32 * j) / 5, off = (32 * j) % 5;   // {0, 6, 12, 19}, {0, 2, 4, 1}
+    int dig[40];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        int v = b[2 + min(first + c, 25)];   // the clamped bytes are never selected below
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const int q = (v * 171) >> 9;
+            dig[5 * c + i] = v - 3 * q;
+            v = q;
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const int d = off == 0 ? dig[i] : off == 1 ? dig[i + 1] : off == 2 ? dig[i + 2] : dig[i + 4];
+        U.c[i] = (float)(d - 1);
+    }
+    U.s_lo = U.s_hi = half_bits_to_f32(ld16(b));
+    U.m = 0.0f;
+}
+
 // acc += dot(w, x) for one 32-weight unit; x in shared memory (fp32).
 __device__ __forceinline__ float unit_dot(const Unit &U, const float *x) {
     float lo = 0.0f, hi = 0.0f, sx = 0.0f;
@@ -349,6 +378,7 @@ __global__ void __launch_bounds__(GV_THREADS) gateup_gemv_kernel(GvArgs A) {
         case MOE_IQ4_NL: gateup_tile<MOE_IQ4_NL>(A, G, Uw, e, r0, nrows, smem, &bar); break;
         case MOE_IQ4_XS: gateup_tile<MOE_IQ4_XS>(A, G, Uw, e, r0, nrows, smem, &bar); break;
         case MOE_IQ3_XXS: gateup_tile<MOE_IQ3_XXS>(A, G, Uw, e, r0, nrows, smem, &bar); break;
+        case MOE_T5_G128: gateup_tile<MOE_T5_G128>(A, G, Uw, e, r0, nrows, smem, &bar); break;
         default: break;
     }
 }
@@ -411,6 +441,7 @@ __global__ void __launch_bounds__(GV_THREADS) down_gemv_kernel(GvArgs A) {
         case MOE_IQ4_NL: down_tile<MOE_IQ4_NL>(A, D, e, r0, nrows, smem, &bar); break;
         case MOE_IQ4_XS: down_tile<MOE_IQ4_XS>(A, D, e, r0, nrows, smem, &bar); break;
         case MOE_IQ3_XXS: down_tile<MOE_IQ3_XXS>(A, D, e, r0, nrows, smem, &bar); break;
+        case MOE_T5_G128: down_tile<MOE_T5_G128>(A, D, e, r0, nrows, smem, &bar); break;
         default: break;
     }
 }

@@ -116,8 +116,8 @@ inline ColdLayout cold_ws_layout(size_t after, int T, int k, int E, int n_cold, 
 cudaError_t launch_cold_staging(const DevExpert *table, const uint8_t *cold, int E, const int32_t *active,
                                 char *ws_base, const ColdLayout &C, cudaStream_t s);
 
-constexpr int BLOCK_ELEMS[8] = {0, 32, 256, 256, 32, 32, 256, 256};
-constexpr int BLOCK_BYTES[8] = {0, 34, 144, 210, 17, 18, 136, 98};
+constexpr int BLOCK_ELEMS[9] = {0, 32, 256, 256, 32, 32, 256, 256, 128};
+constexpr int BLOCK_BYTES[9] = {0, 34, 144, 210, 17, 18, 136, 98, 28};
 
 // Bounded waits: a wait that exceeds this many polls sets MOE_FLAG_WAIT_TIMEOUT.
 constexpr uint32_t WAIT_LIMIT = 1u << 26;

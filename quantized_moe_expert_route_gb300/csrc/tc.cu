@@ -66,18 +66,26 @@ constexpr uint32_t TC_MAGIC = 0x64006400u;    // fp16 pair (1024, 1024)
 
 // Raw stage geometry per format (index = moe_format): a stage holds, for each
 // weight row, the blocks of 256 K as TMA boxes of RAW_W bytes (widened to
-// 16-byte boundaries); Q8_0's 272 bytes take two boxes, 128 bytes apart.
-__host__ __device__ constexpr int raw_w(int f) { return f == MOE_Q6_K ? 240 : f == MOE_IQ3_XXS ? 112 : 144; }
+// 16-byte boundaries); Q8_0's 272 bytes take two boxes, 128 bytes apart;
+// T5_G128's 56 bytes start 0 or 8 bytes into a 64-byte box.
+__host__ __device__ constexpr int raw_w(int f) {
+    return f == MOE_Q6_K ? 240 : f == MOE_IQ3_XXS ? 112 : f == MOE_T5_G128 ? 64 : 144;
+}
 __host__ __device__ constexpr int raw_nbox(int f) { return f == MOE_Q8_0 ? 2 : 1; }
 __host__ __device__ constexpr int blk_elems(int f) {
-    return f == MOE_Q4_K || f == MOE_Q6_K || f == MOE_IQ4_XS || f == MOE_IQ3_XXS ? 256 : 32;
+    return f == MOE_Q4_K || f == MOE_Q6_K || f == MOE_IQ4_XS || f == MOE_IQ3_XXS ? 256
+         : f == MOE_T5_G128 ? 128 : 32;
 }
 __host__ __device__ constexpr int blk_bytes(int f) {
     return f == MOE_Q8_0 ? 34 : f == MOE_Q4_K ? 144 : f == MOE_Q6_K ? 210 : f == MOE_MXFP4 ? 17
-         : f == MOE_IQ4_NL ? 18 : f == MOE_IQ4_XS ? 136 : 98;
+         : f == MOE_IQ4_NL ? 18 : f == MOE_IQ4_XS ? 136 : f == MOE_IQ3_XXS ? 98 : 28;
 }
+// Kernel variants by the decoders they carry: the four standard formats; with
+// the IQ formats (and the IQ3_XXS grid in shared memory); with the IQ formats
+// and T5_G128. Each layer takes the smallest variant that decodes it.
+constexpr int TC_XV_STD = 0, TC_XV_IQ = 1, TC_XV_T5 = 2;
 constexpr uint32_t TC_IQ_FORMATS = (1u << MOE_IQ4_NL) | (1u << MOE_IQ4_XS) | (1u << MOE_IQ3_XXS);
-constexpr int TC_GRID_BYTES = 1024;          // the IQ3_XXS grid in shared memory (IQ variant)
+constexpr int TC_GRID_BYTES = 1024;          // the IQ3_XXS grid in shared memory (IQ variants)
 
 static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
 static_assert(TC_DG * TC_PPG == TC_KR / TC_KA, "groups x pieces cover a raw stage");
@@ -562,6 +570,46 @@ __device__ __forceinline__ void dq_iq3xxs(uint32_t blk, int g, const uint32_t *g
     }
 }
 
+// ---- T5_G128 (T5 variant)
+// Half HALF of a 128-weight block: weights 64 HALF .. + 63, i.e. code digits
+// from 64 HALF on, which begin at digit 4 HALF of code byte 12 HALF. Each code
+// byte is split into its five base-3 digits (floor(v / 3) = (v * 171) >> 9 for
+// every byte value); digit d of weight t goes into half t % 2 of pair t / 2 as
+// the fp16 1024 + d, and (1024 + d) - 1025 = d - 1 and (d - 1) * s are exact.
+template <int HALF>
+__device__ __forceinline__ void t5_half(uint32_t codes, uint32_t S, uint32_t (&r)[32]) {
+    constexpr uint32_t NEG1025 = 0xE401E401u;   // fp16 pair (-1025, -1025)
+    uint32_t w[4];
+    lds_words<4>(codes + 12 * HALF, w);           // code bytes 12 HALF .. + 15
+#pragma unroll
+    for (int m = 0; m < 32; ++m) r[m] = TC_MAGIC;
+#pragma unroll
+    for (int c = 0; c < 14; ++c) {
+        uint32_t v = (w[c >> 2] >> (8 * (c & 3))) & 0xffu;
+#pragma unroll
+        for (int i = 0; i < 5; ++i) {
+            const int t = 5 * c + i - 4 * HALF;   // the piece's weight
+            const uint32_t q = (v * 171u) >> 9;
+            if (t >= 0 && t < 64) r[t >> 1] |= (v - 3u * q) << (16 * (t & 1));
+            v = q;
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < 32; ++m) r[m] = hmul2(hadd2(r[m], NEG1025), S);
+}
+// Piece g = half g % 2 of block g / 2 of the stage (28 bytes each: fp16 s, 26
+// code bytes); w = s * (digit - 1).
+__device__ __forceinline__ void dq_t5(uint32_t blk, int g, uint32_t (&r)[32]) {
+    const uint32_t b = blk + 28 * (g >> 1);
+    uint32_t dw[1];
+    lds_words<1>(b, dw);
+    const uint32_t S = (dw[0] & 0xffffu) * 0x10001u;
+    if (g & 1)
+        t5_half<1>(b + 2, S, r);
+    else
+        t5_half<0>(b + 2, S, r);
+}
+
 // Raw stage rs of a weight row: the byte offset (within the row) of the first
 // block of K range [256 rs, ...), the 16-byte-aligned x of its TMA box and the
 // lead of the block inside the box.
@@ -647,7 +695,7 @@ __device__ __forceinline__ bool counter_spin(const uint32_t *p, uint32_t target,
     return (int32_t)(ld_acquire_shared(p) - target) >= 0 || counter_spin_slow(p, target, abort_flag);
 }
 
-template <bool GATEUP, bool IQ>
+template <bool GATEUP, int XV>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_constant__ CUtensorMap bmap, const TcArgs A) {
     extern __shared__ __align__(16) uint8_t tc_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -664,7 +712,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     uint32_t *tmem_slot = a_ready + TC_EVSLOTS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     uint32_t *grid_s = reinterpret_cast<uint32_t *>(bars + TC_NBARS) + 16;   // IQ variant: after the 64-byte misc area
-    if (IQ && A.grid)
+    if (XV != TC_XV_STD && A.grid)
         for (int i = threadIdx.x; i < 256; i += TC_THREADS) grid_s[i] = A.grid[i];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -876,14 +924,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         dq_q8_0(gp < 2 ? base + 68 * gp : base + (uint32_t)(R * W) + 68 * gp - 128, r);
                     else if (fmt == MOE_Q6_K)
                         dq_q6k(base, gp, r);
-                    else if (!IQ || fmt == MOE_MXFP4)
+                    else if (XV == TC_XV_STD || fmt == MOE_MXFP4)
                         dq_mxfp4(base, gp, r);
                     else if (fmt == MOE_IQ4_NL)
                         dq_iq4nl(base, gp, r);
                     else if (fmt == MOE_IQ4_XS)
                         dq_iq4xs(base, gp, r);
-                    else
+                    else if (XV == TC_XV_IQ || fmt == MOE_IQ3_XXS)
                         dq_iq3xxs(base, gp, grid_s, r);
+                    else
+                        dq_t5(base, gp, r);
                     tmem_st32(tmem + ((uint32_t)(32 * qd) << 16) + TC_ACOL0 + es * (TC_AEV * 32) + gp * 32, r);
                 }
                 }
@@ -1143,7 +1193,7 @@ bool encode_act_map(CUtensorMap *map, const void *base, int rows, int cols) {
 int raw_slot_bytes(uint32_t fmask, bool gateup) {
     const int R = gateup ? 64 : 128, nmat = gateup ? 2 : 1;
     int sb = 0;
-    for (int f = MOE_Q8_0; f <= MOE_IQ3_XXS; ++f)
+    for (int f = MOE_Q8_0; f <= MOE_T5_G128; ++f)
         if (fmask & (1u << f)) sb = std::max(sb, nmat * raw_nbox(f) * R * raw_w(f));
     return sb;
 }
@@ -1155,11 +1205,11 @@ int smem_optin() {
     if (dev < 64 && g_tc_smem_optin[dev]) return g_tc_smem_optin[dev];
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-    if (cudaFuncSetAttribute(tc_gemm_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess)
-        return 0;
+    const void *kernels[6] = {(const void *)tc_gemm_kernel<true, TC_XV_STD>, (const void *)tc_gemm_kernel<false, TC_XV_STD>,
+                              (const void *)tc_gemm_kernel<true, TC_XV_IQ>, (const void *)tc_gemm_kernel<false, TC_XV_IQ>,
+                              (const void *)tc_gemm_kernel<true, TC_XV_T5>, (const void *)tc_gemm_kernel<false, TC_XV_T5>};
+    for (const void *kf : kernels)
+        if (cudaFuncSetAttribute(kf, cudaFuncAttributeMaxDynamicSharedMemorySize, v) != cudaSuccess) return 0;
     if (dev < 64) g_tc_smem_optin[dev] = v;
     return v;
 }
@@ -1213,10 +1263,13 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
     if (T <= 0) return cudaSuccess;
     const int P = T * k;
     const int sb1 = raw_slot_bytes(gu_formats, true), sb2 = raw_slot_bytes(dn_formats, false);
-    // layers with IQ formats take the kernel variant with their decoders (and
-    // the IQ3_XXS grid in shared memory); the others keep the smaller code
-    const bool iq = ((gu_formats | dn_formats) & TC_IQ_FORMATS) != 0;
-    if (iq && ((gu_formats | dn_formats) & (1u << MOE_IQ3_XXS)) && !grid) return cudaErrorInvalidValue;
+    // layers with IQ or T5_G128 formats take a kernel variant with their
+    // decoders (and the IQ3_XXS grid in shared memory); the others keep the
+    // smaller code
+    const uint32_t fm = gu_formats | dn_formats;
+    const int xv = (fm & (1u << MOE_T5_G128)) ? TC_XV_T5 : (fm & TC_IQ_FORMATS) ? TC_XV_IQ : TC_XV_STD;
+    const bool iq = xv != TC_XV_STD;
+    if ((fm & (1u << MOE_IQ3_XXS)) && !grid) return cudaErrorInvalidValue;
     const int rs1 = raw_stages(sb1, iq), rs2 = raw_stages(sb2, iq);
     const CUtensorMap *maps = static_cast<const CUtensorMap *>(wmaps);
     const int G = sm_count();
@@ -1238,10 +1291,13 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
     if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
 
     TcArgs a1{table, maps, chunks, n_chunks, H, I / 64, H, I, sb1, rs1, xinv, h32, hmax, nullptr, status, grid};
-    if (iq)
-        tc_gemm_kernel<true, true><<<G, TC_THREADS, tc_smem_bytes(sb1, rs1, true), s>>>(xmap, a1);
+    const size_t smem1 = tc_smem_bytes(sb1, rs1, iq);
+    if (xv == TC_XV_T5)
+        tc_gemm_kernel<true, TC_XV_T5><<<G, TC_THREADS, smem1, s>>>(xmap, a1);
+    else if (xv == TC_XV_IQ)
+        tc_gemm_kernel<true, TC_XV_IQ><<<G, TC_THREADS, smem1, s>>>(xmap, a1);
     else
-        tc_gemm_kernel<true, false><<<G, TC_THREADS, tc_smem_bytes(sb1, rs1), s>>>(xmap, a1);
+        tc_gemm_kernel<true, TC_XV_STD><<<G, TC_THREADS, smem1, s>>>(xmap, a1);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[1], s)) != cudaSuccess) return err;
 
@@ -1249,10 +1305,13 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
                                                                                              I, h16, hinv);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     TcArgs a2{table, maps, chunks, n_chunks, I, H / TC_M, H, I, sb2, rs2, hinv, nullptr, nullptr, y, status, grid};
-    if (iq)
-        tc_gemm_kernel<false, true><<<G, TC_THREADS, tc_smem_bytes(sb2, rs2, true), s>>>(hmap, a2);
+    const size_t smem2 = tc_smem_bytes(sb2, rs2, iq);
+    if (xv == TC_XV_T5)
+        tc_gemm_kernel<false, TC_XV_T5><<<G, TC_THREADS, smem2, s>>>(hmap, a2);
+    else if (xv == TC_XV_IQ)
+        tc_gemm_kernel<false, TC_XV_IQ><<<G, TC_THREADS, smem2, s>>>(hmap, a2);
     else
-        tc_gemm_kernel<false, false><<<G, TC_THREADS, tc_smem_bytes(sb2, rs2), s>>>(hmap, a2);
+        tc_gemm_kernel<false, TC_XV_STD><<<G, TC_THREADS, smem2, s>>>(hmap, a2);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
     return launch_combine(T, k, H, pos, wts, y, out, s);

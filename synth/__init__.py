@@ -44,6 +44,9 @@ Recipe (all values little-endian):
   The layer's grid (256 entries of four magnitude bytes) is drawn once from
   stream GRID of seed 0: byte j of entry i is ``IQ3_MAGNITUDES[ubelow(16-bit
   chunk j of draw i, 8)]``.
+* T5_G128 (28 B): s = f16(0.25 + 0.75 u24(r0)); code byte i < 25 =
+  ubelow(16-bit chunk i%4 of r_{1+i//4}, 243) (five uniform base-3 digits),
+  code byte 25 = ubelow(chunk 1 of r7, 27) (three digits, the unused two 0).
 * Row padding bytes (``row_stride`` beyond the row's blocks) are zero.
 * Normals: Box-Muller in fp64 on draws (2i, 2i+1):
   ``sqrt(-2 ln u1) cos(2 pi u2)`` with ``u1 = ((r >> 11) + 1) 2**-53``,
@@ -63,11 +66,11 @@ from typing import Dict, List, Optional, Sequence, Tuple
 import numpy as np
 
 # Format tags (the same numeric values as the C ABI's moe_format enum).
-Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS = 1, 2, 3, 4, 5, 6, 7
+Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS, T5_G128 = 1, 2, 3, 4, 5, 6, 7, 8
 FORMAT_NAMES = {Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", MXFP4: "MXFP4", IQ4_NL: "IQ4_NL", IQ4_XS: "IQ4_XS",
-                IQ3_XXS: "IQ3_XXS"}
-BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32, IQ4_NL: 32, IQ4_XS: 256, IQ3_XXS: 256}
-BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17, IQ4_NL: 18, IQ4_XS: 136, IQ3_XXS: 98}
+                IQ3_XXS: "IQ3_XXS", T5_G128: "T5_G128"}
+BLOCK_ELEMS = {Q8_0: 32, Q4_K: 256, Q6_K: 256, MXFP4: 32, IQ4_NL: 32, IQ4_XS: 256, IQ3_XXS: 256, T5_G128: 128}
+BLOCK_BYTES = {Q8_0: 34, Q4_K: 144, Q6_K: 210, MXFP4: 17, IQ4_NL: 18, IQ4_XS: 136, IQ3_XXS: 98, T5_G128: 28}
 # the magnitudes the synthetic IQ3_XXS grid draws from
 IQ3_MAGNITUDES = np.array([4, 12, 20, 28, 36, 44, 52, 62], dtype=np.int64)
 
@@ -202,6 +205,11 @@ def gen_blocks(fmt: int, key: int, block_idx: np.ndarray) -> np.ndarray:
         out[:, 0:2] = _f16_uniform(r[:, 0], 0.001, 0.009).view(np.uint8).reshape(n, 2)
         out[:, 2:66] = _bytes_of(r[:, 1:9])
         out[:, 66:98] = _bytes_of(r[:, 9:13])
+    elif fmt == T5_G128:
+        out[:, 0:2] = _f16_uniform(r[:, 0], 0.25, 0.75).view(np.uint8).reshape(n, 2)
+        ch = _chunks16(r[:, 1:8])
+        out[:, 2:27] = _ubelow16(ch[:, 0:25], 243)
+        out[:, 27] = _ubelow16(ch[:, 25], 27)
     else:
         raise ValueError(f"unknown format {fmt}")
     return out
@@ -243,7 +251,7 @@ class LayerConfig:
     hidden: int
     inter: int
     tokens: int
-    tiers: str            # "q8_0" (all Q8_0), "q4k" (Q4_K gate/up + Q8_0 down), "mixed", "mixed_iq"
+    tiers: str            # "q8_0" (all Q8_0), "q4k" (Q4_K gate/up + Q8_0 down), "mixed", "mixed_iq", "t5"
     zipf_bias: bool
     seed_base: int        # layer l uses seed seed_base + l (tiny: seed 0)
     n_shared: int = 0     # shared experts (Q8_0), entries n_experts .. n_experts + n_shared - 1
@@ -266,6 +274,9 @@ CONFIGS: Dict[str, LayerConfig] = {
     # one Q8_0 shared expert beside the routed ones
     "decode16_shared": LayerConfig("decode16_shared", 512, 10, 2048, 640, 16, "q4k", True, 8000, 1),
     "prefill512_shared": LayerConfig("prefill512_shared", 512, 10, 2048, 640, 512, "mixed", True, 9000, 1),
+    # ternary experts (every matrix T5_G128)
+    "decode16_t5": LayerConfig("decode16_t5", 512, 10, 2048, 640, 16, "t5", True, 10000),
+    "prefill512_t5": LayerConfig("prefill512_t5", 512, 10, 2048, 640, 512, "t5", True, 11000),
 }
 
 
@@ -295,6 +306,8 @@ def _routed_formats(cfg: LayerConfig, seed: int) -> List[Tuple[int, int]]:
         return [(Q8_0, Q8_0)] * E
     if cfg.tiers == "q4k":
         return [(Q4_K, Q8_0)] * E
+    if cfg.tiers == "t5":
+        return [(T5_G128, T5_G128)] * E
     if cfg.tiers in ("mixed", "mixed_iq"):
         iq = cfg.tiers == "mixed_iq"
         perm = permutation(seed, E)

@@ -40,9 +40,10 @@ __device__ __forceinline__ uint8_t byte_of(uint64_t r, int i) { return (uint8_t)
 
 __global__ void synth_fill_kernel(const moe_synth_matrix *__restrict__ descs) {
     const moe_synth_matrix M = descs[blockIdx.y];
-    const int be = (M.format == 2 || M.format == 3 || M.format == 6 || M.format == 7) ? 256 : 32;
+    const int be = (M.format == 2 || M.format == 3 || M.format == 6 || M.format == 7) ? 256
+                 : M.format == 8 ? 128 : 32;
     const int bb = M.format == 1 ? 34 : M.format == 2 ? 144 : M.format == 3 ? 210 : M.format == 4 ? 17
-                 : M.format == 5 ? 18 : M.format == 6 ? 136 : 98;
+                 : M.format == 5 ? 18 : M.format == 6 ? 136 : M.format == 7 ? 98 : 28;
     const int nb = M.cols / be;
     const int64_t nblocks = (int64_t)M.rows * nb;
     const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -100,11 +101,22 @@ __global__ void synth_fill_kernel(const moe_synth_matrix *__restrict__ descs) {
             uint64_t r = draw(key, base + 2 + g);
             for (int c = 0; c < 8; ++c) out[8 + 8 * g + c] = byte_of(r, c);
         }
-    } else {  // IQ3_XXS
+    } else if (M.format == 7) {  // IQ3_XXS
         put16(out, f16_uniform(draw(key, base + 0), (float)0.001, (float)0.009));
         for (int g = 0; g < 12; ++g) {
             uint64_t r = draw(key, base + 1 + g);
             for (int c = 0; c < 8; ++c) out[2 + 8 * g + c] = byte_of(r, c);
+        }
+    } else {  // T5_G128 (fp16 s at an even offset: 28 j is even)
+        put16(out, f16_uniform(draw(key, base + 0), (float)0.25, (float)0.75));
+        for (int g = 0; g < 7; ++g) {
+            uint64_t r = draw(key, base + 1 + g);
+            for (int c = 0; c < 4; ++c) {
+                const int i = 4 * g + c;
+                const uint64_t ch = (r >> (16 * c)) & 0xFFFF;
+                if (i < 25) out[2 + i] = (uint8_t)ubelow16(ch, 243);
+                else if (i == 25) out[2 + i] = (uint8_t)ubelow16(ch, 27);
+            }
         }
     }
     if (j == nb - 1) {  // zero the row padding

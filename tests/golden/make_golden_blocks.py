@@ -242,9 +242,9 @@ def write(name, fmt, block, expected, rule, grid=None):
     with open(path, "w") as f:
         f.write(f"# Hand-built {fmt} block. Construction: {rule}\n")
         f.write("# Expected weights hand-computed from the block layout (see make_golden_blocks.py).\n")
-        f.write("# Layout reading: GGUF block layouts (Q8_0/Q4_K/Q6_K/IQ4_NL/IQ4_XS/IQ3_XXS), OCP MX v1.0, and the\n")
-        f.write("# base-3 packing of 'RTX 4080 SUPER 原生 Windows 跑 27B', 九.2 (T5_G128)\n")
-        f.write("# (MXFP4); format names from '三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南',\n")
+        f.write("# Layout reading: GGUF block layouts (Q8_0/Q4_K/Q6_K/IQ4_NL/IQ4_XS/IQ3_XXS), OCP MX v1.0\n")
+        f.write("# (MXFP4) and the base-3 packing of 'RTX 4080 SUPER 原生 Windows 跑 27B', 九.2 (T5_G128);\n")
+        f.write("# format names from '三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理优化指南',\n")
         f.write("# 优化策略二.\n")
         f.write(f"format {fmt}\n")
         f.write("bytes " + " ".join(f"{x:02x}" for x in block) + "\n")

@@ -39,11 +39,19 @@ def test_block_field_ranges():
     q4 = synth.gen_blocks(synth.Q4_K, key, np.arange(n))
     sc, m = formats.q4_k_scale_min(q4[:, 4:16])
     assert sc.min() == 0 and sc.max() == 63 and m.min() == 0 and m.max() == 63
+    t5 = synth.gen_blocks(synth.T5_G128, key, np.arange(n))
+    s = t5[:, 0:2].copy().view("<f2").astype(np.float64)[:, 0]
+    assert s.min() >= 0.2499 and s.max() <= 1.0001
+    assert t5[:, 2:27].min() == 0 and t5[:, 2:27].max() == 242        # five base-3 digits
+    assert t5[:, 27].min() == 0 and t5[:, 27].max() == 26             # three digits, two unused
+    w = formats.DECODERS[synth.T5_G128](t5) / s[:, None]
+    assert set(np.unique(w).tolist()) == {-1.0, 0.0, 1.0}
+    assert abs((w == 0).mean() - 1 / 3) < 0.01
 
 
 def test_weight_rms_comparable_across_formats():
     key = synth.stream_key(2, 7)
-    for fmt in (synth.Q8_0, synth.Q4_K, synth.Q6_K, synth.MXFP4):
+    for fmt in (synth.Q8_0, synth.Q4_K, synth.Q6_K, synth.MXFP4, synth.T5_G128):
         blk = synth.gen_blocks(fmt, key, np.arange(256))
         w = formats.DECODERS[fmt](blk)
         rms = np.sqrt((w ** 2).mean())
