@@ -105,14 +105,15 @@ def oracle_worker(spec: dict) -> dict:
         toks = list(range(t0_tok, t0_tok + n_tok))
         if pool is None:
             ids, _, _ = orouter.route_topk(L.logits, cfg.k)
-            for e in np.unique(ids[toks]):
+            for e in list(np.unique(ids[toks])) + list(range(cfg.n_experts, cfg.n_entries)):
                 lazy[int(e)]
             t0 = time.perf_counter()
-            offn.moe_ffn(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks, gate_formats=lazy.gate_formats())
+            offn.moe_ffn(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks, gate_formats=lazy.gate_formats(),
+                         n_shared=cfg.n_shared)
         else:
             t0 = time.perf_counter()
             offn.moe_ffn_by_expert(lazy, L.x_bf16, L.logits, cfg.k, tokens=toks,
-                                   gate_formats=lazy.gate_formats(), map_fn=pool.map)
+                                   gate_formats=lazy.gate_formats(), map_fn=pool.map, n_shared=cfg.n_shared)
         dt = time.perf_counter() - t0
         steps.append(dt)
         t_work += dt
@@ -322,8 +323,9 @@ def run_reference(args, world, rank):
 
 
 def workload_name(cfg, NL: int) -> str:
-    return (f"{cfg.name}: E{cfg.n_experts} k{cfg.k} H{cfg.hidden} I{cfg.inter} T{cfg.tokens} ({cfg.tiers} tiers), "
-            f"{NL} stacked layers per step")
+    shared = f" + {cfg.n_shared} shared" if cfg.n_shared else ""
+    return (f"{cfg.name}: E{cfg.n_experts}{shared} k{cfg.k} H{cfg.hidden} I{cfg.inter} T{cfg.tokens} "
+            f"({cfg.tiers} tiers), {NL} stacked layers per step")
 
 
 def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=None):
@@ -345,15 +347,15 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
     for l in range(NL):
         DL = sgpu.make_device_layer(cfg, rank * NL + l)
         layers.append(DL)
-        tables.append(M.WeightTable(DL.experts, H, I))
+        tables.append(M.WeightTable(DL.experts, H, I, grid=DL.grid, n_shared=cfg.n_shared))
         wss.append(M.Workspace(tables[-1], T, k, path=args.path))
         outs.append(torch.empty((T, H), dtype=torch.float32, device=dev))
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(NL)]
-    opts_plain = M.make_options(n_experts=E, path=args.path)
-    opts_timed = [M.make_options(n_experts=E, path=args.path, timing_events=ev[l]) for l in range(NL)]
+    opts_plain = M.make_options(n_experts=cfg.n_entries, path=args.path)
+    opts_timed = [M.make_options(n_experts=cfg.n_entries, path=args.path, timing_events=ev[l]) for l in range(NL)]
 
     def step(timed: bool):
         for l in range(NL):
@@ -393,7 +395,7 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
         per_layer_gu_bytes.append(gu)
         per_layer_dn_bytes.append(dn)
         per_layer_expert_bytes.append(gu + dn)
-        per_layer_pairs.append(int(offsets[E]))
+        per_layer_pairs.append(int(offsets[cfg.n_entries]))
     io_bytes = T * H * 2 + T * E * 4 + T * H * 4
 
     for _ in range(args.warmup):
@@ -541,7 +543,7 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
         "tensor_pipe": tensor_pipe,
         "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
                 "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
-        "gpu_launches": launches_per_layer(path, T * k) * NL * steps,
+        "gpu_launches": launches_per_layer(path, T * (k + cfg.n_shared)) * NL * steps,
         "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
                  M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
         "clocks": clk,
