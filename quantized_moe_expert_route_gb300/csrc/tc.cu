@@ -791,36 +791,39 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
             }
         }
     } else if (warp == TC_BPROD) {
-        // ---- activation producer: q A steps of the unit's rows per B stage
-        if (lane == 0) {
-            uint32_t bg = 0;
-            bool ok = true;
-            Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
-            for (int u = blockIdx.x; u < n_units && ok; u += G) {
-                const Unit cu = nxt;
-                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
-                const int nb = (cu.n + TC_BOX_ROWS - 1) / TC_BOX_ROWS, q = b_steps_per_stage(cu.n);
-                const int sub_bytes = nb * TC_BOX_ROWS * 128;
-                for (int a0 = 0; a0 < nA; a0 += q) {
-                    const uint32_t bs = bg % TC_BSTAGES, buse = bg / TC_BSTAGES;
-                    if (buse > 0 && !tc_wait(&b_empty[bs], (buse - 1) & 1, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const int qa = min(q, nA - a0);
-                    mbar_expect_tx(&b_full[bs], (uint32_t)(qa * sub_bytes));
-                    for (int j = 0; j < qa; ++j)
-                        for (int i = 0; i < nb; ++i)
-                            tma_load_2d(bring + bs * TC_BSTAGE_BYTES + j * sub_bytes + i * TC_BOX_ROWS * 128, &bmap,
-                                        (a0 + j) * TC_KA, cu.row0 + i * TC_BOX_ROWS, &b_full[bs]);
-                    ++bg;
+        // ---- activation producer: q A steps of the unit's rows per B stage. Lane 0
+        // waits for the stage to be free and sets its byte count; then the warp's
+        // lanes issue the stage's boxes, one each (a single thread issuing a
+        // stage's dozen boxes back to back left the MMA issuer waiting on B).
+        uint32_t bg = 0;
+        bool ok = true;
+        Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
+        for (int u = blockIdx.x; u < n_units && ok; u += G) {
+            const Unit cu = nxt;
+            if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+            const int nb = (cu.n + TC_BOX_ROWS - 1) / TC_BOX_ROWS, q = b_steps_per_stage(cu.n);
+            const int sub_bytes = nb * TC_BOX_ROWS * 128;
+            for (int a0 = 0; a0 < nA; a0 += q) {
+                const uint32_t bs = bg % TC_BSTAGES, buse = bg / TC_BSTAGES;
+                if (buse > 0 && !warp_wait(&b_empty[bs], (buse - 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
                 }
+                const int qa = min(q, nA - a0);
+                if (lane == 0) mbar_expect_tx(&b_full[bs], (uint32_t)(qa * sub_bytes));
+                __syncwarp();
+                for (int t = lane; t < qa * nb; t += 32) {
+                    const int j = t / nb, i = t - j * nb;
+                    tma_load_2d(bring + bs * TC_BSTAGE_BYTES + j * sub_bytes + i * TC_BOX_ROWS * 128, &bmap,
+                                (a0 + j) * TC_KA, cu.row0 + i * TC_BOX_ROWS, &b_full[bs]);
+                }
+                ++bg;
             }
-            if (!ok) {
-                tc_fail(abort_flag, A.status);
-                for (uint32_t j = bg > (uint32_t)TC_BSTAGES ? bg - TC_BSTAGES : 0; j < bg; ++j)
-                    mbar_wait(&b_full[j % TC_BSTAGES], (j / TC_BSTAGES) & 1);
-            }
+        }
+        if (!ok && lane == 0) {
+            tc_fail(abort_flag, A.status);
+            for (uint32_t j = bg > (uint32_t)TC_BSTAGES ? bg - TC_BSTAGES : 0; j < bg; ++j)
+                mbar_wait(&b_full[j % TC_BSTAGES], (j / TC_BSTAGES) & 1);
         }
     } else if (warp == TC_MMA) {
         // ---- MMA issuer: one thread; per event (raw stage) one wait on the dequantisers'
