@@ -65,7 +65,7 @@ inline WsLayout ws_layout(int T, int k, int E, int H, int I) {
 // activations in bucket order as fp16 [P][H] with inverse row scales, |h|
 // maxima, h as fp16 [P][I] with inverse row scales, and the chunk table.
 struct TcLayout {
-    size_t xg, xinv, hmax, h16, hinv, chunks, n_chunks, total;
+    size_t xg, xinv, hmax, h16, hinv, chunks, n_chunks, unit_next, total;
 };
 
 inline size_t tc_max_chunks(int T, int k, int E) {
@@ -86,6 +86,7 @@ inline TcLayout tc_ws_layout(int T, int k, int E, int H, int I) {
     C.hinv = take(P * 4);
     C.chunks = take(tc_max_chunks(T, k, E) * 16);
     C.n_chunks = take(4);
+    C.unit_next = take(8);   // the two GEMMs' unit counters
     C.total = o;
     return C;
 }

@@ -86,6 +86,8 @@ __host__ __device__ constexpr int blk_bytes(int f) {
 constexpr int TC_XV_STD = 0, TC_XV_IQ = 1, TC_XV_T5 = 2;
 constexpr uint32_t TC_IQ_FORMATS = (1u << MOE_IQ4_NL) | (1u << MOE_IQ4_XS) | (1u << MOE_IQ3_XXS);
 constexpr int TC_GRID_BYTES = 1024;          // the IQ3_XXS grid in shared memory (IQ variants)
+constexpr int TC_UQ = 16;                    // unit queue entries (per CTA, shared memory)
+constexpr int TC_UQ_BYTES = TC_UQ * 16 + 32; // entries of 16 bytes, the two counters, alignment
 
 static_assert(TC_ACOL0 + TC_ASTAGES * 32 <= TC_TMEM_COLS, "TMEM budget");
 static_assert(TC_DG * TC_PPG == TC_KR / TC_KA, "groups x pieces cover a raw stage");
@@ -107,6 +109,7 @@ struct TcArgs {
     float *y;                  // down: y [rows][H] fp32, bucket order
     uint32_t *status;
     const uint32_t *grid;      // IQ3_XXS grid (256 words) or null
+    int32_t *unit_next;        // next unit to hand out (zeroed by tc_prep_kernel)
 };
 
 // ------------------------------------------------------------------ PTX helpers
@@ -622,23 +625,55 @@ __host__ __device__ __forceinline__ void raw_x(int fmt, int rs, int &x0, int &le
 // ------------------------------------------------------------------ the grouped GEMM
 size_t tc_smem_bytes(int slot_bytes, int RS, bool iq = false) {
     return 1024 + (size_t)TC_BSTAGES * TC_BSTAGE_BYTES + (size_t)RS * slot_bytes + TC_UBUF_FLOATS * 4 +
-           TC_NBARS * 8 + 64 + (iq ? TC_GRID_BYTES : 0);
+           TC_NBARS * 8 + 64 + TC_UQ_BYTES + (iq ? TC_GRID_BYTES : 0);
 }
 
-struct Unit {
-    int e, row0, n, s, fmt;
+struct __align__(16) Unit {
+    int e, row0, n, s;   // e < 0: no more units
 };
 
-// Unit u: its chunk, slice and (for the producer) the weight format.
-template <bool GATEUP>
-__device__ __forceinline__ Unit load_unit(const TcArgs &A, int u, bool want_fmt) {
-    Unit x{0, 0, 0, 0, 0};
+// Units are handed out dynamically: the weight producer takes the next unit
+// index from a global counter and publishes the unit in a per-CTA queue in
+// shared memory; every other role takes the CTA's units from the queue in the
+// same order. (Handing out units round-robin by index left the CTAs finishing
+// up to 6% apart.) Four epilogue warps acknowledge each entry, which bounds
+// how far the producer runs ahead. The IQ variant publishes the static
+// round-robin order through the same queue.
+struct UnitQueue {
+    Unit *q;             // [TC_UQ]
+    uint32_t *n_pub;     // entries published
+    uint32_t *n_ack;     // epilogue acknowledgements (4 per entry)
+};
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p);
+__device__ __noinline__ bool uq_spin_slow(const uint32_t *p, uint32_t target, volatile int *abort_flag);
+template <bool INL>
+__device__ __forceinline__ bool uq_spin_body(const uint32_t *p, uint32_t target, volatile int *abort_flag);
+// Entry k of the queue (bounded wait until it is published).
+__device__ __forceinline__ bool uq_get(const UnitQueue &Q, uint32_t k, volatile int *abort_flag, Unit &out) {
+    if ((int32_t)(ld_acquire_u32(Q.n_pub) - (k + 1)) < 0 && !uq_spin_slow(Q.n_pub, k + 1, abort_flag)) return false;
+    out = Q.q[k % TC_UQ];
+    return true;
+}
+
+// Unit u: its chunk and slice.
+__device__ __forceinline__ Unit load_unit(const TcArgs &A, int u) {
     const int4 ch = A.chunks[u / A.S];
-    x.e = ch.x;
-    x.row0 = ch.y;
-    x.n = ch.z;
-    x.s = u % A.S;
-    if (want_fmt) x.fmt = GATEUP ? A.table[x.e].gate.fmt : A.table[x.e].down.fmt;
+    Unit x{ch.x, ch.y, ch.z, u % A.S};
+    return x;
+}
+
+// The CTA's k-th unit (e = -1 once all are handed out) and its weight format:
+// the next one from the global counter (DYN), or unit blockIdx.x + k * grid.
+template <bool GATEUP, bool DYN>
+__device__ __forceinline__ Unit grab_unit(const TcArgs &A, int n_units, uint32_t k, int &fmt) {
+    const int u = DYN ? atomicAdd(A.unit_next, 1) : (int)(blockIdx.x + k * gridDim.x);
+    fmt = 0;
+    if (u >= n_units) {
+        Unit x{-1, 0, 0, 0};
+        return x;
+    }
+    const Unit x = load_unit(A, u);
+    fmt = GATEUP ? A.table[x.e].gate.fmt : A.table[x.e].down.fmt;
     return x;
 }
 
@@ -647,6 +682,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = tc_wait(bar, parity, abort_flag);
     return __shfl_sync(0xffffffffu, ok, 0);
+}
+// Entry k of the unit queue for a whole warp: lane 0 waits, every lane reads.
+template <bool INL = false>
+__device__ __forceinline__ bool warp_uq_get(const UnitQueue &Q, uint32_t k, volatile int *abort_flag, Unit &out) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0)
+        ok = (int32_t)(ld_acquire_u32(Q.n_pub) - (k + 1)) >= 0 ||
+             (INL ? uq_spin_body<true>(Q.n_pub, k + 1, abort_flag) : uq_spin_slow(Q.n_pub, k + 1, abort_flag));
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+        (void)ld_acquire_u32(Q.n_pub);   // every lane acquires the published entries
+        out = Q.q[k % TC_UQ];
+    }
+    return ok;
 }
 
 // AND of `pred` over the 128 epilogue threads (warps 0-3), with a barrier.
@@ -676,10 +725,30 @@ __device__ __forceinline__ uint32_t ld_acquire_shared(const uint32_t *p) {
     asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
     return v;
 }
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) { return ld_acquire_shared(p); }
+// Spin until the counter reaches `target` (wrapping compare), with a sleep
+// between polls; bounded like the other waits. One out-of-line copy for most
+// roles; the epilogue inlines it (as a call it made the epilogue spill
+// registers around it).
+template <bool INL>
+__device__ __forceinline__ bool uq_spin_body(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
+    const uint64_t t0 = global_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if ((int32_t)(ld_acquire_shared(p) - target) >= 0) return true;
+        if ((i & 15u) == 15u) {
+            if (*abort_flag) return false;
+            if (global_ns() - t0 > bound) return false;
+        }
+        __nanosleep(64);
+    }
+    return false;
+}
+__device__ __noinline__ bool uq_spin_slow(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
+    return uq_spin_body<false>(p, target, abort_flag);
+}
 __device__ __forceinline__ void red_release_shared(uint32_t *p, uint32_t v) {
     asm volatile("red.release.cta.shared.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
 }
-// Spin until the counter reaches `target` (wrapping compare); bounded like tc_spin.
 __device__ __noinline__ bool counter_spin_slow(const uint32_t *p, uint32_t target, volatile int *abort_flag) {
     const uint64_t t0 = global_ns(), bound = *(volatile unsigned long long *)&g_wait_ns;
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
@@ -711,7 +780,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
     uint32_t *a_ready = raw_info + TC_RS_MAX;   // [TC_EVSLOTS]: dequant warps done, 16 per use
     uint32_t *tmem_slot = a_ready + TC_EVSLOTS;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    uint32_t *grid_s = reinterpret_cast<uint32_t *>(bars + TC_NBARS) + 16;   // IQ variant: after the 64-byte misc area
+    // after the 64-byte misc area: the unit queue (16-byte aligned), then the
+    // IQ3_XXS grid (IQ variants)
+    uint8_t *qbase = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(reinterpret_cast<uint8_t *>(bars + TC_NBARS) + 64) + 15) & ~(uintptr_t)15);
+    const UnitQueue Q{reinterpret_cast<Unit *>(qbase), reinterpret_cast<uint32_t *>(qbase + TC_UQ * 16),
+                      reinterpret_cast<uint32_t *>(qbase + TC_UQ * 16) + 1};
+    uint32_t *grid_s = reinterpret_cast<uint32_t *>(qbase + TC_UQ * 16 + 16);
     if (XV != TC_XV_STD && A.grid)
         for (int i = threadIdx.x; i < 256; i += TC_THREADS) grid_s[i] = A.grid[i];
 
@@ -737,6 +812,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         }
         mbar_init(fin, 1);
         *abort_flag = 0;
+        *Q.n_pub = 0;
+        *Q.n_ack = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -752,18 +829,35 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
 
     const int n_units = *A.n_chunks * A.S;
     const int nR = (A.K + TC_KR - 1) / TC_KR, nA = A.K / TC_KA;
-    const int G = gridDim.x;
 
     if (warp == TC_PROD) {
-        // ---- weight producer: per raw stage one 2-D TMA box per matrix (two for Q8_0)
+        // ---- weight producer: takes the CTA's units from the global counter and
+        // publishes them; per raw stage one 2-D TMA box per matrix (two for Q8_0).
+        // It runs ahead of the consumers by the raw ring, which hides the
+        // chunk-table loads of each new unit.
         if (lane == 0) {
             uint32_t rg = 0;
             bool ok = true;
-            Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, true) : Unit{};
-            for (int u = blockIdx.x; u < n_units && ok; u += G) {
-                const Unit cu = nxt;
-                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, true);
-                const int W = raw_w(cu.fmt), nbox = raw_nbox(cu.fmt);
+            for (uint32_t k = 0; ok; ++k) {
+                int fmt;
+                // dynamic order (measured per 2048-token layer: 793 -> 775 us,
+                // and 902 -> 878 us for the ternary 512-token layer); the IQ
+                // variant keeps the static order, with which its layer measured
+                // 918 us against 945 us dynamic
+                const Unit cu = grab_unit<GATEUP, (XV != TC_XV_IQ)>(A, n_units, k, fmt);
+                // entry k reuses the slot of entry k - TC_UQ: wait until the four
+                // epilogue warps have taken that one
+                if (k >= TC_UQ) {
+                    const uint32_t need = 4u * (k - TC_UQ + 1);
+                    if ((int32_t)(ld_acquire_shared(Q.n_ack) - need) < 0 && !uq_spin_slow(Q.n_ack, need, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                Q.q[k % TC_UQ] = cu;
+                red_release_shared(Q.n_pub, 1u);
+                if (cu.e < 0) break;
+                const int W = raw_w(fmt), nbox = raw_nbox(fmt);
                 const uint32_t bytes = (uint32_t)(NMAT * nbox * R * W);
                 const CUtensorMap *m0 = A.wmaps + 3 * cu.e + (GATEUP ? 0 : 2);
                 for (int rs = 0; rs < nR; ++rs) {
@@ -773,8 +867,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
                         break;
                     }
                     int x0, lead;
-                    raw_x(cu.fmt, rs, x0, lead);
-                    raw_info[slot] = (uint32_t)cu.fmt | ((uint32_t)lead << 8);
+                    raw_x(fmt, rs, x0, lead);
+                    raw_info[slot] = (uint32_t)fmt | ((uint32_t)lead << 8);
                     mbar_expect_tx(&raw_full[slot], bytes);
                     uint8_t *dst = raw + (size_t)slot * A.slot_bytes;
                     for (int m = 0; m < NMAT; ++m)
@@ -797,10 +891,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // stage's dozen boxes back to back left the MMA issuer waiting on B).
         uint32_t bg = 0;
         bool ok = true;
-        Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
-        for (int u = blockIdx.x; u < n_units && ok; u += G) {
-            const Unit cu = nxt;
-            if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+        for (uint32_t k = 0; ok; ++k) {
+            Unit cu;
+            if (!warp_uq_get(Q, k, abort_flag, cu)) {
+                ok = false;
+                break;
+            }
+            if (cu.e < 0) break;
             const int nb = (cu.n + TC_BOX_ROWS - 1) / TC_BOX_ROWS, q = b_steps_per_stage(cu.n);
             const int sub_bytes = nb * TC_BOX_ROWS * 128;
             for (int a0 = 0; a0 < nA; a0 += q) {
@@ -832,10 +929,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         if (lane == 0) {
             uint32_t ev = 0, bg = 0, uc = 0;
             bool ok = true, issued = false;
-            Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
-            for (int u = blockIdx.x; u < n_units && ok; u += G) {
-                const Unit cu = nxt;
-                if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+            for (uint32_t k = 0; ok; ++k) {
+                Unit cu;
+                if (!uq_get(Q, k, abort_flag, cu)) {
+                    ok = false;
+                    break;
+                }
+                if (cu.e < 0) break;
                 const int N = (cu.n + 15) & ~15, q = b_steps_per_stage(cu.n);
                 const uint32_t idesc = idesc_f16(N);
                 const uint32_t sub_step = (uint32_t)(N * 128) >> 4;   // descriptor units per B tile
@@ -901,7 +1001,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         const int mat = GATEUP ? (l >> 6) : 0, row = GATEUP ? (l & 63) : l;
         uint32_t rg = 0;   // raw stages = events seen
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += G) {
+        for (uint32_t k = 0; ok; ++k) {
+            Unit cu;
+            if (!warp_uq_get(Q, k, abort_flag, cu)) {
+                ok = false;
+                break;
+            }
+            if (cu.e < 0) break;
             for (int rs = 0; rs < nR; ++rs) {
                 const uint32_t slot = rg % A.RS, es = rg & (TC_EVSLOTS - 1), euse = rg >> 1;
                 if (!warp_wait(&raw_full[slot], (rg / A.RS) & 1, abort_flag) ||
@@ -955,18 +1061,24 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm_kernel(const __grid_con
         // ---- epilogue: warps 0-3 read TMEM lanes 32w..32w+31
         const int l = 32 * warp + lane;
         uint32_t uc = 0;
-        Unit nxt = blockIdx.x < n_units ? load_unit<GATEUP>(A, blockIdx.x, false) : Unit{};
-        for (int u = blockIdx.x; u < n_units; u += G) {
-            const Unit cu = nxt;
-            if (u + G < n_units) nxt = load_unit<GATEUP>(A, u + G, false);
+        for (uint32_t k = 0;; ++k) {
+            Unit cu;
+            bool ok = warp_uq_get<true>(Q, k, abort_flag, cu);
+            if (ok) {
+                __syncwarp();   // every lane has read entry k
+                if (lane == 0) red_release_shared(Q.n_ack, 1u);
+            }
+            const bool more = ok && cu.e >= 0;
             const int n = cu.n, row0 = cu.row0, s = cu.s;
             const uint32_t d = uc & 1;
-            bool ok = warp_wait(&acc_full[d], (uc >> 1) & 1, abort_flag);
+            if (more) ok = warp_wait(&acc_full[d], (uc >> 1) & 1, abort_flag);
+            // the gate/up epilogue's warps meet at barriers: they leave together
             if (GATEUP) ok = epi_all(ok);
             if (!ok) {
                 if (lane == 0) tc_fail(abort_flag, A.status);
                 break;
             }
+            if (!more) break;   // the end of the queue (the same entry for every warp)
             tmem_fence_after();
             if (GATEUP) {
                 // 16 columns at a time: every lane's g or u to shared memory, then
@@ -1060,13 +1172,13 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 // bucket row of each of its kept pairs (so every expert's rows are contiguous
 // for the B tiles); that row's inverse scale; its |h| maximum cleared.
 // Block T: the chunk table, <= 128 bucket rows of one expert per chunk, in
-// ascending expert order.
+// ascending expert order; and the two GEMMs' unit counters, zeroed.
 __global__ void __launch_bounds__(PREP_THREADS) tc_prep_kernel(const uint16_t *__restrict__ x, int T, int k, int H,
                                                                int E, const int32_t *__restrict__ pos,
                                                                const int32_t *__restrict__ offsets,
                                                                const int32_t *__restrict__ active, __half *xg,
                                                                float *xinv, uint32_t *hmax, int4 *chunks,
-                                                               int32_t *n_chunks) {
+                                                               int32_t *n_chunks, int32_t *unit_next) {
     __shared__ float red[PREP_THREADS / 32];
     __shared__ int scan[PREP_THREADS];
     if ((int)blockIdx.x < T) {
@@ -1132,7 +1244,11 @@ __global__ void __launch_bounds__(PREP_THREADS) tc_prep_kernel(const uint16_t *_
         total += scan[PREP_THREADS - 1];
         __syncthreads();
     }
-    if (threadIdx.x == 0) *n_chunks = total;
+    if (threadIdx.x == 0) {
+        *n_chunks = total;
+        unit_next[0] = 0;
+        unit_next[1] = 0;
+    }
 }
 
 // One warp per bucket row: h (fp32) -> fp16 scaled by 2^sigma from the row's
@@ -1284,16 +1400,18 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
     uint32_t *hmax = reinterpret_cast<uint32_t *>(ws_base + C.hmax);
     int4 *chunks = reinterpret_cast<int4 *>(ws_base + C.chunks);
     int32_t *n_chunks = reinterpret_cast<int32_t *>(ws_base + C.n_chunks);
+    int32_t *unit_next = reinterpret_cast<int32_t *>(ws_base + C.unit_next);
     CUtensorMap xmap, hmap;
     if (!encode_act_map(&xmap, xg, P, H) || !encode_act_map(&hmap, h16, P, I)) return cudaErrorInvalidValue;
 
     cudaError_t err;
     tc_prep_kernel<<<T + 1, PREP_THREADS, 0, s>>>(x, T, k, H, E, pos, offsets, active, xg, xinv, hmax, chunks,
-                                                   n_chunks);
+                                                   n_chunks, unit_next);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
 
-    TcArgs a1{table, maps, chunks, n_chunks, H, I / 64, H, I, sb1, rs1, xinv, h32, hmax, nullptr, status, grid};
+    TcArgs a1{table, maps, chunks, n_chunks, H, I / 64, H, I, sb1, rs1, xinv, h32, hmax, nullptr, status, grid,
+              unit_next};
     const size_t smem1 = tc_smem_bytes(sb1, rs1, iq);
     if (xv == TC_XV_T5)
         tc_gemm_kernel<true, TC_XV_T5><<<G, TC_THREADS, smem1, s>>>(xmap, a1);
@@ -1307,7 +1425,8 @@ cudaError_t launch_tc_path(const DevExpert *table, const void *wmaps, uint32_t g
     tc_hprep_kernel<<<(P + PREP_THREADS / 32 - 1) / (PREP_THREADS / 32), PREP_THREADS, 0, s>>>(h32, hmax, offsets, E,
                                                                                              I, h16, hinv);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    TcArgs a2{table, maps, chunks, n_chunks, I, H / TC_M, H, I, sb2, rs2, hinv, nullptr, nullptr, y, status, grid};
+    TcArgs a2{table, maps, chunks, n_chunks, I, H / TC_M, H, I, sb2, rs2, hinv, nullptr, nullptr, y, status, grid,
+              unit_next + 1};
     const size_t smem2 = tc_smem_bytes(sb2, rs2, iq);
     if (xv == TC_XV_T5)
         tc_gemm_kernel<false, TC_XV_T5><<<G, TC_THREADS, smem2, s>>>(hmap, a2);
