@@ -258,11 +258,36 @@ __host__ __device__ inline SgLayoutB sg_layout_b(int I, int E, int nsb, int stag
 // times the expert's n_a pairs of dot products plus one for streaming the
 // rows, so the CTAs holding the rows of experts that many tokens picked get
 // fewer of them. S: shared scratch of n_act + 1 ints (the prefix costs).
-__device__ void sg_range(const SgArgs &A, int n_act, int cpe, int *S, int &c0, int &nloc, int &a0, int &na) {
+// Cost of one row pair (gate/up) or one row (down) of an expert in format f
+// with n tokens: streaming its bytes plus n dot products, in units of 1 ns
+// per chunk of the 16- and 6-row layers on GB300 (least-squares fits of the
+// per-CTA times of layers whose experts all had one format; the Q6_K and
+// MXFP4 dots cost 2.3-2.5 times the Q4_K one per token). The shares are cut
+// by this cost: a split by tokens + 1 left the CTAs of the 6-row mixed-tier
+// layer finishing between 32 and 65 us.
+__device__ __forceinline__ int sg_chunk_cost(bool gateup, int f, int n) {
+    if (gateup) {
+        switch (f) {
+            case MOE_Q8_0: return 95 + 36 * n;
+            case MOE_Q6_K: return 55 + 150 * n;
+            case MOE_MXFP4: return 40 + 160 * n;
+            default: return 45 + 65 * n;   // Q4_K
+        }
+    }
+    return f == MOE_MXFP4 ? 50 + 115 * n : 45 + 80 * n;   // MXFP4 or Q8_0 down rows
+}
+// Bounds that follow from the costs (n >= 1 per active expert): a chunk costs
+// at least SG_CMIN_CHUNK; a chunk row of the whole list at most SG_CMAX_PAIR
+// per pair; one more pair of an expert adds at least SG_CMIN_TOKEN.
+constexpr int SG_CMIN_CHUNK = 110, SG_CMAX_PAIR = 255, SG_CMIN_TOKEN = 36;
+
+__device__ void sg_range(const SgArgs &A, bool gateup, int n_act, int cpe, int *S, int &c0, int &nloc, int &a0,
+                         int &na) {
     const int tid = threadIdx.x, lane = tid & 31;
     for (int a = tid; a < n_act; a += SG_THREADS) {
         const int e = A.active[1 + a];
-        S[a] = cpe * (A.offsets[e + 1] - A.offsets[e] + 1);
+        const int f = gateup ? A.table[e].gate.fmt : A.table[e].down.fmt;
+        S[a] = cpe * sg_chunk_cost(gateup, f, A.offsets[e + 1] - A.offsets[e]);
     }
     __syncthreads();
     if (tid < 32) {   // exclusive prefix sums in place, S[n_act] = total
@@ -325,7 +350,7 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sg_gateup_kernel(SgArgs A) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n_act = A.active[0], cpe = A.I / A.cr;
     int c0, nloc, a0, na;
-    sg_range(A, n_act, cpe, reinterpret_cast<int *>(smem + L.cost), c0, nloc, a0, na);
+    sg_range(A, true, n_act, cpe, reinterpret_cast<int *>(smem + L.cost), c0, nloc, a0, na);
     if (na > A.nexp) {   // beyond the planned bound (cannot happen): skip, flagged
         if (tid == 0) sg_flag(A.status, MOE_FLAG_WAIT_TIMEOUT);
         return;
@@ -543,7 +568,7 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sg_down_kernel(SgArgs A) {
     // the first weight copies need no wait.
     const int n_act = A.active[0], cpe = A.H / SG_DN_ROWS;
     int c0, nloc, a0, na;
-    sg_range(A, n_act, cpe, reinterpret_cast<int *>(smem + L.cost), c0, nloc, a0, na);
+    sg_range(A, false, n_act, cpe, reinterpret_cast<int *>(smem + L.cost), c0, nloc, a0, na);
     if (na > A.nexp) {
         if (tid == 0) sg_flag(A.status, MOE_FLAG_WAIT_TIMEOUT);
         return;
@@ -664,10 +689,11 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
     if ((gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K) | (1u << MOE_Q6_K) | (1u << MOE_MXFP4))) != 0) return p;
     if (gu_stride <= 0 || dn_stride <= 0 || gu_stride % 16 != 0 || dn_stride % 16 != 0) return p;
     const int P = T * k, nmax = std::min(P, E);
-    // experts one CTA's share can touch: an expert costs at least 2 per
-    // chunk, the whole list at most 2 P per chunk row, so a share holds at
-    // most P / G whole experts plus the two it starts and ends in
-    p.nexp = std::max(nmax, P) / G + 2;
+    // experts one CTA's share can touch (sg_chunk_cost): an expert costs at
+    // least SG_CMIN_CHUNK per chunk, the whole list at most SG_CMAX_PAIR * P per
+    // chunk row, so a share holds at most SG_CMAX_PAIR * P / (SG_CMIN_CHUNK * G)
+    // whole experts plus the two it starts and ends in
+    p.nexp = (int)(((long long)SG_CMAX_PAIR * P + (long long)SG_CMIN_CHUNK * G - 1) / ((long long)SG_CMIN_CHUNK * G)) + 2;
     // gate/up: each of the 15 consumer warps holds one slot while it
     // computes, so the slots beyond 15 are the copies in flight: the largest
     // chunk (4, 2 or 1 row pairs) that gives at least 24 slots (the 6-row
@@ -693,7 +719,11 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
     if (p.cr == 0) return p;
     p.smem_a = sg_layout_a(T, H, E, p.ns, p.stage, p.nexp).total;
     // down: 4 rows per chunk, at least 24 slots
-    p.nq = std::min(P, p.nexp * T + 2 * P / G + 1);   // pairs of the experts of one share
+    // pairs of the experts of one share: the whole experts' pairs cost at least
+    // SG_CMIN_TOKEN each, so there are at most SG_CMAX_PAIR * P /
+    // (SG_CMIN_TOKEN * G) of them, plus the two partial experts' T each
+    p.nq = std::min(P, (int)(((long long)SG_CMAX_PAIR * P + (long long)SG_CMIN_TOKEN * G - 1) /
+                             ((long long)SG_CMIN_TOKEN * G)) + 2 * T);
     p.stageb = (int)(SG_DN_ROWS * dn_stride);
     const size_t fixed_b = sg_layout_b(I, E, 0, 0, p.nq, p.nexp).total;
     if ((size_t)optin <= fixed_b + 16) return p;
