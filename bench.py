@@ -12,7 +12,8 @@ Prints one JSON line. The headline workload (``--config``, default the
 timed over exactly ``--steps`` steps. `value` is MoE-layer tokens/s
 (token-layers per second, i.e. T / per-layer time, summed over ranks); `e2e`
 is the same metric through the public API with pinned host buffers copied in
-and out every layer; `roofline` is the dominant kernel's algorithmic bytes
+and out every layer (the copies of one layer overlapping the computation of
+its neighbours, on three streams, one step replayed as a CUDA graph); `roofline` is the dominant kernel's algorithmic bytes
 per launch over its event-timed duration against the measured HBM copy
 bandwidth; `cpu_baseline` is the fp64 oracle on the host cores (all cores,
 and single-threaded in `cpu_baseline.single_thread`) on a bounded sample of
@@ -451,25 +452,63 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
     lg_dev = [torch.empty((T, E), dtype=torch.float32, device=dev) for _ in layers]
     n_e2e = max(1, min(args.e2e_steps, steps))
 
+    # Three streams, as a serving loop would run them: the inputs of layer l
+    # go up on s_in while earlier layers compute on `stream`, and its output
+    # comes back on s_out while later layers compute; one step (all layers,
+    # all copies) is captured as a CUDA graph, like the headline's, so that
+    # the host does not pace the small layers. Replays of the graph on
+    # `stream` run one after another, so every buffer is reused in order.
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(NL)]
+    ev_comp = [torch.cuda.Event() for _ in range(NL)]
+
     def e2e_step():
+        root = torch.cuda.Event()
+        root.record(stream)
+        s_in.wait_event(root)
+        s_out.wait_event(root)
         for l in range(NL):
-            x_dev[l].copy_(x_pin[l], non_blocking=True)
-            lg_dev[l].copy_(lg_pin[l], non_blocking=True)
-            M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
-            out_pin[l].copy_(outs[l], non_blocking=True)
+            with torch.cuda.stream(s_in):
+                x_dev[l].copy_(x_pin[l], non_blocking=True)
+                lg_dev[l].copy_(lg_pin[l], non_blocking=True)
+                ev_in[l].record(s_in)
+            with torch.cuda.stream(stream):
+                stream.wait_event(ev_in[l])
+                M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
+                ev_comp[l].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[l])
+                out_pin[l].copy_(outs[l], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(s_out)
+        stream.wait_event(done)
 
     with torch.cuda.stream(stream):
-        for _ in range(2):
+        e2e_step()          # eager once
+    torch.cuda.synchronize()
+    g_e2e = None
+    if not args.no_graph:
+        g_e2e = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_e2e, stream=stream):
             e2e_step()
-    stream.synchronize()
+
+    def e2e_run():
+        with torch.cuda.stream(stream):
+            if g_e2e is None:
+                e2e_step()
+            else:
+                g_e2e.replay()
+
+    for _ in range(2):
+        e2e_run()
+    torch.cuda.synchronize()
     barrier(world)
     h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        h0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        h1.record(stream)
-    stream.synchronize()
+    h0.record(stream)
+    for _ in range(n_e2e):
+        e2e_run()
+    h1.record(stream)
+    torch.cuda.synchronize()
     e2e_elapsed = allreduce_max(h0.elapsed_time(h1) / 1e3, world)
 
     # status of every workspace (device-detected input errors) after all runs
