@@ -194,12 +194,18 @@ __global__ void __launch_bounds__(BK_THREADS, 1) bucket_scan_kernel(int G, int E
                                                                     int32_t *__restrict__ active) {
     __shared__ int warp_tot[33];
     const int tid = threadIdx.x;
+    constexpr int BATCH = 16;   // independent loads in flight per thread (one range's load at a time took ~15 us)
     int c = 0;
     if (tid < E) {
-        for (int r = 0; r < G; ++r) {
-            const int v = cnt[(size_t)r * E + tid];
-            cnt[(size_t)r * E + tid] = c;
-            c += v;
+        for (int r0 = 0; r0 < G; r0 += BATCH) {
+            int v[BATCH];
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) v[j] = r0 + j < G ? cnt[(size_t)(r0 + j) * E + tid] : 0;
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) {
+                if (r0 + j < G) cnt[(size_t)(r0 + j) * E + tid] = c;
+                c += v[j];
+            }
         }
     }
     int total, nact;
@@ -208,7 +214,14 @@ __global__ void __launch_bounds__(BK_THREADS, 1) bucket_scan_kernel(int G, int E
     if (tid < E) {
         offsets[tid] = excl;
         if (c > 0) active[1 + aexcl] = tid;
-        for (int r = 0; r < G; ++r) cnt[(size_t)r * E + tid] += excl;
+        for (int r0 = 0; r0 < G; r0 += BATCH) {
+            int v[BATCH];
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j) v[j] = r0 + j < G ? cnt[(size_t)(r0 + j) * E + tid] : 0;
+#pragma unroll
+            for (int j = 0; j < BATCH; ++j)
+                if (r0 + j < G) cnt[(size_t)(r0 + j) * E + tid] = v[j] + excl;
+        }
     }
     if (tid == 0) {
         offsets[E] = total;
