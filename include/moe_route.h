@@ -277,8 +277,9 @@ int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_opti
 /* Which kernels the grouped GEMV path (MOE_PATH_GEMV) runs for these
  * arguments: MOE_GEMV_STREAMING (persistent gate/up and down kernels that
  * stream the routed experts' rows through a shared-memory ring; decode
- * batches of 1..16 rows with Q8_0 or MXFP4 down and an activation pointer
- * aligned to 16 bytes at the forward) or MOE_GEMV_TILED (one CTA per expert
+ * batches of 1..16 rows, or 1..32 rows when every gate/up matrix is Q8_0 or
+ * Q4_K, with Q8_0 or MXFP4 down, shared memory permitting, and an activation
+ * pointer aligned to 16 bytes at the forward) or MOE_GEMV_TILED (one CTA per expert
  * tile; any other layer). -1 if the arguments are invalid. Host-only. */
 #define MOE_GEMV_TILED 0
 #define MOE_GEMV_STREAMING 1
@@ -360,8 +361,9 @@ int moe_sum_partials(const float *parts, int32_t n_parts, int64_t count, float *
  *   - Sizes: accepted when the workspace of the path the call takes
  *     (moe_ffn_workspace_size_for_path with opt->path, AUTO by default) fits in
  *     4 MiB: e.g. up to 25 tokens at E = 512, k = 10, H = 2048, I = 640, where
- *     AUTO sends one token to the fused kernel and up to 16 rows to the
- *     streaming GEMV kernels, and a requested tensor path up to about 20
+ *     AUTO sends one token to the fused kernel and up to 16 rows (25 with
+ *     Q8_0 / Q4_K gate/up) to the streaming GEMV kernels, and the tensor path
+ *     (requested, or AUTO's choice for other formats above 16 rows) up to about 20
  *     tokens; larger sizes return MOE_ERR_UNSUPPORTED before anything is
  *     enqueued.
  *   - The first call on a device looks up the array's device address (with

@@ -305,7 +305,13 @@ def ffn_forward(table: WeightTable, x_bf16: torch.Tensor, logits: torch.Tensor, 
         raise ValueError("x / logits shape does not match the table")
     out = out if out is not None else torch.empty((T, H), dtype=torch.float32, device=x_bits.device)
     _dev(out, "out", torch.float32)
-    ws = ws if ws is not None else Workspace(table, T, k, stream)
+    if ws is None:
+        # sized for the requested path; for a path that cannot run this layer,
+        # for AUTO's, so that the forward itself reports the refusal
+        path = options.path if options is not None else 0
+        if path and load().moe_ffn_workspace_size_for_path(ctypes.byref(table.c), T, k, path) == 0:
+            path = 0
+        ws = Workspace(table, T, k, stream, path=path)
     opt = ctypes.byref(options) if options is not None else None
     _check("moe_ffn_forward", load().moe_ffn_forward(ctypes.byref(table.c), _ptr(x_bits), _ptr(logits), T, k,
                                                       opt, _ptr(out), _ptr(ws.buf), ws.nbytes, _stream(stream)))

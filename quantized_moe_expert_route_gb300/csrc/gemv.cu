@@ -514,7 +514,7 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
                              const int32_t *offsets, const int32_t *pairs, const int32_t *active, const int32_t *pos,
                              const float *wts, const uint16_t *x, float *h, float *y, float *out, uint32_t *status,
                              cudaEvent_t const *events, cudaStream_t s) {
-    // decode batches of up to 16 rows: the streaming kernels (stream.cu)
+    // decode batches of up to 16 rows (32 with Q8_0 / Q4_K gate/up): the streaming kernels (stream.cu)
     if (T > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
         const SgPlan p = stream_plan(T, k, E, H, I, gu_formats, down_formats, gu_stride, dn_stride);
         if (p.ok) {

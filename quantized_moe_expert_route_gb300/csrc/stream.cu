@@ -1,5 +1,6 @@
 // Streaming grouped GEMV for decode batches of up to 16 token rows, any mix of
-// the gate/up formats (Q8_0, Q4_K, Q6_K, MXFP4) and Q8_0 or MXFP4 down.
+// the gate/up formats (Q8_0, Q4_K, Q6_K, MXFP4) and Q8_0 or MXFP4 down, and of
+// up to 32 rows when every gate/up matrix is Q8_0 or Q4_K.
 //
 // The grouped multi-session decode of "多卡 CUDA 张量并行：DwarfStar 如何在 8 张
 // L40S 上跑出 120 t/s" (section 120 t/s 的秘密) reads each selected expert's
@@ -43,7 +44,14 @@ constexpr int SG_THREADS = 512;
 constexpr int SG_WARPS = SG_THREADS / 32;
 constexpr int SG_CONS = SG_WARPS - 1;   // consumer warps; lane 0 of the last warp refills the ring
 constexpr int SG_MAX_SLOTS = 64;
-constexpr int SG_MAX_T = 16;
+// Row limits, from per-layer times of the 512-expert layer against the
+// tensor-core path: with Q4_K gate/up the streaming kernels take 159, 179 and
+// 273 us at 20, 24 and 32 rows against 226, 249 and 292 us; with the mixed
+// tiers (Q6_K and MXFP4 dots cost 2.3-2.5 times Q4_K's per token) they break
+// even at 16 rows (213 against 212 us) and lose beyond (249 against 240 us at
+// 20 rows).
+constexpr int SG_MAX_T = 32;        // Q8_0 / Q4_K gate/up
+constexpr int SG_MAX_T_MIXED = 16;  // with Q6_K or MXFP4 gate/up
 constexpr int SG_DN_ROWS = 4;   // down rows per chunk: 8 lanes per row
 constexpr int SG_HQW = 20;      // words per staged 32-block of h: 16 int16 pairs, 2^-sigma, padding to 16 bytes
 
@@ -685,6 +693,7 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
     const int G = sm_count(), optin = optin_smem();
     if (G <= 0 || optin <= 0) return p;
     if (T < 1 || T > SG_MAX_T || H % 64 != 0 || I % 32 != 0 || H % SG_DN_ROWS != 0) return p;
+    if (T > SG_MAX_T_MIXED && (gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K))) != 0) return p;
     if ((down_formats & ~((1u << MOE_Q8_0) | (1u << MOE_MXFP4))) != 0) return p;
     if ((gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K) | (1u << MOE_Q6_K) | (1u << MOE_MXFP4))) != 0) return p;
     if (gu_stride <= 0 || dn_stride <= 0 || gu_stride % 16 != 0 || dn_stride % 16 != 0) return p;

@@ -374,6 +374,47 @@ def test_stream_kernels_small(M, tiers, T, H, I):
     assert np.array_equal(again.cpu().numpy(), out)
 
 
+@pytest.mark.parametrize("tiers,T,H,I", [("q4k", 17, 512, 128), ("q4k", 24, 256, 64), ("q8_0", 32, 512, 96),
+                                         ("q4k", 32, 2048, 64)])
+def test_stream_kernels_up_to_32_rows(M, tiers, T, H, I):
+    """The streaming kernels take up to 32 rows when every gate/up matrix is
+    Q8_0 or Q4_K (17, 24 and 32 rows here), and AUTO takes them there."""
+    cfg = synth.LayerConfig("sg32", 24, 6, H, I, T, tiers, True, 770 + T + H)
+    L = synth.make_layer(cfg, 0)
+    opt = M.make_options(n_experts=cfg.n_experts, path=M.PATH_GEMV)
+    out, table, x, logits = run_layer(M, L, options=opt)
+    assert M.gemv_kernels(table, T, cfg.k) == M.GEMV_STREAMING
+    assert M.ffn_path(table, T, cfg.k) == M.PATH_GEMV
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), f"stream {tiers} T={T}")
+
+
+def test_stream_row_limit_by_format(M):
+    """With Q6_K or MXFP4 gate/up the streaming kernels stop at 16 rows: AUTO
+    takes the tensor path above (it measured faster there)."""
+    L = synth.make_layer(small_cfg(tiers="mixed", E=24, k=6, H=512, I=128, T=20, seed=31), 0)
+    experts, x, logits = host_layer_to_device(L)
+    table = M.WeightTable(experts, L.cfg.hidden, L.cfg.inter)
+    assert M.gemv_kernels(table, 16, L.cfg.k) == M.GEMV_STREAMING
+    assert M.gemv_kernels(table, 17, L.cfg.k) == M.GEMV_TILED
+    assert M.ffn_path(table, 20, L.cfg.k) == M.PATH_TENSOR
+
+
+def test_full_decode24_streaming(M):
+    """The 512-expert Q4_K layer at 24 rows on AUTO (the streaming kernels),
+    every token against the oracle."""
+    from synth import gpu as sgpu
+    cfg = synth.LayerConfig("decode24", 512, 10, 2048, 640, 24, "q4k", True, 12524)
+    DL = sgpu.make_device_layer(cfg, 0)
+    table = M.WeightTable(DL.experts, cfg.hidden, cfg.inter)
+    assert M.ffn_path(table, 24, cfg.k) == M.PATH_GEMV and M.gemv_kernels(table, 24, cfg.k) == M.GEMV_STREAMING
+    ws = M.Workspace(table, 24, cfg.k)
+    out = M.ffn_forward(table, DL.x_bf16, DL.logits, cfg.k, ws=ws).cpu().numpy()
+    assert ws.read_status() == 0
+    assert_parity(out, oracle_full_layer(cfg, DL), "decode24 streaming")
+    del table, DL
+    torch.cuda.empty_cache()
+
+
 def test_full_decode1_gemv_path(M):
     """The general grouped GEMV path on the full-size single-token layer."""
     from synth import gpu as sgpu
