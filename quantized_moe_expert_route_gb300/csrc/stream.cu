@@ -32,6 +32,7 @@
 // its experts and issues its first weight copies while the gate/up kernel
 // finishes, and waits for it only before reading h.
 #include <algorithm>
+#include <climits>
 
 #include "moe_internal.cuh"
 #include "dot16.cuh"
@@ -266,28 +267,38 @@ __host__ __device__ inline SgLayoutB sg_layout_b(int I, int E, int nsb, int stag
 // times the expert's n_a pairs of dot products plus one for streaming the
 // rows, so the CTAs holding the rows of experts that many tokens picked get
 // fewer of them. S: shared scratch of n_act + 1 ints (the prefix costs).
-// Cost of one row pair (gate/up) or one row (down) of an expert in format f
-// with n tokens: streaming its bytes plus n dot products, in units of 1 ns
-// per chunk of the 16- and 6-row layers on GB300 (least-squares fits of the
-// per-CTA times of layers whose experts all had one format; the Q6_K and
-// MXFP4 dots cost 2.3-2.5 times the Q4_K one per token). The shares are cut
-// by this cost: a split by tokens + 1 left the CTAs of the 6-row mixed-tier
-// layer finishing between 32 and 65 us.
+// Cost of one chunk of an expert in format f with n tokens: streaming its
+// rows plus n dot products per row, in ns per gate/up row pair or per 4-row
+// down chunk. Least-squares fits of the per-CTA times of 28 layers (4 to 16
+// rows; Q4_K, Q8_0 and mixed tiers; globaltimer stamps in an instrumented
+// copy) against each CTA's chunks by format, plus a constant per CTA, gave
+// the down costs and the gate/up ratios: the Q6_K and MXFP4 dots cost 3.3
+// and 3.8 times the Q4_K one per token, the Q8_0 one 0.65 times. The gate/up
+// costs keep the Q4_K-only fit (45 + 65 n) and scale the other formats by
+// those ratios: the joint fit's own Q4_K row (53 + 42 n) moved the cuts of
+// the 16-row Q4_K layer and cost it 2.7%. The shares are cut by this cost:
+// a split by tokens + 1 left the CTAs of the 6-row mixed-tier layer
+// finishing between 32 and 65 us.
 __device__ __forceinline__ int sg_chunk_cost(bool gateup, int f, int n) {
     if (gateup) {
         switch (f) {
-            case MOE_Q8_0: return 95 + 36 * n;
-            case MOE_Q6_K: return 55 + 150 * n;
-            case MOE_MXFP4: return 40 + 160 * n;
+            case MOE_Q8_0: return 91 + 42 * n;
+            case MOE_Q6_K: return 41 + 217 * n;
+            case MOE_MXFP4: return 42 + 245 * n;
             default: return 45 + 65 * n;   // Q4_K
         }
     }
-    return f == MOE_MXFP4 ? 50 + 115 * n : 45 + 80 * n;   // MXFP4 or Q8_0 down rows
+    return f == MOE_MXFP4 ? 18 + 94 * n : 22 + 54 * n;   // MXFP4 or Q8_0 down, 4 rows
 }
-// Bounds that follow from the costs (n >= 1 per active expert): a chunk costs
-// at least SG_CMIN_CHUNK; a chunk row of the whole list at most SG_CMAX_PAIR
-// per pair; one more pair of an expert adds at least SG_CMIN_TOKEN.
-constexpr int SG_CMIN_CHUNK = 110, SG_CMAX_PAIR = 255, SG_CMIN_TOKEN = 36;
+// Bounds that follow from the costs a + b n (n >= 1 per active expert, so a +
+// b n <= (a + b) n): a gate/up chunk costs at least SG_GU_CMIN_CHUNK and a
+// chunk row of the whole list at most SG_GU_CMAX_PAIR per pair; a down chunk
+// at least SG_DN_CMIN_CHUNK, a row of the list at most SG_DN_CMAX_PAIR per
+// pair, one more pair of an expert at least SG_DN_CMIN_TOKEN.
+constexpr int SG_GU_CMIN_CHUNK = 110, SG_GU_CMAX_PAIR = 287;
+constexpr int SG_DN_CMIN_CHUNK = 76, SG_DN_CMAX_PAIR = 112, SG_DN_CMIN_TOKEN = 54;
+static_assert(SG_DN_CMAX_PAIR * SG_GU_CMIN_CHUNK <= SG_GU_CMAX_PAIR * SG_DN_CMIN_CHUNK,
+              "the gate/up bound on experts per share covers the down kernel's");
 
 __device__ void sg_range(const SgArgs &A, bool gateup, int n_act, int cpe, int *S, int &c0, int &nloc, int &a0,
                          int &na) {
@@ -698,11 +709,17 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
     if ((gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K) | (1u << MOE_Q6_K) | (1u << MOE_MXFP4))) != 0) return p;
     if (gu_stride <= 0 || dn_stride <= 0 || gu_stride % 16 != 0 || dn_stride % 16 != 0) return p;
     const int P = T * k, nmax = std::min(P, E);
+    // the prefix costs of sg_range are ints: chunks per expert (at most I or
+    // H / 4) times the list's cost per chunk row
+    if ((long long)I * SG_GU_CMAX_PAIR * P > INT_MAX || (long long)(H / SG_DN_ROWS) * SG_DN_CMAX_PAIR * P > INT_MAX)
+        return p;
     // experts one CTA's share can touch (sg_chunk_cost): an expert costs at
-    // least SG_CMIN_CHUNK per chunk, the whole list at most SG_CMAX_PAIR * P per
-    // chunk row, so a share holds at most SG_CMAX_PAIR * P / (SG_CMIN_CHUNK * G)
-    // whole experts plus the two it starts and ends in
-    p.nexp = (int)(((long long)SG_CMAX_PAIR * P + (long long)SG_CMIN_CHUNK * G - 1) / ((long long)SG_CMIN_CHUNK * G)) + 2;
+    // least SG_GU_CMIN_CHUNK per chunk, the whole list at most SG_GU_CMAX_PAIR
+    // * P per chunk row, so a share holds at most SG_GU_CMAX_PAIR * P /
+    // (SG_GU_CMIN_CHUNK * G) whole experts plus the two it starts and ends in
+    // (fewer in the down kernel's shares)
+    p.nexp = (int)(((long long)SG_GU_CMAX_PAIR * P + (long long)SG_GU_CMIN_CHUNK * G - 1) /
+                   ((long long)SG_GU_CMIN_CHUNK * G)) + 2;
     // gate/up: each of the 15 consumer warps holds one slot while it
     // computes, so the slots beyond 15 are the copies in flight: the largest
     // chunk (4, 2 or 1 row pairs) that gives at least 24 slots (the 6-row
@@ -728,11 +745,11 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
     if (p.cr == 0) return p;
     p.smem_a = sg_layout_a(T, H, E, p.ns, p.stage, p.nexp).total;
     // down: 4 rows per chunk, at least 24 slots
-    // pairs of the experts of one share: the whole experts' pairs cost at least
-    // SG_CMIN_TOKEN each, so there are at most SG_CMAX_PAIR * P /
-    // (SG_CMIN_TOKEN * G) of them, plus the two partial experts' T each
-    p.nq = std::min(P, (int)(((long long)SG_CMAX_PAIR * P + (long long)SG_CMIN_TOKEN * G - 1) /
-                             ((long long)SG_CMIN_TOKEN * G)) + 2 * T);
+    // pairs of the experts of one down share: the whole experts' pairs cost at
+    // least SG_DN_CMIN_TOKEN each, so there are at most SG_DN_CMAX_PAIR * P /
+    // (SG_DN_CMIN_TOKEN * G) of them, plus the two partial experts' T each
+    p.nq = std::min(P, (int)(((long long)SG_DN_CMAX_PAIR * P + (long long)SG_DN_CMIN_TOKEN * G - 1) /
+                             ((long long)SG_DN_CMIN_TOKEN * G)) + 2 * T);
     p.stageb = (int)(SG_DN_ROWS * dn_stride);
     const size_t fixed_b = sg_layout_b(I, E, 0, 0, p.nq, p.nexp).total;
     if ((size_t)optin <= fixed_b + 16) return p;
