@@ -447,8 +447,11 @@ __global__ void __launch_bounds__(GV_THREADS) down_gemv_kernel(GvArgs A) {
 }
 
 // out[t] = sum_j w[t, j] * y[pos[t, j]] in ascending j (0 if no pair is kept).
+// With SCALED, row q of y is multiplied first by yscale[q], a power of two,
+// which is exact: the tensor path leaves that scale to this kernel.
+template <bool SCALED>
 __global__ void combine_kernel(int T, int k, int H, const int32_t *__restrict__ pos, const float *__restrict__ wts,
-                               const float *__restrict__ y, float *__restrict__ out) {
+                               const float *__restrict__ y, const float *__restrict__ yscale, float *__restrict__ out) {
     const int t = blockIdx.y;
     const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (i4 * 4 >= H) return;
@@ -458,6 +461,13 @@ __global__ void combine_kernel(int T, int k, int H, const int32_t *__restrict__ 
         if (q < 0) continue;
         float w = wts[t * k + j];
         float4 v = reinterpret_cast<const float4 *>(y + (size_t)q * H)[i4];
+        if (SCALED) {
+            const float sq = yscale[q];
+            v.x *= sq;
+            v.y *= sq;
+            v.z *= sq;
+            v.w *= sq;
+        }
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -497,10 +507,13 @@ int current_device() {
 }
 
 cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float *wts, const float *y, float *out,
-                           cudaStream_t s) {
+                           cudaStream_t s, const float *yscale) {
     if (T <= 0) return cudaSuccess;
     dim3 g((H / 4 + 127) / 128, T);
-    combine_kernel<<<g, 128, 0, s>>>(T, k, H, pos, wts, y, out);
+    if (yscale)
+        combine_kernel<true><<<g, 128, 0, s>>>(T, k, H, pos, wts, y, yscale, out);
+    else
+        combine_kernel<false><<<g, 128, 0, s>>>(T, k, H, pos, wts, y, nullptr, out);
     return cudaGetLastError();
 }
 
@@ -550,7 +563,7 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
     }
     if (T > 0) {
         dim3 g3((H / 4 + 127) / 128, T);
-        combine_kernel<<<g3, 128, 0, s>>>(T, k, H, pos, wts, y, out);
+        combine_kernel<false><<<g3, 128, 0, s>>>(T, k, H, pos, wts, y, nullptr, out);
         return cudaGetLastError();
     }
     return cudaSuccess;

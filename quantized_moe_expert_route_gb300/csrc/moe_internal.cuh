@@ -139,9 +139,10 @@ cudaError_t record_event(cudaEvent_t ev, cudaStream_t s);   // event (graph node
 cudaError_t allow_max_dynamic_smem(const void *fn);         // opt in to all free shared memory
 int current_device();
 int sm_count();
-// out[t] = sum over slots j ascending of w[t,j] * y[pos[t,j]]; y in bucket order
+// out[t] = sum over slots j ascending of w[t,j] * y[pos[t,j]]; y in bucket order,
+// each row q first multiplied by yscale[q] (a power of two) when yscale is given
 cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float *wts, const float *y, float *out,
-                           cudaStream_t s);
+                           cudaStream_t s, const float *yscale = nullptr);
 
 // Streaming grouped GEMV for decode batches (stream.cu): the launch plan
 // (ok == false if the kernels cannot run the layer) and the launcher of its
