@@ -553,6 +553,48 @@ __device__ __forceinline__ float sg_down_block(const uint8_t *wrow, int b, const
     }
 }
 
+// A Q8_0 block of a row that starts on 16 bytes, with the parity of b known:
+// block b starts at byte 34 b, so an even block starts on a word (its scale
+// in the low half of the word, its codes 2 bytes in) and an odd block 2 bytes
+// into one (its scale in the high half, its codes on a word). Each code pair
+// is then one half of a word at a fixed place, which dp2a.lo or dp2a.hi reads
+// as it is: no funnel shifts. The same integer sum and the same fp32 product
+// as sg_down_block.
+template <bool ODD>
+__device__ __forceinline__ float sg_down_q8_0_fixed(const uint8_t *wrow, int b, const uint32_t *hb) {
+    uint32_t hv[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const uint4 q = reinterpret_cast<const uint4 *>(hb)[v];
+        hv[4 * v] = q.x;
+        hv[4 * v + 1] = q.y;
+        hv[4 * v + 2] = q.z;
+        hv[4 * v + 3] = q.w;
+    }
+    const float hs = __uint_as_float(hb[16]);
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(wrow + 34 * b - (ODD ? 2 : 0));
+    uint32_t W[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) W[i] = w[i];
+    int s = 0;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+        // code pair m: bytes 2 + 2m (even block) or 4 + 2m (odd) of the words
+        const int word = ODD ? 1 + (m >> 1) : (m + 1) >> 1;
+        const bool hi = ODD ? (m & 1) != 0 : ((m + 1) & 1) != 0;
+        s = hi ? dp2a_hi(hv[m], W[word], s) : dp2a_lo(hv[m], W[word], s);
+    }
+    return (ODD ? half_hi(W[0]) : half_lo(W[0])) * hs * (float)s;
+}
+
+// Where block b of a staged h row sits: in each whole group of 16 blocks the
+// even blocks come first, then the odd ones, so the eight lanes of a row that
+// read blocks 2i (or 2i + 1) of a group read consecutive staged blocks (80
+// bytes apart: no bank conflicts); blocks after the last whole group stay.
+__device__ __forceinline__ int sg_hslot(int b, int U) {
+    return b < (U & ~15) ? (b & ~15) + ((b & 1) << 3) + ((b & 15) >> 1) : b;
+}
+
 template <int FMT>
 __device__ void sg_down_chunk(const SgArgs &A, const SgExp &X, const uint8_t *st, int r0, const uint32_t *hq,
                               int qbase) {
@@ -562,7 +604,23 @@ __device__ void sg_down_chunk(const SgArgs &A, const SgExp &X, const uint8_t *st
         const int q = X.q0 + qi;
         const uint32_t *hrow = hq + (size_t)(q - qbase) * U * SG_HQW;
         float acc = 0.0f;
-        for (int b = qd; b < U; b += 8) acc += sg_down_block<FMT>(wrow, b, hrow + b * SG_HQW);
+        // blocks in groups of 16: lane qd takes 2 qd and 2 qd + 1, so for
+        // Q8_0 the warp runs one block parity at a time (sg_down_q8_0_fixed),
+        // and the staged h of both lie 80 bytes apart across the lanes
+        // (sg_hslot); the blocks after the last whole group as before
+        const int full = U / 16;
+        for (int o = 0; o < full; ++o) {
+            const int b = 16 * o + 2 * qd;
+            const uint32_t *h0 = hrow + (16 * o + qd) * SG_HQW, *h1 = hrow + (16 * o + 8 + qd) * SG_HQW;
+            if constexpr (FMT == MOE_Q8_0) {
+                acc += sg_down_q8_0_fixed<false>(wrow, b, h0);
+                acc += sg_down_q8_0_fixed<true>(wrow, b + 1, h1);
+            } else {
+                acc += sg_down_block<FMT>(wrow, b, h0);
+                acc += sg_down_block<FMT>(wrow, b + 1, h1);
+            }
+        }
+        for (int b = 16 * full + qd; b < U; b += 8) acc += sg_down_block<FMT>(wrow, b, hrow + b * SG_HQW);
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
         acc += __shfl_xor_sync(0xffffffffu, acc, 4);
@@ -644,7 +702,7 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sg_down_kernel(SgArgs A) {
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
             if (!in) continue;
-            uint32_t *dst = hq + (size_t)blk * SG_HQW;
+            uint32_t *dst = hq + ((size_t)qq * U + sg_hslot(b, U)) * SG_HQW;
             const int be = (int)((__float_as_uint(m) >> 23) & 0xffu);
             if (be == 255) {   // inf or nan in the block: it propagates
                 *reinterpret_cast<uint2 *>(dst + 2 * part) = make_uint2(0u, 0u);
