@@ -445,12 +445,21 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
     clk = clocks.stop()
 
     # ---- e2e: public API with pinned host buffers, copies inside the region
-    x_pin = [torch.from_numpy(L.x_host.view(np.int16).copy()).pin_memory() for L in layers]
-    lg_pin = [torch.from_numpy(L.logits_host.copy()).pin_memory() for L in layers]
-    out_pin = [torch.empty((T, H), dtype=torch.float32).pin_memory() for _ in layers]
-    x_dev = [torch.empty((T, H), dtype=torch.int16, device=dev) for _ in layers]
-    lg_dev = [torch.empty((T, E), dtype=torch.float32, device=dev) for _ in layers]
+    # all layers' inputs and outputs in contiguous pinned and device buffers,
+    # so that a group of consecutive layers moves in one copy each way
+    x_pin = torch.from_numpy(np.stack([L.x_host.view(np.int16) for L in layers])).pin_memory()
+    lg_pin = torch.from_numpy(np.stack([L.logits_host for L in layers])).pin_memory()
+    out_pin = torch.empty((NL, T, H), dtype=torch.float32).pin_memory()
+    x_dev = torch.empty((NL, T, H), dtype=torch.int16, device=dev)
+    lg_dev = torch.empty((NL, T, E), dtype=torch.float32, device=dev)
+    out_dev = torch.empty((NL, T, H), dtype=torch.float32, device=dev)
     n_e2e = max(1, min(args.e2e_steps, steps))
+    # layers per copy: about 2 MB a copy (one layer per copy for the prefill
+    # chunk, whose copies are bandwidth-bound and overlap the compute; every
+    # layer of a 1-token step in one copy, where each copy's fixed cost would
+    # otherwise add ~4 us to a 15 us layer)
+    group = max(1, min(NL, (2 << 20) // max(T * (H * 2 + E * 4), T * H * 4)))
+    groups = [(g0, min(NL, g0 + group)) for g0 in range(0, NL, group)]
 
     # Three streams, as a serving loop would run them: the inputs of layer l
     # go up on s_in while earlier layers compute on `stream`, and its output
@@ -459,26 +468,27 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
     # the host does not pace the small layers. Replays of the graph on
     # `stream` run one after another, so every buffer is reused in order.
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(NL)]
-    ev_comp = [torch.cuda.Event() for _ in range(NL)]
+    ev_in = [torch.cuda.Event() for _ in groups]
+    ev_comp = [torch.cuda.Event() for _ in groups]
 
     def e2e_step():
         root = torch.cuda.Event()
         root.record(stream)
         s_in.wait_event(root)
         s_out.wait_event(root)
-        for l in range(NL):
+        for gi, (g0, g1) in enumerate(groups):
             with torch.cuda.stream(s_in):
-                x_dev[l].copy_(x_pin[l], non_blocking=True)
-                lg_dev[l].copy_(lg_pin[l], non_blocking=True)
-                ev_in[l].record(s_in)
+                x_dev[g0:g1].copy_(x_pin[g0:g1], non_blocking=True)
+                lg_dev[g0:g1].copy_(lg_pin[g0:g1], non_blocking=True)
+                ev_in[gi].record(s_in)
             with torch.cuda.stream(stream):
-                stream.wait_event(ev_in[l])
-                M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=outs[l], ws=wss[l], options=opts_plain)
-                ev_comp[l].record(stream)
+                stream.wait_event(ev_in[gi])
+                for l in range(g0, g1):
+                    M.ffn_forward(tables[l], x_dev[l], lg_dev[l], k, out=out_dev[l], ws=wss[l], options=opts_plain)
+                ev_comp[gi].record(stream)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_comp[l])
-                out_pin[l].copy_(outs[l], non_blocking=True)
+                s_out.wait_event(ev_comp[gi])
+                out_pin[g0:g1].copy_(out_dev[g0:g1], non_blocking=True)
         done = torch.cuda.Event()
         done.record(s_out)
         stream.wait_event(done)
@@ -581,14 +591,15 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
                                          (dn_avg if kname == gu_name else gu_avg) * 1e6)},
         "tensor_pipe": tensor_pipe,
         "e2e": {"value": T * NL * n_e2e * world / e2e_elapsed, "unit": UNIT,
-                "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4},
+                "h2d_bytes_per_step": NL * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": NL * T * H * 4,
+                "layers_per_copy": group},
         "gpu_launches": launches_per_layer(path, T * (k + cfg.n_shared)) * NL * steps,
         "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
                  M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
         "clocks": clk,
         "device_status_flags": bad,
     }
-    del graphs, layers, tables, wss, outs, x_pin, lg_pin, out_pin, x_dev, lg_dev
+    del graphs, layers, tables, wss, outs, x_pin, lg_pin, out_pin, x_dev, lg_dev, out_dev
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
