@@ -67,6 +67,8 @@ bucket_kernel(const int32_t *__restrict__ ids, int T, int k, int E, int lo, int 
               const DevExpert *__restrict__ table, int32_t *__restrict__ offsets, int32_t *__restrict__ pairs,
               int32_t *__restrict__ pos, int32_t *__restrict__ active, uint32_t *__restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem[];
+    pdl_trigger();
+    pdl_wait();   // the ids come from the router kernel
     int *count = reinterpret_cast<int *>(smem);        // [E]
     int *base = count + E;                              // [E] bucket start
     int *run = base + E;                                // [E] pairs placed so far
@@ -166,6 +168,8 @@ __global__ void __launch_bounds__(BM_THREADS) bucket_count_kernel(const int32_t 
                                                                  const DevExpert *__restrict__ table,
                                                                  int32_t *__restrict__ cnt, uint32_t *__restrict__ status) {
     extern __shared__ __align__(16) unsigned char smem[];
+    pdl_trigger();
+    pdl_wait();
     int *hist = reinterpret_cast<int *>(smem);   // [E]
     const int tid = threadIdx.x, P = T * k;
     for (int e = tid; e < E; e += BM_THREADS) hist[e] = 0;
@@ -193,6 +197,8 @@ __global__ void __launch_bounds__(BK_THREADS, 1) bucket_scan_kernel(int G, int E
                                                                     int32_t *__restrict__ offsets,
                                                                     int32_t *__restrict__ active) {
     __shared__ int warp_tot[33];
+    pdl_trigger();
+    pdl_wait();
     const int tid = threadIdx.x;
     constexpr int BATCH = 16;   // independent loads in flight per thread (one range's load at a time took ~15 us)
     int c = 0;
@@ -237,6 +243,8 @@ __global__ void __launch_bounds__(BM_THREADS) bucket_scatter_kernel(const int32_
                                                                    int32_t *__restrict__ pairs,
                                                                    int32_t *__restrict__ pos) {
     extern __shared__ __align__(16) unsigned char smem[];
+    pdl_trigger();
+    pdl_wait();
     uint16_t *wcnt = reinterpret_cast<uint16_t *>(smem);   // [BM_WARPS][E]: exclusive per-warp offsets
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < BM_WARPS * E; i += BM_THREADS) wcnt[i] = 0;
@@ -289,19 +297,16 @@ cudaError_t launch_bucket(const int32_t *ids, int T, int k, int E, int lo, int h
     const int P = T * k;
     if (P > BUCKET_MANY && scratch) {
         const int G = (P + BM_THREADS - 1) / BM_THREADS;
-        bucket_count_kernel<<<G, BM_THREADS, (size_t)E * 4, s>>>(ids, T, k, E, lo, hi, fmt_mask, table, scratch,
-                                                                 status);
-        cudaError_t err = cudaGetLastError();
+        cudaError_t err = launch_pdl(bucket_count_kernel, dim3(G), dim3(BM_THREADS), (size_t)E * 4, s, ids, T, k, E,
+                                     lo, hi, fmt_mask, table, scratch, status);
         if (err != cudaSuccess) return err;
-        bucket_scan_kernel<<<1, BK_THREADS, 0, s>>>(G, E, scratch, offsets, active);
-        if ((err = cudaGetLastError()) != cudaSuccess) return err;
-        bucket_scatter_kernel<<<G, BM_THREADS, (size_t)BM_WARPS * E * 2, s>>>(ids, P, E, lo, hi, fmt_mask, table,
-                                                                             scratch, pairs, pos);
-        return cudaGetLastError();
+        err = launch_pdl(bucket_scan_kernel, dim3(1), dim3(BK_THREADS), 0, s, G, E, scratch, offsets, active);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(bucket_scatter_kernel, dim3(G), dim3(BM_THREADS), (size_t)BM_WARPS * E * 2, s, ids, P, E, lo,
+                          hi, fmt_mask, table, (const int32_t *)scratch, pairs, pos);
     }
-    bucket_kernel<<<1, BK_THREADS, smem, s>>>(ids, T, k, E, lo, hi, fmt_mask, table, offsets, pairs, pos, active,
-                                               status);
-    return cudaGetLastError();
+    return launch_pdl(bucket_kernel, dim3(1), dim3(BK_THREADS), smem, s, ids, T, k, E, lo, hi, fmt_mask, table, offsets,
+                      pairs, pos, active, status);
 }
 
 }  // namespace moe

@@ -452,6 +452,8 @@ __global__ void __launch_bounds__(GV_THREADS) down_gemv_kernel(GvArgs A) {
 template <bool SCALED>
 __global__ void combine_kernel(int T, int k, int H, const int32_t *__restrict__ pos, const float *__restrict__ wts,
                                const float *__restrict__ y, const float *__restrict__ yscale, float *__restrict__ out) {
+    pdl_trigger();
+    pdl_wait();   // y comes from the down kernel
     const int t = blockIdx.y;
     const int i4 = blockIdx.x * blockDim.x + threadIdx.x;
     if (i4 * 4 >= H) return;
@@ -510,11 +512,8 @@ cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float 
                            cudaStream_t s, const float *yscale) {
     if (T <= 0) return cudaSuccess;
     dim3 g((H / 4 + 127) / 128, T);
-    if (yscale)
-        combine_kernel<true><<<g, 128, 0, s>>>(T, k, H, pos, wts, y, yscale, out);
-    else
-        combine_kernel<false><<<g, 128, 0, s>>>(T, k, H, pos, wts, y, nullptr, out);
-    return cudaGetLastError();
+    if (yscale) return launch_pdl(combine_kernel<true>, g, dim3(128), 0, s, T, k, H, pos, wts, y, yscale, out);
+    return launch_pdl(combine_kernel<false>, g, dim3(128), 0, s, T, k, H, pos, wts, y, (const float *)nullptr, out);
 }
 
 size_t gateup_smem_bytes(int H, int64_t wstride) {

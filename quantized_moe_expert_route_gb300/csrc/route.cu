@@ -18,6 +18,9 @@ template <int V>  // logits per lane: E <= 32 * V
 __global__ void __launch_bounds__(ROUTE_WARPS * 32)
 route_topk_kernel(const float *__restrict__ logits, int T, int E, int k, int renorm, int32_t *__restrict__ ids,
                   float *__restrict__ wts, uint32_t *__restrict__ status, int stride, int n_shared) {
+    // the logits may come from the previous kernel in the stream
+    pdl_trigger();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * ROUTE_WARPS + (threadIdx.x >> 5);
     if (row >= T) return;
@@ -39,8 +42,8 @@ template <int V>
 cudaError_t launch_v(const float *logits, int T, int E, int k, int renorm, int32_t *ids, float *wts, uint32_t *status,
                      int stride, int n_shared, cudaStream_t s) {
     dim3 grid((T + ROUTE_WARPS - 1) / ROUTE_WARPS);
-    route_topk_kernel<V><<<grid, ROUTE_WARPS * 32, 0, s>>>(logits, T, E, k, renorm, ids, wts, status, stride, n_shared);
-    return cudaGetLastError();
+    return launch_pdl(route_topk_kernel<V>, grid, dim3(ROUTE_WARPS * 32), 0, s, logits, T, E, k, renorm, ids, wts,
+                      status, stride, n_shared);
 }
 
 }  // namespace
