@@ -27,7 +27,7 @@ LIBS = {
     "moe_route": {
         "out": os.path.join(PKG, "libmoe_route.so"),
         "srcs": [os.path.join(PKG, "csrc", f) for f in ("api.cu", "route.cu", "bucket.cu", "gemv.cu", "stream.cu", "decode.cu", "tc.cu", "noalloc.cu", "shard.cu", "cold.cu")],
-        "deps": [os.path.join(PKG, "csrc", "moe_internal.cuh"), os.path.join(PKG, "csrc", "dot16.cuh"),
+        "deps": [os.path.join(PKG, "csrc", "moe_internal.cuh"), os.path.join(PKG, "csrc", "dot16.cuh"), os.path.join(PKG, "csrc", "pdl.cuh"),
                  os.path.join(INCLUDE, "moe_route.h")],
     },
     "moe_synth": {

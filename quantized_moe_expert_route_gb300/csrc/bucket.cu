@@ -13,6 +13,7 @@
 // that share an expert; per expert, an exclusive scan over the 32 warps of the
 // chunk orders the warps; a running per-expert count orders the chunks.
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 

@@ -19,6 +19,7 @@
 // Every format is handled as 32-weight units: w_i = s_i * c_i - m with small
 // integer codes c_i (exact in fp32), s_i = s_lo for i < 16 and s_hi for i >= 16.
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 

@@ -136,28 +136,6 @@ static inline cudaError_t set_tu_wait_ns(unsigned long long ns) {
 
 // Host helpers shared by the launchers (gemv.cu, decode.cu).
 cudaError_t record_event(cudaEvent_t ev, cudaStream_t s);   // event (graph node when capturing)
-
-// Programmatic dependent launch: a kernel launched this way may begin while
-// the previous kernel in the stream is still running, so it executes
-// pdl_wait() before it reads or writes anything that an earlier kernel
-// writes or reads; pdl_trigger() lets the next such kernel begin its launch.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;"); }
-template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args... args) {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
 cudaError_t allow_max_dynamic_smem(const void *fn);         // opt in to all free shared memory
 int current_device();
 int sm_count();

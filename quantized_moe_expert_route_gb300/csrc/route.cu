@@ -7,6 +7,7 @@
 // last; the weights are the selected softmax probabilities, optionally
 // renormalised to sum to one.
 #include "moe_internal.cuh"
+#include "pdl.cuh"
 
 namespace moe {
 
