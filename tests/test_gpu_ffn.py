@@ -374,6 +374,22 @@ def test_stream_kernels_small(M, tiers, T, H, I):
     assert np.array_equal(again.cpu().numpy(), out)
 
 
+@pytest.mark.parametrize("tiers,T,H,I", [("q8_0", 4, 256, 512), ("q4k", 3, 256, 544), ("mixed", 5, 256, 576),
+                                         ("q4k", 2, 512, 1056), ("mixed", 6, 512, 1024)])
+def test_stream_down_block_groups(M, tiers, T, H, I):
+    """The streaming down kernel's blocks in groups of 16 (I = 512 .. 1056:
+    one or two whole groups, with 0, 1 or 2 blocks after them), Q8_0 and
+    MXFP4 down rows, against the oracle and bit for bit on a second call."""
+    cfg = synth.LayerConfig("sgd", 16, 4, H, I, T, tiers, True, 810 + T + I)
+    L = synth.make_layer(cfg, 0)
+    opt = M.make_options(n_experts=cfg.n_experts, path=M.PATH_GEMV)
+    out, table, x, logits = run_layer(M, L, options=opt)
+    assert M.gemv_kernels(table, T, cfg.k) == M.GEMV_STREAMING
+    assert_parity(out, offn.moe_ffn(L.experts, L.x_bf16, L.logits, cfg.k), f"stream down {tiers} T={T} I={I}")
+    again = M.ffn_forward(table, x, logits, cfg.k, options=opt)
+    assert np.array_equal(again.cpu().numpy(), out)
+
+
 @pytest.mark.parametrize("tiers,T,H,I", [("q4k", 17, 512, 128), ("q4k", 24, 256, 64), ("q8_0", 32, 512, 96),
                                          ("q4k", 32, 2048, 64)])
 def test_stream_kernels_up_to_32_rows(M, tiers, T, H, I):
