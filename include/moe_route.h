@@ -89,8 +89,9 @@ typedef enum {
  * of "三张 RTX 3090 …", section 优化策略二: Q6_K/Q8_0, IQ4_XS/IQ4_NL,
  * IQ3_XXS/MXFP4) but print no layout. IQ3_XXS needs the 256-entry grid of
  * four magnitude bytes per entry that its model file was made with, passed in
- * moe_weight_table.iq3_grid. IQ formats run on the tensor-core and the tiled
- * grouped GEMV paths.
+ * moe_weight_table.iq3_grid. IQ formats run on the tensor-core path and on
+ * both kinds of grouped GEMV kernels (the streaming ones decode batches of up
+ * to 16 rows).
  *   MOE_T5_G128 ternary, 128 weights / 28 B: fp16 s, then 26 code bytes;
  *                                weight 5b + i is base-3 digit i (least
  *                                significant first) of code byte b (the last
@@ -278,7 +279,8 @@ int moe_ffn_path(const moe_weight_table *W, int32_t T, int32_t k, const moe_opti
  * arguments: MOE_GEMV_STREAMING (persistent gate/up and down kernels that
  * stream the routed experts' rows through a shared-memory ring; decode
  * batches of 1..16 rows, or 1..32 rows when every gate/up matrix is Q8_0 or
- * Q4_K, with Q8_0 or MXFP4 down, shared memory permitting, and an activation
+ * Q4_K; gate/up in Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS or IQ3_XXS and down
+ * in Q8_0, MXFP4 or IQ4_NL; shared memory permitting, and an activation
  * pointer aligned to 16 bytes at the forward) or MOE_GEMV_TILED (one CTA per expert
  * tile; any other layer). -1 if the arguments are invalid. Host-only. */
 #define MOE_GEMV_TILED 0

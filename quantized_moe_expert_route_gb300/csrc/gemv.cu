@@ -531,7 +531,8 @@ cudaError_t launch_gemv_path(const DevExpert *table, int T, int k, int E, int H,
     if (T > 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0) {
         const SgPlan p = stream_plan(T, k, E, H, I, gu_formats, down_formats, gu_stride, dn_stride);
         if (p.ok) {
-            cudaError_t err = launch_stream_path(table, p, T, k, E, H, I, offsets, pairs, active, x, h, y, status, events, s);
+            cudaError_t err =
+                launch_stream_path(table, p, T, k, E, H, I, offsets, pairs, active, x, h, y, status, grid, events, s);
             if (err != cudaSuccess) return err;
             return launch_combine(T, k, H, pos, wts, y, out, s);
         }

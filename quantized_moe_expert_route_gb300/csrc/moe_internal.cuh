@@ -149,6 +149,7 @@ cudaError_t launch_combine(int T, int k, int H, const int32_t *pos, const float 
 // gate/up and down kernels (the combine is launched separately).
 struct SgPlan {
     bool ok;
+    bool iq;   // the variant of the kernels that decodes the IQ formats
     int cr, ns, stage, nexp, nsb, stageb, nq;
     size_t smem_a, smem_b;
 };
@@ -156,7 +157,8 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
                    int64_t dn_stride);
 cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, int k, int E, int H, int I,
                                const int32_t *offsets, const int32_t *pairs, const int32_t *active, const uint16_t *x,
-                               float *h, float *y, uint32_t *status, cudaEvent_t const *events, cudaStream_t s);
+                               float *h, float *y, uint32_t *status, const uint32_t *grid, cudaEvent_t const *events,
+                               cudaStream_t s);
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

@@ -68,6 +68,7 @@ struct SgArgs {
     float *h;            // fp32 [kept pairs, I], bucket order
     float *y;            // fp32 [kept pairs, H], bucket order
     uint32_t *status;
+    const uint32_t *grid;   // the IQ3_XXS grid (256 entries), or null
     int T, k, H, I, E;
     int cr, ns, stage, nexp;   // gate/up: row pairs per chunk, ring slots, slot bytes, experts per CTA (bound)
     int nsb, stageb, nq;       // down: ring slots, slot bytes, staged pairs per CTA (bound)
@@ -134,10 +135,149 @@ __device__ void sg_drain(uint64_t *full, const int *last, int ns) {
         if (last[s] >= 0) mbar_wait(&full[s], (uint32_t)(last[s] / ns) & 1u);
 }
 
+// ---- the IQ formats ("三张 RTX 3090 显卡实现 Qwen3.8-Flash-Next 80 Token 每秒的高效推理
+// 优化指南", 优化策略二: IQ4_XS gate/up with IQ4_NL down for the middle tier, IQ3_XXS
+// gate/up for the tail). Codebook values and signed grid magnitudes enter dp2a
+// as bytes, so the sums per scale group stay exact int32 as for the other
+// formats.
+
+// prmt.b32 in its default mode: a selector nibble with bit 3 set gives the
+// selected byte's sign bit in all eight bits (__byte_perm ignores that bit).
+__device__ __forceinline__ uint32_t sg_prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+// The codes of bytes 0..3 of w (low nibbles, or high nibbles with hi) as a
+// 16-bit selector, code i in nibble i.
+__device__ __forceinline__ uint32_t sg_nibble_sel(uint32_t w, bool hi) {
+    const uint32_t v = hi ? (w >> 4) : w;
+    const uint32_t x = (v & 0x000F000Fu) | ((v >> 4) & 0x00F000F0u);
+    return __byte_perm(x, 0u, 0x0020u);
+}
+// The IQ4 codebook entries (signed bytes) of four codes (nibbles 0..3 of
+// sel16): -127 -104 -83 -65 -49 -35 -22 -10 1 13 25 38 53 69 89 113, by a byte
+// permute of each half of the book and a byte select from bit 3 of each code.
+__device__ __forceinline__ uint32_t sg_iq4_bytes(uint32_t sel16) {
+    const uint32_t s7 = sel16 & 0x7777u;
+    const uint32_t lo = __byte_perm(0xBFAD9881u, 0xF6EADDCFu, s7);
+    const uint32_t hi = __byte_perm(0x26190D01u, 0x71594535u, s7);
+    const uint32_t m = sg_prmt(0u, 0x80808080u, ((sel16 >> 1) & 0x4444u) | 0x8888u);
+    return (hi & m) | (lo & ~m);
+}
+// 32 IQ4 codes (words w[0..3]: weight i < 16 the low nibble of byte i, 16 + i
+// the high nibble) against the activation pairs xq[o + 4m], xq[o + 4m + 1]
+// of columns 4m .. 4m + 3 (o = 0: part A, 2: part B).
+__device__ __forceinline__ int sg_iq4_sum32(const uint32_t (&w)[4], const uint32_t xq[32], int o) {
+    int s = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = sg_iq4_bytes(sg_nibble_sel(w[k], false)), hi = sg_iq4_bytes(sg_nibble_sel(w[k], true));
+        s = dp2a_lo(xq[4 * k + o], lo, s);
+        s = dp2a_hi(xq[4 * k + o + 1], lo, s);
+        s = dp2a_lo(xq[4 * (k + 4) + o], hi, s);
+        s = dp2a_hi(xq[4 * (k + 4) + o + 1], hi, s);
+    }
+    return s;
+}
+// IQ4_XS (136 bytes per 256 weights: fp16 d, uint16 high scale bits, 4 bytes
+// of low scale nibbles, 128 code bytes): group g is sub-blocks 2j, 2j + 1
+// (j = g & 3) of super-block g >> 2, which starts on 8 bytes; scale
+// d (ls - 32) with ls the 6-bit field of the sub-block.
+__device__ __forceinline__ float iq4xs_dot64(const uint8_t *row, int g, const uint32_t xq[32]) {
+    const uint8_t *sb = row + 136 * (g >> 2);
+    const int j = g & 3;
+    const uint2 hdr = *reinterpret_cast<const uint2 *>(sb);
+    uint32_t wa[4], wb[4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(sb + 8 + 32 * j + 8 * k);
+        const uint2 b = *reinterpret_cast<const uint2 *>(sb + 24 + 32 * j + 8 * k);
+        wa[2 * k] = a.x;
+        wa[2 * k + 1] = a.y;
+        wb[2 * k] = b.x;
+        wb[2 * k + 1] = b.y;
+    }
+    const int sA = sg_iq4_sum32(wa, xq, 0), sB = sg_iq4_sum32(wb, xq, 2);
+    const uint32_t sh = hdr.x >> 16;
+    const int ja = 2 * j, jb = 2 * j + 1;
+    const int lsA = (int)((hdr.y >> (8 * (ja >> 1) + 4 * (ja & 1))) & 15u) | (int)(((sh >> (2 * ja)) & 3u) << 4);
+    const int lsB = (int)((hdr.y >> (8 * (jb >> 1) + 4 * (jb & 1))) & 15u) | (int)(((sh >> (2 * jb)) & 3u) << 4);
+    return half_lo(hdr.x) * ((float)(lsA - 32) * (float)sA + (float)(lsB - 32) * (float)sB);
+}
+// IQ4_NL (18 bytes per 32 weights: fp16 d, 16 code bytes): group g is blocks
+// 2g (part A) and 2g + 1 (part B), 36 bytes from byte 36 g (4-byte aligned).
+__device__ __forceinline__ float iq4nl_dot64(const uint8_t *row, int g, const uint32_t xq[32]) {
+    const uint32_t *w = reinterpret_cast<const uint32_t *>(row + 36 * g);
+    uint32_t W[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) W[i] = w[i];
+    // block A: d in the low half of W[0], codes from byte 2; block B: d in
+    // the high half of W[4], codes from byte 20 (W[5..8])
+    uint32_t wa[4], wb[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        wa[k] = __funnelshift_r(W[k], W[k + 1], 16);
+        wb[k] = W[5 + k];
+    }
+    return half_lo(W[0]) * (float)sg_iq4_sum32(wa, xq, 0) + half_hi(W[4]) * (float)sg_iq4_sum32(wb, xq, 2);
+}
+// IQ3_XXS (98 bytes per 256 weights: fp16 d, 64 grid-index bytes, 8 words of
+// scale and signs): group g is sub-blocks 2j, 2j + 1 (j = g & 3) of
+// super-block g >> 2 (2-byte aligned). Group l of 8 weights of sub-block b
+// takes magnitudes from grid entries q[8b + 2l] (weights 0..3) and
+// q[8b + 2l + 1] (4..7) and signs from its 7-bit index in word b with the
+// parity as the eighth; scale d (0.5 + (word >> 28)) / 2. The magnitudes go to
+// dp2a as unsigned bytes, and the ones with a sign bit again masked: sum =
+// all - 2 negatives.
+__device__ __forceinline__ int dp2a_lo_u8(uint32_t a, uint32_t b, int c) {
+    asm("dp2a.lo.s32.u32 %0, %1, %2, %0;" : "+r"(c) : "r"(a), "r"(b));
+    return c;
+}
+__device__ __forceinline__ int dp2a_hi_u8(uint32_t a, uint32_t b, int c) {
+    asm("dp2a.hi.s32.u32 %0, %1, %2, %0;" : "+r"(c) : "r"(a), "r"(b));
+    return c;
+}
+__device__ __forceinline__ int sg_iq3_sum32(const uint32_t q0, const uint32_t q1, uint32_t a, const uint32_t *grid,
+                                            const uint32_t xq[32], int o) {
+    int sp = 0, sn = 0;
+#pragma unroll
+    for (int l = 0; l < 4; ++l) {
+        const uint32_t s7 = (a >> (7 * l)) & 127u;
+        const uint32_t sb = s7 | ((__popc(s7) & 1u) << 7);
+        const uint32_t qw = l < 2 ? q0 : q1;
+        const uint32_t e0 = __ldg(grid + ((qw >> (16 * (l & 1))) & 0xffu));
+        const uint32_t e1 = __ldg(grid + ((qw >> (16 * (l & 1) + 8)) & 0xffu));
+        // bit i of a 4-bit sign field -> bit 7 of byte i, then each byte's bit 7 replicated
+        const uint32_t m0 = sg_prmt((sb & 15u) * 0x10204080u, 0u, 0xBA98u);
+        const uint32_t m1 = sg_prmt((sb >> 4) * 0x10204080u, 0u, 0xBA98u);
+        sp = dp2a_lo_u8(xq[8 * l + o], e0, sp);
+        sp = dp2a_hi_u8(xq[8 * l + o + 1], e0, sp);
+        sp = dp2a_lo_u8(xq[8 * l + 4 + o], e1, sp);
+        sp = dp2a_hi_u8(xq[8 * l + 4 + o + 1], e1, sp);
+        sn = dp2a_lo_u8(xq[8 * l + o], e0 & m0, sn);
+        sn = dp2a_hi_u8(xq[8 * l + o + 1], e0 & m0, sn);
+        sn = dp2a_lo_u8(xq[8 * l + 4 + o], e1 & m1, sn);
+        sn = dp2a_hi_u8(xq[8 * l + 4 + o + 1], e1 & m1, sn);
+    }
+    return sp - 2 * sn;
+}
+__device__ __forceinline__ float iq3xxs_dot64(const uint8_t *row, int g, const uint32_t xq[32], const uint32_t *grid) {
+    const uint8_t *sb = row + 98 * (g >> 2);
+    const int j = g & 3;
+    const uint32_t qa0 = ld_u32_any(sb + 2 + 16 * j), qa1 = ld_u32_any(sb + 6 + 16 * j);
+    const uint32_t qb0 = ld_u32_any(sb + 10 + 16 * j), qb1 = ld_u32_any(sb + 14 + 16 * j);
+    const uint32_t aA = ld_u32_any(sb + 66 + 8 * j), aB = ld_u32_any(sb + 70 + 8 * j);
+    const float d = __half2float(__ushort_as_half((uint16_t)ld_u16(sb)));
+    const int sA = sg_iq3_sum32(qa0, qa1, aA, grid, xq, 0), sB = sg_iq3_sum32(qb0, qb1, aB, grid, xq, 2);
+    return d * ((0.5f + (float)(aA >> 28)) * 0.5f * (float)sA + (0.5f + (float)(aB >> 28)) * 0.5f * (float)sB);
+}
+
 // One 64-column group of CR rows of gate and of up against one token.
 template <int FMT, int CR>
 __device__ __forceinline__ void sg_rows(const uint8_t *g0, int gs, const uint8_t *u0, int us, int G64,
-                                        const uint32_t xv[32], int4 X16, float ag[CR], float au[CR]) {
+                                        const uint32_t xv[32], int4 X16, float ag[CR], float au[CR],
+                                        const uint32_t *grid) {
     const float XA = (float)(X16.x + X16.y), XB = (float)(X16.z + X16.w);
 #pragma unroll
     for (int r = 0; r < CR; ++r) {
@@ -151,9 +291,18 @@ __device__ __forceinline__ void sg_rows(const uint8_t *g0, int gs, const uint8_t
         } else if constexpr (FMT == MOE_Q6_K) {
             ag[r] += q6k_dot64(gr, G64, xv, X16);
             au[r] += q6k_dot64(ur, G64, xv, X16);
-        } else {
+        } else if constexpr (FMT == MOE_MXFP4) {
             ag[r] += mxfp4_dot64(gr, G64, xv);
             au[r] += mxfp4_dot64(ur, G64, xv);
+        } else if constexpr (FMT == MOE_IQ4_XS) {
+            ag[r] += iq4xs_dot64(gr, G64, xv);
+            au[r] += iq4xs_dot64(ur, G64, xv);
+        } else if constexpr (FMT == MOE_IQ4_NL) {
+            ag[r] += iq4nl_dot64(gr, G64, xv);
+            au[r] += iq4nl_dot64(ur, G64, xv);
+        } else {
+            ag[r] += iq3xxs_dot64(gr, G64, xv, grid);
+            au[r] += iq3xxs_dot64(ur, G64, xv, grid);
         }
     }
 }
@@ -182,7 +331,7 @@ __device__ void sg_gateup_chunk(const SgArgs &A, const SgExp &X, const int *tok,
                 xv[4 * v + 2] = q.z;
                 xv[4 * v + 3] = q.w;
             }
-            sg_rows<FMT, CR>(st, gs, u0, us, G64, xv, x16[(size_t)t * H64 + G64], ag, au);
+            sg_rows<FMT, CR>(st, gs, u0, us, G64, xv, x16[(size_t)t * H64 + G64], ag, au, A.grid);
         }
         const float s = xsc[t];
 #pragma unroll
@@ -195,7 +344,7 @@ __device__ void sg_gateup_chunk(const SgArgs &A, const SgExp &X, const int *tok,
     }
 }
 
-template <int CR>
+template <int CR, bool IQ>
 __device__ __forceinline__ void sg_gateup_dispatch(const SgArgs &A, const SgExp &X, const int *tok, const uint8_t *st,
                                                    int r0, const uint4 *xs4, const int4 *x16, const float *xsc) {
     switch (X.a.fmt) {
@@ -203,7 +352,16 @@ __device__ __forceinline__ void sg_gateup_dispatch(const SgArgs &A, const SgExp 
         case MOE_Q8_0: sg_gateup_chunk<MOE_Q8_0, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
         case MOE_Q6_K: sg_gateup_chunk<MOE_Q6_K, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
         case MOE_MXFP4: sg_gateup_chunk<MOE_MXFP4, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
-        default: break;
+        default:
+            if constexpr (IQ) {
+                switch (X.a.fmt) {
+                    case MOE_IQ4_XS: sg_gateup_chunk<MOE_IQ4_XS, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+                    case MOE_IQ4_NL: sg_gateup_chunk<MOE_IQ4_NL, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+                    case MOE_IQ3_XXS: sg_gateup_chunk<MOE_IQ3_XXS, CR>(A, X, tok, st, r0, xs4, x16, xsc); break;
+                    default: break;
+                }
+            }
+            break;
     }
 }
 
@@ -285,10 +443,13 @@ __device__ __forceinline__ int sg_chunk_cost(bool gateup, int f, int n) {
             case MOE_Q8_0: return 91 + 42 * n;
             case MOE_Q6_K: return 41 + 217 * n;
             case MOE_MXFP4: return 42 + 245 * n;
+            case MOE_IQ4_XS:   // codebook lookups like MXFP4's; IQ3_XXS two dots per grid entry
+            case MOE_IQ4_NL: return 42 + 245 * n;
+            case MOE_IQ3_XXS: return 41 + 217 * n;
             default: return 45 + 65 * n;   // Q4_K
         }
     }
-    return f == MOE_MXFP4 ? 18 + 94 * n : 22 + 54 * n;   // MXFP4 or Q8_0 down, 4 rows
+    return f == MOE_Q8_0 ? 22 + 54 * n : 18 + 94 * n;   // Q8_0, or MXFP4 / IQ4_NL down, 4 rows
 }
 // Bounds that follow from the costs a + b n (n >= 1 per active expert, so a +
 // b n <= (a + b) n): a gate/up chunk costs at least SG_GU_CMIN_CHUNK and a
@@ -349,6 +510,10 @@ __device__ void sg_range(const SgArgs &A, bool gateup, int n_act, int cpe, int *
     na = nloc > 0 ? (c1 - 1) / cpe - a0 + 1 : 0;
 }
 
+// IQ: the variant that also decodes the IQ formats (layers without them keep
+// the smaller code: with it the 16-row Q4_K layer measured 137.2 us against
+// 135.0 us).
+template <bool IQ>
 __global__ void __launch_bounds__(SG_THREADS, 1) sg_gateup_kernel(SgArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -486,9 +651,9 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sg_gateup_kernel(SgArgs A) {
             const uint8_t *st = ring + (size_t)s * A.stage;
             const SgExp &X = ex[la];
             const int *tk = tok + la * T;
-            if (A.cr == 4) sg_gateup_dispatch<4>(A, X, tk, st, r0, xs4, x16, xsc);
-            else if (A.cr == 2) sg_gateup_dispatch<2>(A, X, tk, st, r0, xs4, x16, xsc);
-            else sg_gateup_dispatch<1>(A, X, tk, st, r0, xs4, x16, xsc);
+            if (A.cr == 4) sg_gateup_dispatch<4, IQ>(A, X, tk, st, r0, xs4, x16, xsc);
+            else if (A.cr == 2) sg_gateup_dispatch<2, IQ>(A, X, tk, st, r0, xs4, x16, xsc);
+            else sg_gateup_dispatch<1, IQ>(A, X, tk, st, r0, xs4, x16, xsc);
             __syncwarp();
             if (lane == 0) *reinterpret_cast<volatile int *>(&used[s]) = j;
         }
@@ -531,7 +696,7 @@ __device__ __forceinline__ float sg_down_block(const uint8_t *wrow, int b, const
             s = dp2a_hi(hv[2 * i + 1], c, s);
         }
         return __half2float(__ushort_as_half((uint16_t)ld_u16(blk))) * hs * (float)s;
-    } else {
+    } else if constexpr (FMT == MOE_MXFP4) {
         // MXFP4, 17 bytes per block: E8M0 e, then 16 code bytes
         const uint8_t *blk = wrow + 17 * b;
         const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 1);
@@ -550,6 +715,25 @@ __device__ __forceinline__ float sg_down_block(const uint8_t *wrow, int b, const
             s = dp2a_hi(hv[8 + 2 * i + 1], hi, s);
         }
         return e8m0_half_scale(blk[0]) * hs * (float)s;
+    } else {
+        // IQ4_NL, 18 bytes per 32 weights: fp16 d, then 16 code bytes
+        const uint8_t *blk = wrow + 18 * b;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(blk + 2);
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(a & ~(uintptr_t)3);
+        const uint32_t sh = 8 * (uint32_t)(a & 3);
+        uint32_t W[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) W[i] = w[i];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t c = __funnelshift_r(W[i], W[i + 1], sh);
+            const uint32_t lo = sg_iq4_bytes(sg_nibble_sel(c, false)), hi = sg_iq4_bytes(sg_nibble_sel(c, true));
+            s = dp2a_lo(hv[2 * i], lo, s);
+            s = dp2a_hi(hv[2 * i + 1], lo, s);
+            s = dp2a_lo(hv[8 + 2 * i], hi, s);
+            s = dp2a_hi(hv[8 + 2 * i + 1], hi, s);
+        }
+        return __half2float(__ushort_as_half((uint16_t)ld_u16(blk))) * hs * (float)s;
     }
 }
 
@@ -628,6 +812,7 @@ __device__ void sg_down_chunk(const SgArgs &A, const SgExp &X, const uint8_t *st
     }
 }
 
+template <bool IQ>
 __global__ void __launch_bounds__(SG_THREADS, 1) sg_down_kernel(SgArgs A) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -730,7 +915,8 @@ __global__ void __launch_bounds__(SG_THREADS, 1) sg_down_kernel(SgArgs A) {
             const SgExp &X = ex[la];
             const uint8_t *st = ring + (size_t)s * A.stageb;
             if (X.a.fmt == MOE_Q8_0) sg_down_chunk<MOE_Q8_0>(A, X, st, r0, hq, qbase);
-            else sg_down_chunk<MOE_MXFP4>(A, X, st, r0, hq, qbase);
+            else if (!IQ || X.a.fmt == MOE_MXFP4) sg_down_chunk<MOE_MXFP4>(A, X, st, r0, hq, qbase);
+            else if constexpr (IQ) sg_down_chunk<MOE_IQ4_NL>(A, X, st, r0, hq, qbase);
             __syncwarp();
             if (lane == 0) *reinterpret_cast<volatile int *>(&used[s]) = j;
         }
@@ -763,10 +949,14 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
     if (G <= 0 || optin <= 0) return p;
     if (T < 1 || T > SG_MAX_T || H % 64 != 0 || I % 32 != 0 || H % SG_DN_ROWS != 0) return p;
     if (T > SG_MAX_T_MIXED && (gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K))) != 0) return p;
-    if ((down_formats & ~((1u << MOE_Q8_0) | (1u << MOE_MXFP4))) != 0) return p;
-    if ((gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K) | (1u << MOE_Q6_K) | (1u << MOE_MXFP4))) != 0) return p;
+    if ((down_formats & ~((1u << MOE_Q8_0) | (1u << MOE_MXFP4) | (1u << MOE_IQ4_NL))) != 0) return p;
+    if ((gu_formats & ~((1u << MOE_Q8_0) | (1u << MOE_Q4_K) | (1u << MOE_Q6_K) | (1u << MOE_MXFP4) |
+                        (1u << MOE_IQ4_XS) | (1u << MOE_IQ4_NL) | (1u << MOE_IQ3_XXS))) != 0)
+        return p;
     if (gu_stride <= 0 || dn_stride <= 0 || gu_stride % 16 != 0 || dn_stride % 16 != 0) return p;
     const int P = T * k, nmax = std::min(P, E);
+    p.iq = ((gu_formats | down_formats) &
+            ((1u << MOE_IQ4_XS) | (1u << MOE_IQ4_NL) | (1u << MOE_IQ3_XXS))) != 0;
     // the prefix costs of sg_range are ints: chunks per expert (at most I or
     // H / 4) times the list's cost per chunk row
     if ((long long)I * SG_GU_CMAX_PAIR * P > INT_MAX || (long long)(H / SG_DN_ROWS) * SG_DN_CMAX_PAIR * P > INT_MAX)
@@ -820,12 +1010,15 @@ SgPlan stream_plan(int T, int k, int E, int H, int I, uint32_t gu_formats, uint3
 
 cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, int k, int E, int H, int I,
                                const int32_t *offsets, const int32_t *pairs, const int32_t *active, const uint16_t *x,
-                               float *h, float *y, uint32_t *status, cudaEvent_t const *events, cudaStream_t s) {
+                               float *h, float *y, uint32_t *status, const uint32_t *grid, cudaEvent_t const *events,
+                               cudaStream_t s) {
     static bool attr_done[64] = {};
     const int dev = current_device();
     if (dev >= 64 || !attr_done[dev]) {
-        cudaError_t err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_gateup_kernel));
-        if (err == cudaSuccess) err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_down_kernel));
+        cudaError_t err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_gateup_kernel<false>));
+        if (err == cudaSuccess) err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_down_kernel<false>));
+        if (err == cudaSuccess) err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_gateup_kernel<true>));
+        if (err == cudaSuccess) err = allow_max_dynamic_smem(reinterpret_cast<const void *>(sg_down_kernel<true>));
         if (err != cudaSuccess) return err;
         if (dev < 64) attr_done[dev] = true;
     }
@@ -838,6 +1031,7 @@ cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, i
     A.h = h;
     A.y = y;
     A.status = status;
+    A.grid = grid;
     A.T = T;
     A.k = k;
     A.H = H;
@@ -862,13 +1056,13 @@ cudaError_t launch_stream_path(const DevExpert *table, const SgPlan &p, int T, i
     cudaError_t err;
     if (events && (err = record_event(events[0], s)) != cudaSuccess) return err;
     cfg.dynamicSmemBytes = p.smem_a;
-    err = cudaLaunchKernelEx(&cfg, sg_gateup_kernel, A);
+    err = p.iq ? cudaLaunchKernelEx(&cfg, sg_gateup_kernel<true>, A) : cudaLaunchKernelEx(&cfg, sg_gateup_kernel<false>, A);
     if (err != cudaSuccess) return err;
     // with timing events the down kernel's early start (its prologue under
     // the gate/up kernel's tail) is given up for a clean split
     if (events && (err = record_event(events[1], s)) != cudaSuccess) return err;
     cfg.dynamicSmemBytes = p.smem_b;
-    err = cudaLaunchKernelEx(&cfg, sg_down_kernel, A);
+    err = p.iq ? cudaLaunchKernelEx(&cfg, sg_down_kernel<true>, A) : cudaLaunchKernelEx(&cfg, sg_down_kernel<false>, A);
     if (err != cudaSuccess) return err;
     if (events && (err = record_event(events[2], s)) != cudaSuccess) return err;
     return cudaSuccess;
