@@ -1,6 +1,8 @@
 // Streaming grouped GEMV for decode batches of up to 16 token rows, any mix of
-// the gate/up formats (Q8_0, Q4_K, Q6_K, MXFP4) and Q8_0 or MXFP4 down, and of
-// up to 32 rows when every gate/up matrix is Q8_0 or Q4_K.
+// the gate/up formats (Q8_0, Q4_K, Q6_K, MXFP4, IQ4_NL, IQ4_XS, IQ3_XXS) and
+// Q8_0, MXFP4 or IQ4_NL down, and of up to 32 rows when every gate/up matrix
+// is Q8_0 or Q4_K. Layers with IQ formats run a variant of the two kernels
+// that carries their decoders.
 //
 // The grouped multi-session decode of "多卡 CUDA 张量并行：DwarfStar 如何在 8 张
 // L40S 上跑出 120 t/s" (section 120 t/s 的秘密) reads each selected expert's
