@@ -596,6 +596,11 @@ def measure_workload(M, name, args, world, rank, local, steps=None, min_seconds=
         "gpu_launches": launches_per_layer(path, T * (k + cfg.n_shared)) * NL * steps,
         "path": {M.PATH_FUSED: "fused decode kernel", M.PATH_GEMV: "grouped GEMV kernels",
                  M.PATH_TENSOR: "tensor-core grouped GEMM"}.get(path, str(path)),
+        # the arithmetic of the mat-muls: fp16 operands with fp32 accumulation on
+        # the tensor cores; int16 activations times the integer codes (int32 sums,
+        # fp32 scales) in the fused and streaming kernels; fp32 in the tiled ones
+        "dtype": ("f16" if path == M.PATH_TENSOR else
+                  "i16" if path == M.PATH_FUSED or M.gemv_kernels(tables[0], T, k) == M.GEMV_STREAMING else "f32"),
         "clocks": clk,
         "device_status_flags": bad,
     }
@@ -617,7 +622,7 @@ def run_ours(args, world, rank, local):
     head = measure_workload(M, args.config, args, world, rank, local, steps=args.steps)
     line = {"metric": METRIC, "value": head.pop("value"), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head.pop("ms_per_step"), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "scaling": "weak", "vs_baseline": None, "dtype": head.pop("dtype"),
             "data": "synthetic (seeded SplitMix64 weights written on the device; bf16 N(0,1) activations; "
                     "Zipf-biased fp32 logits)"}
     head.pop("steps")
